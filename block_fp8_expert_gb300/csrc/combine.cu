@@ -1,0 +1,48 @@
+// Combine: out[t] = sum_j w[t,j] y_perm[tok_slot_row[t*k+j]] (+ shared_y[t]),
+// summed in fp32 in slot order j, rounded once to bf16.
+#include "moe_internal.h"
+
+namespace moe {
+
+__global__ void __launch_bounds__(256)
+k_combine(const float* __restrict__ y_perm, const int32_t* __restrict__ tok_slot_row,
+          const float* __restrict__ topk_w, const float* __restrict__ shared_y, int T, int H,
+          int k, uint16_t* __restrict__ out) {
+  const int H4 = H / 4;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)T * H4) return;
+  const int t = (int)(i / H4), h = (int)(i % H4) * 4;
+  float4 acc = shared_y ? __ldg(reinterpret_cast<const float4*>(shared_y + (size_t)t * H + h))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < k; ++j) {
+    const int row = tok_slot_row[(size_t)t * k + j];
+    if (row < 0) continue;
+    const float w = topk_w[(size_t)t * k + j];
+    const float4 y = __ldg(reinterpret_cast<const float4*>(y_perm + (size_t)row * H + h));
+    r.x = fmaf(w, y.x, r.x);
+    r.y = fmaf(w, y.y, r.y);
+    r.z = fmaf(w, y.z, r.z);
+    r.w = fmaf(w, y.w, r.w);
+  }
+  acc.x += r.x;
+  acc.y += r.y;
+  acc.z += r.z;
+  acc.w += r.w;
+  uint2 o;
+  o.x = pack_bf16x2(acc.x, acc.y);
+  o.y = pack_bf16x2(acc.z, acc.w);
+  *reinterpret_cast<uint2*>(out + (size_t)t * H + h) = o;
+}
+
+cudaError_t launch_combine(const float* y_perm, const int32_t* tok_slot_row, const float* topk_w,
+                           const float* shared_y, int T, int H, int k, uint16_t* out,
+                           cudaStream_t s) {
+  const long long n = (long long)T * (H / 4);
+  if (n == 0) return cudaSuccess;
+  k_combine<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(y_perm, tok_slot_row, topk_w, shared_y,
+                                                        T, H, k, out);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,330 @@
+// The C ABI (include/moe_fp8.h): argument checks, workspace layout, launches.
+// Nothing here allocates device memory or synchronises the host, except
+// moe_read_device_status, whose job is to read a device word back.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+thread_local std::string g_last_error;
+
+moe_status fail(moe_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+moe_status fail(moe_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+moe_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(MOE_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+size_t align_up(size_t v) { return (v + 255) & ~size_t(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define REQUIRE_PTR(p)                                                                    \
+  do {                                                                                    \
+    if ((p) == nullptr) return fail(MOE_ERR_INVALID_ARG, "%s is NULL", #p);               \
+    if (!aligned16(p)) return fail(MOE_ERR_INVALID_ARG, "%s is not 16-byte aligned", #p); \
+  } while (0)
+
+#define REQUIRE_OPT_PTR(p)                                                   \
+  do {                                                                       \
+    if ((p) != nullptr && !aligned16(p))                                     \
+      return fail(MOE_ERR_INVALID_ARG, "%s is not 16-byte aligned", #p);    \
+  } while (0)
+
+#define CUDA_CHECK(expr, where)                           \
+  do {                                                    \
+    cudaError_t e_ = (expr);                              \
+    if (e_ != cudaSuccess) return cuda_fail(e_, where);   \
+  } while (0)
+
+moe_status check_dims(const moe_dims& d) {
+  if (d.T < 0) return fail(MOE_ERR_INVALID_ARG, "T = %d < 0", d.T);
+  auto dim_ok = [](int v) { return v >= 64 && v <= 16384 && v % 64 == 0; };
+  if (!dim_ok(d.H))
+    return fail(MOE_ERR_UNSUPPORTED, "H = %d: need a multiple of 64 in [64, 16384]", d.H);
+  if (!dim_ok(d.I))
+    return fail(MOE_ERR_UNSUPPORTED, "I = %d: need a multiple of 64 in [64, 16384]", d.I);
+  if (d.I_shared != 0 && !dim_ok(d.I_shared))
+    return fail(MOE_ERR_UNSUPPORTED, "I_shared = %d: need 0 or a multiple of 64 in [64, 16384]",
+                d.I_shared);
+  if (d.E < 1 || d.E > 1024) return fail(MOE_ERR_UNSUPPORTED, "E = %d outside [1, 1024]", d.E);
+  if (d.k < 1 || d.k > 32 || d.k > d.E)
+    return fail(MOE_ERR_UNSUPPORTED, "k = %d outside [1, min(E, 32)]", d.k);
+  if ((long long)d.T * d.k >= (1LL << 31)) return fail(MOE_ERR_UNSUPPORTED, "T*k too large");
+  return MOE_OK;
+}
+
+moe_status check_mat(const moe_fp8_mat& m, const char* name) {
+  if (!m.codes || !m.scales) return fail(MOE_ERR_INVALID_ARG, "%s: NULL codes or scales", name);
+  if (!aligned16(m.codes) || !aligned16(m.scales))
+    return fail(MOE_ERR_INVALID_ARG, "%s: codes/scales not 16-byte aligned", name);
+  return MOE_OK;
+}
+
+moe_status check_ffn(const moe_fp8_ffn& w, const char* name) {
+  std::string n(name);
+  moe_status s;
+  if ((s = check_mat(w.gate, (n + ".gate").c_str())) != MOE_OK) return s;
+  if ((s = check_mat(w.up, (n + ".up").c_str())) != MOE_OK) return s;
+  return check_mat(w.down, (n + ".down").c_str());
+}
+
+moe_status check_ws(const moe_dims& d, const void* ws, size_t ws_bytes) {
+  REQUIRE_PTR(ws);
+  const size_t need = ws_layout(d).total;
+  if (ws_bytes < need)
+    return fail(MOE_ERR_WORKSPACE, "workspace of %zu bytes, need %zu", ws_bytes, need);
+  return MOE_OK;
+}
+
+template <class T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+}  // namespace
+
+WsLayout ws_layout(const moe_dims& d) {
+  const size_t T = d.T, E = d.E, P = (size_t)d.T * d.k, H = d.H, I = d.I, Is = d.I_shared;
+  const size_t nb = (P + 255) / 256;
+  WsLayout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align_up(bytes ? bytes : 1);
+    return at;
+  };
+  L.status = take(256);
+  L.logits = take(T * E * 4);
+  L.rank = take(P * 4);
+  L.block_cnt = take(nb * E * 4);
+  L.block_base = take(nb * E * 4);
+  L.active = take((1 + E) * 4);
+  L.idx = take(P * 4);
+  L.w = take(P * 4);
+  L.off = take((E + 1) * 4);
+  L.row_token = take(P * 4);
+  L.tok_slot_row = take(P * 4);
+  L.hid = take(P * I * 2);
+  L.y_perm = take(P * H * 4);
+  L.sh_hid = take(Is ? T * Is * 2 : 0);
+  L.sh_y = take(Is ? T * H * 4 : 0);
+  L.sh_off = take(2 * 4);
+  L.sh_rows = take(Is ? T * 4 : 0);
+  L.sh_active = take(2 * 4);
+  L.total = o;
+  return L;
+}
+
+__global__ void k_identity_perm(int T, int32_t* off, int32_t* rows, int32_t* active) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < T) rows[i] = i;
+  if (i == 0) {
+    off[0] = 0;
+    off[1] = T;
+    active[0] = T > 0 ? 1 : 0;
+    active[1] = 0;
+  }
+}
+
+cudaError_t launch_identity_perm(int T, int32_t* off, int32_t* rows, int32_t* active,
+                                 cudaStream_t s) {
+  k_identity_perm<<<cdiv(T > 0 ? T : 1, 256), 256, 0, s>>>(T, off, rows, active);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_STATUS: return "device reported bad input";
+    case MOE_ERR_TIMEOUT: return "bounded device wait timed out";
+    case MOE_ERR_NOT_IMPLEMENTED: return "not implemented";
+    default: return "unknown status";
+  }
+}
+
+const char* moe_last_error_message(void) { return g_last_error.c_str(); }
+
+const char* moe_version(void) { return "moe_fp8 0.1 sm_103a"; }
+
+moe_status moe_workspace_bytes(moe_dims d, size_t* bytes) {
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  if (!bytes) return fail(MOE_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = ws_layout(d).total;
+  return MOE_OK;
+}
+
+moe_status moe_route(const uint16_t* x, const float* Wr, const float* bias, moe_dims d,
+                     int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
+                     void* stream) {
+  moe_status s;
+  if ((s = check_dims(d)) != MOE_OK) return s;
+  REQUIRE_PTR(x);
+  REQUIRE_PTR(Wr);
+  REQUIRE_OPT_PTR(bias);
+  REQUIRE_PTR(topk_idx);
+  REQUIRE_PTR(topk_w);
+  if ((s = check_ws(d, ws, ws_bytes)) != MOE_OK) return s;
+  const WsLayout L = ws_layout(d);
+  CUDA_CHECK(launch_route(x, Wr, bias, d.T, d.H, d.E, d.k, at<float>(ws, L.logits), topk_idx,
+                          topk_w, (cudaStream_t)stream),
+             "moe_route");
+  return MOE_OK;
+}
+
+moe_status moe_permute(const int32_t* topk_idx, moe_dims d, int32_t* expert_off,
+                       int32_t* row_token, int32_t* tok_slot_row, void* ws, size_t ws_bytes,
+                       void* stream) {
+  moe_status s;
+  if ((s = check_dims(d)) != MOE_OK) return s;
+  REQUIRE_PTR(topk_idx);
+  REQUIRE_PTR(expert_off);
+  REQUIRE_PTR(row_token);
+  REQUIRE_PTR(tok_slot_row);
+  if ((s = check_ws(d, ws, ws_bytes)) != MOE_OK) return s;
+  const WsLayout L = ws_layout(d);
+  cudaStream_t st = (cudaStream_t)stream;
+  CUDA_CHECK(cudaMemsetAsync(at<int32_t>(ws, L.status), 0, sizeof(int32_t), st), "moe_permute");
+  CUDA_CHECK(launch_permute(topk_idx, d.T, d.E, d.k, at<int32_t>(ws, L.rank),
+                            at<int32_t>(ws, L.block_cnt), at<int32_t>(ws, L.block_base),
+                            expert_off, row_token, tok_slot_row, at<int32_t>(ws, L.active),
+                            at<int32_t>(ws, L.status), st),
+             "moe_permute");
+  return MOE_OK;
+}
+
+moe_status moe_expert_ffn_fp8(const uint16_t* x, const int32_t* expert_off,
+                              const int32_t* row_token, moe_fp8_ffn w, moe_dims d,
+                              float* y_perm, void* ws, size_t ws_bytes, void* stream) {
+  moe_status s;
+  if ((s = check_dims(d)) != MOE_OK) return s;
+  REQUIRE_PTR(x);
+  REQUIRE_PTR(expert_off);
+  REQUIRE_PTR(row_token);
+  REQUIRE_PTR(y_perm);
+  if ((s = check_ffn(w, "w")) != MOE_OK) return s;
+  if ((s = check_ws(d, ws, ws_bytes)) != MOE_OK) return s;
+  if (d.T == 0) return MOE_OK;
+  const WsLayout L = ws_layout(d);
+  cudaStream_t st = (cudaStream_t)stream;
+  int32_t* active = at<int32_t>(ws, L.active);
+  CUDA_CHECK(launch_active_from_offsets(expert_off, d.E, active, st), "moe_expert_ffn_fp8");
+  const int P = d.T * d.k;
+  CUDA_CHECK(launch_expert_gemv(x, expert_off, row_token, active, d.E < P ? d.E : P, w, d.H, d.I,
+                                d.T, at<uint16_t>(ws, L.hid), y_perm, st),
+             "moe_expert_ffn_fp8");
+  return MOE_OK;
+}
+
+moe_status moe_combine(const float* y_perm, const int32_t* tok_slot_row, const float* topk_w,
+                       const float* shared_y, moe_dims d, uint16_t* out, void* stream) {
+  moe_status s;
+  if ((s = check_dims(d)) != MOE_OK) return s;
+  REQUIRE_PTR(y_perm);
+  REQUIRE_PTR(tok_slot_row);
+  REQUIRE_PTR(topk_w);
+  REQUIRE_OPT_PTR(shared_y);
+  REQUIRE_PTR(out);
+  CUDA_CHECK(launch_combine(y_perm, tok_slot_row, topk_w, shared_y, d.T, d.H, d.k, out,
+                            (cudaStream_t)stream),
+             "moe_combine");
+  return MOE_OK;
+}
+
+moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bias,
+                             moe_fp8_ffn routed, const moe_fp8_ffn* shared, moe_dims d,
+                             uint16_t* out, int32_t* topk_idx_out, float* topk_w_out, void* ws,
+                             size_t ws_bytes, void* stream) {
+  moe_status s;
+  if ((s = check_dims(d)) != MOE_OK) return s;
+  REQUIRE_PTR(x);
+  REQUIRE_PTR(Wr);
+  REQUIRE_OPT_PTR(bias);
+  REQUIRE_PTR(out);
+  REQUIRE_OPT_PTR(topk_idx_out);
+  REQUIRE_OPT_PTR(topk_w_out);
+  if ((s = check_ffn(routed, "routed")) != MOE_OK) return s;
+  if (d.I_shared > 0) {
+    if (!shared) return fail(MOE_ERR_INVALID_ARG, "I_shared > 0 but shared is NULL");
+    if ((s = check_ffn(*shared, "shared")) != MOE_OK) return s;
+  } else if (shared) {
+    return fail(MOE_ERR_INVALID_ARG, "shared given but I_shared == 0");
+  }
+  if ((s = check_ws(d, ws, ws_bytes)) != MOE_OK) return s;
+  if (d.T == 0) return MOE_OK;
+  const WsLayout L = ws_layout(d);
+  cudaStream_t st = (cudaStream_t)stream;
+  const int P = d.T * d.k;
+  int32_t* idx = topk_idx_out ? topk_idx_out : at<int32_t>(ws, L.idx);
+  float* w = topk_w_out ? topk_w_out : at<float>(ws, L.w);
+  int32_t* off = at<int32_t>(ws, L.off);
+  int32_t* row_token = at<int32_t>(ws, L.row_token);
+  int32_t* tok_slot_row = at<int32_t>(ws, L.tok_slot_row);
+  int32_t* active = at<int32_t>(ws, L.active);
+  float* y_perm = at<float>(ws, L.y_perm);
+
+  CUDA_CHECK(cudaMemsetAsync(at<int32_t>(ws, L.status), 0, sizeof(int32_t), st),
+             "moe_layer_forward");
+  CUDA_CHECK(launch_route(x, Wr, bias, d.T, d.H, d.E, d.k, at<float>(ws, L.logits), idx, w, st),
+             "moe_layer_forward: route");
+  CUDA_CHECK(launch_permute(idx, d.T, d.E, d.k, at<int32_t>(ws, L.rank),
+                            at<int32_t>(ws, L.block_cnt), at<int32_t>(ws, L.block_base), off,
+                            row_token, tok_slot_row, active, at<int32_t>(ws, L.status), st),
+             "moe_layer_forward: permute");
+  CUDA_CHECK(launch_expert_gemv(x, off, row_token, active, d.E < P ? d.E : P, routed, d.H, d.I,
+                                d.T, at<uint16_t>(ws, L.hid), y_perm, st),
+             "moe_layer_forward: experts");
+  float* shared_y = nullptr;
+  if (d.I_shared > 0) {
+    int32_t* soff = at<int32_t>(ws, L.sh_off);
+    int32_t* srows = at<int32_t>(ws, L.sh_rows);
+    int32_t* sact = at<int32_t>(ws, L.sh_active);
+    shared_y = at<float>(ws, L.sh_y);
+    CUDA_CHECK(launch_identity_perm(d.T, soff, srows, sact, st), "moe_layer_forward: shared");
+    CUDA_CHECK(launch_expert_gemv(x, soff, srows, sact, 1, *shared, d.H, d.I_shared, d.T,
+                                  at<uint16_t>(ws, L.sh_hid), shared_y, st),
+               "moe_layer_forward: shared expert");
+  }
+  CUDA_CHECK(launch_combine(y_perm, tok_slot_row, w, shared_y, d.T, d.H, d.k, out, st),
+             "moe_layer_forward: combine");
+  return MOE_OK;
+}
+
+moe_status moe_read_device_status(const void* ws, int32_t* status, void* stream) {
+  REQUIRE_PTR(ws);
+  if (!status) return fail(MOE_ERR_INVALID_ARG, "status is NULL");
+  cudaStream_t st = (cudaStream_t)stream;
+  int32_t v = 0;
+  CUDA_CHECK(cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, st),
+             "moe_read_device_status");
+  CUDA_CHECK(cudaStreamSynchronize(st), "moe_read_device_status");
+  *status = v;
+  if (v != 0) return fail(MOE_ERR_DEVICE_STATUS, "device status word 0x%x", v);
+  return MOE_OK;
+}
+
+}  // extern "C"

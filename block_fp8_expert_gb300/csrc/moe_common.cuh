@@ -1,0 +1,100 @@
+// Device helpers shared by the kernels of the block-FP8 MoE layer (sm_103a).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "moe_fp8.h"
+
+namespace moe {
+
+constexpr int kScaleBlock = 128;  // edge of one block-FP8 scale block
+
+// 2^112 as a float: the register decode below yields dec(code) * 2^-112, and
+// the block scale applied after the MMA carries the 2^112 back.
+constexpr float kPow2_112 = 5.192296858534828e33f;
+
+__host__ __device__ constexpr int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------------------
+// bf16 helpers (bf16 = top half of an IEEE binary32)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// Two floats -> bf16x2 (lo in bits 0..15), round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// E4M3 decode in registers
+// ---------------------------------------------------------------------------
+// Two E4M3 codes (bits 0..7 = element 0, bits 8..15 = element 1) -> f16x2.
+// Every E4M3 value, subnormals included, is an f16 normal or zero, so this is
+// exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  uint32_t r;
+  const unsigned short v = static_cast<unsigned short>(two_codes & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
+
+// f16x2 holding E4M3-derived values -> bf16x2 holding the same values times
+// 2^-112, exactly.  Such an f16 has only its top 3 mantissa bits set, so
+// moving exponent and mantissa down by 3 bits re-reads the f16 exponent field
+// (bias 15) as a bf16 exponent field (bias 127); the sign stays in place and
+// zero stays zero.  Two integer instructions, no float conversion.
+__device__ __forceinline__ uint32_t f16x2_e4m3_to_bf16x2_scaled(uint32_t h) {
+  return ((h >> 3) & 0x0FFF0FFFu) | (h & 0x80008000u);
+}
+
+// 16 E4M3 codes (one 16-byte load) -> 8 bf16x2 registers holding
+// dec(code) * 2^-112; out[m] holds elements 2m (low half) and 2m+1.
+__device__ __forceinline__ void decode16_scaled(const uint4& c, uint32_t (&out)[8]) {
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    out[2 * q + 0] = f16x2_e4m3_to_bf16x2_scaled(e4m3x2_to_f16x2(w[q] & 0xFFFFu));
+    out[2 * q + 1] = f16x2_e4m3_to_bf16x2_scaled(e4m3x2_to_f16x2(w[q] >> 16));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Warp-level bf16 tensor-core MMA: D(16x8 f32) += A(16x16 bf16) B(16x8 bf16)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mma_bf16_16x8x16(float (&d)[4], const uint32_t (&a)[4],
+                                                 const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// ---------------------------------------------------------------------------
+// Loads
+// ---------------------------------------------------------------------------
+// Streamed once: do not keep in L1.
+__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint4 ldg16(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// ---------------------------------------------------------------------------
+// Device status word
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void raise_status(int32_t* status, int32_t bits) {
+  if (status) atomicOr(status, bits);
+}
+
+}  // namespace moe

@@ -1,0 +1,199 @@
+// Permutation of the T*k (token, slot) pairs into expert-contiguous rows:
+// a stable counting sort of the flattened pair index q = t*k + j by expert.
+// Inside one expert, ascending q is ascending t (a token never picks the same
+// expert twice), which is the order the layer's rows use.
+//
+// Three launches, no atomics that decide an order:
+//   count   per block of kPermBlock pairs: per-expert counts and each pair's
+//           rank among the block's pairs of the same expert (warp match +
+//           per-warp prefix);
+//   scan    one CTA: per-expert totals, exclusive prefix over blocks, the
+//           expert offsets (exclusive scan over experts) and the list of
+//           experts that received rows;
+//   scatter row = off[e] + block prefix + rank.
+#include "moe_internal.h"
+
+namespace moe {
+
+constexpr int kPermBlock = 256;  // pairs per count/scatter CTA (8 warps)
+
+__global__ void __launch_bounds__(kPermBlock)
+k_perm_count(const int32_t* __restrict__ topk_idx, int P, int E,
+             int32_t* __restrict__ rank, int32_t* __restrict__ block_cnt,
+             int32_t* __restrict__ status) {
+  extern __shared__ int32_t cnt_w[];  // [8][E]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < 8 * E; i += kPermBlock) cnt_w[i] = 0;
+  __syncthreads();
+  const int q = blockIdx.x * kPermBlock + tid;
+  int e = -2;  // -2: past the end, -1: invalid index
+  if (q < P) {
+    e = topk_idx[q];
+    if (e < 0 || e >= E) {
+      raise_status(status, MOE_DEV_BAD_EXPERT_INDEX);
+      e = -1;
+    }
+  }
+  const uint32_t peers = __match_any_sync(0xffffffffu, e);
+  const int rank_w = __popc(peers & ((1u << lane) - 1u));
+  if (e >= 0 && rank_w == 0) cnt_w[warp * E + e] = __popc(peers);
+  __syncthreads();
+  for (int x = tid; x < E; x += kPermBlock) {
+    int run = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const int c = cnt_w[w * E + x];
+      cnt_w[w * E + x] = run;
+      run += c;
+    }
+    block_cnt[(size_t)blockIdx.x * E + x] = run;
+  }
+  __syncthreads();
+  if (q < P) rank[q] = e >= 0 ? cnt_w[warp * E + e] + rank_w : -1;
+}
+
+// One CTA of 1024 threads; E <= 1024.
+__global__ void __launch_bounds__(1024)
+k_perm_scan(const int32_t* __restrict__ block_cnt, int nblocks, int E,
+            int32_t* __restrict__ block_base, int32_t* __restrict__ expert_off,
+            int32_t* __restrict__ active) {
+  __shared__ int32_t warp_sum[32];
+  __shared__ int32_t warp_act[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int total = 0;
+  if (tid < E) {
+    // exclusive prefix over blocks for expert tid
+    int b = 0;
+    for (; b + 4 <= nblocks; b += 4) {
+      const int c0 = block_cnt[(size_t)(b + 0) * E + tid];
+      const int c1 = block_cnt[(size_t)(b + 1) * E + tid];
+      const int c2 = block_cnt[(size_t)(b + 2) * E + tid];
+      const int c3 = block_cnt[(size_t)(b + 3) * E + tid];
+      block_base[(size_t)(b + 0) * E + tid] = total;
+      block_base[(size_t)(b + 1) * E + tid] = total + c0;
+      block_base[(size_t)(b + 2) * E + tid] = total + c0 + c1;
+      block_base[(size_t)(b + 3) * E + tid] = total + c0 + c1 + c2;
+      total += c0 + c1 + c2 + c3;
+    }
+    for (; b < nblocks; ++b) {
+      const int c = block_cnt[(size_t)b * E + tid];
+      block_base[(size_t)b * E + tid] = total;
+      total += c;
+    }
+  }
+  // exclusive scan of totals (and of the non-empty flags) over experts
+  int incl = total, act = total > 0 ? 1 : 0;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    const int a = __shfl_up_sync(0xffffffffu, act, o);
+    if (lane >= o) {
+      incl += v;
+      act += a;
+    }
+  }
+  if (lane == 31) {
+    warp_sum[warp] = incl;
+    warp_act[warp] = act;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int s = warp_sum[lane], a = warp_act[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, s, o);
+      const int w = __shfl_up_sync(0xffffffffu, a, o);
+      if (lane >= o) {
+        s += v;
+        a += w;
+      }
+    }
+    warp_sum[lane] = s;  // inclusive over warps
+    warp_act[lane] = a;
+  }
+  __syncthreads();
+  const int before = warp ? warp_sum[warp - 1] : 0;
+  const int before_a = warp ? warp_act[warp - 1] : 0;
+  if (tid < E) {
+    expert_off[tid] = before + incl - total;
+    if (total > 0) active[1 + before_a + act - 1] = tid;
+  }
+  if (tid == E - 1) {
+    expert_off[E] = before + incl;
+    active[0] = before_a + act;
+  }
+}
+
+__global__ void __launch_bounds__(kPermBlock)
+k_perm_scatter(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ rank,
+               const int32_t* __restrict__ block_base, const int32_t* __restrict__ expert_off,
+               int P, int E, int k, int32_t* __restrict__ row_token,
+               int32_t* __restrict__ tok_slot_row) {
+  const int q = blockIdx.x * kPermBlock + threadIdx.x;
+  if (q >= P) return;
+  const int r = rank[q];
+  if (r < 0) {
+    tok_slot_row[q] = -1;
+    return;
+  }
+  const int e = topk_idx[q];
+  const int row = expert_off[e] + block_base[(size_t)blockIdx.x * E + e] + r;
+  row_token[row] = q / k;
+  tok_slot_row[q] = row;
+}
+
+// Active-expert list from offsets alone (for callers of the expert FFN that
+// did not run the permutation here).  One CTA; E <= 1024.
+__global__ void __launch_bounds__(1024)
+k_active_from_offsets(const int32_t* __restrict__ expert_off, int E,
+                      int32_t* __restrict__ active) {
+  __shared__ int32_t warp_act[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ne = (tid < E && expert_off[tid + 1] > expert_off[tid]) ? 1 : 0;
+  int act = ne;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int a = __shfl_up_sync(0xffffffffu, act, o);
+    if (lane >= o) act += a;
+  }
+  if (lane == 31) warp_act[warp] = act;
+  __syncthreads();
+  if (warp == 0) {
+    int a = warp_act[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int w = __shfl_up_sync(0xffffffffu, a, o);
+      if (lane >= o) a += w;
+    }
+    warp_act[lane] = a;
+  }
+  __syncthreads();
+  const int before = warp ? warp_act[warp - 1] : 0;
+  if (ne) active[1 + before + act - 1] = tid;
+  if (tid == 1023) active[0] = warp_act[31];
+}
+
+cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, int32_t* rank,
+                           int32_t* block_cnt, int32_t* block_base, int32_t* expert_off,
+                           int32_t* row_token, int32_t* tok_slot_row, int32_t* active,
+                           int32_t* status, cudaStream_t s) {
+  const int P = T * k;
+  const int nb = cdiv(P, kPermBlock);
+  if (nb > 0) {
+    const size_t smem = sizeof(int32_t) * 8 * E;
+    k_perm_count<<<nb, kPermBlock, smem, s>>>(topk_idx, P, E, rank, block_cnt, status);
+  }
+  k_perm_scan<<<1, 1024, 0, s>>>(block_cnt, nb, E, block_base, expert_off, active);
+  if (nb > 0)
+    k_perm_scatter<<<nb, kPermBlock, 0, s>>>(topk_idx, rank, block_base, expert_off, P, E, k,
+                                             row_token, tok_slot_row);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_active_from_offsets(const int32_t* expert_off, int E, int32_t* active,
+                                       cudaStream_t s) {
+  k_active_from_offsets<<<1, 1024, 0, s>>>(expert_off, E, active);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

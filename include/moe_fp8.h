@@ -1,0 +1,188 @@
+/*
+ * moe_fp8.h - C ABI of a block-FP8 (E4M3) Mixture-of-Experts FFN layer for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The layer, as the colizig README states its parts (model table under "What
+ * this project is trying to prove": experts, top-k routing, an optional shared
+ * expert; "Features": block-FP8 E4M3 expert weights evaluated with a fused
+ * decode+FMA dot product, MoE per-expert evaluation):
+ *
+ *   l[t,e]  = sum_h x[t,h] Wr[e,h] (+ b[e])                       router GEMM
+ *   p[t,:]  = softmax(l[t,:]) over the E experts
+ *   idx,w   = the k largest p[t,e] (descending, ties to the lower e),
+ *             w_j = p_j / sum_{selected} p                        top-k, renorm
+ *   rows    = the (t,j) pairs sorted by expert, ascending t inside an expert
+ *   W[r,c]  = dec(C[r,c]) * S[r/128, c/128]                       block-FP8
+ *   hid     = silu(x Wg^T) * (x Wu^T),  silu(z) = z/(1+exp(-z))   SwiGLU
+ *   y       = hid Wd^T                                            down proj.
+ *   out[t]  = sum_j w[t,j] y[row(t,j)] (+ shared(x[t]))           combine
+ *
+ * Conventions shared by every call:
+ *  - Every pointer is a DEVICE pointer the caller owns (allocated, for
+ *    example, by PyTorch); the library allocates no memory.  Every array must
+ *    start on a 16-byte boundary.
+ *  - bf16 arrays are passed as uint16_t bit patterns (IEEE binary32 top half).
+ *  - `stream` is a cudaStream_t passed as void*; every call only enqueues
+ *    work on it and returns without synchronising the host, so a sequence of
+ *    calls can be captured into a CUDA graph.  Host-side argument errors are
+ *    returned before anything is enqueued.
+ *  - `ws` is a caller-owned device workspace of at least the size returned
+ *    by moe_workspace_bytes() for the same dims; its contents on entry do not
+ *    matter.  Calls that overlap on the GPU must not share one workspace.
+ *  - Supported shapes: H, I and I_shared (when non-zero) multiples of 64 and
+ *    at most 16384; 1 <= E <= 1024; 1 <= k <= min(E, 32); 0 <= T and
+ *    T*k < 2^31.  Other shapes return MOE_ERR_UNSUPPORTED.
+ *  - Errors are never silent.  A call returns MOE_OK only after every check
+ *    it can make on the host; errors the kernels detect (for example an
+ *    expert index out of range given to moe_permute) set a status word in the
+ *    workspace that moe_read_device_status() returns.  There is no CPU
+ *    fallback: without a usable GPU every call fails with MOE_ERR_CUDA.
+ */
+#ifndef MOE_FP8_H
+#define MOE_FP8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t moe_status;
+
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG 1     /* null or misaligned pointer, bad value  */
+#define MOE_ERR_UNSUPPORTED 2     /* shape outside the supported set        */
+#define MOE_ERR_WORKSPACE 3       /* workspace smaller than required        */
+#define MOE_ERR_CUDA 4            /* a CUDA launch or runtime call failed   */
+#define MOE_ERR_DEVICE_STATUS 5   /* a kernel flagged bad input on device   */
+#define MOE_ERR_TIMEOUT 6         /* a bounded device wait gave up          */
+#define MOE_ERR_NOT_IMPLEMENTED 7
+
+/* Device status bits (moe_read_device_status). */
+#define MOE_DEV_BAD_EXPERT_INDEX 1 /* moe_permute saw idx < 0 or idx >= E   */
+#define MOE_DEV_WAIT_TIMEOUT 2     /* a kernel's bounded wait ran out       */
+
+/* Layer dimensions. T tokens, hidden size H, routed-expert intermediate I,
+ * E routed experts, top-k, shared-expert intermediate I_shared (0 = none). */
+typedef struct {
+  int32_t T, H, I, E, k, I_shared;
+} moe_dims;
+
+/* One block-FP8 weight stack: codes are E4M3 bytes, scales one float per
+ * 128x128 block.  For a stack of n matrices of shape [rows, cols] (rows =
+ * output features, cols = input features, cols contiguous):
+ *   codes  uint8 [n, rows, cols]
+ *   scales float [n, ceil(rows/128), ceil(cols/128)]                       */
+typedef struct {
+  const uint8_t* codes;
+  const float* scales;
+} moe_fp8_mat;
+
+/* The three projections of n experts: gate and up [n, I, H], down [n, H, I]. */
+typedef struct {
+  moe_fp8_mat gate, up, down;
+} moe_fp8_ffn;
+
+/* Short text for a status code (static storage). */
+const char* moe_status_string(moe_status s);
+
+/* Text of the most recent failure on the calling host thread ("" if none). */
+const char* moe_last_error_message(void);
+
+/* Library version string, e.g. "moe_fp8 0.1 sm_103a". */
+const char* moe_version(void);
+
+/* Workspace size in bytes that every call below needs for dims d. */
+moe_status moe_workspace_bytes(moe_dims d, size_t* bytes);
+
+/*
+ * Router: logits, softmax over experts, top-k with renormalisation.
+ *   x        bf16  [T, H]
+ *   Wr       float [E, H]
+ *   bias     float [E] or NULL
+ *   topk_idx int32 [T, k]  out: experts in descending probability, ties to
+ *                          the lower expert index
+ *   topk_w   float [T, k]  out: p_j / sum of the k selected p
+ * Logits are accumulated in fp32.  The renormalised weights equal the softmax
+ * over the k selected logits, which is how they are computed.
+ */
+moe_status moe_route(const uint16_t* x, const float* Wr, const float* bias,
+                     moe_dims d, int32_t* topk_idx, float* topk_w, void* ws,
+                     size_t ws_bytes, void* stream);
+
+/*
+ * Permutation of the T*k (token, slot) pairs into expert-contiguous rows.
+ *   topk_idx     int32 [T, k]   in
+ *   expert_off   int32 [E + 1]  out: segment e is rows [off[e], off[e+1]),
+ *                               off[0] = 0, off[E] = T*k
+ *   row_token    int32 [T*k]    out: token of each permuted row; inside one
+ *                               segment tokens ascend
+ *   tok_slot_row int32 [T*k]    out: row of pair (t, j) at index t*k + j
+ * The result is unique and deterministic (no atomics decide an order).  An
+ * index outside [0, E) sets MOE_DEV_BAD_EXPERT_INDEX; its pair gets no row
+ * (tok_slot_row = -1) and off[E] counts only valid pairs.
+ */
+moe_status moe_permute(const int32_t* topk_idx, moe_dims d,
+                       int32_t* expert_off, int32_t* row_token,
+                       int32_t* tok_slot_row, void* ws, size_t ws_bytes,
+                       void* stream);
+
+/*
+ * Routed experts: for every permuted row r of expert e,
+ *   y_perm[r] = (silu(x[row_token[r]] Wg_e^T) * (x[row_token[r]] Wu_e^T)) Wd_e^T
+ * with W = dec(codes) * block scale.
+ *   x          bf16  [T, H]
+ *   expert_off int32 [E + 1], row_token int32 [T*k]  (from moe_permute)
+ *   w          the E routed experts
+ *   y_perm     float [T*k, H] out (rows past off[E] are left untouched)
+ * d.T and d.k size the row space; d.I_shared is ignored.
+ */
+moe_status moe_expert_ffn_fp8(const uint16_t* x, const int32_t* expert_off,
+                              const int32_t* row_token, moe_fp8_ffn w,
+                              moe_dims d, float* y_perm, void* ws,
+                              size_t ws_bytes, void* stream);
+
+/*
+ * Combine: out[t] = sum_j topk_w[t,j] y_perm[tok_slot_row[t*k+j]]
+ *                   (+ shared_y[t] when shared_y is not NULL),
+ * summed in fp32 in slot order and rounded once to bf16 (nearest-even).
+ * Pairs with tok_slot_row < 0 contribute nothing.
+ *   y_perm float [T*k, H], tok_slot_row int32 [T*k], topk_w float [T, k],
+ *   shared_y float [T, H] or NULL, out bf16 [T, H].
+ */
+moe_status moe_combine(const float* y_perm, const int32_t* tok_slot_row,
+                       const float* topk_w, const float* shared_y, moe_dims d,
+                       uint16_t* out, void* stream);
+
+/*
+ * The whole layer: route, permute, routed experts, the shared expert when
+ * d.I_shared > 0 (applied to every token with weight 1), combine.
+ *   shared       NULL when d.I_shared == 0, else one expert (n = 1) with
+ *                gate/up [I_shared, H] and down [H, I_shared]
+ *   out          bf16 [T, H]
+ *   topk_idx_out int32 [T, k] or NULL: the routing, for inspection
+ *   topk_w_out   float [T, k] or NULL
+ * The regime (few tokens per expert: streamed grouped GEMV; many tokens per
+ * expert: tensor-core grouped GEMM) is chosen on the host from T*k/E only.
+ */
+moe_status moe_layer_forward(const uint16_t* x, const float* Wr,
+                             const float* bias, moe_fp8_ffn routed,
+                             const moe_fp8_ffn* shared, moe_dims d,
+                             uint16_t* out, int32_t* topk_idx_out,
+                             float* topk_w_out, void* ws, size_t ws_bytes,
+                             void* stream);
+
+/*
+ * Copy the workspace's device status word to *status (MOE_DEV_* bits) after
+ * synchronising `stream`.  Returns MOE_ERR_DEVICE_STATUS when any bit is set.
+ * The word is cleared at the start of moe_permute and moe_layer_forward.
+ */
+moe_status moe_read_device_status(const void* ws, int32_t* status,
+                                  void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FP8_H */

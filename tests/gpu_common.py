@@ -1,0 +1,53 @@
+"""Helpers of the GPU parity tests: the tolerance rule, cached layers, and a
+GPU fixture that fails (never skips) without a device."""
+import numpy as np
+import pytest
+
+import moe_inputs as mi
+
+# Per-element bound of the layer statement: |gpu - ref| <= 1e-2 (|ref| + rms(ref)).
+REL = 1e-2
+
+_layers = {}
+
+
+def within_tol(gpu, ref, rel=REL):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert gpu.shape == ref.shape, (gpu.shape, ref.shape)
+    if ref.size == 0:
+        return True, 0.0
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    bound = rel * (np.abs(ref) + rms)
+    err = np.abs(gpu - ref)
+    worst = float(np.max(err / np.maximum(bound, 1e-300)))
+    return bool(np.all(err <= bound)), worst
+
+
+def assert_within_tol(gpu, ref, what, rel=REL):
+    ok, worst = within_tol(gpu, ref, rel)
+    assert ok, f"{what}: worst |err|/bound = {worst:.3g}"
+    return worst
+
+
+def host_layer(name, seed=0):
+    key = (name, seed)
+    if key not in _layers:
+        _layers[key] = mi.make_layer(name, seed=seed)
+    return _layers[key]
+
+
+def require_gpu():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA GPU is required for tests marked gpu")
+    from block_fp8_expert_gb300 import build
+    build.build()
+    return torch
+
+
+def bf16_bits(t):
+    """bf16 device tensor -> uint16 numpy bits."""
+    import torch
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
