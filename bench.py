@@ -1,0 +1,485 @@
+"""Benchmark of the block-FP8 MoE FFN layer on GB300.
+
+One step = one full layer forward (router, softmax/top-k, permutation,
+gate/up + SwiGLU, down projection, combine) over one batch of synthetic tokens,
+replayed from a CUDA graph.  The headline workload is the Qwen3-MoE-shaped
+decode layer (hidden 2048, expert intermediate 768, 128 experts, top-8,
+block-FP8 E4M3 weights with 128x128 fp32 scales) at a batch of 64 tokens.
+
+Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the
+launching stream; L2 is flushed (a 512 MiB write) before every timed step,
+outside the events.  Max over ranks; under torchrun each rank runs its own
+replica of the layer on its own tokens (weak scaling, no collective in the
+data path).
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+on a bounded token sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_inputs as mi  # noqa: E402
+
+HEADLINE = ("qwen3moe_decode", 64)
+METRIC = "MoE-layer tokens/s at decode & prefill; HBM GB/s or TC util vs GB300 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["_source"] = "measured"
+        return d
+    d = dict(FALLBACK_PEAKS)
+    d["_source"] = "fallback"
+    return d
+
+
+def expert_bytes(H, I):
+    """Codes + scales of one expert's gate, up and down matrices."""
+    nb = lambda n: -(-n // 128)
+    return 3 * H * I + 4 * (2 * nb(I) * nb(H) + nb(H) * nb(I))
+
+
+def algorithmic(w: mi.Workload, T: int, D: int):
+    """Bytes and FLOPs the layer must move/compute for one call: router
+    weights, the D distinct experts hit (plus the shared expert), the tokens in
+    and the output out; FLOPs of the router and of every (token, expert) pair."""
+    B = w.E * w.H * 4 + D * expert_bytes(w.H, w.I) + 2 * T * w.H * 2
+    F = T * w.k * 6 * w.H * w.I + 2 * T * w.H * w.E
+    if w.I_shared:
+        B += expert_bytes(w.H, w.I_shared)
+        F += T * 6 * w.H * w.I_shared
+    expert_B = D * expert_bytes(w.H, w.I) + T * w.H * 2
+    if w.I_shared:
+        expert_B += expert_bytes(w.H, w.I_shared)
+    return B, F, expert_B
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def file_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def kernel_traffic(kernel_key: str, src_files):
+    """DRAM bytes per launch from the committed ncu summary, only while the
+    kernel sources still hash to the value the counters were taken at."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        table = json.load(f)
+    ent = table.get(kernel_key)
+    if not ent or ent.get("src_hash") != file_hash(src_files):
+        return None
+    return ent.get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle arm
+# ---------------------------------------------------------------------------
+
+def oracle_rate(layer, x_bits, reps=1):
+    import oracle
+    t = time.perf_counter()
+    for _ in range(reps):
+        oracle.moe_layer(x_bits, layer, keep_intermediates=False)
+    dt = (time.perf_counter() - t) / reps
+    return x_bits.shape[0] / dt, dt
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    name, T = HEADLINE
+    w = mi.WORKLOADS[name]
+    layer = mi.make_layer(name, seed=0)
+    x_bits, _ = mi.make_tokens(layer, T, seed=0)
+    sample = 16
+    xs = x_bits[:sample]
+    for _ in range(args.warmup):
+        oracle_rate(layer, xs)
+    times = []
+    for _ in range(args.steps):
+        times.append(oracle_rate(layer, xs)[1])
+    dt = sum(times) / len(times)
+    val = sample / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{name}_T{T}", "H": w.H, "I": w.I, "E": w.E, "k": w.k,
+                   "T": T, "sample_tokens_per_step": sample},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+                         "sample": f"{sample} of the {T} tokens per step, fp64 NumPy oracle"},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+class LayerRun:
+    """A captured layer forward for one (layer, T) with static buffers."""
+
+    def __init__(self, torch, D, x_bits, graph=True):
+        from block_fp8_expert_gb300.device import x_to_device
+        self.torch = torch
+        self.D = D
+        self.T = x_bits.shape[0]
+        self.x = x_to_device(x_bits)
+        self.out = torch.empty((self.T, D.H), dtype=torch.bfloat16, device="cuda")
+        self.idx = torch.empty((self.T, D.k), dtype=torch.int32, device="cuda")
+        self.w = torch.empty((self.T, D.k), dtype=torch.float32, device="cuda")
+        self.ws = D.workspace(self.T)
+        self.graph = None
+        self.fwd()
+        torch.cuda.synchronize()
+        if graph:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                self.fwd()
+            torch.cuda.current_stream().wait_stream(s)
+            torch.cuda.synchronize()
+            self.graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph):
+                self.fwd()
+            torch.cuda.synchronize()
+
+    def fwd(self):
+        self.D.forward(self.x, out=self.out, ws=self.ws, topk_idx=self.idx, topk_w=self.w)
+
+    def step(self):
+        if self.graph is not None:
+            self.graph.replay()
+        else:
+            self.fwd()
+
+    def distinct_experts(self):
+        return int(np.unique(self.idx.cpu().numpy()).size)
+
+
+def time_steps(torch, fn, steps, warmup, flush):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b) * 1e-3)
+    return times
+
+
+def phase_times(torch, D, run, steps, flush):
+    """Per ABI call timing of one forward, split into route / permute /
+    experts / combine (each call timed with events on the same stream)."""
+    import block_fp8_expert_gb300 as m
+    T = run.T
+    d = D.dims(T)
+    P = T * D.k
+    dev = "cuda"
+    idx = torch.empty((T, D.k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, D.k), dtype=torch.float32, device=dev)
+    off = torch.empty(D.E + 1, dtype=torch.int32, device=dev)
+    rt = torch.empty(P, dtype=torch.int32, device=dev)
+    tsr = torch.empty(P, dtype=torch.int32, device=dev)
+    y = torch.empty((P, D.H), dtype=torch.float32, device=dev)
+    sy = None
+    out = torch.empty((T, D.H), dtype=torch.bfloat16, device=dev)
+    ws = run.ws
+    calls = {
+        "route": lambda: m.moe_route(run.x, D.Wr, D.bias, d, idx, w, ws),
+        "permute": lambda: m.moe_permute(idx, d, off, rt, tsr, ws),
+        "experts": lambda: m.moe_expert_ffn_fp8(run.x, off, rt, D.routed.abi(), d, y, ws),
+        "combine": lambda: m.moe_combine(y, tsr, w, sy, d, out),
+    }
+    res = {k: [] for k in calls}
+    for it in range(steps + 2):
+        flush()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+        ev[0].record()
+        for i, f in enumerate(calls.values()):
+            f()
+            ev[i + 1].record()
+        ev[-1].synchronize()
+        if it >= 2:
+            for i, k in enumerate(calls):
+                res[k].append(ev[i].elapsed_time(ev[i + 1]) * 1e-3)
+    return {k: sum(v) / len(v) for k, v in res.items()}
+
+
+def measure_workload(torch, name, T, steps, warmup, flush, pk, dev_cache, seed=0):
+    from block_fp8_expert_gb300.device import DeviceLayer
+    w = mi.WORKLOADS[name]
+    key = (w.H, w.I, w.E, w.k, w.I_shared, w.zipf_s)
+    if key not in dev_cache:
+        dev_cache.clear()
+        torch.cuda.empty_cache()
+        host = mi.make_layer(w, seed=seed)
+        dev_cache[key] = (host, DeviceLayer.from_host(host))
+    host, D = dev_cache[key]
+    x_bits, _ = mi.make_tokens(host, T, seed=seed)
+    run = LayerRun(torch, D, x_bits)
+    times = time_steps(torch, run.step, steps, warmup, flush)
+    t = sum(times) / len(times)
+    Dn = run.distinct_experts()
+    B, F, _ = algorithmic(w, T, Dn)
+    t_hbm = B / (pk["hbm_gbs"] * 1e9)
+    t_tc = F / (pk["bf16_tflops"] * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    res = {"workload": f"{name}_T{T}", "T": T, "ms": t * 1e3, "tokens_per_s": T / t,
+           "distinct_experts": Dn, "bytes": B, "flops": F,
+           "hbm_gbs": B / t / 1e9, "tflops": F / t / 1e12, "bound": bound,
+           "roofline_frac": max(t_hbm, t_tc) / t}
+    return res, run, D, host
+
+
+def run_gpu(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    from block_fp8_expert_gb300 import build
+    build.build()
+    import block_fp8_expert_gb300 as m
+    m.lib()
+    pk = peaks()
+    flush_buf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    flush = lambda: flush_buf.fill_(1)
+
+    name, T = HEADLINE
+    w = mi.WORKLOADS[name]
+    dev_cache = {}
+    # headline: graph replay, K timed steps
+    from block_fp8_expert_gb300.device import DeviceLayer
+    host = mi.make_layer(name, seed=rank)
+    D = DeviceLayer.from_host(host)
+    dev_cache[(w.H, w.I, w.E, w.k, w.I_shared, w.zipf_s)] = (host, D)
+    x_bits, _ = mi.make_tokens(host, T, seed=rank)
+    run = LayerRun(torch, D, x_bits)
+    for _ in range(args.warmup):
+        run.step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        times = time_steps(torch, run.step, args.steps, 0, flush)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t_rank = sum(times)
+    if dist:
+        tt = torch.tensor([t_rank], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_all = float(tt.item())
+    else:
+        t_all = t_rank
+    ms_per_step = t_all / args.steps * 1e3
+    value = world * T * args.steps / t_all
+    Dn = run.distinct_experts()
+    B, F, expert_B = algorithmic(w, T, Dn)
+
+    # phase table and the dominant unit's roofline
+    ph = phase_times(torch, D, run, max(5, min(args.steps, 20)), flush)
+    dom = max(ph, key=ph.get)
+    src = [os.path.join(ROOT, "block_fp8_expert_gb300", "csrc", "expert_gemv.cu"),
+           os.path.join(ROOT, "block_fp8_expert_gb300", "csrc", "moe_common.cuh")]
+    achieved = expert_B / ph["experts"] / 1e9
+    roof = {"bound": "hbm", "unit": "GB/s", "kernel": "expert FFN call: gate/up+SwiGLU GEMV "
+            "and down GEMV (moe_expert_ffn_fp8)", "achieved": achieved,
+            "peak": pk["hbm_gbs"], "peak_source": pk["_source"] + " hbm_gbs",
+            "frac": achieved / pk["hbm_gbs"],
+            "algorithmic_bytes_per_launch": expert_B,
+            "avg_duration_us": ph["experts"] * 1e6,
+            "traffic": kernel_traffic("expert_ffn_decode_T64", src)}
+
+    # e2e: host buffers, copies inside the timed region
+    x_host = torch.from_numpy(x_bits.view(np.int16)).pin_memory()
+    out_host = torch.empty((T, w.H), dtype=torch.int16).pin_memory()
+
+    def e2e_step():
+        run.x.view(torch.int16).copy_(x_host, non_blocking=True)
+        run.step()
+        out_host.copy_(run.out.view(torch.int16), non_blocking=True)
+
+    e2e_times = time_steps(torch, e2e_step, args.steps, 2, flush)
+    e2e_t = sum(e2e_times) / len(e2e_times)
+
+    # launches of this library's kernels per layer call (route 2, permute 3,
+    # expert GEMVs 2, combine 1); the memset of the status word is not a kernel
+    launches_per_step = 8 + (3 if w.I_shared else 0)
+
+    sweep = []
+    if not args.no_sweep and rank == 0:
+        plan = [("qwen3moe_decode", 1), ("qwen3moe_decode", 8), ("qwen3moe_decode", 64),
+                ("qwen3moe_prefill", 4096), ("skewed", 1), ("skewed", 16), ("skewed", 256),
+                ("skewed", 2048), ("skewed", 16384), ("large_sparse", 1), ("large_sparse", 256),
+                ("tiny", 8)]
+        for nm, tt_ in plan:
+            try:
+                r, *_ = measure_workload(torch, nm, tt_, args.sweep_steps, 2, flush, pk, dev_cache)
+                sweep.append(r)
+            except Exception as ex:  # report, do not hide
+                sweep.append({"workload": f"{nm}_T{tt_}", "error": repr(ex)[:200]})
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        os.environ.setdefault("OPENBLAS_NUM_THREADS", str(cores()))
+        rate, dt = oracle_rate(host, x_bits)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+               "sample": f"one full {name} layer call on all {T} tokens ({dt:.1f} s), "
+                         "fp64 NumPy oracle"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{name}_T{T}", "H": w.H, "I": w.I, "E": w.E, "k": w.k,
+                       "T": T, "weights": "E4M3 codes + fp32 scale per 128x128 block",
+                       "distinct_experts": Dn, "l2": "flushed before every timed step "
+                       "(512 MiB write)", "graph": "CUDA graph replay per step",
+                       "parallelism": f"replicas{world}"},
+            "layer_roofline": {"bytes": B, "flops": F, "achieved_gbs": B / (t_all / args.steps) / 1e9,
+                               "frac_hbm": B / (t_all / args.steps) / 1e9 / pk["hbm_gbs"]},
+            "roofline": roof,
+            "phases_us": {k: v * 1e6 for k, v in ph.items()},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * T / e2e_t, "unit": "tokens/s",
+                    "h2d_bytes_per_step": T * w.H * 2, "d2h_bytes_per_step": T * w.H * 2},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(),
+            "sweep": sweep,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--sweep-steps", type=int, default=10)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

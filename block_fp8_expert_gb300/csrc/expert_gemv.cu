@@ -25,13 +25,20 @@ namespace moe {
 
 constexpr int kGemvWarps = 8;
 
-// One 64-column chunk: 16 weight rows (g, g+8) x NT*8 tokens.
-template <int NT>
+// One 64-column chunk: 16 weight rows (g, g+8) x NT*8 tokens.  F16: weights
+// decoded exactly to fp16 and activations in fp16; otherwise weights decoded
+// to bf16 * 2^-112 and activations in bf16.
+template <int NT, bool F16>
 __device__ __forceinline__ void chunk_mma(const uint4& w_lo, const uint4& w_hi,
                                           const uint4 (&xa)[NT][2], float (&part)[NT][4]) {
   uint32_t wl[8], wh[8];
-  decode16_scaled(w_lo, wl);
-  decode16_scaled(w_hi, wh);
+  if (F16) {
+    decode16_f16(w_lo, wl);
+    decode16_f16(w_hi, wh);
+  } else {
+    decode16_scaled(w_lo, wl);
+    decode16_scaled(w_hi, wh);
+  }
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const uint32_t xr[8] = {xa[nt][0].x, xa[nt][0].y, xa[nt][0].z, xa[nt][0].w,
@@ -40,14 +47,17 @@ __device__ __forceinline__ void chunk_mma(const uint4& w_lo, const uint4& w_hi,
     for (int s = 0; s < 4; ++s) {
       const uint32_t a[4] = {wl[2 * s], wh[2 * s], wl[2 * s + 1], wh[2 * s + 1]};
       const uint32_t b[2] = {xr[2 * s], xr[2 * s + 1]};
-      mma_bf16_16x8x16(part[nt], a, b);
+      if (F16)
+        mma_f16_16x8x16(part[nt], a, b);
+      else
+        mma_bf16_16x8x16(part[nt], a, b);
     }
   }
 }
 
 // ---------------------------------------------------------------------------
 // gate/up + SwiGLU.  grid (I/16, max active experts), 8 warps split K = H.
-// hid[r, i] = silu(g) * u in bf16 for every row r of the expert.
+// hid[r, i] = silu(g) * u in fp16 for every row r of the expert.
 // ---------------------------------------------------------------------------
 template <int NT>
 __global__ void __launch_bounds__(kGemvWarps * 32)
@@ -56,7 +66,7 @@ k_gateup_gemv(const uint16_t* __restrict__ x, int H, int I,
               const int32_t* __restrict__ active,
               const uint8_t* __restrict__ gcodes, const float* __restrict__ gscales,
               const uint8_t* __restrict__ ucodes, const float* __restrict__ uscales,
-              uint16_t* __restrict__ hid) {
+              uint16_t* __restrict__ hid, int32_t* __restrict__ status) {
   __shared__ float red[kGemvWarps][NT][2][4][32];
   __shared__ int tok[NT * 8];
   const int a = blockIdx.y;
@@ -111,8 +121,8 @@ k_gateup_gemv(const uint16_t* __restrict__ x, int H, int I,
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int q = 0; q < 4; ++q) pg[nt][q] = pu[nt][q] = 0.f;
-      chunk_mma<NT>(g_lo, g_hi, xa, pg);
-      chunk_mma<NT>(u_lo, u_hi, xa, pu);
+      chunk_mma<NT, false>(g_lo, g_hi, xa, pg);
+      chunk_mma<NT, false>(u_lo, u_hi, xa, pu);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -142,8 +152,8 @@ k_gateup_gemv(const uint16_t* __restrict__ x, int H, int I,
       const int n = n0 + nt * 8 + 2 * (L & 3) + (q & 1);
       if (n < ne) {
         const float hv = gv / (1.f + expf(-gv)) * uv;
-        const uint32_t b = pack_bf16x2(hv, 0.f);
-        hid[(size_t)(r0 + n) * I + i0 + row] = static_cast<uint16_t>(b & 0xFFFFu);
+        if (!(fabsf(hv) <= kF16Max)) raise_status(status, MOE_DEV_FP16_RANGE);
+        hid[(size_t)(r0 + n) * I + i0 + row] = f32_to_f16_bits(hv);
       }
     }
     __syncthreads();
@@ -153,7 +163,8 @@ k_gateup_gemv(const uint16_t* __restrict__ x, int H, int I,
 // ---------------------------------------------------------------------------
 // down projection.  grid (H/128, max active experts); warp w owns output rows
 // [h0 + 16w, h0 + 16w + 16) over the whole K = I.
-// y[r, h] = sum_i hid[r, i] Wd[h, i] in fp32 for every row r of the expert.
+// y[r, h] = sum_i hid[r, i] Wd[h, i] in fp32 for every row r of the expert;
+// hid (fp16) times the exactly decoded fp16 weights, block scale in fp32.
 // ---------------------------------------------------------------------------
 template <int NT>
 __global__ void __launch_bounds__(kGemvWarps * 32)
@@ -200,13 +211,13 @@ k_down_gemv(const uint16_t* __restrict__ hid, int H, int I,
           xa[nt][0] = xa[nt][1] = make_uint4(0, 0, 0, 0);
         }
       }
-      const float sd = ds[k0 / kScaleBlock] * kPow2_112;
+      const float sd = ds[k0 / kScaleBlock];
       float p[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int q = 0; q < 4; ++q) p[nt][q] = 0.f;
-      chunk_mma<NT>(w_lo, w_hi, xa, p);
+      chunk_mma<NT, true>(w_lo, w_hi, xa, p);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -227,18 +238,18 @@ k_down_gemv(const uint16_t* __restrict__ hid, int H, int I,
 cudaError_t launch_expert_gemv(const uint16_t* x, const int32_t* expert_off,
                                const int32_t* row_token, const int32_t* active, int max_active,
                                const moe_fp8_ffn& w, int H, int I, int max_rows_per_expert,
-                               uint16_t* hid, float* y, cudaStream_t s) {
+                               uint16_t* hid, float* y, int32_t* status, cudaStream_t s) {
   if (max_active <= 0) return cudaSuccess;
   const dim3 block(kGemvWarps * 32);
   const dim3 g1(I / 16, max_active), g2(cdiv(H, 128), max_active);
   if (max_rows_per_expert <= 8) {
     k_gateup_gemv<1><<<g1, block, 0, s>>>(x, H, I, expert_off, row_token, active, w.gate.codes,
-                                          w.gate.scales, w.up.codes, w.up.scales, hid);
+                                          w.gate.scales, w.up.codes, w.up.scales, hid, status);
     k_down_gemv<1><<<g2, block, 0, s>>>(hid, H, I, expert_off, active, w.down.codes,
                                         w.down.scales, y);
   } else {
     k_gateup_gemv<2><<<g1, block, 0, s>>>(x, H, I, expert_off, row_token, active, w.gate.codes,
-                                          w.gate.scales, w.up.codes, w.up.scales, hid);
+                                          w.gate.scales, w.up.codes, w.up.scales, hid, status);
     k_down_gemv<2><<<g2, block, 0, s>>>(hid, H, I, expert_off, active, w.down.codes,
                                         w.down.scales, y);
   }

@@ -191,7 +191,7 @@ moe_status moe_route(const uint16_t* x, const float* Wr, const float* bias, moe_
   if ((s = check_ws(d, ws, ws_bytes)) != MOE_OK) return s;
   const WsLayout L = ws_layout(d);
   CUDA_CHECK(launch_route(x, Wr, bias, d.T, d.H, d.E, d.k, at<float>(ws, L.logits), topk_idx,
-                          topk_w, (cudaStream_t)stream),
+                          topk_w, at<int32_t>(ws, L.status), (cudaStream_t)stream),
              "moe_route");
   return MOE_OK;
 }
@@ -232,10 +232,12 @@ moe_status moe_expert_ffn_fp8(const uint16_t* x, const int32_t* expert_off,
   const WsLayout L = ws_layout(d);
   cudaStream_t st = (cudaStream_t)stream;
   int32_t* active = at<int32_t>(ws, L.active);
-  CUDA_CHECK(launch_active_from_offsets(expert_off, d.E, active, st), "moe_expert_ffn_fp8");
+  int32_t* status = at<int32_t>(ws, L.status);
+  CUDA_CHECK(launch_active_from_offsets(expert_off, d.E, active, status, st),
+             "moe_expert_ffn_fp8");
   const int P = d.T * d.k;
   CUDA_CHECK(launch_expert_gemv(x, expert_off, row_token, active, d.E < P ? d.E : P, w, d.H, d.I,
-                                d.T, at<uint16_t>(ws, L.hid), y_perm, st),
+                                d.T, at<uint16_t>(ws, L.hid), y_perm, status, st),
              "moe_expert_ffn_fp8");
   return MOE_OK;
 }
@@ -287,16 +289,16 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
   int32_t* active = at<int32_t>(ws, L.active);
   float* y_perm = at<float>(ws, L.y_perm);
 
-  CUDA_CHECK(cudaMemsetAsync(at<int32_t>(ws, L.status), 0, sizeof(int32_t), st),
-             "moe_layer_forward");
-  CUDA_CHECK(launch_route(x, Wr, bias, d.T, d.H, d.E, d.k, at<float>(ws, L.logits), idx, w, st),
+  int32_t* status = at<int32_t>(ws, L.status);
+  CUDA_CHECK(launch_route(x, Wr, bias, d.T, d.H, d.E, d.k, at<float>(ws, L.logits), idx, w,
+                          status, st),
              "moe_layer_forward: route");
   CUDA_CHECK(launch_permute(idx, d.T, d.E, d.k, at<int32_t>(ws, L.rank),
                             at<int32_t>(ws, L.block_cnt), at<int32_t>(ws, L.block_base), off,
-                            row_token, tok_slot_row, active, at<int32_t>(ws, L.status), st),
+                            row_token, tok_slot_row, active, status, st),
              "moe_layer_forward: permute");
   CUDA_CHECK(launch_expert_gemv(x, off, row_token, active, d.E < P ? d.E : P, routed, d.H, d.I,
-                                d.T, at<uint16_t>(ws, L.hid), y_perm, st),
+                                d.T, at<uint16_t>(ws, L.hid), y_perm, status, st),
              "moe_layer_forward: experts");
   float* shared_y = nullptr;
   if (d.I_shared > 0) {
@@ -306,7 +308,7 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
     shared_y = at<float>(ws, L.sh_y);
     CUDA_CHECK(launch_identity_perm(d.T, soff, srows, sact, st), "moe_layer_forward: shared");
     CUDA_CHECK(launch_expert_gemv(x, soff, srows, sact, 1, *shared, d.H, d.I_shared, d.T,
-                                  at<uint16_t>(ws, L.sh_hid), shared_y, st),
+                                  at<uint16_t>(ws, L.sh_hid), shared_y, status, st),
                "moe_layer_forward: shared expert");
   }
   CUDA_CHECK(launch_combine(y_perm, tok_slot_row, w, shared_y, d.T, d.H, d.k, out, st),

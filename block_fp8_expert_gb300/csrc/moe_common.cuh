@@ -62,6 +62,25 @@ __device__ __forceinline__ void decode16_scaled(const uint4& c, uint32_t (&out)[
   }
 }
 
+// 16 E4M3 codes -> 8 f16x2 registers holding dec(code) exactly.
+__device__ __forceinline__ void decode16_f16(const uint4& c, uint32_t (&out)[8]) {
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    out[2 * q + 0] = e4m3x2_to_f16x2(w[q] & 0xFFFFu);
+    out[2 * q + 1] = e4m3x2_to_f16x2(w[q] >> 16);
+  }
+}
+
+// float -> fp16 bits, round to nearest even (saturates to inf beyond 65504).
+__device__ __forceinline__ uint16_t f32_to_f16_bits(float v) {
+  unsigned short r;
+  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(r) : "f"(v));
+  return r;
+}
+
+constexpr float kF16Max = 65504.f;
+
 // ---------------------------------------------------------------------------
 // Warp-level bf16 tensor-core MMA: D(16x8 f32) += A(16x16 bf16) B(16x8 bf16)
 // ---------------------------------------------------------------------------
@@ -69,6 +88,16 @@ __device__ __forceinline__ void mma_bf16_16x8x16(float (&d)[4], const uint32_t (
                                                  const uint32_t (&b)[2]) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// Same shape with fp16 operands.
+__device__ __forceinline__ void mma_f16_16x8x16(float (&d)[4], const uint32_t (&a)[4],
+                                                const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));

@@ -19,7 +19,7 @@ WsLayout ws_layout(const moe_dims& d);
 
 cudaError_t launch_route(const uint16_t* x, const float* Wr, const float* bias, int T, int H,
                          int E, int k, float* logits, int32_t* topk_idx, float* topk_w,
-                         cudaStream_t s);
+                         int32_t* status, cudaStream_t s);
 
 cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, int32_t* rank,
                            int32_t* block_cnt, int32_t* block_base, int32_t* expert_off,
@@ -27,14 +27,14 @@ cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, int32_t
                            int32_t* status, cudaStream_t s);
 
 cudaError_t launch_active_from_offsets(const int32_t* expert_off, int E, int32_t* active,
-                                       cudaStream_t s);
+                                       int32_t* status, cudaStream_t s);
 
 // Grouped GEMV over the experts listed in `active` (count, then ids).
 // max_active bounds the list length; max_rows_per_expert bounds any segment.
 cudaError_t launch_expert_gemv(const uint16_t* x, const int32_t* expert_off,
                                const int32_t* row_token, const int32_t* active, int max_active,
                                const moe_fp8_ffn& w, int H, int I, int max_rows_per_expert,
-                               uint16_t* hid, float* y, cudaStream_t s);
+                               uint16_t* hid, float* y, int32_t* status, cudaStream_t s);
 
 cudaError_t launch_combine(const float* y_perm, const int32_t* tok_slot_row, const float* topk_w,
                            const float* shared_y, int T, int H, int k, uint16_t* out,

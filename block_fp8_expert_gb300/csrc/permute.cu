@@ -146,9 +146,10 @@ k_perm_scatter(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__
 // did not run the permutation here).  One CTA; E <= 1024.
 __global__ void __launch_bounds__(1024)
 k_active_from_offsets(const int32_t* __restrict__ expert_off, int E,
-                      int32_t* __restrict__ active) {
+                      int32_t* __restrict__ active, int32_t* __restrict__ status) {
   __shared__ int32_t warp_act[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0 && status) *status = 0;  // first kernel of an expert-FFN call
   const int ne = (tid < E && expert_off[tid + 1] > expert_off[tid]) ? 1 : 0;
   int act = ne;
 #pragma unroll
@@ -191,8 +192,8 @@ cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, int32_t
 }
 
 cudaError_t launch_active_from_offsets(const int32_t* expert_off, int E, int32_t* active,
-                                       cudaStream_t s) {
-  k_active_from_offsets<<<1, 1024, 0, s>>>(expert_off, E, active);
+                                       int32_t* status, cudaStream_t s) {
+  k_active_from_offsets<<<1, 1024, 0, s>>>(expert_off, E, active, status);
   return cudaGetLastError();
 }
 

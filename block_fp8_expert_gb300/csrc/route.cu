@@ -16,8 +16,11 @@ constexpr int kRouteWarps = 4;  // experts per CTA
 __global__ void __launch_bounds__(kRouteWarps * 32)
 k_router_logits(const uint16_t* __restrict__ x, const float* __restrict__ Wr,
                 const float* __restrict__ bias, int T, int H, int E,
-                float* __restrict__ logits) {
+                float* __restrict__ logits, int32_t* __restrict__ status) {
   const int lane = threadIdx.x & 31;
+  // The router runs first in a layer call: it clears the status word that
+  // later kernels of the call may raise.
+  if (status && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *status = 0;
   const int e = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
   const int t0 = blockIdx.y * kRouteTok;
   if (e >= E) return;
@@ -116,10 +119,10 @@ k_router_topk(const float* __restrict__ logits, int T, int E, int k,
 
 cudaError_t launch_route(const uint16_t* x, const float* Wr, const float* bias, int T, int H,
                          int E, int k, float* logits, int32_t* topk_idx, float* topk_w,
-                         cudaStream_t s) {
+                         int32_t* status, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   dim3 g1(cdiv(E, kRouteWarps), cdiv(T, kRouteTok));
-  k_router_logits<<<g1, kRouteWarps * 32, 0, s>>>(x, Wr, bias, T, H, E, logits);
+  k_router_logits<<<g1, kRouteWarps * 32, 0, s>>>(x, Wr, bias, T, H, E, logits, status);
   const int g2 = cdiv(T, 8);
   const int epl = cdiv(E, 32);
   if (epl <= 1)

@@ -62,6 +62,7 @@ typedef int32_t moe_status;
 /* Device status bits (moe_read_device_status). */
 #define MOE_DEV_BAD_EXPERT_INDEX 1 /* moe_permute saw idx < 0 or idx >= E   */
 #define MOE_DEV_WAIT_TIMEOUT 2     /* a kernel's bounded wait ran out       */
+#define MOE_DEV_FP16_RANGE 4       /* an intermediate exceeded fp16 range   */
 
 /* Layer dimensions. T tokens, hidden size H, routed-expert intermediate I,
  * E routed experts, top-k, shared-expert intermediate I_shared (0 = none). */
@@ -105,7 +106,8 @@ moe_status moe_workspace_bytes(moe_dims d, size_t* bytes);
  *                          the lower expert index
  *   topk_w   float [T, k]  out: p_j / sum of the k selected p
  * Logits are accumulated in fp32.  The renormalised weights equal the softmax
- * over the k selected logits, which is how they are computed.
+ * over the k selected logits, which is how they are computed.  Clears the
+ * workspace's device status word.
  */
 moe_status moe_route(const uint16_t* x, const float* Wr, const float* bias,
                      moe_dims d, int32_t* topk_idx, float* topk_w, void* ws,
@@ -137,6 +139,10 @@ moe_status moe_permute(const int32_t* topk_idx, moe_dims d,
  *   w          the E routed experts
  *   y_perm     float [T*k, H] out (rows past off[E] are left untouched)
  * d.T and d.k size the row space; d.I_shared is ignored.
+ * Precision: gate/up products are exact (bf16 activations times decoded
+ * E4M3 weights, fp32 accumulation, block scale applied in fp32); the SwiGLU
+ * output hid is rounded to fp16 for the down projection.  |hid| above 65504
+ * sets MOE_DEV_FP16_RANGE.  Clears the device status word first.
  */
 moe_status moe_expert_ffn_fp8(const uint16_t* x, const int32_t* expert_off,
                               const int32_t* row_token, moe_fp8_ffn w,
@@ -176,7 +182,8 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr,
 /*
  * Copy the workspace's device status word to *status (MOE_DEV_* bits) after
  * synchronising `stream`.  Returns MOE_ERR_DEVICE_STATUS when any bit is set.
- * The word is cleared at the start of moe_permute and moe_layer_forward.
+ * The word is cleared at the start of moe_route, moe_permute,
+ * moe_expert_ffn_fp8 and moe_layer_forward.
  */
 moe_status moe_read_device_status(const void* ws, int32_t* status,
                                   void* stream);

@@ -259,3 +259,24 @@ def test_identity_expert_closed_form(torch):
     expect = c ** 3 * x ** 2 / (1 + np.exp(-c * x))
     assert idx.cpu().numpy().ravel().tolist() == [0] * 5
     assert_within_tol(oracle.bf16_to_f64(bf16_bits(out)), expect, "identity expert")
+
+
+def test_fp16_range_is_flagged(torch):
+    """A SwiGLU output beyond fp16 range raises MOE_DEV_FP16_RANGE instead of
+    passing silently."""
+    import block_fp8_expert_gb300 as m
+    from block_fp8_expert_gb300.device import DeviceLayer
+    L = mi.make_layer("tiny", seed=6)
+    L.gate.scales[:] = 300.0
+    L.up.scales[:] = 300.0
+    D = DeviceLayer.from_host(L)
+    xb, _ = mi.make_tokens(L, 4, seed=6)
+    ws = D.workspace(4)
+    D.forward(_x(torch, xb), ws=ws)
+    with pytest.raises(m.MoeError) as ei:
+        m.moe_read_device_status(ws)
+    assert "0x4" in str(ei.value)
+    # the next normal call clears the word
+    D2 = dev_layer("tiny")
+    D2.forward(_x(torch, xb), ws=ws)
+    assert m.moe_read_device_status(ws) == 0
