@@ -183,6 +183,7 @@ moe_status moe_route(const uint16_t* x, const float* Wr, const float* bias, moe_
                      void* stream) {
   moe_status s;
   if ((s = check_dims(d)) != MOE_OK) return s;
+  if (d.T == 0) return MOE_OK;  // no token: nothing is read or written
   REQUIRE_PTR(x);
   REQUIRE_PTR(Wr);
   REQUIRE_OPT_PTR(bias);
@@ -201,10 +202,12 @@ moe_status moe_permute(const int32_t* topk_idx, moe_dims d, int32_t* expert_off,
                        void* stream) {
   moe_status s;
   if ((s = check_dims(d)) != MOE_OK) return s;
-  REQUIRE_PTR(topk_idx);
   REQUIRE_PTR(expert_off);
-  REQUIRE_PTR(row_token);
-  REQUIRE_PTR(tok_slot_row);
+  if (d.T > 0) {  // with no token only the offsets (all zero) are written
+    REQUIRE_PTR(topk_idx);
+    REQUIRE_PTR(row_token);
+    REQUIRE_PTR(tok_slot_row);
+  }
   if ((s = check_ws(d, ws, ws_bytes)) != MOE_OK) return s;
   const WsLayout L = ws_layout(d);
   cudaStream_t st = (cudaStream_t)stream;
@@ -222,13 +225,13 @@ moe_status moe_expert_ffn_fp8(const uint16_t* x, const int32_t* expert_off,
                               float* y_perm, void* ws, size_t ws_bytes, void* stream) {
   moe_status s;
   if ((s = check_dims(d)) != MOE_OK) return s;
+  if (d.T == 0) return MOE_OK;  // no token: nothing is read or written
   REQUIRE_PTR(x);
   REQUIRE_PTR(expert_off);
   REQUIRE_PTR(row_token);
   REQUIRE_PTR(y_perm);
   if ((s = check_ffn(w, "w")) != MOE_OK) return s;
   if ((s = check_ws(d, ws, ws_bytes)) != MOE_OK) return s;
-  if (d.T == 0) return MOE_OK;
   const WsLayout L = ws_layout(d);
   cudaStream_t st = (cudaStream_t)stream;
   int32_t* active = at<int32_t>(ws, L.active);
@@ -246,6 +249,7 @@ moe_status moe_combine(const float* y_perm, const int32_t* tok_slot_row, const f
                        const float* shared_y, moe_dims d, uint16_t* out, void* stream) {
   moe_status s;
   if ((s = check_dims(d)) != MOE_OK) return s;
+  if (d.T == 0) return MOE_OK;  // no token: nothing is read or written
   REQUIRE_PTR(y_perm);
   REQUIRE_PTR(tok_slot_row);
   REQUIRE_PTR(topk_w);
@@ -263,6 +267,7 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
                              size_t ws_bytes, void* stream) {
   moe_status s;
   if ((s = check_dims(d)) != MOE_OK) return s;
+  if (d.T == 0) return MOE_OK;  // no token: nothing is read or written
   REQUIRE_PTR(x);
   REQUIRE_PTR(Wr);
   REQUIRE_OPT_PTR(bias);
@@ -277,7 +282,6 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
     return fail(MOE_ERR_INVALID_ARG, "shared given but I_shared == 0");
   }
   if ((s = check_ws(d, ws, ws_bytes)) != MOE_OK) return s;
-  if (d.T == 0) return MOE_OK;
   const WsLayout L = ws_layout(d);
   cudaStream_t st = (cudaStream_t)stream;
   const int P = d.T * d.k;

@@ -29,6 +29,9 @@
  *  - `ws` is a caller-owned device workspace of at least the size returned
  *    by moe_workspace_bytes() for the same dims; its contents on entry do not
  *    matter.  Calls that overlap on the GPU must not share one workspace.
+ *  - T = 0 is valid: the call checks its dims and returns MOE_OK without
+ *    touching any array (moe_permute still writes the E+1 zero offsets), so
+ *    token-sized pointers may then be NULL.
  *  - Supported shapes: H, I and I_shared (when non-zero) multiples of 64 and
  *    at most 16384; 1 <= E <= 1024; 1 <= k <= min(E, 32); 0 <= T and
  *    T*k < 2^31.  Other shapes return MOE_ERR_UNSUPPORTED.
