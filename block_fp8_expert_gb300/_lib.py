@@ -65,6 +65,7 @@ _SIGNATURES = {
     "moe_layer_forward": (_st, [_vp, _vp, _vp, Fp8Ffn, ctypes.POINTER(Fp8Ffn), Dims, _vp, _vp,
                                 _vp, _vp, _sz, _vp]),
     "moe_read_device_status": (_st, [_vp, ctypes.POINTER(ctypes.c_int32), _vp]),
+    "moe_permute_static_scratch": (_st, [_vp, Dims, _vp, _vp, _vp, _vp]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -146,6 +147,15 @@ def moe_permute(topk_idx, d: Dims, expert_off, row_token, tok_slot_row, ws, stre
     _check(lib().moe_permute(_ptr(topk_idx), d, _ptr(expert_off), _ptr(row_token),
                              _ptr(tok_slot_row), _ptr(ws), _nbytes(ws), _stream(stream)),
            "moe_permute")
+
+
+def moe_permute_static_scratch(topk_idx, d: Dims, expert_off, row_token, tok_slot_row,
+                               stream=None) -> None:
+    """moe_permute with its scratch in the library's fixed device array
+    (no workspace argument; T*k <= 65536, E <= 512)."""
+    _check(lib().moe_permute_static_scratch(_ptr(topk_idx), d, _ptr(expert_off),
+                                            _ptr(row_token), _ptr(tok_slot_row),
+                                            _stream(stream)), "moe_permute_static_scratch")
 
 
 def moe_expert_ffn_fp8(x, expert_off, row_token, w: Fp8Ffn, d: Dims, y_perm, ws,

@@ -97,6 +97,8 @@ T* at(void* ws, size_t off) {
 
 }  // namespace
 
+void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+
 WsLayout ws_layout(const moe_dims& d) {
   const size_t T = d.T, E = d.E, P = (size_t)d.T * d.k, H = d.H, I = d.I, Is = d.I_shared;
   const size_t nb = (P + 255) / 256;

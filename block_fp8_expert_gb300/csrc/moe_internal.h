@@ -10,6 +10,13 @@
 
 namespace moe {
 
+// Pairs handled by one CTA of the permutation's count and scatter kernels;
+// the per-block scratch arrays are sized by it.
+constexpr int kPermPairsPerBlock = 256;
+
+// Sets the text returned by moe_last_error_message() on this host thread.
+void set_last_error(const char* msg);
+
 // Workspace layout for one set of dims (byte offsets, each 256-aligned).
 struct WsLayout {
   size_t status, logits, rank, block_cnt, block_base, active, idx, w, off, row_token,

@@ -16,6 +16,7 @@
 namespace moe {
 
 constexpr int kPermBlock = 256;  // pairs per count/scatter CTA (8 warps)
+static_assert(kPermBlock == kPermPairsPerBlock, "scratch sizing assumes 256 pairs per block");
 
 __global__ void __launch_bounds__(kPermBlock)
 k_perm_count(const int32_t* __restrict__ topk_idx, int P, int E,

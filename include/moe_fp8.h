@@ -183,6 +183,34 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr,
                              void* stream);
 
 /*
+ * moe_permute without a workspace, for callers that cannot allocate device
+ * memory: for example a plugin whose host framework passes it only the input
+ * and output buffers of each call, or a serving loop whose device memory is
+ * fixed at start-up.  The pages describe no such call; it has no counterpart
+ * there.
+ *
+ * Same arguments, results and determinism as moe_permute, minus ws/ws_bytes.
+ * Its scratch is one array compiled into the library (about 1.3 MB, held on
+ * every GPU that loads the library until the process exits), sized for
+ * T*k <= 65536 and E <= 512; larger sizes return MOE_ERR_UNSUPPORTED before
+ * anything is enqueued.  It calls no allocator.
+ *  - The first call on a device looks up the array's device address with
+ *    that device current (cudaGetSymbolAddress) and caches it; make that
+ *    first call before any stream capture on the device.
+ *  - All calls on a device share the array, and it keeps the last call's
+ *    contents: calls that overlap on the GPU race and give undefined
+ *    results; order them on one stream (or with events).  Each call clears
+ *    the status word it uses before its kernels run; every other scratch
+ *    value is written before it is read.
+ *  - An expert index outside [0, E) gives its pair tok_slot_row = -1 and no
+ *    row, as in moe_permute; the status bit is kept in the fixed array and is
+ *    not readable through moe_read_device_status.
+ */
+moe_status moe_permute_static_scratch(const int32_t* topk_idx, moe_dims d,
+                                      int32_t* expert_off, int32_t* row_token,
+                                      int32_t* tok_slot_row, void* stream);
+
+/*
  * Copy the workspace's device status word to *status (MOE_DEV_* bits) after
  * synchronising `stream`.  Returns MOE_ERR_DEVICE_STATUS when any bit is set.
  * The word is cleared at the start of moe_route, moe_permute,
