@@ -91,7 +91,7 @@ class Clocks:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -175,6 +175,9 @@ def cores():
 
 
 def run_reference(args):
+    global HEADLINE
+    nm, tt = args.workload.split(":")
+    HEADLINE = (nm, int(tt))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
@@ -182,7 +185,11 @@ def run_reference(args):
     w = mi.WORKLOADS[name]
     layer = mi.make_layer(name, seed=0)
     x_bits, _ = mi.make_tokens(layer, T, seed=0)
-    sample = 16
+    # Bound the whole run to about two minutes of CPU time whatever K and W
+    # are: time one small sample, then size every step's token sample.
+    probe = oracle_rate(layer, x_bits[:1])[1]
+    budget = 120.0 / (args.steps + args.warmup)
+    sample = int(max(1, min(16, T, budget / max(probe, 1e-3))))
     xs = x_bits[:sample]
     for _ in range(args.warmup):
         oracle_rate(layer, xs)
@@ -335,6 +342,9 @@ def measure_workload(torch, name, T, steps, warmup, flush, pk, dev_cache, seed=0
 
 def run_gpu(args):
     import torch
+    global HEADLINE
+    nm, tt = args.workload.split(":")
+    HEADLINE = (nm, int(tt))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -407,7 +417,7 @@ def run_gpu(args):
         run.step()
         out_host.copy_(run.out.view(torch.int16), non_blocking=True)
 
-    e2e_times = time_steps(torch, e2e_step, args.steps, 2, flush)
+    e2e_times = time_steps(torch, e2e_step, min(args.steps, 500), 3, flush)
     e2e_t = sum(e2e_times) / len(e2e_times)
 
     # launches of this library's kernels per layer call (route 2, permute 3,
@@ -467,8 +477,10 @@ def run_gpu(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="%s:%d" % HEADLINE,
+                    help="name:T of the timed workload (default: the headline)")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--sweep-steps", type=int, default=10)
     ap.add_argument("--no-sweep", action="store_true")

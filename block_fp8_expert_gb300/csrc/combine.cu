@@ -8,6 +8,8 @@ __global__ void __launch_bounds__(256)
 k_combine(const float* __restrict__ y_perm, const int32_t* __restrict__ tok_slot_row,
           const float* __restrict__ topk_w, const float* __restrict__ shared_y, int T, int H,
           int k, uint16_t* __restrict__ out) {
+  griddep_wait();
+  griddep_trigger();
   const int H4 = H / 4;
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long long)T * H4) return;
@@ -37,12 +39,11 @@ k_combine(const float* __restrict__ y_perm, const int32_t* __restrict__ tok_slot
 
 cudaError_t launch_combine(const float* y_perm, const int32_t* tok_slot_row, const float* topk_w,
                            const float* shared_y, int T, int H, int k, uint16_t* out,
-                           cudaStream_t s) {
+                           cudaStream_t s, bool pdl) {
   const long long n = (long long)T * (H / 4);
   if (n == 0) return cudaSuccess;
-  k_combine<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(y_perm, tok_slot_row, topk_w, shared_y,
-                                                        T, H, k, out);
-  return cudaGetLastError();
+  return launch_k(k_combine, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, pdl, y_perm,
+                  tok_slot_row, topk_w, shared_y, T, H, k, out);
 }
 
 }  // namespace moe

@@ -3,11 +3,16 @@
 // block-FP8 weights, fused decode+FMA dot products; "MoE per-expert
 // evaluation").
 //
-// Weight bytes go from HBM straight into registers with 16-byte loads (no
-// shared-memory round trip), are decoded there, and feed warp-level bf16
-// tensor-core MMAs whose N side is the expert's tokens (8 per MMA).  The
-// tensor core here is only a cheap multiply-accumulate for 1..16 tokens; the
-// kernel's bound is the weight stream.
+// Streaming: every thread issues all of its weight copies for a work item up
+// front as 16-byte cp.async into shared-memory slots that only it reads back
+// (slot j of thread t at index j*256 + t: conflict-free, no barrier needed),
+// then loads the matching activations straight into registers, waits once and
+// computes.  Registers stay low, so several CTAs share an SM and up to
+// ~200 KB of weights per SM are in flight, which is what HBM3e needs.
+//
+// Compute: the codes are decoded in registers and fed to warp-level
+// tensor-core MMAs (m16n8k16) whose N side is the expert's tokens, 8 per MMA;
+// the tensor core is only a cheap multiply-accumulate here.
 //
 // K permutation: an MMA's 16 logical K positions are fed from physical
 // columns so that a thread owns 16 consecutive bytes of a weight row: for
@@ -16,18 +21,18 @@
 // 16c + 4s + {0,1} and 16c + 4s + {2,3}.  The activations use the same map,
 // so every product pairs the right weight with the right activation.
 //
-// Block scale: weights are decoded as dec(code) * 2^-112 (exact); each
-// 64-column chunk lies inside one 128x128 scale block, so the chunk's MMA sum
-// is multiplied by scale * 2^112 and added to an fp32 accumulator.
+// Block scale: each 64-column chunk lies inside one 128x128 scale block, so
+// the chunk's MMA sum is multiplied by its scale in fp32 and added to an fp32
+// accumulator.  Both projections multiply fp16 activations (x16, the fp16
+// copy of x written by the router, and hid) by dec(code) decoded exactly to
+// fp16 with one cvt per pair; the scale is applied in fp32.
 #include "moe_internal.h"
 
 namespace moe {
 
-constexpr int kGemvWarps = 8;
+constexpr int kThreads = 256;
 
-// One 64-column chunk: 16 weight rows (g, g+8) x NT*8 tokens.  F16: weights
-// decoded exactly to fp16 and activations in fp16; otherwise weights decoded
-// to bf16 * 2^-112 and activations in bf16.
+// One 64-column chunk: 16 weight rows (g, g+8) x NT*8 tokens.
 template <int NT, bool F16>
 __device__ __forceinline__ void chunk_mma(const uint4& w_lo, const uint4& w_hi,
                                           const uint4 (&xa)[NT][2], float (&part)[NT][4]) {
@@ -56,19 +61,27 @@ __device__ __forceinline__ void chunk_mma(const uint4& w_lo, const uint4& w_hi,
 }
 
 // ---------------------------------------------------------------------------
-// gate/up + SwiGLU.  grid (I/16, max active experts), 8 warps split K = H.
+// gate/up + SwiGLU.  grid (I/16, max active experts).  A CTA owns 16 rows of
+// the expert's gate and up matrices; its 8 warps split K = H into 64-column
+// chunks (warp w: chunks w, w+8, ...), kGuChunks per warp per K-group.
 // hid[r, i] = silu(g) * u in fp16 for every row r of the expert.
 // ---------------------------------------------------------------------------
+constexpr int kGuChunks = 4;  // chunks per warp per K-group: H <= 2048 in one group
+constexpr size_t kGuSmem = sizeof(uint4) * kGuChunks * 4 * kThreads;  // 64 KB
+
 template <int NT>
-__global__ void __launch_bounds__(kGemvWarps * 32)
-k_gateup_gemv(const uint16_t* __restrict__ x, int H, int I,
-              const int32_t* __restrict__ expert_off, const int32_t* __restrict__ row_token,
-              const int32_t* __restrict__ active,
-              const uint8_t* __restrict__ gcodes, const float* __restrict__ gscales,
-              const uint8_t* __restrict__ ucodes, const float* __restrict__ uscales,
-              uint16_t* __restrict__ hid, int32_t* __restrict__ status) {
-  __shared__ float red[kGemvWarps][NT][2][4][32];
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2)
+k_gateup_stream(const uint16_t* __restrict__ x16, int H, int I,
+                const int32_t* __restrict__ expert_off, const int32_t* __restrict__ row_token,
+                const int32_t* __restrict__ active,
+                const uint8_t* __restrict__ gcodes, const float* __restrict__ gscales,
+                const uint8_t* __restrict__ ucodes, const float* __restrict__ uscales,
+                uint16_t* __restrict__ hid, int32_t* __restrict__ status) {
+  extern __shared__ uint4 wbuf[];  // [kGuChunks * 4][kThreads]
+  __shared__ float red[8][NT][2][4][32];
   __shared__ int tok[NT * 8];
+  griddep_wait();
+  griddep_trigger();
   const int a = blockIdx.y;
   if (a >= active[0]) return;
   const int e = active[1 + a];
@@ -98,38 +111,62 @@ k_gateup_gemv(const uint16_t* __restrict__ x, int H, int I,
 #pragma unroll
       for (int q = 0; q < 4; ++q) accg[nt][q] = accu[nt][q] = 0.f;
 
-#pragma unroll 2
-    for (int ch = warp; ch < nch; ch += kGemvWarps) {
-      const int k0 = ch * 64;
-      const uint4 g_lo = ldg_stream16(gp + k0), g_hi = ldg_stream16(gp + r8 + k0);
-      const uint4 u_lo = ldg_stream16(up + k0), u_hi = ldg_stream16(up + r8 + k0);
-      uint4 xa[NT][2];
+    for (int kg = 0; kg < nch; kg += 8 * kGuChunks) {
+      // 1. all weight copies of this K-group
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        if (trow[nt] >= 0) {
-          const uint16_t* xp = x + (size_t)trow[nt] * H + k0 + 16 * c;
-          xa[nt][0] = ldg16(xp);
-          xa[nt][1] = ldg16(xp + 8);
-        } else {
-          xa[nt][0] = xa[nt][1] = make_uint4(0, 0, 0, 0);
+      for (int j = 0; j < kGuChunks; ++j) {
+        const int ch = kg + warp + 8 * j;
+        if (ch < nch) {
+          const int k0 = ch * 64;
+          cp_async16(&wbuf[(j * 4 + 0) * kThreads + tid], gp + k0);
+          cp_async16(&wbuf[(j * 4 + 1) * kThreads + tid], gp + r8 + k0);
+          cp_async16(&wbuf[(j * 4 + 2) * kThreads + tid], up + k0);
+          cp_async16(&wbuf[(j * 4 + 3) * kThreads + tid], up + r8 + k0);
         }
       }
-      const float sg = gs[k0 / kScaleBlock] * kPow2_112;
-      const float su = us[k0 / kScaleBlock] * kPow2_112;
-      float pg[NT][4], pu[NT][4];
+      cp_async_commit();
+      // 2. the activations, straight into registers
+      uint4 xa[kGuChunks][NT][2];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+      for (int j = 0; j < kGuChunks; ++j) {
+        const int ch = kg + warp + 8 * j;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) pg[nt][q] = pu[nt][q] = 0.f;
-      chunk_mma<NT, false>(g_lo, g_hi, xa, pg);
-      chunk_mma<NT, false>(u_lo, u_hi, xa, pu);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          accg[nt][q] = fmaf(pg[nt][q], sg, accg[nt][q]);
-          accu[nt][q] = fmaf(pu[nt][q], su, accu[nt][q]);
+        for (int nt = 0; nt < NT; ++nt) {
+          if (ch < nch && trow[nt] >= 0) {
+            const uint16_t* xp = x16 + (size_t)trow[nt] * H + ch * 64 + 16 * c;
+            xa[j][nt][0] = ldg16(xp);
+            xa[j][nt][1] = ldg16(xp + 8);
+          } else {
+            xa[j][nt][0] = xa[j][nt][1] = make_uint4(0, 0, 0, 0);
+          }
         }
+      }
+      cp_async_wait<0>();
+      // 3. decode + MMA per chunk, block scale in fp32
+#pragma unroll
+      for (int j = 0; j < kGuChunks; ++j) {
+        const int ch = kg + warp + 8 * j;
+        if (ch < nch) {
+          const float sg = gs[ch * 64 / kScaleBlock];
+          const float su = us[ch * 64 / kScaleBlock];
+          float pg[NT][4], pu[NT][4];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) pg[nt][q] = pu[nt][q] = 0.f;
+          chunk_mma<NT, true>(wbuf[(j * 4 + 0) * kThreads + tid],
+                              wbuf[(j * 4 + 1) * kThreads + tid], xa[j], pg);
+          chunk_mma<NT, true>(wbuf[(j * 4 + 2) * kThreads + tid],
+                              wbuf[(j * 4 + 3) * kThreads + tid], xa[j], pu);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              accg[nt][q] = fmaf(pg[nt][q], sg, accg[nt][q]);
+              accu[nt][q] = fmaf(pu[nt][q], su, accu[nt][q]);
+            }
+        }
+      }
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -144,7 +181,7 @@ k_gateup_gemv(const uint16_t* __restrict__ x, int H, int I,
       const int nt = tid >> 7, q = (tid >> 5) & 3, L = tid & 31;
       float gv = 0.f, uv = 0.f;
 #pragma unroll
-      for (int w = 0; w < kGemvWarps; ++w) {
+      for (int w = 0; w < 8; ++w) {
         gv += red[w][nt][0][q][L];
         uv += red[w][nt][1][q][L];
       }
@@ -161,26 +198,33 @@ k_gateup_gemv(const uint16_t* __restrict__ x, int H, int I,
 }
 
 // ---------------------------------------------------------------------------
-// down projection.  grid (H/128, max active experts); warp w owns output rows
-// [h0 + 16w, h0 + 16w + 16) over the whole K = I.
-// y[r, h] = sum_i hid[r, i] Wd[h, i] in fp32 for every row r of the expert;
-// hid (fp16) times the exactly decoded fp16 weights, block scale in fp32.
+// down projection.  grid (H/32, max active experts).  A CTA owns 32 output
+// rows (two 16-row MMA tiles); warp w works on tile w & 1 and K-part w >> 1 of
+// 4 (chunks kp, kp+4, ...), kDnChunks per warp per K-group.
+// y[r, h] = sum_i hid[r, i] Wd[h, i] in fp32 for every row r of the expert.
 // ---------------------------------------------------------------------------
+constexpr int kDnChunks = 3;  // I <= 768 in one K-group
+constexpr size_t kDnSmem = sizeof(uint4) * kDnChunks * 2 * kThreads;  // 24 KB
+
 template <int NT>
-__global__ void __launch_bounds__(kGemvWarps * 32)
-k_down_gemv(const uint16_t* __restrict__ hid, int H, int I,
-            const int32_t* __restrict__ expert_off, const int32_t* __restrict__ active,
-            const uint8_t* __restrict__ dcodes, const float* __restrict__ dscales,
-            float* __restrict__ y) {
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
+k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
+              const int32_t* __restrict__ expert_off, const int32_t* __restrict__ active,
+              const uint8_t* __restrict__ dcodes, const float* __restrict__ dscales,
+              float* __restrict__ y) {
+  extern __shared__ uint4 wbuf[];  // [kDnChunks * 2][kThreads]
+  __shared__ float red[4][2][NT][4][32];
+  griddep_wait();
+  griddep_trigger();
   const int a = blockIdx.y;
   if (a >= active[0]) return;
   const int e = active[1 + a];
   const int r0 = expert_off[e];
   const int ne = expert_off[e + 1] - r0;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
-  const int h0 = blockIdx.x * 128 + warp * 16;
-  if (h0 >= H) return;
+  const int mt = warp & 1, kp = warp >> 1;
+  const int h0 = blockIdx.x * 32 + mt * 16;
   const int nch = I / 64;
   const int nIb = cdiv(I, kScaleBlock);
   const uint8_t* dp = dcodes + ((size_t)e * H + h0 + g) * I + 16 * c;
@@ -196,64 +240,127 @@ k_down_gemv(const uint16_t* __restrict__ hid, int H, int I,
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
-#pragma unroll 2
-    for (int ch = 0; ch < nch; ++ch) {
-      const int k0 = ch * 64;
-      const uint4 w_lo = ldg_stream16(dp + k0), w_hi = ldg_stream16(dp + r8 + k0);
-      uint4 xa[NT][2];
+    for (int kg = 0; kg < nch; kg += 4 * kDnChunks) {
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        if (valid[nt]) {
-          const uint16_t* hp = hid + (size_t)(r0 + n0 + nt * 8 + g) * I + k0 + 16 * c;
-          xa[nt][0] = ldg16(hp);
-          xa[nt][1] = ldg16(hp + 8);
-        } else {
-          xa[nt][0] = xa[nt][1] = make_uint4(0, 0, 0, 0);
+      for (int j = 0; j < kDnChunks; ++j) {
+        const int ch = kg + kp + 4 * j;
+        if (ch < nch) {
+          cp_async16(&wbuf[(j * 2 + 0) * kThreads + tid], dp + ch * 64);
+          cp_async16(&wbuf[(j * 2 + 1) * kThreads + tid], dp + r8 + ch * 64);
         }
       }
-      const float sd = ds[k0 / kScaleBlock];
-      float p[NT][4];
+      cp_async_commit();
+      uint4 xa[kDnChunks][NT][2];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+      for (int j = 0; j < kDnChunks; ++j) {
+        const int ch = kg + kp + 4 * j;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) p[nt][q] = 0.f;
-      chunk_mma<NT, true>(w_lo, w_hi, xa, p);
+        for (int nt = 0; nt < NT; ++nt) {
+          if (ch < nch && valid[nt]) {
+            const uint16_t* hp = hid + (size_t)(r0 + n0 + nt * 8 + g) * I + ch * 64 + 16 * c;
+            xa[j][nt][0] = ldg16(hp);
+            xa[j][nt][1] = ldg16(hp + 8);
+          } else {
+            xa[j][nt][0] = xa[j][nt][1] = make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+      cp_async_wait<0>();
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+      for (int j = 0; j < kDnChunks; ++j) {
+        const int ch = kg + kp + 4 * j;
+        if (ch < nch) {
+          const float sd = ds[ch * 64 / kScaleBlock];
+          float p[NT][4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[nt][q] = fmaf(p[nt][q], sd, acc[nt][q]);
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) p[nt][q] = 0.f;
+          chunk_mma<NT, true>(wbuf[(j * 2 + 0) * kThreads + tid],
+                              wbuf[(j * 2 + 1) * kThreads + tid], xa[j], p);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[nt][q] = fmaf(p[nt][q], sd, acc[nt][q]);
+        }
+      }
     }
-    // C fragment: q=0,1 -> row g, tokens 2c, 2c+1; q=2,3 -> row g+8.
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int n = n0 + nt * 8 + 2 * c + (q & 1);
-        const int row = g + 8 * (q >> 1);
-        if (n < ne) y[(size_t)(r0 + n) * H + h0 + row] = acc[nt][q];
-      }
+      for (int q = 0; q < 4; ++q) red[kp][mt][nt][q][lane] = acc[nt][q];
+    __syncthreads();
+    // outputs: (tile, nt, q, L) -> one per thread per round
+    for (int o = tid; o < 2 * NT * 128; o += kThreads) {
+      const int t2 = o / (NT * 128), nt = (o >> 7) % NT, q = (o >> 5) & 3, L = o & 31;
+      float v = 0.f;
+#pragma unroll
+      for (int p = 0; p < 4; ++p) v += red[p][t2][nt][q][L];
+      const int row = (L >> 2) + 8 * (q >> 1);
+      const int n = n0 + nt * 8 + 2 * (L & 3) + (q & 1);
+      if (n < ne) y[(size_t)(r0 + n) * H + blockIdx.x * 32 + t2 * 16 + row] = v;
+    }
+    __syncthreads();
   }
 }
 
-cudaError_t launch_expert_gemv(const uint16_t* x, const int32_t* expert_off,
+cudaError_t launch_expert_gemv(const uint16_t* x16, const int32_t* expert_off,
                                const int32_t* row_token, const int32_t* active, int max_active,
-                               const moe_fp8_ffn& w, int H, int I, int max_rows_per_expert,
-                               uint16_t* hid, float* y, int32_t* status, cudaStream_t s) {
+                               const moe_fp8_ffn& w, int H, int I, int tokens_per_expert_hint,
+                               uint16_t* hid, float* y, int32_t* status, cudaStream_t s,
+                               bool pdl) {
   if (max_active <= 0) return cudaSuccess;
-  const dim3 block(kGemvWarps * 32);
-  const dim3 g1(I / 16, max_active), g2(cdiv(H, 128), max_active);
-  if (max_rows_per_expert <= 8) {
-    k_gateup_gemv<1><<<g1, block, 0, s>>>(x, H, I, expert_off, row_token, active, w.gate.codes,
-                                          w.gate.scales, w.up.codes, w.up.scales, hid, status);
-    k_down_gemv<1><<<g2, block, 0, s>>>(hid, H, I, expert_off, active, w.down.codes,
-                                        w.down.scales, y);
-  } else {
-    k_gateup_gemv<2><<<g1, block, 0, s>>>(x, H, I, expert_off, row_token, active, w.gate.codes,
-                                          w.gate.scales, w.up.codes, w.up.scales, hid, status);
-    k_down_gemv<2><<<g2, block, 0, s>>>(hid, H, I, expert_off, active, w.down.codes,
-                                        w.down.scales, y);
+  const dim3 block(kThreads);
+  const dim3 g1(I / 16, max_active), g2(H / 32, max_active);
+  cudaError_t e;
+  if (tokens_per_expert_hint <= 8) {
+    if ((e = ensure_smem((const void*)k_gateup_stream<1>, kGuSmem)) != cudaSuccess) return e;
+    if ((e = ensure_smem((const void*)k_down_stream<1>, kDnSmem)) != cudaSuccess) return e;
+    e = launch_k(k_gateup_stream<1>, g1, block, kGuSmem, s, pdl, x16, H, I, expert_off,
+                 row_token, active, w.gate.codes, w.gate.scales, w.up.codes, w.up.scales, hid,
+                 status);
+    if (e != cudaSuccess) return e;
+    return launch_k(k_down_stream<1>, g2, block, kDnSmem, s, pdl, (const uint16_t*)hid, H, I,
+                    expert_off, active, w.down.codes, w.down.scales, y);
   }
-  return cudaGetLastError();
+  if ((e = ensure_smem((const void*)k_gateup_stream<2>, kGuSmem)) != cudaSuccess) return e;
+  if ((e = ensure_smem((const void*)k_down_stream<2>, kDnSmem)) != cudaSuccess) return e;
+  e = launch_k(k_gateup_stream<2>, g1, block, kGuSmem, s, pdl, x16, H, I, expert_off, row_token,
+               active, w.gate.codes, w.gate.scales, w.up.codes, w.up.scales, hid, status);
+  if (e != cudaSuccess) return e;
+  return launch_k(k_down_stream<2>, g2, block, kDnSmem, s, pdl, (const uint16_t*)hid, H, I,
+                  expert_off, active, w.down.codes, w.down.scales, y);
+}
+
+// x (bf16) -> x16 (fp16), flagging values beyond fp16 range; for callers of
+// the expert FFN that did not run the router here.
+__global__ void __launch_bounds__(256)
+k_x_to_f16(const uint16_t* __restrict__ x, long long n8, uint16_t* __restrict__ x16,
+           int32_t* __restrict__ status) {
+  griddep_wait();
+  griddep_trigger();
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const uint4 v = ldg16(x + 8 * i);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t h[4];
+  bool overflow = false;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const float lo = bf16_lo(w[m]), hi = bf16_hi(w[m]);
+    overflow |= !(fabsf(lo) <= kF16Max) || !(fabsf(hi) <= kF16Max);
+    h[m] = (uint32_t)f32_to_f16_bits(lo) | ((uint32_t)f32_to_f16_bits(hi) << 16);
+  }
+  if (overflow) raise_status(status, MOE_DEV_FP16_RANGE);
+  *reinterpret_cast<uint4*>(x16 + 8 * i) = make_uint4(h[0], h[1], h[2], h[3]);
+}
+
+cudaError_t launch_x_to_f16(const uint16_t* x, long long n, uint16_t* x16, int32_t* status,
+                            cudaStream_t s, bool pdl) {
+  const long long n8 = n / 8;
+  if (n8 == 0) return cudaSuccess;
+  return launch_k(k_x_to_f16, dim3((unsigned)((n8 + 255) / 256)), dim3(256), 0, s, pdl, x, n8,
+                  x16, status);
 }
 
 }  // namespace moe

@@ -4,7 +4,10 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
+#include <set>
 #include <string>
+#include <utility>
 
 #include "moe_internal.h"
 
@@ -99,6 +102,19 @@ T* at(void* ws, size_t off) {
 
 void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
 
+cudaError_t ensure_smem(const void* func, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<int, const void*>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({dev, func})) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert({dev, func});
+  return e;
+}
+
 WsLayout ws_layout(const moe_dims& d) {
   const size_t T = d.T, E = d.E, P = (size_t)d.T * d.k, H = d.H, I = d.I, Is = d.I_shared;
   const size_t nb = (P + 255) / 256;
@@ -110,7 +126,7 @@ WsLayout ws_layout(const moe_dims& d) {
     return at;
   };
   L.status = take(256);
-  L.logits = take(T * E * 4);
+  L.logits = take(4 * T * E * 4);  // up to 4 K-slices of partial router logits
   L.rank = take(P * 4);
   L.block_cnt = take(nb * E * 4);
   L.block_base = take(nb * E * 4);
@@ -120,6 +136,8 @@ WsLayout ws_layout(const moe_dims& d) {
   L.off = take((E + 1) * 4);
   L.row_token = take(P * 4);
   L.tok_slot_row = take(P * 4);
+  L.row_pair = take(P * 4);
+  L.x16 = take(T * H * 2);
   L.hid = take(P * I * 2);
   L.y_perm = take(P * H * 4);
   L.sh_hid = take(Is ? T * Is * 2 : 0);
@@ -132,6 +150,8 @@ WsLayout ws_layout(const moe_dims& d) {
 }
 
 __global__ void k_identity_perm(int T, int32_t* off, int32_t* rows, int32_t* active) {
+  griddep_wait();
+  griddep_trigger();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < T) rows[i] = i;
   if (i == 0) {
@@ -143,9 +163,9 @@ __global__ void k_identity_perm(int T, int32_t* off, int32_t* rows, int32_t* act
 }
 
 cudaError_t launch_identity_perm(int T, int32_t* off, int32_t* rows, int32_t* active,
-                                 cudaStream_t s) {
-  k_identity_perm<<<cdiv(T > 0 ? T : 1, 256), 256, 0, s>>>(T, off, rows, active);
-  return cudaGetLastError();
+                                 cudaStream_t s, bool pdl) {
+  return launch_k(k_identity_perm, dim3(cdiv(T > 0 ? T : 1, 256)), dim3(256), 0, s, pdl, T, off,
+                  rows, active);
 }
 
 }  // namespace moe
@@ -194,7 +214,8 @@ moe_status moe_route(const uint16_t* x, const float* Wr, const float* bias, moe_
   if ((s = check_ws(d, ws, ws_bytes)) != MOE_OK) return s;
   const WsLayout L = ws_layout(d);
   CUDA_CHECK(launch_route(x, Wr, bias, d.T, d.H, d.E, d.k, at<float>(ws, L.logits), topk_idx,
-                          topk_w, at<int32_t>(ws, L.status), (cudaStream_t)stream),
+                          topk_w, nullptr, at<int32_t>(ws, L.status), (cudaStream_t)stream,
+                          true),
              "moe_route");
   return MOE_OK;
 }
@@ -216,8 +237,8 @@ moe_status moe_permute(const int32_t* topk_idx, moe_dims d, int32_t* expert_off,
   CUDA_CHECK(cudaMemsetAsync(at<int32_t>(ws, L.status), 0, sizeof(int32_t), st), "moe_permute");
   CUDA_CHECK(launch_permute(topk_idx, d.T, d.E, d.k, at<int32_t>(ws, L.rank),
                             at<int32_t>(ws, L.block_cnt), at<int32_t>(ws, L.block_base),
-                            expert_off, row_token, tok_slot_row, at<int32_t>(ws, L.active),
-                            at<int32_t>(ws, L.status), st),
+                            expert_off, row_token, tok_slot_row, nullptr,
+                            at<int32_t>(ws, L.active), at<int32_t>(ws, L.status), st, false),
              "moe_permute");
   return MOE_OK;
 }
@@ -238,11 +259,15 @@ moe_status moe_expert_ffn_fp8(const uint16_t* x, const int32_t* expert_off,
   cudaStream_t st = (cudaStream_t)stream;
   int32_t* active = at<int32_t>(ws, L.active);
   int32_t* status = at<int32_t>(ws, L.status);
-  CUDA_CHECK(launch_active_from_offsets(expert_off, d.E, active, status, st),
+  uint16_t* x16 = at<uint16_t>(ws, L.x16);
+  CUDA_CHECK(launch_active_from_offsets(expert_off, d.E, active, status, st, true),
+             "moe_expert_ffn_fp8");
+  CUDA_CHECK(launch_x_to_f16(x, (long long)d.T * d.H, x16, status, st, true),
              "moe_expert_ffn_fp8");
   const int P = d.T * d.k;
-  CUDA_CHECK(launch_expert_gemv(x, expert_off, row_token, active, d.E < P ? d.E : P, w, d.H, d.I,
-                                d.T, at<uint16_t>(ws, L.hid), y_perm, status, st),
+  CUDA_CHECK(launch_expert_gemv(x16, expert_off, row_token, active, d.E < P ? d.E : P, w, d.H,
+                                d.I, cdiv(P, d.E), at<uint16_t>(ws, L.hid), y_perm, status, st,
+                                true),
              "moe_expert_ffn_fp8");
   return MOE_OK;
 }
@@ -258,7 +283,7 @@ moe_status moe_combine(const float* y_perm, const int32_t* tok_slot_row, const f
   REQUIRE_OPT_PTR(shared_y);
   REQUIRE_PTR(out);
   CUDA_CHECK(launch_combine(y_perm, tok_slot_row, topk_w, shared_y, d.T, d.H, d.k, out,
-                            (cudaStream_t)stream),
+                            (cudaStream_t)stream, true),
              "moe_combine");
   return MOE_OK;
 }
@@ -296,28 +321,44 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
   float* y_perm = at<float>(ws, L.y_perm);
 
   int32_t* status = at<int32_t>(ws, L.status);
-  CUDA_CHECK(launch_route(x, Wr, bias, d.T, d.H, d.E, d.k, at<float>(ws, L.logits), idx, w,
-                          status, st),
-             "moe_layer_forward: route");
-  CUDA_CHECK(launch_permute(idx, d.T, d.E, d.k, at<int32_t>(ws, L.rank),
-                            at<int32_t>(ws, L.block_cnt), at<int32_t>(ws, L.block_base), off,
-                            row_token, tok_slot_row, active, status, st),
-             "moe_layer_forward: permute");
-  CUDA_CHECK(launch_expert_gemv(x, off, row_token, active, d.E < P ? d.E : P, routed, d.H, d.I,
-                                d.T, at<uint16_t>(ws, L.hid), y_perm, status, st),
+  uint16_t* x16 = at<uint16_t>(ws, L.x16);
+  int32_t* soff = at<int32_t>(ws, L.sh_off);
+  int32_t* srows = at<int32_t>(ws, L.sh_rows);
+  int32_t* sact = at<int32_t>(ws, L.sh_active);
+  const bool has_shared = d.I_shared > 0;
+  if (small_route_permute_ok(d.T, d.E, d.k)) {
+    // router logits, then top-k + permutation (+ the shared expert's identity
+    // permutation) in one CTA
+    CUDA_CHECK(launch_route_permute_small(
+                   x, Wr, bias, d.T, d.H, d.E, d.k, at<float>(ws, L.logits), idx, w, off,
+                   row_token, tok_slot_row, at<int32_t>(ws, L.row_pair), active,
+                   has_shared ? soff : nullptr, has_shared ? srows : nullptr,
+                   has_shared ? sact : nullptr, x16, status, st, true),
+               "moe_layer_forward: route+permute");
+  } else {
+    CUDA_CHECK(launch_route(x, Wr, bias, d.T, d.H, d.E, d.k, at<float>(ws, L.logits), idx, w,
+                            x16, status, st, true),
+               "moe_layer_forward: route");
+    CUDA_CHECK(launch_permute(idx, d.T, d.E, d.k, at<int32_t>(ws, L.rank),
+                              at<int32_t>(ws, L.block_cnt), at<int32_t>(ws, L.block_base), off,
+                              row_token, tok_slot_row, at<int32_t>(ws, L.row_pair), active,
+                              status, st, true),
+               "moe_layer_forward: permute");
+    if (has_shared)
+      CUDA_CHECK(launch_identity_perm(d.T, soff, srows, sact, st, true),
+                 "moe_layer_forward: shared");
+  }
+  CUDA_CHECK(launch_expert_gemv(x16, off, row_token, active, d.E < P ? d.E : P, routed, d.H, d.I,
+                                cdiv(P, d.E), at<uint16_t>(ws, L.hid), y_perm, status, st, true),
              "moe_layer_forward: experts");
   float* shared_y = nullptr;
-  if (d.I_shared > 0) {
-    int32_t* soff = at<int32_t>(ws, L.sh_off);
-    int32_t* srows = at<int32_t>(ws, L.sh_rows);
-    int32_t* sact = at<int32_t>(ws, L.sh_active);
+  if (has_shared) {
     shared_y = at<float>(ws, L.sh_y);
-    CUDA_CHECK(launch_identity_perm(d.T, soff, srows, sact, st), "moe_layer_forward: shared");
-    CUDA_CHECK(launch_expert_gemv(x, soff, srows, sact, 1, *shared, d.H, d.I_shared, d.T,
-                                  at<uint16_t>(ws, L.sh_hid), shared_y, status, st),
+    CUDA_CHECK(launch_expert_gemv(x16, soff, srows, sact, 1, *shared, d.H, d.I_shared, d.T,
+                                  at<uint16_t>(ws, L.sh_hid), shared_y, status, st, true),
                "moe_layer_forward: shared expert");
   }
-  CUDA_CHECK(launch_combine(y_perm, tok_slot_row, w, shared_y, d.T, d.H, d.k, out, st),
+  CUDA_CHECK(launch_combine(y_perm, tok_slot_row, w, shared_y, d.T, d.H, d.k, out, st, true),
              "moe_layer_forward: combine");
   return MOE_OK;
 }

@@ -119,6 +119,45 @@ __device__ __forceinline__ uint4 ldg16(const void* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
+// Asynchronous 16-byte global -> shared copy, cached in L2 only.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// fp32 -> (hi, mid, lo) bf16 with w == hi + mid + lo to within 2^-24 |w|:
+// each part is the bf16 rounding of what the previous parts left.
+__device__ __forceinline__ void split3_bf16(float w, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
+  const float h = __uint_as_float(pack_bf16x2(w, 0.f) << 16);
+  const float r = w - h;
+  const float m = __uint_as_float(pack_bf16x2(r, 0.f) << 16);
+  hi = __float_as_uint(h) >> 16;
+  mid = __float_as_uint(m) >> 16;
+  lo = pack_bf16x2(r - m, 0.f) & 0xFFFFu;
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of a layer call starts with
+// griddep_wait(): when it was launched with the programmatic-serialisation
+// attribute it may be scheduled before its predecessor finishes, and this
+// wait returns once the predecessor grid has completed and its writes are
+// visible (without the attribute it returns at once).  griddep_trigger()
+// then lets the next kernel's launch begin early.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+__device__ __forceinline__ void griddep_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Device status word
 // ---------------------------------------------------------------------------

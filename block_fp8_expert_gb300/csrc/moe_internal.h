@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "moe_common.cuh"
@@ -17,39 +18,84 @@ constexpr int kPermPairsPerBlock = 256;
 // Sets the text returned by moe_last_error_message() on this host thread.
 void set_last_error(const char* msg);
 
+// Kernel launch on `s`, optionally with programmatic stream serialisation
+// (the kernel must begin with griddep_wait()).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t s, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Raises `func`'s dynamic shared-memory limit to `bytes`, once per device
+// (host-side attribute; the first call on a device should precede capture).
+cudaError_t ensure_smem(const void* func, int bytes);
+
 // Workspace layout for one set of dims (byte offsets, each 256-aligned).
 struct WsLayout {
   size_t status, logits, rank, block_cnt, block_base, active, idx, w, off, row_token,
-      tok_slot_row, hid, y_perm, sh_hid, sh_y, sh_off, sh_rows, sh_active, total;
+      tok_slot_row, row_pair, x16, hid, y_perm, sh_hid, sh_y, sh_off, sh_rows, sh_active, total;
 };
 WsLayout ws_layout(const moe_dims& d);
 
+// All launchers enqueue on `s`; with pdl the kernels are launched with
+// programmatic stream serialisation (each begins with griddep_wait()).
+
+// Router logits (+ optional fp16 copy of x) and top-k.  `part` holds up to 4
+// K-slices of partial logits, [4][T][E] floats.
 cudaError_t launch_route(const uint16_t* x, const float* Wr, const float* bias, int T, int H,
-                         int E, int k, float* logits, int32_t* topk_idx, float* topk_w,
-                         int32_t* status, cudaStream_t s);
+                         int E, int k, float* part, int32_t* topk_idx, float* topk_w,
+                         uint16_t* x16, int32_t* status, cudaStream_t s, bool pdl);
+
+// Router logits, then top-k and the full permutation in one CTA, for
+// T*k <= 4096 (small_route_permute_ok).  sh_* may be NULL (no shared expert).
+bool small_route_permute_ok(int T, int E, int k);
+cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const float* bias,
+                                       int T, int H, int E, int k, float* part,
+                                       int32_t* topk_idx, float* topk_w, int32_t* expert_off,
+                                       int32_t* row_token, int32_t* tok_slot_row,
+                                       int32_t* row_pair, int32_t* active, int32_t* sh_off,
+                                       int32_t* sh_rows, int32_t* sh_active, uint16_t* x16,
+                                       int32_t* status, cudaStream_t s, bool pdl);
 
 cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, int32_t* rank,
                            int32_t* block_cnt, int32_t* block_base, int32_t* expert_off,
-                           int32_t* row_token, int32_t* tok_slot_row, int32_t* active,
-                           int32_t* status, cudaStream_t s);
+                           int32_t* row_token, int32_t* tok_slot_row, int32_t* row_pair,
+                           int32_t* active, int32_t* status, cudaStream_t s, bool pdl);
 
 cudaError_t launch_active_from_offsets(const int32_t* expert_off, int E, int32_t* active,
-                                       int32_t* status, cudaStream_t s);
+                                       int32_t* status, cudaStream_t s, bool pdl);
 
-// Grouped GEMV over the experts listed in `active` (count, then ids).
-// max_active bounds the list length; max_rows_per_expert bounds any segment.
-cudaError_t launch_expert_gemv(const uint16_t* x, const int32_t* expert_off,
+// bf16 x -> fp16 x16 (n elements, a multiple of 8), flagging fp16 overflow.
+cudaError_t launch_x_to_f16(const uint16_t* x, long long n, uint16_t* x16, int32_t* status,
+                            cudaStream_t s, bool pdl);
+
+// Grouped GEMV over the experts listed in `active` (count, then ids), on the
+// fp16 activations x16.  max_active bounds the list length;
+// tokens_per_expert_hint (the expected rows per expert) picks the MMA's N
+// width; any segment length is handled.
+cudaError_t launch_expert_gemv(const uint16_t* x16, const int32_t* expert_off,
                                const int32_t* row_token, const int32_t* active, int max_active,
-                               const moe_fp8_ffn& w, int H, int I, int max_rows_per_expert,
-                               uint16_t* hid, float* y, int32_t* status, cudaStream_t s);
+                               const moe_fp8_ffn& w, int H, int I, int tokens_per_expert_hint,
+                               uint16_t* hid, float* y, int32_t* status, cudaStream_t s,
+                               bool pdl);
 
 cudaError_t launch_combine(const float* y_perm, const int32_t* tok_slot_row, const float* topk_w,
                            const float* shared_y, int T, int H, int k, uint16_t* out,
-                           cudaStream_t s);
+                           cudaStream_t s, bool pdl);
 
 // Identity permutation of T tokens onto one expert (the shared expert):
 // off = {0, T}, rows = 0..T-1, active = {1, 0}.
 cudaError_t launch_identity_perm(int T, int32_t* off, int32_t* rows, int32_t* active,
-                                 cudaStream_t s);
+                                 cudaStream_t s, bool pdl);
 
 }  // namespace moe

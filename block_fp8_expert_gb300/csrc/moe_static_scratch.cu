@@ -109,7 +109,8 @@ extern "C" moe_status moe_permute_static_scratch(const int32_t* topk_idx, moe_di
     e = launch_permute(topk_idx, d.T, d.E, d.k, reinterpret_cast<int32_t*>(b + kOffRank),
                        reinterpret_cast<int32_t*>(b + kOffCnt),
                        reinterpret_cast<int32_t*>(b + kOffBase), expert_off, row_token,
-                       tok_slot_row, reinterpret_cast<int32_t*>(b + kOffActive), status, st);
+                       tok_slot_row, nullptr, reinterpret_cast<int32_t*>(b + kOffActive), status,
+                       st, false);
   if (e != cudaSuccess) {
     set_last_error(cudaGetErrorString(e));
     return MOE_ERR_CUDA;

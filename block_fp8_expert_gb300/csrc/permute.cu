@@ -23,6 +23,8 @@ k_perm_count(const int32_t* __restrict__ topk_idx, int P, int E,
              int32_t* __restrict__ rank, int32_t* __restrict__ block_cnt,
              int32_t* __restrict__ status) {
   extern __shared__ int32_t cnt_w[];  // [8][E]
+  griddep_wait();
+  griddep_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int i = tid; i < 8 * E; i += kPermBlock) cnt_w[i] = 0;
   __syncthreads();
@@ -60,6 +62,8 @@ k_perm_scan(const int32_t* __restrict__ block_cnt, int nblocks, int E,
             int32_t* __restrict__ active) {
   __shared__ int32_t warp_sum[32];
   __shared__ int32_t warp_act[32];
+  griddep_wait();
+  griddep_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int total = 0;
   if (tid < E) {
@@ -129,7 +133,9 @@ __global__ void __launch_bounds__(kPermBlock)
 k_perm_scatter(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ rank,
                const int32_t* __restrict__ block_base, const int32_t* __restrict__ expert_off,
                int P, int E, int k, int32_t* __restrict__ row_token,
-               int32_t* __restrict__ tok_slot_row) {
+               int32_t* __restrict__ tok_slot_row, int32_t* __restrict__ row_pair) {
+  griddep_wait();
+  griddep_trigger();
   const int q = blockIdx.x * kPermBlock + threadIdx.x;
   if (q >= P) return;
   const int r = rank[q];
@@ -141,6 +147,7 @@ k_perm_scatter(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__
   const int row = expert_off[e] + block_base[(size_t)blockIdx.x * E + e] + r;
   row_token[row] = q / k;
   tok_slot_row[q] = row;
+  if (row_pair) row_pair[row] = q;
 }
 
 // Active-expert list from offsets alone (for callers of the expert FFN that
@@ -149,6 +156,8 @@ __global__ void __launch_bounds__(1024)
 k_active_from_offsets(const int32_t* __restrict__ expert_off, int E,
                       int32_t* __restrict__ active, int32_t* __restrict__ status) {
   __shared__ int32_t warp_act[32];
+  griddep_wait();
+  griddep_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0 && status) *status = 0;  // first kernel of an expert-FFN call
   const int ne = (tid < E && expert_off[tid + 1] > expert_off[tid]) ? 1 : 0;
@@ -177,25 +186,29 @@ k_active_from_offsets(const int32_t* __restrict__ expert_off, int E,
 
 cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, int32_t* rank,
                            int32_t* block_cnt, int32_t* block_base, int32_t* expert_off,
-                           int32_t* row_token, int32_t* tok_slot_row, int32_t* active,
-                           int32_t* status, cudaStream_t s) {
+                           int32_t* row_token, int32_t* tok_slot_row, int32_t* row_pair,
+                           int32_t* active, int32_t* status, cudaStream_t s, bool pdl) {
   const int P = T * k;
   const int nb = cdiv(P, kPermBlock);
+  cudaError_t e;
   if (nb > 0) {
     const size_t smem = sizeof(int32_t) * 8 * E;
-    k_perm_count<<<nb, kPermBlock, smem, s>>>(topk_idx, P, E, rank, block_cnt, status);
+    e = launch_k(k_perm_count, dim3(nb), dim3(kPermBlock), smem, s, pdl, topk_idx, P, E, rank,
+                 block_cnt, status);
+    if (e != cudaSuccess) return e;
   }
-  k_perm_scan<<<1, 1024, 0, s>>>(block_cnt, nb, E, block_base, expert_off, active);
-  if (nb > 0)
-    k_perm_scatter<<<nb, kPermBlock, 0, s>>>(topk_idx, rank, block_base, expert_off, P, E, k,
-                                             row_token, tok_slot_row);
-  return cudaGetLastError();
+  e = launch_k(k_perm_scan, dim3(1), dim3(1024), 0, s, pdl, (const int32_t*)block_cnt, nb, E,
+               block_base, expert_off, active);
+  if (e != cudaSuccess || nb == 0) return e;
+  return launch_k(k_perm_scatter, dim3(nb), dim3(kPermBlock), 0, s, pdl, topk_idx,
+                  (const int32_t*)rank, (const int32_t*)block_base, (const int32_t*)expert_off, P,
+                  E, k, row_token, tok_slot_row, row_pair);
 }
 
 cudaError_t launch_active_from_offsets(const int32_t* expert_off, int E, int32_t* active,
-                                       int32_t* status, cudaStream_t s) {
-  k_active_from_offsets<<<1, 1024, 0, s>>>(expert_off, E, active, status);
-  return cudaGetLastError();
+                                       int32_t* status, cudaStream_t s, bool pdl) {
+  return launch_k(k_active_from_offsets, dim3(1), dim3(1024), 0, s, pdl, expert_off, E, active,
+                  status);
 }
 
 }  // namespace moe

@@ -2,85 +2,163 @@
 // renormalised weights (colizig README, model table: experts with top-k
 // routing).  The renormalised weight p_j / sum_sel p equals the softmax over
 // the k selected logits, because the full softmax's normaliser cancels; the
-// kernel computes it that way and never forms the E probabilities.
+// kernels compute it that way and never form the E probabilities.
 #include "moe_internal.h"
 
 namespace moe {
 
 // ---------------------------------------------------------------------------
-// logits: one warp per expert, 8 tokens per CTA row of the grid
+// logits on the tensor cores.  fp32 router weights are split into three bf16
+// parts (w = hi + mid + lo to within 2^-24 |w|); bf16 activations are exact,
+// so three bf16 MMAs accumulating in fp32 give fp32-accurate logits.
+// grid (ceil(E/16), KS, ceil(T/(8*NT))): a CTA owns 16 experts, one of KS
+// slices of K = H and 8*NT tokens; its 4 warps take the slice's 64-column
+// chunks round-robin.  Partial sums go to part[ks][t][e]; the top-k kernels
+// add the KS slices in a fixed order (deterministic).
+// The CTAs of expert tile 0 also write x16, the fp16 copy of x that the
+// expert kernels use, and flag values beyond fp16 range.
 // ---------------------------------------------------------------------------
-constexpr int kRouteTok = 8;    // tokens per CTA
-constexpr int kRouteWarps = 4;  // experts per CTA
+constexpr int kRouteWarps = 4;
 
+template <int NT>
 __global__ void __launch_bounds__(kRouteWarps * 32)
-k_router_logits(const uint16_t* __restrict__ x, const float* __restrict__ Wr,
-                const float* __restrict__ bias, int T, int H, int E,
-                float* __restrict__ logits, int32_t* __restrict__ status) {
-  const int lane = threadIdx.x & 31;
+k_router_mma(const uint16_t* __restrict__ x, const float* __restrict__ Wr, int T, int H, int E,
+             int kslice, float* __restrict__ part, uint16_t* __restrict__ x16,
+             int32_t* __restrict__ status) {
+  __shared__ float red[kRouteWarps][NT][4][32];
+  griddep_wait();
+  griddep_trigger();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c = lane & 3;
   // The router runs first in a layer call: it clears the status word that
   // later kernels of the call may raise.
-  if (status && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *status = 0;
-  const int e = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
-  const int t0 = blockIdx.y * kRouteTok;
-  if (e >= E) return;
-  const int nt = min(kRouteTok, T - t0);
-  float acc[kRouteTok];
+  if (status && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && tid == 0) *status = 0;
+  const int e0 = blockIdx.x * 16;
+  const int t0 = blockIdx.z * NT * 8;
+  const int kbeg = blockIdx.y * kslice, kend = min(H, kbeg + kslice);
+  const int ea = e0 + g, eb = e0 + g + 8;
+  const bool write_x16 = x16 != nullptr && blockIdx.x == 0;
+  bool overflow = false;
+  int trow[NT];
 #pragma unroll
-  for (int t = 0; t < kRouteTok; ++t) acc[t] = 0.f;
-  const float* wrow = Wr + (size_t)e * H;
-  for (int h = lane * 4; h < H; h += 128) {
-    const float4 w4 = __ldg(reinterpret_cast<const float4*>(wrow + h));
+  for (int nt = 0; nt < NT; ++nt) trow[nt] = (t0 + nt * 8 + g < T) ? t0 + nt * 8 + g : -1;
+  float acc[NT][4];
 #pragma unroll
-    for (int t = 0; t < kRouteTok; ++t) {
-      if (t < nt) {
-        const uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + (size_t)(t0 + t) * H + h));
-        acc[t] = fmaf(bf16_lo(xv.x), w4.x, acc[t]);
-        acc[t] = fmaf(bf16_hi(xv.x), w4.y, acc[t]);
-        acc[t] = fmaf(bf16_lo(xv.y), w4.z, acc[t]);
-        acc[t] = fmaf(bf16_hi(xv.y), w4.w, acc[t]);
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
+
+  for (int k0 = kbeg + warp * 64; k0 < kend; k0 += kRouteWarps * 64) {
+    const int kk = k0 + 16 * c;
+    float wa[16], wb[16];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const float4 fa = ea < E ? __ldg(reinterpret_cast<const float4*>(Wr + (size_t)ea * H + kk) + v)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 fb = eb < E ? __ldg(reinterpret_cast<const float4*>(Wr + (size_t)eb * H + kk) + v)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+      wa[4 * v + 0] = fa.x; wa[4 * v + 1] = fa.y; wa[4 * v + 2] = fa.z; wa[4 * v + 3] = fa.w;
+      wb[4 * v + 0] = fb.x; wb[4 * v + 1] = fb.y; wb[4 * v + 2] = fb.z; wb[4 * v + 3] = fb.w;
+    }
+    uint4 xa[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      if (trow[nt] >= 0) {
+        const uint16_t* xp = x + (size_t)trow[nt] * H + kk;
+        xa[nt][0] = ldg16(xp);
+        xa[nt][1] = ldg16(xp + 8);
+        if (write_x16) {
+          // 16 bf16 -> 16 fp16 (round to nearest even), two 16-byte stores
+          uint32_t h[8];
+          const uint32_t v[8] = {xa[nt][0].x, xa[nt][0].y, xa[nt][0].z, xa[nt][0].w,
+                                 xa[nt][1].x, xa[nt][1].y, xa[nt][1].z, xa[nt][1].w};
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            const float lo = bf16_lo(v[m]), hi = bf16_hi(v[m]);
+            overflow |= !(fabsf(lo) <= kF16Max) || !(fabsf(hi) <= kF16Max);
+            h[m] = (uint32_t)f32_to_f16_bits(lo) | ((uint32_t)f32_to_f16_bits(hi) << 16);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(x16 + (size_t)trow[nt] * H + kk);
+          dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+          dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+        }
+      } else {
+        xa[nt][0] = xa[nt][1] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    // bf16x2 registers of the three parts, element pairs (2m, 2m+1)
+    uint32_t ah[8], am[8], al[8], bh[8], bm[8], bl[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      uint32_t h0, m0, l0, h1, m1, l1;
+      split3_bf16(wa[2 * m], h0, m0, l0);
+      split3_bf16(wa[2 * m + 1], h1, m1, l1);
+      ah[m] = h0 | (h1 << 16); am[m] = m0 | (m1 << 16); al[m] = l0 | (l1 << 16);
+      split3_bf16(wb[2 * m], h0, m0, l0);
+      split3_bf16(wb[2 * m + 1], h1, m1, l1);
+      bh[m] = h0 | (h1 << 16); bm[m] = m0 | (m1 << 16); bl[m] = l0 | (l1 << 16);
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const uint32_t xr[8] = {xa[nt][0].x, xa[nt][0].y, xa[nt][0].z, xa[nt][0].w,
+                              xa[nt][1].x, xa[nt][1].y, xa[nt][1].z, xa[nt][1].w};
+#pragma unroll
+      for (int st = 0; st < 4; ++st) {
+        const uint32_t b[2] = {xr[2 * st], xr[2 * st + 1]};
+        const uint32_t A0[4] = {al[2 * st], bl[2 * st], al[2 * st + 1], bl[2 * st + 1]};
+        const uint32_t A1[4] = {am[2 * st], bm[2 * st], am[2 * st + 1], bm[2 * st + 1]};
+        const uint32_t A2[4] = {ah[2 * st], bh[2 * st], ah[2 * st + 1], bh[2 * st + 1]};
+        mma_bf16_16x8x16(acc[nt], A0, b);  // smallest part first
+        mma_bf16_16x8x16(acc[nt], A1, b);
+        mma_bf16_16x8x16(acc[nt], A2, b);
       }
     }
   }
+  if (overflow) raise_status(status, MOE_DEV_FP16_RANGE);
 #pragma unroll
-  for (int t = 0; t < kRouteTok; ++t) {
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
-  }
-  if (lane == 0) {
-    const float b = bias ? bias[e] : 0.f;
+    for (int q = 0; q < 4; ++q) red[warp][nt][q][lane] = acc[nt][q];
+  __syncthreads();
+  for (int o = tid; o < NT * 128; o += kRouteWarps * 32) {
+    const int nt = o >> 7, q = (o >> 5) & 3, L = o & 31;
+    float v = 0.f;
 #pragma unroll
-    for (int t = 0; t < kRouteTok; ++t)
-      if (t < nt) logits[(size_t)(t0 + t) * E + e] = acc[t] + b;
+    for (int w = 0; w < kRouteWarps; ++w) v += red[w][nt][q][L];
+    const int e = e0 + (L >> 2) + 8 * (q >> 1);
+    const int t = t0 + nt * 8 + 2 * (L & 3) + (q & 1);
+    if (e < E && t < T) part[((size_t)blockIdx.y * T + t) * E + e] = v;
   }
 }
 
 // ---------------------------------------------------------------------------
-// top-k + renormalisation: one warp per token, EPL logits per lane
+// top-k + renormalisation of one token by one warp: EPL logits per lane.
+// Lane j < k ends up holding slot j (expert index and weight).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
 template <int EPL>
-__global__ void __launch_bounds__(256)
-k_router_topk(const float* __restrict__ logits, int T, int E, int k,
-              int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const float* lrow = logits + (size_t)t * E;
+__device__ __forceinline__ void warp_topk(const float* __restrict__ part, int KS,
+                                          const float* __restrict__ bias, int T, int E, int k,
+                                          int t, int lane, int& my_idx, float& my_w) {
   float v[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = lane + 32 * i;
-    v[i] = e < E ? lrow[e] : -INFINITY;
+    if (e < E) {
+      float l = 0.f;
+      for (int ks = 0; ks < KS; ++ks) l += part[((size_t)ks * T + t) * E + e];
+      v[i] = bias ? l + bias[e] : l;
+    } else {
+      v[i] = -INFINITY;
+    }
   }
   uint32_t taken = 0;
   float my_val = -INFINITY;
-  int my_idx = 0;
+  my_idx = 0;
   for (int j = 0; j < k; ++j) {
-    // best not-yet-taken candidate of this lane
     float bv = -INFINITY;
     int bi = 0x7fffffff;
 #pragma unroll
@@ -111,33 +189,247 @@ k_router_topk(const float* __restrict__ logits, int T, int E, int k,
   float s = ex;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  my_w = ex / s;
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(256)
+k_router_topk(const float* __restrict__ part, int KS, const float* __restrict__ bias, int T,
+              int E, int k, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+  griddep_wait();
+  griddep_trigger();
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  int idx;
+  float w;
+  warp_topk<EPL>(part, KS, bias, T, E, k, t, lane, idx, w);
   if (lane < k) {
-    topk_idx[(size_t)t * k + lane] = my_idx;
-    topk_w[(size_t)t * k + lane] = ex / s;
+    topk_idx[(size_t)t * k + lane] = idx;
+    topk_w[(size_t)t * k + lane] = w;
   }
 }
 
+// ---------------------------------------------------------------------------
+// Small batches: top-k and the whole permutation in ONE CTA of 1024 threads
+// (T*k <= kSmallPairs, E <= 1024), replacing four launches.  Same results as
+// k_router_topk followed by the three permutation kernels: pairs are ranked
+// inside each expert in ascending pair index q = t*k + j (ascending t).
+//   1. warp per token: top-k, written to global and to shared memory;
+//   2. per-expert counts (order-free shared atomics), exclusive scan ->
+//      expert_off and the active-expert list;
+//   3. rounds of 1024 pairs: warp match ranks, per-warp counts, prefix over
+//      warps, row = off[e] + pairs of e in earlier rounds + prefix + rank.
+// Also writes the shared expert's identity permutation when asked, and
+// row_pair[row] = q (the pair of each permuted row).
+// ---------------------------------------------------------------------------
+constexpr int kSmallPairs = 4096;
+
+size_t small_route_smem(int E) {
+  return sizeof(int32_t) * (kSmallPairs + 3 * 1024 + 1 + 64) + sizeof(uint16_t) * 32 * (size_t)E;
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(1024)
+k_topk_permute_small(const float* __restrict__ part, int KS, const float* __restrict__ bias,
+                     int T, int E, int k, int32_t* __restrict__ topk_idx,
+                     float* __restrict__ topk_w, int32_t* __restrict__ expert_off,
+                     int32_t* __restrict__ row_token, int32_t* __restrict__ tok_slot_row,
+                     int32_t* __restrict__ row_pair, int32_t* __restrict__ active,
+                     int32_t* __restrict__ sh_off, int32_t* __restrict__ sh_rows,
+                     int32_t* __restrict__ sh_active) {
+  extern __shared__ int32_t sm[];
+  int32_t* s_idx = sm;                   // [kSmallPairs] expert of pair q
+  int32_t* s_cnt = s_idx + kSmallPairs;  // [1024] counts, then rows taken so far
+  int32_t* s_tot = s_cnt + 1024;         // [1024] this round's count per expert
+  int32_t* s_off = s_tot + 1024;         // [1025] expert offsets
+  int32_t* s_wsum = s_off + 1025;        // [32]
+  int32_t* s_wact = s_wsum + 32;         // [32]
+  uint16_t* s_cw = reinterpret_cast<uint16_t*>(s_wact + 32);  // [32][E] per-warp counts
+  griddep_wait();
+  griddep_trigger();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int P = T * k;
+
+  // 1. top-k
+  for (int t = warp; t < T; t += 32) {
+    int idx;
+    float w;
+    warp_topk<EPL>(part, KS, bias, T, E, k, t, lane, idx, w);
+    if (lane < k) {
+      topk_idx[(size_t)t * k + lane] = idx;
+      topk_w[(size_t)t * k + lane] = w;
+      s_idx[t * k + lane] = idx;
+    }
+  }
+  s_cnt[tid] = 0;
+  if (sh_rows) {  // shared expert: every token, in order
+    for (int t = tid; t < T; t += 1024) sh_rows[t] = t;
+    if (tid == 0) {
+      sh_off[0] = 0;
+      sh_off[1] = T;
+      sh_active[0] = T > 0 ? 1 : 0;
+      sh_active[1] = 0;
+    }
+  }
+  __syncthreads();
+  // 2. counts, offsets, active list
+  for (int q = tid; q < P; q += 1024) atomicAdd(&s_cnt[s_idx[q]], 1);
+  __syncthreads();
+  const int c = tid < E ? s_cnt[tid] : 0;
+  int incl = c, act = c > 0 ? 1 : 0;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    const int a = __shfl_up_sync(0xffffffffu, act, o);
+    if (lane >= o) {
+      incl += v;
+      act += a;
+    }
+  }
+  if (lane == 31) {
+    s_wsum[warp] = incl;
+    s_wact[warp] = act;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int s = s_wsum[lane], a = s_wact[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, s, o);
+      const int w = __shfl_up_sync(0xffffffffu, a, o);
+      if (lane >= o) {
+        s += v;
+        a += w;
+      }
+    }
+    s_wsum[lane] = s;
+    s_wact[lane] = a;
+  }
+  __syncthreads();
+  {
+    const int before = warp ? s_wsum[warp - 1] : 0;
+    const int before_a = warp ? s_wact[warp - 1] : 0;
+    if (tid < E) {
+      const int o = before + incl - c;
+      s_off[tid] = o;
+      expert_off[tid] = o;
+      if (c > 0) active[1 + before_a + act - 1] = tid;
+    }
+    if (tid == E - 1) {
+      s_off[E] = before + incl;
+      expert_off[E] = before + incl;
+      active[0] = before_a + act;
+    }
+  }
+  __syncthreads();
+  s_cnt[tid] = 0;  // rows of each expert placed by earlier rounds
+  // 3. rank rounds of 1024 pairs
+  for (int r0 = 0; r0 < P; r0 += 1024) {
+    const int q = r0 + tid;
+    const int e = q < P ? s_idx[q] : -1;
+    for (int i = tid; i < 32 * E; i += 1024) s_cw[i] = 0;
+    __syncthreads();
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    const int rank_w = __popc(peers & ((1u << lane) - 1u));
+    if (e >= 0 && rank_w == 0) s_cw[warp * E + e] = (uint16_t)__popc(peers);
+    __syncthreads();
+    for (int x = tid; x < E; x += 1024) {  // exclusive prefix over the 32 warps
+      int run = 0;
+      for (int w = 0; w < 32; ++w) {
+        const int cw = s_cw[w * E + x];
+        s_cw[w * E + x] = (uint16_t)run;
+        run += cw;
+      }
+      s_tot[x] = run;
+    }
+    __syncthreads();
+    if (e >= 0) {
+      const int row = s_off[e] + s_cnt[e] + s_cw[warp * E + e] + rank_w;
+      row_token[row] = q / k;
+      tok_slot_row[q] = row;
+      if (row_pair) row_pair[row] = q;
+    }
+    __syncthreads();
+    for (int x = tid; x < E; x += 1024) s_cnt[x] += s_tot[x];
+    __syncthreads();
+  }
+}
+
+int route_kslices(int T, int H) {
+  // Split K across CTAs when few tokens leave too few CTAs to stream Wr.
+  int ks = T <= 64 ? 4 : 1;
+  while (ks > 1 && (H / ks) % 64 != 0) ks >>= 1;
+  return ks;
+}
+
+cudaError_t launch_router_logits(const uint16_t* x, const float* Wr, int T, int H, int E,
+                                 float* part, uint16_t* x16, int32_t* status, cudaStream_t s,
+                                 bool pdl) {
+  const int KS = route_kslices(T, H);
+  const int kslice = H / KS;
+  const dim3 blk(kRouteWarps * 32);
+  if (T <= 8)
+    return launch_k(k_router_mma<1>, dim3(cdiv(E, 16), KS, cdiv(T, 8)), blk, 0, s, pdl, x, Wr,
+                    T, H, E, kslice, part, x16, status);
+  if (T <= 64)
+    return launch_k(k_router_mma<2>, dim3(cdiv(E, 16), KS, cdiv(T, 16)), blk, 0, s, pdl, x, Wr,
+                    T, H, E, kslice, part, x16, status);
+  return launch_k(k_router_mma<4>, dim3(cdiv(E, 16), KS, cdiv(T, 32)), blk, 0, s, pdl, x, Wr,
+                  T, H, E, kslice, part, x16, status);
+}
+
 cudaError_t launch_route(const uint16_t* x, const float* Wr, const float* bias, int T, int H,
-                         int E, int k, float* logits, int32_t* topk_idx, float* topk_w,
-                         int32_t* status, cudaStream_t s) {
+                         int E, int k, float* part, int32_t* topk_idx, float* topk_w,
+                         uint16_t* x16, int32_t* status, cudaStream_t s, bool pdl) {
   if (T == 0) return cudaSuccess;
-  dim3 g1(cdiv(E, kRouteWarps), cdiv(T, kRouteTok));
-  k_router_logits<<<g1, kRouteWarps * 32, 0, s>>>(x, Wr, bias, T, H, E, logits, status);
-  const int g2 = cdiv(T, 8);
+  cudaError_t err = launch_router_logits(x, Wr, T, H, E, part, x16, status, s, pdl);
+  if (err != cudaSuccess) return err;
+  const int KS = route_kslices(T, H);
   const int epl = cdiv(E, 32);
-  if (epl <= 1)
-    k_router_topk<1><<<g2, 256, 0, s>>>(logits, T, E, k, topk_idx, topk_w);
-  else if (epl <= 2)
-    k_router_topk<2><<<g2, 256, 0, s>>>(logits, T, E, k, topk_idx, topk_w);
-  else if (epl <= 4)
-    k_router_topk<4><<<g2, 256, 0, s>>>(logits, T, E, k, topk_idx, topk_w);
-  else if (epl <= 8)
-    k_router_topk<8><<<g2, 256, 0, s>>>(logits, T, E, k, topk_idx, topk_w);
-  else if (epl <= 16)
-    k_router_topk<16><<<g2, 256, 0, s>>>(logits, T, E, k, topk_idx, topk_w);
-  else
-    k_router_topk<32><<<g2, 256, 0, s>>>(logits, T, E, k, topk_idx, topk_w);
-  return cudaGetLastError();
+  const dim3 g2(cdiv(T, 8)), blk(256);
+#define MOE_TOPK(EPLV) \
+  launch_k(k_router_topk<EPLV>, g2, blk, 0, s, pdl, part, KS, bias, T, E, k, topk_idx, topk_w)
+  if (epl <= 1) return MOE_TOPK(1);
+  if (epl <= 2) return MOE_TOPK(2);
+  if (epl <= 4) return MOE_TOPK(4);
+  if (epl <= 8) return MOE_TOPK(8);
+  if (epl <= 16) return MOE_TOPK(16);
+  return MOE_TOPK(32);
+#undef MOE_TOPK
+}
+
+bool small_route_permute_ok(int T, int E, int k) {
+  return (long long)T * k <= kSmallPairs && E <= 1024;
+}
+
+cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const float* bias,
+                                       int T, int H, int E, int k, float* part,
+                                       int32_t* topk_idx, float* topk_w, int32_t* expert_off,
+                                       int32_t* row_token, int32_t* tok_slot_row,
+                                       int32_t* row_pair, int32_t* active, int32_t* sh_off,
+                                       int32_t* sh_rows, int32_t* sh_active, uint16_t* x16,
+                                       int32_t* status, cudaStream_t s, bool pdl) {
+  cudaError_t err = launch_router_logits(x, Wr, T, H, E, part, x16, status, s, pdl);
+  if (err != cudaSuccess) return err;
+  const int KS = route_kslices(T, H);
+  const size_t smem = small_route_smem(E);
+  const int epl = cdiv(E, 32);
+#define MOE_SMALL(EPLV)                                                                      \
+  do {                                                                                       \
+    err = ensure_smem((const void*)k_topk_permute_small<EPLV>, (int)small_route_smem(1024)); \
+    if (err != cudaSuccess) return err;                                                      \
+    return launch_k(k_topk_permute_small<EPLV>, dim3(1), dim3(1024), smem, s, pdl, part, KS, \
+                    bias, T, E, k, topk_idx, topk_w, expert_off, row_token, tok_slot_row,    \
+                    row_pair, active, sh_off, sh_rows, sh_active);                           \
+  } while (0)
+  if (epl <= 1) MOE_SMALL(1);
+  if (epl <= 2) MOE_SMALL(2);
+  if (epl <= 4) MOE_SMALL(4);
+  if (epl <= 8) MOE_SMALL(8);
+  if (epl <= 16) MOE_SMALL(16);
+  MOE_SMALL(32);
+#undef MOE_SMALL
 }
 
 }  // namespace moe
