@@ -16,16 +16,31 @@ k_combine(const float* __restrict__ y_perm, const int32_t* __restrict__ tok_slot
   const int t = (int)(i / H4), h = (int)(i % H4) * 4;
   float4 acc = shared_y ? __ldg(reinterpret_cast<const float4*>(shared_y + (size_t)t * H + h))
                         : make_float4(0.f, 0.f, 0.f, 0.f);
+  // Slots in groups of 8: row indices and weights first, then the 8 row
+  // gathers, so the loads of a group are in flight together.
   float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = 0; j < k; ++j) {
-    const int row = tok_slot_row[(size_t)t * k + j];
-    if (row < 0) continue;
-    const float w = topk_w[(size_t)t * k + j];
-    const float4 y = __ldg(reinterpret_cast<const float4*>(y_perm + (size_t)row * H + h));
-    r.x = fmaf(w, y.x, r.x);
-    r.y = fmaf(w, y.y, r.y);
-    r.z = fmaf(w, y.z, r.z);
-    r.w = fmaf(w, y.w, r.w);
+  for (int j0 = 0; j0 < k; j0 += 8) {
+    int row[8];
+    float w[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = j0 + u;
+      row[u] = j < k ? tok_slot_row[(size_t)t * k + j] : -1;
+      w[u] = j < k ? topk_w[(size_t)t * k + j] : 0.f;
+    }
+    float4 y[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      y[u] = row[u] >= 0 ? __ldg(reinterpret_cast<const float4*>(y_perm + (size_t)row[u] * H + h))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (row[u] < 0) continue;
+      r.x = fmaf(w[u], y[u].x, r.x);
+      r.y = fmaf(w[u], y[u].y, r.y);
+      r.z = fmaf(w[u], y[u].z, r.z);
+      r.w = fmaf(w[u], y[u].w, r.w);
+    }
   }
   acc.x += r.x;
   acc.y += r.y;

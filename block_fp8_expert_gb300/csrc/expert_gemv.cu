@@ -310,10 +310,11 @@ cudaError_t launch_expert_gemv(const uint16_t* x16, const int32_t* expert_off,
                                uint16_t* hid, float* y, int32_t* status, cudaStream_t s,
                                bool pdl) {
   if (max_active <= 0) return cudaSuccess;
+  cudaError_t e;
+  const bool nt1 = tokens_per_expert_hint <= 8;
   const dim3 block(kThreads);
   const dim3 g1(I / 16, max_active), g2(H / 32, max_active);
-  cudaError_t e;
-  if (tokens_per_expert_hint <= 8) {
+  if (nt1) {
     if ((e = ensure_smem((const void*)k_gateup_stream<1>, kGuSmem)) != cudaSuccess) return e;
     if ((e = ensure_smem((const void*)k_down_stream<1>, kDnSmem)) != cudaSuccess) return e;
     e = launch_k(k_gateup_stream<1>, g1, block, kGuSmem, s, pdl, x16, H, I, expert_off,

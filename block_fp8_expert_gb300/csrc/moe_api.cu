@@ -3,6 +3,7 @@
 // moe_read_device_status, whose job is to read a device word back.
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <set>
@@ -102,6 +103,18 @@ T* at(void* ws, size_t off) {
 
 void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
 
+// Average tokens per expert from which the tensor-core GEMM replaces the
+// streamed GEMV.
+constexpr int kGemmMinRowsPerExpert = 32;
+
+bool use_expert_gemm(int rows, int experts, int H, int I) {
+  if (!expert_gemm_tc_ok(H, I)) return false;
+  const char* f = getenv("MOE_FP8_EXPERT_PATH");
+  if (f && strcmp(f, "gemm") == 0) return true;
+  if (f && strcmp(f, "gemv") == 0) return false;
+  return rows >= kGemmMinRowsPerExpert * experts;
+}
+
 cudaError_t ensure_smem(const void* func, int bytes) {
   static std::mutex mu;
   static std::set<std::pair<int, const void*>> done;
@@ -145,6 +158,8 @@ WsLayout ws_layout(const moe_dims& d) {
   L.sh_off = take(2 * 4);
   L.sh_rows = take(Is ? T * 4 : 0);
   L.sh_active = take(2 * 4);
+  L.tile_off = take((E + 1) * 4);
+  L.sh_tile_off = take(2 * 4);
   L.total = o;
   return L;
 }
@@ -265,10 +280,16 @@ moe_status moe_expert_ffn_fp8(const uint16_t* x, const int32_t* expert_off,
   CUDA_CHECK(launch_x_to_f16(x, (long long)d.T * d.H, x16, status, st, true),
              "moe_expert_ffn_fp8");
   const int P = d.T * d.k;
-  CUDA_CHECK(launch_expert_gemv(x16, expert_off, row_token, active, d.E < P ? d.E : P, w, d.H,
-                                d.I, cdiv(P, d.E), at<uint16_t>(ws, L.hid), y_perm, status, st,
-                                true),
-             "moe_expert_ffn_fp8");
+  if (use_expert_gemm(P, d.E, d.H, d.I))
+    CUDA_CHECK(launch_expert_gemm_tc(x16, expert_off, row_token, d.E, P, w, d.H, d.I,
+                                     at<int32_t>(ws, L.tile_off), at<uint16_t>(ws, L.hid), y_perm,
+                                     status, st, true),
+               "moe_expert_ffn_fp8");
+  else
+    CUDA_CHECK(launch_expert_gemv(x16, expert_off, row_token, active, d.E < P ? d.E : P, w, d.H,
+                                  d.I, cdiv(P, d.E), at<uint16_t>(ws, L.hid), y_perm, status, st,
+                                  true),
+               "moe_expert_ffn_fp8");
   return MOE_OK;
 }
 
@@ -348,15 +369,28 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
       CUDA_CHECK(launch_identity_perm(d.T, soff, srows, sact, st, true),
                  "moe_layer_forward: shared");
   }
-  CUDA_CHECK(launch_expert_gemv(x16, off, row_token, active, d.E < P ? d.E : P, routed, d.H, d.I,
-                                cdiv(P, d.E), at<uint16_t>(ws, L.hid), y_perm, status, st, true),
-             "moe_layer_forward: experts");
+  if (use_expert_gemm(P, d.E, d.H, d.I))
+    CUDA_CHECK(launch_expert_gemm_tc(x16, off, row_token, d.E, P, routed, d.H, d.I,
+                                     at<int32_t>(ws, L.tile_off), at<uint16_t>(ws, L.hid), y_perm,
+                                     status, st, true),
+               "moe_layer_forward: experts");
+  else
+    CUDA_CHECK(launch_expert_gemv(x16, off, row_token, active, d.E < P ? d.E : P, routed, d.H,
+                                  d.I, cdiv(P, d.E), at<uint16_t>(ws, L.hid), y_perm, status, st,
+                                  true),
+               "moe_layer_forward: experts");
   float* shared_y = nullptr;
   if (has_shared) {
     shared_y = at<float>(ws, L.sh_y);
-    CUDA_CHECK(launch_expert_gemv(x16, soff, srows, sact, 1, *shared, d.H, d.I_shared, d.T,
-                                  at<uint16_t>(ws, L.sh_hid), shared_y, status, st, true),
-               "moe_layer_forward: shared expert");
+    if (use_expert_gemm(d.T, 1, d.H, d.I_shared))
+      CUDA_CHECK(launch_expert_gemm_tc(x16, soff, srows, 1, d.T, *shared, d.H, d.I_shared,
+                                       at<int32_t>(ws, L.sh_tile_off), at<uint16_t>(ws, L.sh_hid),
+                                       shared_y, status, st, true),
+                 "moe_layer_forward: shared expert");
+    else
+      CUDA_CHECK(launch_expert_gemv(x16, soff, srows, sact, 1, *shared, d.H, d.I_shared, d.T,
+                                    at<uint16_t>(ws, L.sh_hid), shared_y, status, st, true),
+                 "moe_layer_forward: shared expert");
   }
   CUDA_CHECK(launch_combine(y_perm, tok_slot_row, w, shared_y, d.T, d.H, d.k, out, st, true),
              "moe_layer_forward: combine");

@@ -43,7 +43,8 @@ cudaError_t ensure_smem(const void* func, int bytes);
 // Workspace layout for one set of dims (byte offsets, each 256-aligned).
 struct WsLayout {
   size_t status, logits, rank, block_cnt, block_base, active, idx, w, off, row_token,
-      tok_slot_row, row_pair, x16, hid, y_perm, sh_hid, sh_y, sh_off, sh_rows, sh_active, total;
+      tok_slot_row, row_pair, x16, hid, y_perm, sh_hid, sh_y, sh_off, sh_rows, sh_active,
+      tile_off, sh_tile_off, total;
 };
 WsLayout ws_layout(const moe_dims& d);
 
@@ -88,6 +89,20 @@ cudaError_t launch_expert_gemv(const uint16_t* x16, const int32_t* expert_off,
                                const moe_fp8_ffn& w, int H, int I, int tokens_per_expert_hint,
                                uint16_t* hid, float* y, int32_t* status, cudaStream_t s,
                                bool pdl);
+
+// Grouped GEMM on the tensor cores (tcgen05) for many tokens per expert:
+// gate/up + SwiGLU -> hid, then down -> y.  Needs H % 256 == 0 and
+// I % 128 == 0 (expert_gemm_tc_ok).  tile_off: E + 1 ints of scratch.
+bool expert_gemm_tc_ok(int H, int I);
+cudaError_t launch_expert_gemm_tc(const uint16_t* x16, const int32_t* expert_off,
+                                  const int32_t* row_token, int E, int P, const moe_fp8_ffn& w,
+                                  int H, int I, int32_t* tile_off, uint16_t* hid, float* y,
+                                  int32_t* status, cudaStream_t s, bool pdl);
+
+// Regime: true -> tensor-core grouped GEMM, false -> streamed grouped GEMV.
+// Decided on the host from shapes only; MOE_FP8_EXPERT_PATH=gemm|gemv in the
+// environment overrides it (when the GEMM supports the shapes).
+bool use_expert_gemm(int rows, int experts, int H, int I);
 
 cudaError_t launch_combine(const float* y_perm, const int32_t* tok_slot_row, const float* topk_w,
                            const float* shared_y, int T, int H, int k, uint16_t* out,

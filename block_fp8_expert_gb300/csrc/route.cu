@@ -19,6 +19,7 @@ namespace moe {
 // expert kernels use, and flag values beyond fp16 range.
 // ---------------------------------------------------------------------------
 constexpr int kRouteWarps = 4;
+constexpr int kMaxKSlices = 4;  // K-slices of the router logits (route_kslices)
 
 template <int NT>
 __global__ void __launch_bounds__(kRouteWarps * 32)
@@ -143,17 +144,28 @@ template <int EPL>
 __device__ __forceinline__ void warp_topk(const float* __restrict__ part, int KS,
                                           const float* __restrict__ bias, int T, int E, int k,
                                           int t, int lane, int& my_idx, float& my_w) {
+  // All partial logits of this lane first (independent loads), then the sums
+  // in slice order.
   float v[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) v[i] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < kMaxKSlices; ++ks) {
+    if (ks < KS) {
+      float p[EPL];
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        p[i] = e < E ? part[((size_t)ks * T + t) * E + e] : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) v[i] += p[i];
+    }
+  }
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = lane + 32 * i;
-    if (e < E) {
-      float l = 0.f;
-      for (int ks = 0; ks < KS; ++ks) l += part[((size_t)ks * T + t) * E + e];
-      v[i] = bias ? l + bias[e] : l;
-    } else {
-      v[i] = -INFINITY;
-    }
+    v[i] = e < E ? (bias ? v[i] + bias[e] : v[i]) : -INFINITY;
   }
   uint32_t taken = 0;
   float my_val = -INFINITY;
