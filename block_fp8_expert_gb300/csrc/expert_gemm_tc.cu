@@ -2,24 +2,32 @@
 // the 5th-generation tensor cores (colizig README, "Features": block-FP8
 // weights; "MoE per-expert evaluation").
 //
-// One CTA computes one 128 x 256 output tile of one expert:
+// Output tiles are 128 rows x 256 columns of one expert:
 //   gate/up: rows = 128 permuted token rows of the expert, columns = 128 gate
 //            features and the same 128 up features (one 128-row scale block
-//            each), K = H; the epilogue forms hid = silu(g) * u in fp16.
+//            each), K = H; the epilogue writes hid = silu(g) * u in fp16.
 //   down:    rows = 128 permuted rows, columns = 256 output features, K = I;
 //            the epilogue writes y in fp32.
-// Operands (fp16, K-major, 128-byte swizzle) live in shared memory, the fp32
-// accumulator in TMEM (256 columns).  Per 64-wide K step:
-//   - cp.async brings the step's activation rows (gathered by token for
-//     gate/up, contiguous for down; rows past the expert's segment are
-//     zero-filled) and the E4M3 code tile (256 rows x 64 bytes) into a 4-deep
-//     ring, two steps ahead;
-//   - all 8 warps decode the codes to fp16 and apply the block scale
-//     (fp16(dec * fp16(scale))), writing the swizzled B tile (double buffer);
-//   - thread 0 issues four tcgen05.mma (M=128, N=256, K=16) and commits to an
-//     mbarrier; the MMA of step k runs while the warps decode step k+1.
-// Precision: the same fp16 operands and fp32 accumulation as the GEMV path's
-// down projection; x16 (fp16 x) comes from the router.
+// Operands are fp16, K-major, 128-byte swizzled in shared memory; the fp32
+// accumulator lives in TMEM.  Persistent CTAs (one per SM) walk the tiles with
+// warp-specialised roles that hand work to each other through mbarriers:
+//   warp 0      TMA: the E4M3 code tile of each 64-wide K step (2-D tensor
+//               maps over the stacked code matrices) into a 4-deep ring;
+//   warps 1-2   gather the step's activation rows with cp.async (rows past the
+//               expert's segment are zero-filled) into a 4-deep ring;
+//   warps 3-10  decode codes to fp16 times the block scale
+//               (fp16(dec * fp16(scale))) into a double-buffered B tile;
+//   warp 11     one thread issues tcgen05.mma (M=128, N=256, K=16) into one of
+//               two TMEM accumulators (512 columns) and commits to mbarriers;
+//   warps 12-15 epilogue: tcgen05.ld from the finished accumulator while the
+//               next tile accumulates in the other one.
+// Every wait is bounded (about 2 s) and also gives up as soon as another
+// role has given up, recording MOE_DEV_WAIT_TIMEOUT; the CTA then drains its
+// copies and MMAs and frees its TMEM before it exits.
+#include <cuda.h>
+
+#include <mutex>
+
 #include "moe_internal.h"
 #include "tcgen05.cuh"
 
@@ -27,244 +35,387 @@ namespace moe {
 
 namespace {
 constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int kThreadsTC = 256;
-constexpr int NA = 4;  // activation / code ring depth
-constexpr int DIST = 2;  // prefetch distance (steps ahead), <= NA - 2
-constexpr int A_BYTES = BM * BK * 2;   // 16 KB
-constexpr int B8_BYTES = BN * BK;      // 16 KB
-constexpr int B16_BYTES = BN * BK * 2; // 32 KB
+constexpr int NA = 4, NB = 4, NC = 2;  // ring depths: activations, codes, fp16 B tiles
+constexpr int A_BYTES = BM * BK * 2;    // 16 KB
+constexpr int B8_BYTES = BN * BK;       // 16 KB
+constexpr int B16_BYTES = BN * BK * 2;  // 32 KB
 constexpr int OFF_A = 0;
 constexpr int OFF_B8 = OFF_A + NA * A_BYTES;
-constexpr int OFF_B16 = OFF_B8 + NA * B8_BYTES;
-constexpr int SMEM_TC = OFF_B16 + 2 * B16_BYTES + 1024;  // + alignment slack
-constexpr uint32_t TMEM_COLS = 256;
+constexpr int OFF_B16 = OFF_B8 + NB * B8_BYTES;
+constexpr int SMEM_WS = OFF_B16 + NC * B16_BYTES + 1024;  // + alignment slack
+constexpr int kWarps = 16;
+constexpr int kThreadsWS = kWarps * 32;
+constexpr int kLoadWarps = 2, kDecWarps = 8;
+constexpr int W_TMA = 0, W_LOAD0 = 1, W_DEC0 = 3, W_MMA = 11;  // warps 12-15: epilogue
+constexpr int kLoadThreads = kLoadWarps * 32, kDecThreads = kDecWarps * 32;
+constexpr uint32_t TMEM_COLS = 512;  // two 256-column accumulators
+
+struct GemmArgs {
+  const uint16_t* asrc;  // gate/up: x16 [T, K]; down: hid [P, K]
+  int K;                 // H for gate/up, I for down
+  int rows_per_expert;   // I for gate/up, H for down
+  const int32_t* expert_off;
+  const int32_t* row_token;
+  const int32_t* tile_off;  // m-tile prefix per expert, [E + 1]
+  int E;
+  const float* s0;  // gate (or down) scales
+  const float* s1;  // up scales (gate/up only)
+  void* out;        // hid fp16 [P, I] or y fp32 [P, H]
+  int out_ld;
+  int n_ntiles;  // column tiles per expert
+  int32_t* status;
+};
+
+struct WsShared {
+  uint64_t b8_full[NB], b8_empty[NB];
+  uint64_t a_full[NA], a_empty[NA];
+  uint64_t b16_full[NC], b16_empty[NC];
+  uint64_t acc_full[2], acc_empty[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Bounded wait that also returns (false) once another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const WaitBudget b = wait_budget();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (budget_spent(b)) return false;
+  }
+}
+
+// One warp waits (lane 0, bounded + abort-aware), then every lane observes
+// the completed phase itself.  Returns the same verdict in all lanes.  The
+// first wait in the grid that runs out records where: status[1] = warp,
+// status[2] = barrier id, status[3] = step, status[4] = parity.
+__device__ __forceinline__ bool warp_wait(WsShared& sh, uint64_t* bar, uint32_t parity,
+                                          int32_t* status, int bar_id = 0, int step = 0) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) {
+    ok = wait_or_abort(bar, parity, &sh.abort_flag);
+    if (!ok && !sh.abort_flag) {
+      sh.abort_flag = 1;
+      raise_status(status, MOE_DEV_WAIT_TIMEOUT);
+      if (status && atomicCAS(status + 1, 0, 1 + (int)(threadIdx.x >> 5)) == 0) {
+        status[2] = bar_id;
+        status[3] = step;
+        status[4] = (int)parity;
+        status[5] = (int)blockIdx.x;
+      }
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) mbar_wait(bar, parity);  // already complete: acquire for this lane
+  return ok;
+}
+
+struct TileInfo {
+  int e, r0, mrows, m0, n0;
+};
+
+__device__ __forceinline__ TileInfo tile_info(const GemmArgs& a, int t, bool gateup) {
+  TileInfo ti;
+  const int slot = t / a.n_ntiles, nt = t % a.n_ntiles;
+  int lo = 0, hi = a.E;  // largest e with tile_off[e] <= slot
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (a.tile_off[mid] <= slot) lo = mid; else hi = mid;
+  }
+  ti.e = lo;
+  ti.r0 = a.expert_off[lo];
+  ti.m0 = (slot - a.tile_off[lo]) * BM;
+  ti.mrows = min(BM, a.expert_off[lo + 1] - ti.r0 - ti.m0);
+  ti.n0 = nt * (gateup ? BN / 2 : BN);
+  return ti;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar))
+               : "memory");
+}
 }  // namespace
 
 template <bool GATEUP>
-__global__ void __launch_bounds__(kThreadsTC, 1)
-k_expert_gemm_tc(const uint16_t* __restrict__ asrc, int K, int rows_per_expert,
-                 const int32_t* __restrict__ expert_off, const int32_t* __restrict__ row_token,
-                 const int32_t* __restrict__ tile_off, int E,
-                 const uint8_t* __restrict__ w0, const float* __restrict__ s0,
-                 const uint8_t* __restrict__ w1, const float* __restrict__ s1,
-                 void* __restrict__ out, int out_ld, int32_t* __restrict__ status) {
+__global__ void __launch_bounds__(kThreadsWS, 1)
+k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
+                 const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t mma_bar[2];
-  __shared__ uint32_t tmem_base_sh;
-  __shared__ int row_src[BM];  // gate/up: token of each tile row; down: hid row (-1: none)
-  __shared__ int abort_sh;
+  __shared__ WsShared sh;
   griddep_wait();
   griddep_trigger();
-
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // ---- which tile
-  const int slot = blockIdx.y;
-  const int total = tile_off[E];
-  if (slot >= total) return;
-  int lo = 0, hi = E;  // largest e with tile_off[e] <= slot
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (tile_off[mid] <= slot) lo = mid; else hi = mid;
-  }
-  const int e = lo;
-  const int r0 = expert_off[e];
-  const int cnt = expert_off[e + 1] - r0;
-  const int m0 = (slot - tile_off[e]) * BM;
-  const int mrows = min(BM, cnt - m0);
-  const int n0 = blockIdx.x * (GATEUP ? BN / 2 : BN);  // first feature (gate/up) or h
-  const int nKb = cdiv(K, kScaleBlock);
-  const int nRb = cdiv(rows_per_expert, kScaleBlock);
+  const GemmArgs& a = args;
+  const int n_tiles = a.tile_off[a.E] * a.n_ntiles;
+  if ((int)blockIdx.x >= n_tiles) return;  // uniform per CTA, before any barrier
+  const int nK = a.K / BK;
+  const int nKb = cdiv(a.K, kScaleBlock);
+  const int nRb = cdiv(a.rows_per_expert, kScaleBlock);
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t smem_base = smem_u32(smem);
 
-  if (tid < BM) {
-    const int m = tid;
-    row_src[m] = m < mrows ? (GATEUP ? row_token[r0 + m0 + m] : r0 + m0 + m) : -1;
-  }
   if (tid == 0) {
-    mbar_init(&mma_bar[0], 1);
-    mbar_init(&mma_bar[1], 1);
-    abort_sh = 0;
+    for (int s = 0; s < NB; ++s) {
+      mbar_init(&sh.b8_full[s], 1);
+      mbar_init(&sh.b8_empty[s], kDecWarps);
+    }
+    for (int s = 0; s < NA; ++s) {
+      mbar_init(&sh.a_full[s], kLoadThreads);
+      mbar_init(&sh.a_empty[s], 1);
+    }
+    for (int s = 0; s < NC; ++s) {
+      mbar_init(&sh.b16_full[s], kDecWarps);
+      mbar_init(&sh.b16_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sh.acc_full[s], 1);
+      mbar_init(&sh.acc_empty[s], 4);
+    }
+    sh.abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
-    tc::tmem_alloc(&tmem_base_sh, TMEM_COLS);
+    tc::tmem_alloc(&sh.tmem_base, TMEM_COLS);
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const uint32_t tmem = tmem_base_sh;
+  const uint32_t tmem = sh.tmem_base;
 
-  // ---- B row sources: row r of the 256-row code tile
-  auto wrow = [&](int r) -> const uint8_t* {
-    if (GATEUP) {
-      const uint8_t* base = r < 128 ? w0 : w1;
-      return base + ((size_t)e * rows_per_expert + n0 + (r & 127)) * K;
-    }
-    return w0 + ((size_t)e * rows_per_expert + n0 + r) * K;
-  };
-
-  auto load_step = [&](int step) {
-    const int k0 = step * BK;
-    const int sa = step % NA;
-    uint8_t* A = smem + OFF_A + sa * A_BYTES;
-    uint8_t* B8 = smem + OFF_B8 + sa * B8_BYTES;
-#pragma unroll
-    for (int u = 0; u < (BM * 8) / kThreadsTC; ++u) {  // 4 x 16 B of activations
-      const int q = tid + kThreadsTC * u;
-      const int m = q >> 3, j = q & 7;
-      const int src = row_src[m];
-      const uint16_t* g = asrc + (size_t)(src < 0 ? 0 : src) * K + k0 + 8 * j;
-      tc::cp_async16_zfill(A + tc::sw128_off(m, j), g, src >= 0);
-    }
-#pragma unroll
-    for (int u = 0; u < (BN * 4) / kThreadsTC; ++u) {  // 4 x 16 B of codes
-      const int q = tid + kThreadsTC * u;
-      const int r = q >> 2, j = q & 3;
-      cp_async16(B8 + r * 64 + 16 * j, wrow(r) + k0 + 16 * j);
-    }
-  };
-
-  const int nK = K / BK;
-  const uint32_t idesc = tc::idesc_f16_f32(BM, BN);
-#pragma unroll
-  for (int p = 0; p < DIST; ++p) {
-    if (p < nK) load_step(p);
-    cp_async_commit();
-  }
-
-  bool ok = true;
-  int issued = 0;  // MMA steps issued (same count in every thread)
-  for (int ks = 0; ks < nK; ++ks) {
-    cp_async_wait<DIST - 1>();  // this thread's copies of step ks have landed
-    if (tid == 0 && ks >= 2) {  // MMA(ks-2) done: its A stage and B16 buffer are free
-      if (!mbar_wait(&mma_bar[ks & 1], (uint32_t)(((ks - 2) >> 1) & 1))) {
-        abort_sh = 1;
-        raise_status(status, MOE_DEV_WAIT_TIMEOUT);
-      }
-    }
-    __syncthreads();  // all copies of step ks visible; verdict of thread 0 visible
-    if (abort_sh) {
-      ok = false;
-      break;
-    }
-    if (ks + DIST < nK) load_step(ks + DIST);
-    cp_async_commit();
-
-    // decode the code tile of step ks into the fp16 B tile
-    {
-      const int k0 = ks * BK;
-      const uint8_t* B8 = smem + OFF_B8 + (ks % NA) * B8_BYTES;
-      uint8_t* B16 = smem + OFF_B16 + (ks & 1) * B16_BYTES;
-      const int kb = k0 / kScaleBlock;
-      float sc[2];
-      if (GATEUP) {
-        const size_t srow = (size_t)e * nRb + n0 / kScaleBlock;
-        sc[0] = s0[srow * nKb + kb];
-        sc[1] = s1[srow * nKb + kb];
-      } else {
-        const size_t srow = (size_t)e * nRb + n0 / kScaleBlock;
-        sc[0] = s0[srow * nKb + kb];
-        sc[1] = s0[(srow + 1) * nKb + kb];
-      }
-      const uint32_t s2[2] = {(uint32_t)f32_to_f16_bits(sc[0]) * 0x10001u,
-                              (uint32_t)f32_to_f16_bits(sc[1]) * 0x10001u};
-#pragma unroll
-      for (int u = 0; u < (BN * 8) / kThreadsTC; ++u) {  // 8 items of 8 codes
-        const int q = tid + kThreadsTC * u;
-        const int r = q >> 3, j = q & 7;
-        const uint2 c8 = *reinterpret_cast<const uint2*>(B8 + r * 64 + 8 * j);
-        const uint32_t sv = s2[r >> 7];
-        uint32_t h[4];
-        h[0] = e4m3x2_to_f16x2(c8.x & 0xFFFFu);
-        h[1] = e4m3x2_to_f16x2(c8.x >> 16);
-        h[2] = e4m3x2_to_f16x2(c8.y & 0xFFFFu);
-        h[3] = e4m3x2_to_f16x2(c8.y >> 16);
-#pragma unroll
-        for (int v = 0; v < 4; ++v)
-          asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(h[v]) : "r"(h[v]), "r"(sv));
-        *reinterpret_cast<uint4*>(B16 + tc::sw128_off(r, j)) = make_uint4(h[0], h[1], h[2], h[3]);
-      }
-    }
-    tc::fence_proxy_async();  // decoded B tile and copied A tile -> tensor-core reads
-    __syncthreads();
-    if (tid == 0) {
-      tc::fence_after_sync();
-      const uint32_t a_addr = smem_base + OFF_A + (ks % NA) * A_BYTES;
-      const uint32_t b_addr = smem_base + OFF_B16 + (ks & 1) * B16_BYTES;
-#pragma unroll
-      for (int kk = 0; kk < BK / 16; ++kk)
-        tc::mma_f16(tmem, tc::sw128_desc(a_addr + kk * 32), tc::sw128_desc(b_addr + kk * 32),
-                    idesc, (ks > 0 || kk > 0) ? 1u : 0u);
-      tc::commit(&mma_bar[ks & 1]);
-    }
-    ++issued;
-  }
-  cp_async_wait<0>();  // no copy may still land in shared memory after this point
-
-  // ---- wait (bounded) for the newest MMA issued: commits are cumulative
-  if (tid == 0 && issued > 0) {
-    const int last = issued - 1;
-    if (!mbar_wait(&mma_bar[last & 1], (uint32_t)((last >> 1) & 1))) {
-      abort_sh = 1;
-      raise_status(status, MOE_DEV_WAIT_TIMEOUT);
-    }
-  }
-  __syncthreads();
-  tc::fence_after_sync();
-  if (ok && !abort_sh) {
-    const int quad = warp & 3, half = warp >> 2;
-    const int m = quad * 32 + lane;
-    const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
-    if (GATEUP) {
-      uint16_t* hid = reinterpret_cast<uint16_t*>(out);
-      bool overflow = false;
-#pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        const int col = half * 64 + c2 * 32;
-        uint32_t gr[32], ur[32];
-        tc::ld_32x32b_x32(tl + col, gr);
-        tc::ld_32x32b_x32(tl + 128 + col, ur);
-        tc::wait_ld();
-        if (m < mrows) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int v = 0; v < 16; ++v) {
-            const float g0 = __uint_as_float(gr[2 * v]), g1 = __uint_as_float(gr[2 * v + 1]);
-            const float u0 = __uint_as_float(ur[2 * v]), u1 = __uint_as_float(ur[2 * v + 1]);
-            const float h0 = g0 / (1.f + expf(-g0)) * u0;
-            const float h1 = g1 / (1.f + expf(-g1)) * u1;
-            overflow |= !(fabsf(h0) <= kF16Max) || !(fabsf(h1) <= kF16Max);
-            pk[v] = (uint32_t)f32_to_f16_bits(h0) | ((uint32_t)f32_to_f16_bits(h1) << 16);
+  if (warp == W_TMA) {
+    // ------------------------------------------------ E4M3 code tiles (TMA)
+    int j = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+      const TileInfo ti = tile_info(a, t, GATEUP);
+      for (int ks = 0; ks < nK; ++ks, ++j) {
+        const int sb = j % NB;
+        if (j >= NB && !warp_wait(sh, &sh.b8_empty[sb], (uint32_t)(((j / NB) - 1) & 1), a.status, 1, j)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          uint8_t* dst = smem + OFF_B8 + sb * B8_BYTES;
+          mbar_arrive_expect_tx(&sh.b8_full[sb], B8_BYTES);
+          const int row = ti.e * a.rows_per_expert + ti.n0;
+          if (GATEUP) {
+            tma_load_2d(dst, &tm0, ks * BK, row, &sh.b8_full[sb]);
+            tma_load_2d(dst + 128 * BK, &tm1, ks * BK, row, &sh.b8_full[sb]);
+          } else {
+            tma_load_2d(dst, &tm0, ks * BK, row, &sh.b8_full[sb]);
           }
-          uint4* dst = reinterpret_cast<uint4*>(hid + (size_t)(r0 + m0 + m) * out_ld + n0 + col);
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
+        __syncwarp();
       }
-      if (overflow) raise_status(status, MOE_DEV_FP16_RANGE);
-    } else {
-      float* y = reinterpret_cast<float*>(out);
+    }
+    // drain: the copies of the last NB steps issued must have landed
+    if (lane == 0)
+      for (int i = max(0, j - NB); i < j; ++i) mbar_wait(&sh.b8_full[i % NB], (uint32_t)((i / NB) & 1));
+  } else if (warp >= W_LOAD0 && warp < W_LOAD0 + kLoadWarps) {
+    // ------------------------------------------------ activation rows (cp.async)
+    constexpr int RPT = (BM * 8) / kLoadThreads;  // 16-byte chunks per thread per step
+    const int lt = tid - W_LOAD0 * 32;
+    const int jj = lt & 7, mb = lt >> 3;  // chunk in row; rows mb + (kLoadThreads/8) u
+    int j = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+      const TileInfo ti = tile_info(a, t, GATEUP);
+      int src[RPT];
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        const int col = half * 128 + c4 * 32;
-        uint32_t v[32];
-        tc::ld_32x32b_x32(tl + col, v);
-        tc::wait_ld();
-        if (m < mrows) {
-          float4* dst = reinterpret_cast<float4*>(y + (size_t)(r0 + m0 + m) * out_ld + n0 + col);
+      for (int u = 0; u < RPT; ++u) {
+        const int m = mb + (kLoadThreads / 8) * u;
+        src[u] = m < ti.mrows ? (GATEUP ? a.row_token[ti.r0 + ti.m0 + m] : ti.r0 + ti.m0 + m) : -1;
+      }
+      for (int ks = 0; ks < nK; ++ks, ++j) {
+        const int sa = j % NA;
+        if (j >= NA && !warp_wait(sh, &sh.a_empty[sa], (uint32_t)(((j / NA) - 1) & 1), a.status, 2, j)) {
+          ok = false;
+          break;
+        }
+        uint8_t* A = smem + OFF_A + sa * A_BYTES;
+        const int k0 = ks * BK;
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                 __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        for (int u = 0; u < RPT; ++u) {
+          const int m = mb + (kLoadThreads / 8) * u;
+          const uint16_t* g = a.asrc + (size_t)(src[u] < 0 ? 0 : src[u]) * a.K + k0 + 8 * jj;
+          tc::cp_async16_zfill(A + tc::sw128_off(m, jj), g, src[u] >= 0);
+        }
+        cp_async_arrive_noinc(&sh.a_full[sa]);
+      }
+    }
+    cp_async_wait<0>();
+  } else if (warp >= W_DEC0 && warp < W_DEC0 + kDecWarps) {
+    // ------------------------------------------------ decode E4M3 -> fp16
+    const int dt = tid - W_DEC0 * 32;
+    int j = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+      const TileInfo ti = tile_info(a, t, GATEUP);
+      const size_t srow = (size_t)ti.e * nRb + ti.n0 / kScaleBlock;
+      for (int ks = 0; ks < nK; ++ks, ++j) {
+        const int sb = j % NB, c = j % NC;
+        if (!warp_wait(sh, &sh.b8_full[sb], (uint32_t)((j / NB) & 1), a.status, 3, j) ||
+            (j >= NC && !warp_wait(sh, &sh.b16_empty[c], (uint32_t)(((j / NC) - 1) & 1), a.status, 4, j))) {
+          ok = false;
+          break;
+        }
+        const int kb = ks * BK / kScaleBlock;
+        const float sc0 = a.s0[srow * nKb + kb];
+        const float sc1 = GATEUP ? a.s1[srow * nKb + kb] : a.s0[(srow + 1) * nKb + kb];
+        const uint32_t s2[2] = {(uint32_t)f32_to_f16_bits(sc0) * 0x10001u,
+                                (uint32_t)f32_to_f16_bits(sc1) * 0x10001u};
+        const uint8_t* B8 = smem + OFF_B8 + sb * B8_BYTES;
+        uint8_t* B16 = smem + OFF_B16 + c * B16_BYTES;
+        constexpr int IPT = (BN * 4) / kDecThreads;  // items of 16 codes per thread
+        uint4 c16[IPT];
+#pragma unroll
+        for (int u = 0; u < IPT; ++u) {
+          const int q = dt + kDecThreads * u;
+          c16[u] = *reinterpret_cast<const uint4*>(B8 + (q >> 2) * 64 + 16 * (q & 3));
+        }
+#pragma unroll
+        for (int u = 0; u < IPT; ++u) {
+          const int q = dt + kDecThreads * u;
+          const int r = q >> 2, jp = 2 * (q & 3);
+          const uint32_t sv = s2[r >> 7];
+          const uint32_t w[4] = {c16[u].x, c16[u].y, c16[u].z, c16[u].w};
+          uint32_t h[8];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            h[2 * v] = e4m3x2_to_f16x2(w[v] & 0xFFFFu);
+            h[2 * v + 1] = e4m3x2_to_f16x2(w[v] >> 16);
+          }
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(h[v]) : "r"(h[v]), "r"(sv));
+          *reinterpret_cast<uint4*>(B16 + tc::sw128_off(r, jp)) = make_uint4(h[0], h[1], h[2], h[3]);
+          *reinterpret_cast<uint4*>(B16 + tc::sw128_off(r, jp + 1)) =
+              make_uint4(h[4], h[5], h[6], h[7]);
+        }
+        tc::fence_proxy_async();  // decoded tile -> tensor-core reads
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&sh.b16_full[c]);
+          mbar_arrive(&sh.b8_empty[sb]);
         }
       }
     }
+  } else if (warp == W_MMA) {
+    // ------------------------------------------------ tcgen05.mma issue
+    const uint32_t idesc = tc::idesc_f16_f32(BM, BN);
+    int j = 0, tl = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++tl) {
+      const int acc = tl & 1;
+      if (tl >= 2 && !warp_wait(sh, &sh.acc_empty[acc], (uint32_t)(((tl >> 1) - 1) & 1), a.status, 5, tl)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t dcol = tmem + (uint32_t)(acc * BN);
+      for (int ks = 0; ks < nK; ++ks, ++j) {
+        const int sa = j % NA, c = j % NC;
+        if (!warp_wait(sh, &sh.a_full[sa], (uint32_t)((j / NA) & 1), a.status, 6, j) ||
+            !warp_wait(sh, &sh.b16_full[c], (uint32_t)((j / NC) & 1), a.status, 7, j)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        if (lane == 0) {
+          const uint32_t a_addr = smem_base + OFF_A + sa * A_BYTES;
+          const uint32_t b_addr = smem_base + OFF_B16 + c * B16_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc::mma_f16(dcol, tc::sw128_desc(a_addr + kk * 32), tc::sw128_desc(b_addr + kk * 32),
+                        idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+          tc::commit(&sh.a_empty[sa]);
+          tc::commit(&sh.b16_empty[c]);
+          if (ks == nK - 1) tc::commit(&sh.acc_full[acc]);
+        }
+        __syncwarp();
+      }
+    }
+    // drain: every MMA issued has completed once the newest commit has
+    if (lane == 0 && j > 0) mbar_wait(&sh.a_empty[(j - 1) % NA], (uint32_t)(((j - 1) / NA) & 1));
+  } else {
+    // ------------------------------------------------ epilogue (warps 12-15)
+    const int quad = warp & 3;
+    const int m = quad * 32 + lane;
+    int tl = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tl) {
+      const int acc = tl & 1;
+      if (!warp_wait(sh, &sh.acc_full[acc], (uint32_t)((tl >> 1) & 1), a.status, 8, tl)) break;
+      tc::fence_after_sync();
+      const TileInfo ti = tile_info(a, t, GATEUP);
+      const uint32_t tl_addr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
+      if (GATEUP) {
+        uint16_t* hid = reinterpret_cast<uint16_t*>(a.out);
+        bool overflow = false;
+#pragma unroll 1
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const int col = c4 * 32;
+          uint32_t gr[32], ur[32];
+          tc::ld_32x32b_x32(tl_addr + col, gr);
+          tc::ld_32x32b_x32(tl_addr + 128 + col, ur);
+          tc::wait_ld();
+          if (m < ti.mrows) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int v = 0; v < 16; ++v) {
+              const float g0 = __uint_as_float(gr[2 * v]), g1 = __uint_as_float(gr[2 * v + 1]);
+              const float u0 = __uint_as_float(ur[2 * v]), u1 = __uint_as_float(ur[2 * v + 1]);
+              const float h0 = g0 / (1.f + expf(-g0)) * u0;
+              const float h1 = g1 / (1.f + expf(-g1)) * u1;
+              overflow |= !(fabsf(h0) <= kF16Max) || !(fabsf(h1) <= kF16Max);
+              pk[v] = (uint32_t)f32_to_f16_bits(h0) | ((uint32_t)f32_to_f16_bits(h1) << 16);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(
+                hid + (size_t)(ti.r0 + ti.m0 + m) * a.out_ld + ti.n0 + col);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+        if (overflow) raise_status(a.status, MOE_DEV_FP16_RANGE);
+      } else {
+        float* y = reinterpret_cast<float*>(a.out);
+#pragma unroll 1
+        for (int c8 = 0; c8 < 8; ++c8) {
+          const int col = c8 * 32;
+          uint32_t v[32];
+          tc::ld_32x32b_x32(tl_addr + col, v);
+          tc::wait_ld();
+          if (m < ti.mrows) {
+            float4* dst = reinterpret_cast<float4*>(
+                y + (size_t)(ti.r0 + ti.m0 + m) * a.out_ld + ti.n0 + col);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                   __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+          }
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.acc_empty[acc]);
+    }
   }
+
+  // ---- all roles done: free TMEM
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) {
@@ -305,6 +456,62 @@ k_tile_offsets(const int32_t* __restrict__ expert_off, int E, int32_t* __restric
   if (tid == E - 1) tile_off[E] = before + incl;
 }
 
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+namespace {
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+cudaError_t get_encoder(EncodeTiled* out) {
+  static std::once_flag once;
+  static EncodeTiled fn = nullptr;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                           &q);
+    if (err == cudaSuccess && q != cudaDriverEntryPointSuccess) err = cudaErrorNotSupported;
+    fn = reinterpret_cast<EncodeTiled>(p);
+  });
+  *out = fn;
+  return fn ? cudaSuccess : (err != cudaSuccess ? err : cudaErrorNotSupported);
+}
+
+// 2-D map over a stack of code matrices [rows_total, K] (uint8, row-major),
+// box = 64 bytes of K x box_rows rows, no swizzle.
+cudaError_t code_map(CUtensorMap* map, const uint8_t* codes, long long rows_total, int K,
+                     int box_rows) {
+  EncodeTiled enc;
+  cudaError_t e = get_encoder(&enc);
+  if (e != cudaSuccess) return e;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows_total};
+  const cuuint64_t strides[1] = {(cuuint64_t)K};
+  const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int num_sms() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 148;
+  }
+  return cached[dev];
+}
+}  // namespace
+
 bool expert_gemm_tc_ok(int H, int I) {
   return H % 256 == 0 && I % 128 == 0 && H >= 256 && I >= 128;
 }
@@ -314,20 +521,27 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x16, const int32_t* expert_off
                                   int H, int I, int32_t* tile_off, uint16_t* hid, float* y,
                                   int32_t* status, cudaStream_t s, bool pdl) {
   cudaError_t err;
-  if ((err = ensure_smem((const void*)k_expert_gemm_tc<true>, SMEM_TC)) != cudaSuccess) return err;
-  if ((err = ensure_smem((const void*)k_expert_gemm_tc<false>, SMEM_TC)) != cudaSuccess) return err;
+  if ((err = ensure_smem((const void*)k_expert_gemm_ws<true>, SMEM_WS)) != cudaSuccess) return err;
+  if ((err = ensure_smem((const void*)k_expert_gemm_ws<false>, SMEM_WS)) != cudaSuccess) return err;
+  CUtensorMap gmap, umap, dmap;
+  if ((err = code_map(&gmap, w.gate.codes, (long long)E * I, H, 128)) != cudaSuccess) return err;
+  if ((err = code_map(&umap, w.up.codes, (long long)E * I, H, 128)) != cudaSuccess) return err;
+  if ((err = code_map(&dmap, w.down.codes, (long long)E * H, I, 256)) != cudaSuccess) return err;
   err = launch_k(k_tile_offsets, dim3(1), dim3(1024), 0, s, pdl, expert_off, E, tile_off);
   if (err != cudaSuccess) return err;
-  const int max_tiles = cdiv(P, BM) + min(E, P);  // each expert adds at most one partial tile
-  const dim3 blk(kThreadsTC);
-  err = launch_k(k_expert_gemm_tc<true>, dim3(I / (BN / 2), max_tiles), blk, (size_t)SMEM_TC, s,
-                 pdl, x16, H, I, expert_off, row_token, (const int32_t*)tile_off, E, w.gate.codes,
-                 w.gate.scales, w.up.codes, w.up.scales, (void*)hid, I, status);
+  // Host bound on the tile count: each expert adds at most one partial tile.
+  const int max_mtiles = cdiv(P, BM) + min(E, P);
+  const int nsm = num_sms();
+  const dim3 blk(kThreadsWS);
+  GemmArgs g{x16, H, I, expert_off, row_token, tile_off, E, w.gate.scales, w.up.scales,
+             (void*)hid, I, I / (BN / 2), status};
+  err = launch_k(k_expert_gemm_ws<true>, dim3(min(nsm, max_mtiles * g.n_ntiles)), blk,
+                 (size_t)SMEM_WS, s, pdl, gmap, umap, g);
   if (err != cudaSuccess) return err;
-  return launch_k(k_expert_gemm_tc<false>, dim3(H / BN, max_tiles), blk, (size_t)SMEM_TC, s, pdl,
-                  (const uint16_t*)hid, I, H, expert_off, row_token, (const int32_t*)tile_off, E,
-                  w.down.codes, w.down.scales, (const uint8_t*)nullptr, (const float*)nullptr,
-                  (void*)y, H, status);
+  GemmArgs d{(const uint16_t*)hid, I, H, expert_off, row_token, tile_off, E, w.down.scales,
+             nullptr, (void*)y, H, H / BN, status};
+  return launch_k(k_expert_gemm_ws<false>, dim3(min(nsm, max_mtiles * d.n_ntiles)), blk,
+                  (size_t)SMEM_WS, s, pdl, dmap, dmap, d);
 }
 
 }  // namespace moe

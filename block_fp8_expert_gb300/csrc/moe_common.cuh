@@ -195,16 +195,34 @@ __device__ __forceinline__ uint64_t global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Bounded wait for the phase with the given parity: gives up after about
-// kWaitLimitNs and returns false (the caller records MOE_DEV_WAIT_TIMEOUT).
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// Wait budget: a wait gives up only when both the SM cycle counter (monotonic
+// on this SM) and the global nanosecond timer (which the driver may step)
+// say the budget is spent, so a timer step cannot end a wait early and the
+// wait stays bounded either way.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;       // 2 s
+constexpr long long kWaitLimitCycles = 4000000000ll;   // about 2 s at 2 GHz
+struct WaitBudget {
+  uint64_t t0;
+  long long c0;
+};
+__device__ __forceinline__ WaitBudget wait_budget() {
+  WaitBudget b;
+  b.t0 = global_ns();
+  b.c0 = clock64();
+  return b;
+}
+__device__ __forceinline__ bool budget_spent(const WaitBudget& b) {
+  return clock64() - b.c0 > kWaitLimitCycles && global_ns() - b.t0 > kWaitLimitNs;
+}
+// Bounded wait for the phase with the given parity: returns false once the
+// budget is spent (the caller records MOE_DEV_WAIT_TIMEOUT).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
+  const WaitBudget b = wait_budget();
   while (true) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (budget_spent(b)) return false;
   }
 }
 // 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16);
