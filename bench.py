@@ -258,6 +258,11 @@ class LayerRun:
     def distinct_experts(self):
         return int(np.unique(self.idx.cpu().numpy()).size)
 
+    def device_status(self):
+        """The workspace's status word and the record of any bounded wait that
+        ran out (words 1-5), after the timed steps."""
+        return self.ws[:24].view(self.torch.int32).cpu().numpy()[:6].tolist()
+
 
 def time_steps(torch, fn, steps, warmup, flush):
     for _ in range(warmup):
@@ -334,6 +339,7 @@ def measure_workload(torch, name, T, steps, warmup, flush, pk, dev_cache, seed=0
     t_tc = F / (pk["bf16_tflops"] * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
     res = {"workload": f"{name}_T{T}", "T": T, "ms": t * 1e3, "tokens_per_s": T / t,
+           "ms_max": max(times) * 1e3, "device_status": run.device_status(),
            "distinct_experts": Dn, "bytes": B, "flops": F,
            "hbm_gbs": B / t / 1e9, "tflops": F / t / 1e12, "bound": bound,
            "roofline_frac": max(t_hbm, t_tc) / t}
@@ -464,6 +470,8 @@ def run_gpu(args):
             "e2e": {"value": world * T / e2e_t, "unit": "tokens/s",
                     "h2d_bytes_per_step": T * w.H * 2, "d2h_bytes_per_step": T * w.H * 2},
             "gpu_launches": launches_per_step * args.steps,
+            "device_status": run.device_status(),
+            "ms_step_max": max(times) * 1e3,
             "clocks": clk.summary(),
             "sweep": sweep,
         }

@@ -14,7 +14,8 @@
 //   warp 0      TMA: the E4M3 code tile of each 64-wide K step (2-D tensor
 //               maps over the stacked code matrices) into a 4-deep ring;
 //   warps 1-2   gather the step's activation rows with cp.async (rows past the
-//               expert's segment are zero-filled) into a 4-deep ring;
+//               expert's segment are zero-filled) into a 4-deep ring; a step is
+//               published once its copies landed, after a proxy fence;
 //   warps 3-10  decode codes to fp16 times the block scale
 //               (fp16(dec * fp16(scale))) into a double-buffered B tile;
 //   warp 11     one thread issues tcgen05.mma (M=128, N=256, K=16) into one of
@@ -141,10 +142,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar))
-               : "memory");
-}
 }  // namespace
 
 template <bool GATEUP>
@@ -254,10 +251,20 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
           const uint16_t* g = a.asrc + (size_t)(src[u] < 0 ? 0 : src[u]) * a.K + k0 + 8 * jj;
           tc::cp_async16_zfill(A + tc::sw128_off(m, jj), g, src[u] >= 0);
         }
-        cp_async_arrive_noinc(&sh.a_full[sa]);
+        cp_async_commit();
+        // Publish the previous step: its copies have landed (this thread's),
+        // then the proxy fence makes them visible to tensor-core reads.
+        if (j > 0) {
+          cp_async_wait<1>();
+          tc::fence_proxy_async();
+          mbar_arrive(&sh.a_full[(j - 1) % NA]);
+        }
       }
     }
+    // publish the last step
     cp_async_wait<0>();
+    tc::fence_proxy_async();
+    if (j > 0 && ok) mbar_arrive(&sh.a_full[(j - 1) % NA]);
   } else if (warp >= W_DEC0 && warp < W_DEC0 + kDecWarps) {
     // ------------------------------------------------ decode E4M3 -> fp16
     const int dt = tid - W_DEC0 * 32;

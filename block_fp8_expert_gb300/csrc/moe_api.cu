@@ -249,7 +249,8 @@ moe_status moe_permute(const int32_t* topk_idx, moe_dims d, int32_t* expert_off,
   if ((s = check_ws(d, ws, ws_bytes)) != MOE_OK) return s;
   const WsLayout L = ws_layout(d);
   cudaStream_t st = (cudaStream_t)stream;
-  CUDA_CHECK(cudaMemsetAsync(at<int32_t>(ws, L.status), 0, sizeof(int32_t), st), "moe_permute");
+  CUDA_CHECK(cudaMemsetAsync(at<int32_t>(ws, L.status), 0, sizeof(int32_t) * kStatusWords, st),
+             "moe_permute");
   CUDA_CHECK(launch_permute(topk_idx, d.T, d.E, d.k, at<int32_t>(ws, L.rank),
                             at<int32_t>(ws, L.block_cnt), at<int32_t>(ws, L.block_base),
                             expert_off, row_token, tok_slot_row, nullptr,

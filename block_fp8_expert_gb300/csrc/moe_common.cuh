@@ -246,6 +246,11 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
 // ---------------------------------------------------------------------------
 // Device status word
 // ---------------------------------------------------------------------------
+// Word 0 holds the MOE_DEV_* bits; words 1-5 record the first bounded wait
+// of a call that ran out (warp, barrier, step, parity, CTA).  The first
+// kernel of each call clears all of them.
+constexpr int kStatusWords = 6;
+
 __device__ __forceinline__ void raise_status(int32_t* status, int32_t bits) {
   if (status) atomicOr(status, bits);
 }

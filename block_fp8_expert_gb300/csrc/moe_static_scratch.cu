@@ -104,7 +104,7 @@ extern "C" moe_status moe_permute_static_scratch(const int32_t* topk_idx, moe_di
   char* b = static_cast<char*>(base);
   cudaStream_t st = (cudaStream_t)stream;
   int32_t* status = reinterpret_cast<int32_t*>(b + kOffStatus);
-  e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+  e = cudaMemsetAsync(status, 0, sizeof(int32_t) * kStatusWords, st);
   if (e == cudaSuccess)
     e = launch_permute(topk_idx, d.T, d.E, d.k, reinterpret_cast<int32_t*>(b + kOffRank),
                        reinterpret_cast<int32_t*>(b + kOffCnt),

@@ -159,7 +159,7 @@ k_active_from_offsets(const int32_t* __restrict__ expert_off, int E,
   griddep_wait();
   griddep_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0 && status) *status = 0;  // first kernel of an expert-FFN call
+  if (tid < kStatusWords && status) status[tid] = 0;  // first kernel of an expert-FFN call
   const int ne = (tid < E && expert_off[tid + 1] > expert_off[tid]) ? 1 : 0;
   int act = ne;
 #pragma unroll

@@ -33,7 +33,8 @@ k_router_mma(const uint16_t* __restrict__ x, const float* __restrict__ Wr, int T
   const int g = lane >> 2, c = lane & 3;
   // The router runs first in a layer call: it clears the status word that
   // later kernels of the call may raise.
-  if (status && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && tid == 0) *status = 0;
+  if (status && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && tid < kStatusWords)
+    status[tid] = 0;
   const int e0 = blockIdx.x * 16;
   const int t0 = blockIdx.z * NT * 8;
   const int kbeg = blockIdx.y * kslice, kend = min(H, kbeg + kslice);
