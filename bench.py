@@ -264,6 +264,20 @@ class LayerRun:
         return self.ws[:24].view(self.torch.int32).cpu().numpy()[:6].tolist()
 
 
+def aggregate(t_rank: float, world: int, tokens_per_rank: int, steps: int, dist=None,
+              device=None):
+    """Whole-job throughput from each rank's summed step time: the slowest
+    rank's time (max over ranks) bounds the job; every rank processed
+    tokens_per_rank tokens per step.  Returns (tokens/s, max time)."""
+    t_all = t_rank
+    if dist is not None and world > 1:
+        import torch
+        tt = torch.tensor([t_rank], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_all = float(tt.item())
+    return world * tokens_per_rank * steps / t_all, t_all
+
+
 def time_steps(torch, fn, steps, warmup, flush):
     for _ in range(warmup):
         fn()
@@ -388,15 +402,8 @@ def run_gpu(args):
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    t_rank = sum(times)
-    if dist:
-        tt = torch.tensor([t_rank], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_all = float(tt.item())
-    else:
-        t_all = t_rank
+    value, t_all = aggregate(sum(times), world, T, args.steps, dist, "cuda")
     ms_per_step = t_all / args.steps * 1e3
-    value = world * T * args.steps / t_all
     Dn = run.distinct_experts()
     B, F, expert_B = algorithmic(w, T, Dn)
 
