@@ -118,10 +118,10 @@ k_gateup_stream(const uint16_t* __restrict__ x16, int H, int I,
         const int ch = kg + warp + 8 * j;
         if (ch < nch) {
           const int k0 = ch * 64;
-          cp_async16(&wbuf[(j * 4 + 0) * kThreads + tid], gp + k0);
-          cp_async16(&wbuf[(j * 4 + 1) * kThreads + tid], gp + r8 + k0);
-          cp_async16(&wbuf[(j * 4 + 2) * kThreads + tid], up + k0);
-          cp_async16(&wbuf[(j * 4 + 3) * kThreads + tid], up + r8 + k0);
+          cp_async16_stream(&wbuf[(j * 4 + 0) * kThreads + tid], gp + k0);
+          cp_async16_stream(&wbuf[(j * 4 + 1) * kThreads + tid], gp + r8 + k0);
+          cp_async16_stream(&wbuf[(j * 4 + 2) * kThreads + tid], up + k0);
+          cp_async16_stream(&wbuf[(j * 4 + 3) * kThreads + tid], up + r8 + k0);
         }
       }
       cp_async_commit();
@@ -245,8 +245,8 @@ k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
       for (int j = 0; j < kDnChunks; ++j) {
         const int ch = kg + kp + 4 * j;
         if (ch < nch) {
-          cp_async16(&wbuf[(j * 2 + 0) * kThreads + tid], dp + ch * 64);
-          cp_async16(&wbuf[(j * 2 + 1) * kThreads + tid], dp + r8 + ch * 64);
+          cp_async16_stream(&wbuf[(j * 2 + 0) * kThreads + tid], dp + ch * 64);
+          cp_async16_stream(&wbuf[(j * 2 + 1) * kThreads + tid], dp + r8 + ch * 64);
         }
       }
       cp_async_commit();

@@ -139,7 +139,7 @@ WsLayout ws_layout(const moe_dims& d) {
     return at;
   };
   L.status = take(256);
-  L.logits = take(4 * T * E * 4);  // up to 4 K-slices of partial router logits
+  L.logits = take(8 * T * E * 4);  // up to 8 K-slices of partial router logits
   L.rank = take(P * 4);
   L.block_cnt = take(nb * E * 4);
   L.block_base = take(nb * E * 4);

@@ -51,8 +51,8 @@ WsLayout ws_layout(const moe_dims& d);
 // All launchers enqueue on `s`; with pdl the kernels are launched with
 // programmatic stream serialisation (each begins with griddep_wait()).
 
-// Router logits (+ optional fp16 copy of x) and top-k.  `part` holds up to 4
-// K-slices of partial logits, [4][T][E] floats.
+// Router logits (+ optional fp16 copy of x) and top-k.  `part` holds up to 8
+// K-slices of partial logits, [8][T][E] floats.
 cudaError_t launch_route(const uint16_t* x, const float* Wr, const float* bias, int T, int H,
                          int E, int k, float* part, int32_t* topk_idx, float* topk_w,
                          uint16_t* x16, int32_t* status, cudaStream_t s, bool pdl);

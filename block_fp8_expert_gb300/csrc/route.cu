@@ -3,6 +3,8 @@
 // routing).  The renormalised weight p_j / sum_sel p equals the softmax over
 // the k selected logits, because the full softmax's normaliser cancels; the
 // kernels compute it that way and never form the E probabilities.
+#include <climits>
+
 #include "moe_internal.h"
 
 namespace moe {
@@ -19,7 +21,7 @@ namespace moe {
 // expert kernels use, and flag values beyond fp16 range.
 // ---------------------------------------------------------------------------
 constexpr int kRouteWarps = 4;
-constexpr int kMaxKSlices = 4;  // K-slices of the router logits (route_kslices)
+constexpr int kMaxKSlices = 8;  // K-slices of the router logits (route_kslices)
 
 template <int NT>
 __global__ void __launch_bounds__(kRouteWarps * 32)
@@ -168,33 +170,37 @@ __device__ __forceinline__ void warp_topk(const float* __restrict__ part, int KS
     const int e = lane + 32 * i;
     v[i] = e < E ? (bias ? v[i] + bias[e] : v[i]) : -INFINITY;
   }
+  // Order-preserving integer keys (exact: -0 is first folded into +0), so the
+  // warp arg-max is two redux.sync reductions per selected expert: the
+  // largest key, then the lowest expert index among lanes holding it.
+  int key[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int b = __float_as_int(v[i] + 0.0f);
+    key[i] = (lane + 32 * i < E) ? (b ^ ((b >> 31) & 0x7FFFFFFF)) : INT_MIN;
+  }
   uint32_t taken = 0;
   float my_val = -INFINITY;
   my_idx = 0;
   for (int j = 0; j < k; ++j) {
+    int bk = INT_MIN, bi = 0x7fffffff;
     float bv = -INFINITY;
-    int bi = 0x7fffffff;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       const int e = lane + 32 * i;
-      if (e < E && !(taken & (1u << i)) && better(v[i], e, bv, bi)) {
-        bv = v[i];
+      if (e < E && !(taken & (1u << i)) && key[i] > bk) {  // first (lowest e) of equal keys
+        bk = key[i];
         bi = e;
+        bv = v[i];
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (better(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    const int wk = __reduce_max_sync(0xffffffffu, bk);
+    const int wi = __reduce_min_sync(0xffffffffu, bk == wk ? bi : 0x7fffffff);
+    if ((wi & 31) == lane) taken |= 1u << (wi >> 5);
+    const float wv = __shfl_sync(0xffffffffu, bv, wi & 31);
     if (lane == j) {
-      my_val = bv;
-      my_idx = bi;
+      my_val = wv;
+      my_idx = wi;
     }
   }
   const float vmax = __shfl_sync(0xffffffffu, my_val, 0);
@@ -370,8 +376,9 @@ k_topk_permute_small(const float* __restrict__ part, int KS, const float* __rest
 }
 
 int route_kslices(int T, int H) {
-  // Split K across CTAs when few tokens leave too few CTAs to stream Wr.
-  int ks = T <= 64 ? 4 : 1;
+  // Split K across CTAs when few tokens leave too few CTAs to stream Wr: with
+  // 8 slices each of the 4 warps of a CTA owns one 64-column chunk (H = 2048).
+  int ks = T <= 64 ? kMaxKSlices : 1;
   while (ks > 1 && (H / ks) % 64 != 0) ks >>= 1;
   return ks;
 }
