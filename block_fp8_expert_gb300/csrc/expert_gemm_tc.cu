@@ -74,43 +74,68 @@ struct WsShared {
   uint64_t acc_full[2], acc_empty[2];
   uint32_t tmem_base;
   int abort_flag;
+  // Steps each role has completed, for the timeout record: [0] codes
+  // issued, [1..2] activation steps published per loader warp, [3..10]
+  // steps decoded per decoder warp, [11] steps issued to the tensor core,
+  // [12] tiles started by it, [13] tiles finished by the epilogue.
+  int prog[14];
 };
 
-// Bounded wait that also returns (false) once another role has aborted.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const WaitBudget b = wait_budget();
-  while (true) {
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (budget_spent(b)) return false;
-  }
-}
-
-// One warp waits (lane 0, bounded + abort-aware), then every lane observes
-// the completed phase itself.  Returns the same verdict in all lanes.  The
-// first wait in the grid that runs out records where: status[1] = warp,
-// status[2] = barrier id, status[3] = step, status[4] = parity.
+// Warp-uniform bounded wait: every lane polls the barrier together (the
+// suspending try_wait, executed convergently), the lanes agree with a vote,
+// and the warp gives up together once the budget is spent or another role
+// has aborted.  Returns the same verdict in all lanes; on success every lane
+// has itself observed the completed phase.  The first wait in the grid that
+// runs out records where: status[1] = warp + 1, status[2] = barrier id,
+// status[3] = step, status[4] = parity, status[5] = CTA, status[6..13] = how
+// far each role of that CTA had got.
 __device__ __forceinline__ bool warp_wait(WsShared& sh, uint64_t* bar, uint32_t parity,
                                           int32_t* status, int bar_id = 0, int step = 0) {
-  bool ok = true;
-  if ((threadIdx.x & 31) == 0) {
-    ok = wait_or_abort(bar, parity, &sh.abort_flag);
-    if (!ok && !sh.abort_flag) {
-      sh.abort_flag = 1;
-      raise_status(status, MOE_DEV_WAIT_TIMEOUT);
-      if (status && atomicCAS(status + 1, 0, 1 + (int)(threadIdx.x >> 5)) == 0) {
-        status[2] = bar_id;
-        status[3] = step;
-        status[4] = (int)parity;
-        status[5] = (int)blockIdx.x;
+  constexpr unsigned kAll = 0xffffffffu;
+  bool done = mbar_try_wait(bar, parity);
+  if (__all_sync(kAll, done)) return true;
+  const WaitBudget b = wait_budget();
+  for (uint32_t n = 1;; ++n) {
+    if (__any_sync(kAll, done)) {
+      // the phase is complete: lanes that polled just before it completed
+      // observe it now (bounded, although the phase cannot move on while
+      // this warp has not consumed it)
+      for (int r = 0; !done && r < (1 << 16); ++r) done = mbar_try_wait(bar, parity);
+      if (__all_sync(kAll, done)) return true;
+      break;
+    }
+    if ((n & 31) == 0) {
+      const bool give_up = *reinterpret_cast<volatile int*>(&sh.abort_flag) != 0 || budget_spent(b);
+      if (__any_sync(kAll, give_up)) break;
+    }
+    done = mbar_try_wait(bar, parity);
+  }
+  if ((threadIdx.x & 31) == 0 && !sh.abort_flag) {
+    sh.abort_flag = 1;
+    raise_status(status, MOE_DEV_WAIT_TIMEOUT);
+    if (status && atomicCAS(status + 1, 0, 1 + (int)(threadIdx.x >> 5)) == 0) {
+      status[2] = bar_id;
+      status[3] = step;
+      status[4] = (int)parity;
+      status[5] = (int)blockIdx.x;
+      const volatile int* pg = sh.prog;
+      int dmin = pg[3], dmax = pg[3];
+      for (int i = 4; i < 11; ++i) {
+        dmin = min(dmin, pg[i]);
+        dmax = max(dmax, pg[i]);
       }
+      status[6] = pg[0];
+      status[7] = pg[1];
+      status[8] = pg[2];
+      status[9] = dmin;
+      status[10] = dmax;
+      status[11] = pg[11];
+      status[12] = pg[12];
+      status[13] = pg[13];
     }
   }
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (ok) mbar_wait(bar, parity);  // already complete: acquire for this lane
-  return ok;
+  __syncwarp();
+  return false;
 }
 
 struct TileInfo {
@@ -182,6 +207,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
       mbar_init(&sh.acc_empty[s], 4);
     }
     sh.abort_flag = 0;
+    for (int i = 0; i < 14; ++i) sh.prog[i] = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -215,6 +241,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
           } else {
             tma_load_2d(dst, &tm0, ks * BK, row, &sh.b8_full[sb]);
           }
+          reinterpret_cast<volatile int*>(sh.prog)[0] = j + 1;
         }
         __syncwarp();
       }
@@ -258,6 +285,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
           cp_async_wait<1>();
           tc::fence_proxy_async();
           mbar_arrive(&sh.a_full[(j - 1) % NA]);
+          if (lane == 0) reinterpret_cast<volatile int*>(sh.prog)[warp] = j;
         }
       }
     }
@@ -318,6 +346,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
         if (lane == 0) {
           mbar_arrive(&sh.b16_full[c]);
           mbar_arrive(&sh.b8_empty[sb]);
+          reinterpret_cast<volatile int*>(sh.prog)[warp] = j + 1;  // warps 3-10
         }
       }
     }
@@ -352,6 +381,8 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
           tc::commit(&sh.a_empty[sa]);
           tc::commit(&sh.b16_empty[c]);
           if (ks == nK - 1) tc::commit(&sh.acc_full[acc]);
+          reinterpret_cast<volatile int*>(sh.prog)[11] = j + 1;
+          reinterpret_cast<volatile int*>(sh.prog)[12] = tl + 1;
         }
         __syncwarp();
       }
@@ -419,6 +450,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.acc_empty[acc]);
+      if (lane == 0 && quad == 0) reinterpret_cast<volatile int*>(sh.prog)[13] = tl + 1;
     }
   }
 
@@ -506,17 +538,6 @@ cudaError_t code_map(CUtensorMap* map, const uint8_t* codes, long long rows_tota
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-int num_sms() {
-  static int cached[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (!cached[dev]) {
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = n > 0 ? n : 148;
-  }
-  return cached[dev];
-}
 }  // namespace
 
 bool expert_gemm_tc_ok(int H, int I) {

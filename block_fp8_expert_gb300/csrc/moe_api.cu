@@ -6,8 +6,10 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <map>
 #include <set>
 #include <string>
+#include <tuple>
 #include <utility>
 
 #include "moe_internal.h"
@@ -64,7 +66,8 @@ moe_status check_dims(const moe_dims& d) {
   if (d.I_shared != 0 && !dim_ok(d.I_shared))
     return fail(MOE_ERR_UNSUPPORTED, "I_shared = %d: need 0 or a multiple of 64 in [64, 16384]",
                 d.I_shared);
-  if (d.E < 1 || d.E > 1024) return fail(MOE_ERR_UNSUPPORTED, "E = %d outside [1, 1024]", d.E);
+  if (d.E < 1 || d.E > kMaxExperts)
+    return fail(MOE_ERR_UNSUPPORTED, "E = %d outside [1, %d]", d.E, kMaxExperts);
   if (d.k < 1 || d.k > 32 || d.k > d.E)
     return fail(MOE_ERR_UNSUPPORTED, "k = %d outside [1, min(E, 32)]", d.k);
   if ((long long)d.T * d.k >= (1LL << 31)) return fail(MOE_ERR_UNSUPPORTED, "T*k too large");
@@ -126,6 +129,34 @@ cudaError_t ensure_smem(const void* func, int bytes) {
   e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess) done.insert({dev, func});
   return e;
+}
+
+int num_sms() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 148;
+  }
+  return cached[dev];
+}
+
+int resident_ctas(const void* func, int threads, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void*, int, size_t>, int> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_tuple(dev, func, threads, smem);
+  auto it = done.find(key);
+  if (it != done.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, threads, smem) != cudaSuccess || n < 1)
+    n = 1;
+  done[key] = n;
+  return n;
 }
 
 WsLayout ws_layout(const moe_dims& d) {

@@ -197,6 +197,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking probe of the same phase (the thread is never suspended).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -221,14 +232,17 @@ __device__ __forceinline__ WaitBudget wait_budget() {
 __device__ __forceinline__ bool budget_spent(const WaitBudget& b) {
   return clock64() - b.c0 > kWaitLimitCycles && global_ns() - b.t0 > kWaitLimitNs;
 }
-// Bounded wait for the phase with the given parity: returns false once the
-// budget is spent (the caller records MOE_DEV_WAIT_TIMEOUT).
+// Bounded wait for the phase with the given parity by a single thread (the
+// rest of its warp may be elsewhere): it polls with the non-suspending probe
+// and returns false once the budget is spent (the caller records
+// MOE_DEV_WAIT_TIMEOUT).  Warps that wait together use a warp-uniform loop
+// over the suspending form instead.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const WaitBudget b = wait_budget();
   while (true) {
     for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (mbar_test_wait(bar, parity)) return true;
     if (budget_spent(b)) return false;
   }
 }
@@ -254,9 +268,10 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
 // Device status word
 // ---------------------------------------------------------------------------
 // Word 0 holds the MOE_DEV_* bits; words 1-5 record the first bounded wait
-// of a call that ran out (warp, barrier, step, parity, CTA).  The first
-// kernel of each call clears all of them.
-constexpr int kStatusWords = 6;
+// of a call that ran out (warp, barrier, step, parity, CTA) and words 6-15
+// how far each role of that CTA had got (kernel-specific).  The first kernel
+// of each call clears all of them.
+constexpr int kStatusWords = 16;
 
 __device__ __forceinline__ void raise_status(int32_t* status, int32_t bits) {
   if (status) atomicOr(status, bits);

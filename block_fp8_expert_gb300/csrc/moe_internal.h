@@ -39,6 +39,14 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
 // Raises `func`'s dynamic shared-memory limit to `bytes`, once per device
 // (host-side attribute; the first call on a device should precede capture).
 cudaError_t ensure_smem(const void* func, int bytes);
+// Largest expert count the library accepts.
+constexpr int kMaxExperts = 1024;
+
+// Streaming multiprocessors of the current device (cached per device).
+int num_sms();
+// CTAs of `func` that fit on one SM with this block size and dynamic shared
+// memory (occupancy query, cached per device, function and size; at least 1).
+int resident_ctas(const void* func, int threads, size_t smem);
 
 // Workspace layout for one set of dims (byte offsets, each 256-aligned).
 struct WsLayout {

@@ -37,8 +37,12 @@ def _forward(torch, D, xd):
     T = xd.shape[0]
     idx = torch.empty((T, D.k), dtype=torch.int32, device="cuda")
     w = torch.empty((T, D.k), dtype=torch.float32, device="cuda")
-    out = D.forward(xd, topk_idx=idx, topk_w=w)
+    ws = D.workspace(T)
+    out = D.forward(xd, ws=ws, topk_idx=idx, topk_w=w)
     torch.cuda.synchronize()
+    # word 0: status bits; words 1-5: where a bounded wait ran out, if one did
+    words = ws[:32].view(torch.int32).cpu().numpy()
+    assert words[0] == 0, f"device status {words[:6].tolist()}"
     return out, idx, w
 
 
