@@ -158,15 +158,6 @@ __device__ __forceinline__ TileInfo tile_info(const GemmArgs& a, int t, bool gat
   return ti;
 }
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-      : "memory");
-}
-
 }  // namespace
 
 template <bool GATEUP>
@@ -231,15 +222,18 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
           ok = false;
           break;
         }
+        // the decoders' reads of this slot (generic proxy) are ordered before
+        // the copies that overwrite it (async proxy)
+        tc::fence_proxy_async();
         if (lane == 0) {
           uint8_t* dst = smem + OFF_B8 + sb * B8_BYTES;
           mbar_arrive_expect_tx(&sh.b8_full[sb], B8_BYTES);
           const int row = ti.e * a.rows_per_expert + ti.n0;
           if (GATEUP) {
-            tma_load_2d(dst, &tm0, ks * BK, row, &sh.b8_full[sb]);
-            tma_load_2d(dst + 128 * BK, &tm1, ks * BK, row, &sh.b8_full[sb]);
+            tc::tma_load_2d(dst, &tm0, ks * BK, row, &sh.b8_full[sb]);
+            tc::tma_load_2d(dst + 128 * BK, &tm1, ks * BK, row, &sh.b8_full[sb]);
           } else {
-            tma_load_2d(dst, &tm0, ks * BK, row, &sh.b8_full[sb]);
+            tc::tma_load_2d(dst, &tm0, ks * BK, row, &sh.b8_full[sb]);
           }
           reinterpret_cast<volatile int*>(sh.prog)[0] = j + 1;
         }
@@ -519,23 +513,31 @@ cudaError_t get_encoder(EncodeTiled* out) {
   *out = fn;
   return fn ? cudaSuccess : (err != cudaSuccess ? err : cudaErrorNotSupported);
 }
+}  // namespace
 
+cudaError_t make_u8_tensor_map(CUtensorMap* map, const uint8_t* base, long long rows, int cols,
+                               int box_cols, int box_rows, bool swizzle128) {
+  EncodeTiled enc;
+  cudaError_t e = get_encoder(&enc);
+  if (e != cudaSuccess) return e;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r =
+      enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box,
+          estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+namespace {
 // 2-D map over a stack of code matrices [rows_total, K] (uint8, row-major),
 // box = 64 bytes of K x box_rows rows, no swizzle.
 cudaError_t code_map(CUtensorMap* map, const uint8_t* codes, long long rows_total, int K,
                      int box_rows) {
-  EncodeTiled enc;
-  cudaError_t e = get_encoder(&enc);
-  if (e != cudaSuccess) return e;
-  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows_total};
-  const cuuint64_t strides[1] = {(cuuint64_t)K};
-  const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), dims,
-                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+  return make_u8_tensor_map(map, codes, rows_total, K, BK, box_rows, false);
 }
 
 }  // namespace

@@ -32,34 +32,6 @@ namespace moe {
 
 constexpr int kThreads = 256;
 
-// One 64-column chunk: 16 weight rows (g, g+8) x NT*8 tokens.
-template <int NT, bool F16>
-__device__ __forceinline__ void chunk_mma(const uint4& w_lo, const uint4& w_hi,
-                                          const uint4 (&xa)[NT][2], float (&part)[NT][4]) {
-  uint32_t wl[8], wh[8];
-  if (F16) {
-    decode16_f16(w_lo, wl);
-    decode16_f16(w_hi, wh);
-  } else {
-    decode16_scaled(w_lo, wl);
-    decode16_scaled(w_hi, wh);
-  }
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const uint32_t xr[8] = {xa[nt][0].x, xa[nt][0].y, xa[nt][0].z, xa[nt][0].w,
-                            xa[nt][1].x, xa[nt][1].y, xa[nt][1].z, xa[nt][1].w};
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const uint32_t a[4] = {wl[2 * s], wh[2 * s], wl[2 * s + 1], wh[2 * s + 1]};
-      const uint32_t b[2] = {xr[2 * s], xr[2 * s + 1]};
-      if (F16)
-        mma_f16_16x8x16(part[nt], a, b);
-      else
-        mma_bf16_16x8x16(part[nt], a, b);
-    }
-  }
-}
-
 // ---------------------------------------------------------------------------
 // gate/up + SwiGLU.  grid (I/16, max active experts).  A CTA owns 16 rows of
 // the expert's gate and up matrices; its 8 warps split K = H into 64-column
@@ -85,8 +57,6 @@ k_gateup_stream(const uint16_t* __restrict__ x16, int H, int I,
   const int a = blockIdx.y;
   if (a >= active[0]) return;
   const int e = active[1 + a];
-  const int r0 = expert_off[e];
-  const int ne = expert_off[e + 1] - r0;
   const int i0 = blockIdx.x * 16;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
@@ -98,6 +68,27 @@ k_gateup_stream(const uint16_t* __restrict__ x16, int H, int I,
   const size_t r8 = (size_t)8 * H;
   const float* gs = gscales + ((size_t)e * cdiv(I, kScaleBlock) + i0 / kScaleBlock) * nHb;
   const float* us = uscales + ((size_t)e * cdiv(I, kScaleBlock) + i0 / kScaleBlock) * nHb;
+  // All weight copies of one K-group (2048 columns of H).
+  auto issue = [&](int kg) {
+#pragma unroll
+    for (int j = 0; j < kGuChunks; ++j) {
+      const int ch = kg + warp + 8 * j;
+      if (ch < nch) {
+        const int k0 = ch * 64;
+        cp_async16_stream(&wbuf[(j * 4 + 0) * kThreads + tid], gp + k0);
+        cp_async16_stream(&wbuf[(j * 4 + 1) * kThreads + tid], gp + r8 + k0);
+        cp_async16_stream(&wbuf[(j * 4 + 2) * kThreads + tid], up + k0);
+        cp_async16_stream(&wbuf[(j * 4 + 3) * kThreads + tid], up + r8 + k0);
+      }
+      cp_async_commit();  // one group per chunk: chunk j is computed while later ones land
+    }
+  };
+  // The first K-group's weights depend only on the expert: start them before
+  // the expert's rows and tokens are read.
+  issue(0);
+  const int r0 = expert_off[e];
+  const int ne = expert_off[e + 1] - r0;
+  bool issued = true;
 
   for (int n0 = 0; n0 < ne; n0 += NT * 8) {
     if (tid < NT * 8) tok[tid] = (n0 + tid < ne) ? row_token[r0 + n0 + tid] : -1;
@@ -112,24 +103,17 @@ k_gateup_stream(const uint16_t* __restrict__ x16, int H, int I,
       for (int q = 0; q < 4; ++q) accg[nt][q] = accu[nt][q] = 0.f;
 
     for (int kg = 0; kg < nch; kg += 8 * kGuChunks) {
-      // 1. all weight copies of this K-group
-#pragma unroll
-      for (int j = 0; j < kGuChunks; ++j) {
-        const int ch = kg + warp + 8 * j;
-        if (ch < nch) {
-          const int k0 = ch * 64;
-          cp_async16_stream(&wbuf[(j * 4 + 0) * kThreads + tid], gp + k0);
-          cp_async16_stream(&wbuf[(j * 4 + 1) * kThreads + tid], gp + r8 + k0);
-          cp_async16_stream(&wbuf[(j * 4 + 2) * kThreads + tid], up + k0);
-          cp_async16_stream(&wbuf[(j * 4 + 3) * kThreads + tid], up + r8 + k0);
-        }
-      }
-      cp_async_commit();
-      // 2. the activations, straight into registers
+      // 1. all weight copies of this K-group (unless already in flight)
+      if (!issued) issue(kg);
+      issued = false;
+      // 2. block scales and activations, straight into registers
+      float sg[kGuChunks], su[kGuChunks];
       uint4 xa[kGuChunks][NT][2];
 #pragma unroll
       for (int j = 0; j < kGuChunks; ++j) {
         const int ch = kg + warp + 8 * j;
+        sg[j] = ch < nch ? gs[ch * 64 / kScaleBlock] : 0.f;
+        su[j] = ch < nch ? us[ch * 64 / kScaleBlock] : 0.f;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           if (ch < nch && trow[nt] >= 0) {
@@ -141,14 +125,12 @@ k_gateup_stream(const uint16_t* __restrict__ x16, int H, int I,
           }
         }
       }
-      cp_async_wait<0>();
-      // 3. decode + MMA per chunk, block scale in fp32
+      // 3. decode + MMA per chunk as its copies land, block scale in fp32
 #pragma unroll
       for (int j = 0; j < kGuChunks; ++j) {
         const int ch = kg + warp + 8 * j;
+        cp_async_wait_n(kGuChunks - 1 - j);
         if (ch < nch) {
-          const float sg = gs[ch * 64 / kScaleBlock];
-          const float su = us[ch * 64 / kScaleBlock];
           float pg[NT][4], pu[NT][4];
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
@@ -162,8 +144,8 @@ k_gateup_stream(const uint16_t* __restrict__ x16, int H, int I,
           for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              accg[nt][q] = fmaf(pg[nt][q], sg, accg[nt][q]);
-              accu[nt][q] = fmaf(pu[nt][q], su, accu[nt][q]);
+              accg[nt][q] = fmaf(pg[nt][q], sg[j], accg[nt][q]);
+              accu[nt][q] = fmaf(pu[nt][q], su[j], accu[nt][q]);
             }
         }
       }
@@ -219,8 +201,6 @@ k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
   const int a = blockIdx.y;
   if (a >= active[0]) return;
   const int e = active[1 + a];
-  const int r0 = expert_off[e];
-  const int ne = expert_off[e + 1] - r0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
   const int mt = warp & 1, kp = warp >> 1;
@@ -230,6 +210,24 @@ k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
   const uint8_t* dp = dcodes + ((size_t)e * H + h0 + g) * I + 16 * c;
   const size_t r8 = (size_t)8 * I;
   const float* ds = dscales + ((size_t)e * cdiv(H, kScaleBlock) + h0 / kScaleBlock) * nIb;
+  // All weight copies of one K-group (768 columns of I).
+  auto issue = [&](int kg) {
+#pragma unroll
+    for (int j = 0; j < kDnChunks; ++j) {
+      const int ch = kg + kp + 4 * j;
+      if (ch < nch) {
+        cp_async16_stream(&wbuf[(j * 2 + 0) * kThreads + tid], dp + ch * 64);
+        cp_async16_stream(&wbuf[(j * 2 + 1) * kThreads + tid], dp + r8 + ch * 64);
+      }
+      cp_async_commit();  // one group per chunk
+    }
+  };
+  // The first K-group's weights depend only on the expert: start them before
+  // the expert's rows are read.
+  issue(0);
+  const int r0 = expert_off[e];
+  const int ne = expert_off[e + 1] - r0;
+  bool issued = true;
 
   for (int n0 = 0; n0 < ne; n0 += NT * 8) {
     bool valid[NT];
@@ -241,19 +239,14 @@ k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
 #pragma unroll
       for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
     for (int kg = 0; kg < nch; kg += 4 * kDnChunks) {
-#pragma unroll
-      for (int j = 0; j < kDnChunks; ++j) {
-        const int ch = kg + kp + 4 * j;
-        if (ch < nch) {
-          cp_async16_stream(&wbuf[(j * 2 + 0) * kThreads + tid], dp + ch * 64);
-          cp_async16_stream(&wbuf[(j * 2 + 1) * kThreads + tid], dp + r8 + ch * 64);
-        }
-      }
-      cp_async_commit();
+      if (!issued) issue(kg);
+      issued = false;
+      float sd[kDnChunks];
       uint4 xa[kDnChunks][NT][2];
 #pragma unroll
       for (int j = 0; j < kDnChunks; ++j) {
         const int ch = kg + kp + 4 * j;
+        sd[j] = ch < nch ? ds[ch * 64 / kScaleBlock] : 0.f;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           if (ch < nch && valid[nt]) {
@@ -265,12 +258,11 @@ k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
           }
         }
       }
-      cp_async_wait<0>();
 #pragma unroll
       for (int j = 0; j < kDnChunks; ++j) {
         const int ch = kg + kp + 4 * j;
+        cp_async_wait_n(kDnChunks - 1 - j);
         if (ch < nch) {
-          const float sd = ds[ch * 64 / kScaleBlock];
           float p[NT][4];
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
@@ -281,7 +273,7 @@ k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) acc[nt][q] = fmaf(p[nt][q], sd, acc[nt][q]);
+            for (int q = 0; q < 4; ++q) acc[nt][q] = fmaf(p[nt][q], sd[j], acc[nt][q]);
         }
       }
     }

@@ -6,10 +6,8 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
-#include <map>
 #include <set>
 #include <string>
-#include <tuple>
 #include <utility>
 
 #include "moe_internal.h"
@@ -141,22 +139,6 @@ int num_sms() {
     cached[dev] = n > 0 ? n : 148;
   }
   return cached[dev];
-}
-
-int resident_ctas(const void* func, int threads, size_t smem) {
-  static std::mutex mu;
-  static std::map<std::tuple<int, const void*, int, size_t>, int> done;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-  std::lock_guard<std::mutex> lock(mu);
-  const auto key = std::make_tuple(dev, func, threads, smem);
-  auto it = done.find(key);
-  if (it != done.end()) return it->second;
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, threads, smem) != cudaSuccess || n < 1)
-    n = 1;
-  done[key] = n;
-  return n;
 }
 
 WsLayout ws_layout(const moe_dims& d) {

@@ -138,6 +138,19 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
+// cp_async_wait with a count known only after unrolling (0..7).
+__device__ __forceinline__ void cp_async_wait_n(int n) {
+  switch (n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 5: cp_async_wait<5>(); break;
+    case 6: cp_async_wait<6>(); break;
+    default: cp_async_wait<7>(); break;
+  }
+}
 
 // fp32 -> (hi, mid, lo) bf16 with w == hi + mid + lo to within 2^-24 |w|:
 // each part is the bf16 rounding of what the previous parts left.
@@ -262,6 +275,43 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
 // Barrier among the first `nthreads` threads of the CTA (named barrier `id`).
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Grouped-GEMV building block (decode kernels).  K permutation: an MMA's 16
+// logical K positions are fed from physical columns so that a thread owns 16
+// consecutive bytes of a weight row: for thread (g = lane/4, c = lane%4) and
+// MMA step s of a 64-column chunk, the logical pairs (2c, 2c+1) and
+// (2c+8, 2c+9) are physical columns 16c + 4s + {0,1} and 16c + 4s + {2,3}.
+// The activations use the same map, so every product pairs the right weight
+// with the right activation.
+// ---------------------------------------------------------------------------
+// One 64-column chunk: 16 weight rows (g, g+8) x NT*8 tokens.
+template <int NT, bool F16>
+__device__ __forceinline__ void chunk_mma(const uint4& w_lo, const uint4& w_hi,
+                                          const uint4 (&xa)[NT][2], float (&part)[NT][4]) {
+  uint32_t wl[8], wh[8];
+  if (F16) {
+    decode16_f16(w_lo, wl);
+    decode16_f16(w_hi, wh);
+  } else {
+    decode16_scaled(w_lo, wl);
+    decode16_scaled(w_hi, wh);
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const uint32_t xr[8] = {xa[nt][0].x, xa[nt][0].y, xa[nt][0].z, xa[nt][0].w,
+                            xa[nt][1].x, xa[nt][1].y, xa[nt][1].z, xa[nt][1].w};
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const uint32_t a[4] = {wl[2 * s], wh[2 * s], wl[2 * s + 1], wh[2 * s + 1]};
+      const uint32_t b[2] = {xr[2 * s], xr[2 * s + 1]};
+      if (F16)
+        mma_f16_16x8x16(part[nt], a, b);
+      else
+        mma_bf16_16x8x16(part[nt], a, b);
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------

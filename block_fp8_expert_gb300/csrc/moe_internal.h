@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <utility>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "moe_common.cuh"
@@ -39,14 +40,16 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
 // Raises `func`'s dynamic shared-memory limit to `bytes`, once per device
 // (host-side attribute; the first call on a device should precede capture).
 cudaError_t ensure_smem(const void* func, int bytes);
+// 2-D TMA map over a row-major uint8 matrix [rows, cols]: box = box_cols x
+// box_rows, optionally 128-byte swizzled; L2 256-byte promotion.
+cudaError_t make_u8_tensor_map(CUtensorMap* map, const uint8_t* base, long long rows, int cols,
+                               int box_cols, int box_rows, bool swizzle128);
+
 // Largest expert count the library accepts.
 constexpr int kMaxExperts = 1024;
 
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms();
-// CTAs of `func` that fit on one SM with this block size and dynamic shared
-// memory (occupancy query, cached per device, function and size; at least 1).
-int resident_ctas(const void* func, int threads, size_t smem);
 
 // Workspace layout for one set of dims (byte offsets, each 256-aligned).
 struct WsLayout {

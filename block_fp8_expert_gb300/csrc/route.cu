@@ -150,19 +150,37 @@ __device__ __forceinline__ void warp_topk(const float* __restrict__ part, int KS
   // All partial logits of this lane first (independent loads), then the sums
   // in slice order.
   float v[EPL];
+  if (EPL * kMaxKSlices <= 32) {
+    // every load in flight at once, then the sums in slice order
+    float p[kMaxKSlices][EPL];
 #pragma unroll
-  for (int i = 0; i < EPL; ++i) v[i] = 0.f;
-#pragma unroll
-  for (int ks = 0; ks < kMaxKSlices; ++ks) {
-    if (ks < KS) {
-      float p[EPL];
+    for (int ks = 0; ks < kMaxKSlices; ++ks)
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
         const int e = lane + 32 * i;
-        p[i] = e < E ? part[((size_t)ks * T + t) * E + e] : 0.f;
+        p[ks][i] = (ks < KS && e < E) ? __ldcg(&part[((size_t)ks * T + t) * E + e]) : 0.f;
       }
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) v[i] += p[i];
+    for (int i = 0; i < EPL; ++i) {
+      v[i] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < kMaxKSlices; ++ks) v[i] += p[ks][i];
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) v[i] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < kMaxKSlices; ++ks) {
+      if (ks < KS) {
+        float p[EPL];
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+          const int e = lane + 32 * i;
+          p[i] = e < E ? __ldcg(&part[((size_t)ks * T + t) * E + e]) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) v[i] += p[i];
+      }
     }
   }
 #pragma unroll
@@ -170,9 +188,13 @@ __device__ __forceinline__ void warp_topk(const float* __restrict__ part, int KS
     const int e = lane + 32 * i;
     v[i] = e < E ? (bias ? v[i] + bias[e] : v[i]) : -INFINITY;
   }
-  // Order-preserving integer keys (exact: -0 is first folded into +0), so the
-  // warp arg-max is two redux.sync reductions per selected expert: the
-  // largest key, then the lowest expert index among lanes holding it.
+  // Order-preserving integer keys (exact: -0 is first folded into +0; the
+  // map is its own inverse, so a key gives back its logit).  Each lane keeps
+  // the best of its not-yet-taken experts (largest key, lowest index); a
+  // round is two redux.sync reductions over the lanes' heads (largest key,
+  // then the lowest expert index holding it), and only the winning lane
+  // rescans its own experts.  The round results are warp-uniform, so lane j
+  // keeps the j-th selection without a shuffle.
   int key[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
@@ -180,29 +202,36 @@ __device__ __forceinline__ void warp_topk(const float* __restrict__ part, int KS
     key[i] = (lane + 32 * i < E) ? (b ^ ((b >> 31) & 0x7FFFFFFF)) : INT_MIN;
   }
   uint32_t taken = 0;
-  float my_val = -INFINITY;
-  my_idx = 0;
-  for (int j = 0; j < k; ++j) {
-    int bk = INT_MIN, bi = 0x7fffffff;
-    float bv = -INFINITY;
+  int hk = INT_MIN, he = 0x7fffffff, hs = 0;
+  auto rescan = [&]() {
+    hk = INT_MIN;
+    he = 0x7fffffff;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       const int e = lane + 32 * i;
-      if (e < E && !(taken & (1u << i)) && key[i] > bk) {  // first (lowest e) of equal keys
-        bk = key[i];
-        bi = e;
-        bv = v[i];
+      if (e < E && !(taken & (1u << i)) && key[i] > hk) {  // first (lowest e) of equal keys
+        hk = key[i];
+        he = e;
+        hs = i;
       }
     }
-    const int wk = __reduce_max_sync(0xffffffffu, bk);
-    const int wi = __reduce_min_sync(0xffffffffu, bk == wk ? bi : 0x7fffffff);
-    if ((wi & 31) == lane) taken |= 1u << (wi >> 5);
-    const float wv = __shfl_sync(0xffffffffu, bv, wi & 31);
+  };
+  rescan();
+  int my_key = INT_MIN;
+  my_idx = 0;
+  for (int j = 0; j < k; ++j) {
+    const int wk = __reduce_max_sync(0xffffffffu, hk);
+    const int wi = __reduce_min_sync(0xffffffffu, hk == wk ? he : 0x7fffffff);
     if (lane == j) {
-      my_val = wv;
+      my_key = wk;
       my_idx = wi;
     }
+    if (he == wi) {
+      taken |= 1u << hs;
+      rescan();
+    }
   }
+  const float my_val = __int_as_float(my_key ^ ((my_key >> 31) & 0x7FFFFFFF));
   const float vmax = __shfl_sync(0xffffffffu, my_val, 0);
   const float ex = lane < k ? expf(my_val - vmax) : 0.f;
   float s = ex;
@@ -249,7 +278,7 @@ size_t small_route_smem(int E) {
 }
 
 template <int EPL>
-__global__ void __launch_bounds__(1024)
+__global__ void __launch_bounds__(1024, 1)
 k_topk_permute_small(const float* __restrict__ part, int KS, const float* __restrict__ bias,
                      int T, int E, int k, int32_t* __restrict__ topk_idx,
                      float* __restrict__ topk_w, int32_t* __restrict__ expert_off,
@@ -375,10 +404,15 @@ k_topk_permute_small(const float* __restrict__ part, int KS, const float* __rest
   }
 }
 
-int route_kslices(int T, int H) {
+int route_kslices(int T, int H, int E) {
   // Split K across CTAs when few tokens leave too few CTAs to stream Wr: with
   // 8 slices each of the 4 warps of a CTA owns one 64-column chunk (H = 2048).
+  // The top-k lane sums every slice of its experts; slices x experts per lane
+  // stay <= 32 so all of those loads are in flight at once.
   int ks = T <= 64 ? kMaxKSlices : 1;
+  int epl = 1;
+  while (epl < cdiv(E, 32)) epl <<= 1;
+  while (ks > 1 && ks * epl > 32) ks >>= 1;
   while (ks > 1 && (H / ks) % 64 != 0) ks >>= 1;
   return ks;
 }
@@ -386,7 +420,7 @@ int route_kslices(int T, int H) {
 cudaError_t launch_router_logits(const uint16_t* x, const float* Wr, int T, int H, int E,
                                  float* part, uint16_t* x16, int32_t* status, cudaStream_t s,
                                  bool pdl) {
-  const int KS = route_kslices(T, H);
+  const int KS = route_kslices(T, H, E);
   const int kslice = H / KS;
   const dim3 blk(kRouteWarps * 32);
   if (T <= 8)
@@ -405,7 +439,7 @@ cudaError_t launch_route(const uint16_t* x, const float* Wr, const float* bias, 
   if (T == 0) return cudaSuccess;
   cudaError_t err = launch_router_logits(x, Wr, T, H, E, part, x16, status, s, pdl);
   if (err != cudaSuccess) return err;
-  const int KS = route_kslices(T, H);
+  const int KS = route_kslices(T, H, E);
   const int epl = cdiv(E, 32);
   const dim3 g2(cdiv(T, 8)), blk(256);
 #define MOE_TOPK(EPLV) \
@@ -432,7 +466,7 @@ cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const
                                        int32_t* status, cudaStream_t s, bool pdl) {
   cudaError_t err = launch_router_logits(x, Wr, T, H, E, part, x16, status, s, pdl);
   if (err != cudaSuccess) return err;
-  const int KS = route_kslices(T, H);
+  const int KS = route_kslices(T, H, E);
   const size_t smem = small_route_smem(E);
   const int epl = cdiv(E, 32);
 #define MOE_SMALL(EPLV)                                                                      \

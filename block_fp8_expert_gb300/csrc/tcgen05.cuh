@@ -5,6 +5,8 @@
 
 #include <cstdint>
 
+#include <cuda.h>
+
 #include "moe_common.cuh"
 
 namespace moe {
@@ -95,6 +97,19 @@ __device__ __forceinline__ void ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32])
 }
 __device__ __forceinline__ void wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+}
+
+// --- TMA ---------------------------------------------------------------------
+// 2-D tiled tensor copy global -> shared; completion counted in bytes on
+// `bar`.  c0 is the inner (column) coordinate: c0 x element size must be a
+// multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // --- cp.async with zero fill -----------------------------------------------
