@@ -37,6 +37,9 @@ namespace moe {
 namespace {
 constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int NA = 4, NB = 4, NC = 2;  // ring depths: activations, codes, fp16 B tiles
+// Steps an activation loader publishes behind the one it issues (<= NA - 2,
+// so it never waits for a slot whose step it has not published yet).
+constexpr int kALag = NA - 2 > 0 ? NA - 2 : 1;
 constexpr int A_BYTES = BM * BK * 2;    // 16 KB
 constexpr int B8_BYTES = BN * BK;       // 16 KB
 constexpr int B16_BYTES = BN * BK * 2;  // 32 KB
@@ -273,20 +276,23 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
           tc::cp_async16_zfill(A + tc::sw128_off(m, jj), g, src[u] >= 0);
         }
         cp_async_commit();
-        // Publish the previous step: its copies have landed (this thread's),
-        // then the proxy fence makes them visible to tensor-core reads.
-        if (j > 0) {
-          cp_async_wait<1>();
+        // Publish step j - kALag: this thread's copies of it have landed (at
+        // most kALag newer groups still pending, so kALag + 1 steps of
+        // gathers stay in flight), then the proxy fence makes them visible
+        // to tensor-core reads.
+        if (j >= kALag) {
+          cp_async_wait<kALag>();
           tc::fence_proxy_async();
-          mbar_arrive(&sh.a_full[(j - 1) % NA]);
-          if (lane == 0) reinterpret_cast<volatile int*>(sh.prog)[warp] = j;
+          mbar_arrive(&sh.a_full[(j - kALag) % NA]);
+          if (lane == 0) reinterpret_cast<volatile int*>(sh.prog)[warp] = j - kALag + 1;
         }
       }
     }
-    // publish the last step
+    // publish the last steps
     cp_async_wait<0>();
     tc::fence_proxy_async();
-    if (j > 0 && ok) mbar_arrive(&sh.a_full[(j - 1) % NA]);
+    if (ok)
+      for (int p = max(0, j - kALag); p < j; ++p) mbar_arrive(&sh.a_full[p % NA]);
   } else if (warp >= W_DEC0 && warp < W_DEC0 + kDecWarps) {
     // ------------------------------------------------ decode E4M3 -> fp16
     const int dt = tid - W_DEC0 * 32;
