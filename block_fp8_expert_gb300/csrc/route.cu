@@ -272,6 +272,9 @@ k_router_topk(const float* __restrict__ part, int KS, const float* __restrict__ 
 // row_pair[row] = q (the pair of each permuted row).
 // ---------------------------------------------------------------------------
 constexpr int kSmallPairs = 4096;
+// From this many tokens on, top-k runs as its own multi-CTA launch before the
+// one-CTA permutation (below it, the single fused CTA is faster).
+constexpr int kSplitTopkTokens = 16;
 
 size_t small_route_smem(int E) {
   return sizeof(int32_t) * (kSmallPairs + 3 * 1024 + 1 + 64) + sizeof(uint16_t) * 32 * (size_t)E;
@@ -299,15 +302,19 @@ k_topk_permute_small(const float* __restrict__ part, int KS, const float* __rest
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int P = T * k;
 
-  // 1. top-k
-  for (int t = warp; t < T; t += 32) {
-    int idx;
-    float w;
-    warp_topk<EPL>(part, KS, bias, T, E, k, t, lane, idx, w);
-    if (lane < k) {
-      topk_idx[(size_t)t * k + lane] = idx;
-      topk_w[(size_t)t * k + lane] = w;
-      s_idx[t * k + lane] = idx;
+  // 1. top-k (EPL = 0: already selected by k_router_topk, read it back)
+  if constexpr (EPL == 0) {
+    for (int q = tid; q < P; q += 1024) s_idx[q] = topk_idx[q];
+  } else {
+    for (int t = warp; t < T; t += 32) {
+      int idx;
+      float w;
+      warp_topk<EPL>(part, KS, bias, T, E, k, t, lane, idx, w);
+      if (lane < k) {
+        topk_idx[(size_t)t * k + lane] = idx;
+        topk_w[(size_t)t * k + lane] = w;
+        s_idx[t * k + lane] = idx;
+      }
     }
   }
   s_cnt[tid] = 0;
@@ -469,6 +476,23 @@ cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const
   const int KS = route_kslices(T, H, E);
   const size_t smem = small_route_smem(E);
   const int epl = cdiv(E, 32);
+  if (T >= kSplitTopkTokens) {
+    // top-k spread over T/8 CTAs (a warp per token), then the permutation
+    // alone in one CTA: one launch more, but the selections no longer queue
+    // on a single SM
+    const dim3 g2(cdiv(T, 8)), blk(256);
+#define MOE_TOPK(EPLV) \
+  launch_k(k_router_topk<EPLV>, g2, blk, 0, s, pdl, part, KS, bias, T, E, k, topk_idx, topk_w)
+    err = epl <= 1 ? MOE_TOPK(1) : epl <= 2 ? MOE_TOPK(2) : epl <= 4 ? MOE_TOPK(4)
+        : epl <= 8 ? MOE_TOPK(8) : epl <= 16 ? MOE_TOPK(16) : MOE_TOPK(32);
+#undef MOE_TOPK
+    if (err != cudaSuccess) return err;
+    err = ensure_smem((const void*)k_topk_permute_small<0>, (int)small_route_smem(1024));
+    if (err != cudaSuccess) return err;
+    return launch_k(k_topk_permute_small<0>, dim3(1), dim3(1024), smem, s, pdl, part, KS, bias,
+                    T, E, k, topk_idx, topk_w, expert_off, row_token, tok_slot_row, row_pair,
+                    active, sh_off, sh_rows, sh_active);
+  }
 #define MOE_SMALL(EPLV)                                                                      \
   do {                                                                                       \
     err = ensure_smem((const void*)k_topk_permute_small<EPLV>, (int)small_route_smem(1024)); \
