@@ -232,6 +232,7 @@ class LayerRun:
         self.w = torch.empty((self.T, D.k), dtype=torch.float32, device="cuda")
         self.ws = D.workspace(self.T)
         self.graph = None
+        self.launches = None
         self.fwd()
         torch.cuda.synchronize()
         if graph:
@@ -241,10 +242,14 @@ class LayerRun:
                 self.fwd()
             torch.cuda.current_stream().wait_stream(s)
             torch.cuda.synchronize()
+            from block_fp8_expert_gb300 import _lib
             self.graph = torch.cuda.CUDAGraph()
+            n0 = _lib.kernel_launches()
             with torch.cuda.graph(self.graph):
                 self.fwd()
             torch.cuda.synchronize()
+            # this library's kernels in one captured layer call
+            self.launches = _lib.kernel_launches() - n0
 
     def fwd(self):
         self.D.forward(self.x, out=self.out, ws=self.ws, topk_idx=self.idx, topk_w=self.w)
@@ -433,9 +438,9 @@ def run_gpu(args):
     e2e_times = time_steps(torch, e2e_step, min(args.steps, 500), 3, flush)
     e2e_t = sum(e2e_times) / len(e2e_times)
 
-    # launches of this library's kernels per layer call (route 2, permute 3,
-    # expert GEMVs 2, combine 1); the memset of the status word is not a kernel
-    launches_per_step = 8 + (3 if w.I_shared else 0)
+    # this library's kernels per layer call, counted by the library itself
+    # while the call was captured into the replayed graph
+    launches_per_step = run.launches
 
     sweep = []
     if not args.no_sweep and rank == 0:

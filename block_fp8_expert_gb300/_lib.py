@@ -57,6 +57,7 @@ _SIGNATURES = {
     "moe_status_string": (ctypes.c_char_p, [_st]),
     "moe_last_error_message": (ctypes.c_char_p, []),
     "moe_version": (ctypes.c_char_p, []),
+    "moe_kernel_launches": (ctypes.c_ulonglong, []),
     "moe_workspace_bytes": (_st, [Dims, ctypes.POINTER(_sz)]),
     "moe_route": (_st, [_vp, _vp, _vp, Dims, _vp, _vp, _vp, _sz, _vp]),
     "moe_permute": (_st, [_vp, Dims, _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -122,6 +123,11 @@ def ffn(gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales) -
 
 def version() -> str:
     return lib().moe_version().decode()
+
+
+def kernel_launches() -> int:
+    """Kernel launches this library has issued in this process (diagnostic)."""
+    return int(lib().moe_kernel_launches())
 
 
 def status_string(status: int) -> str:

@@ -14,42 +14,7 @@ k_combine(const float* __restrict__ y_perm, const int32_t* __restrict__ tok_slot
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long long)T * H4) return;
   const int t = (int)(i / H4), h = (int)(i % H4) * 4;
-  float4 acc = shared_y ? __ldg(reinterpret_cast<const float4*>(shared_y + (size_t)t * H + h))
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
-  // Slots in groups of 8: row indices and weights first, then the 8 row
-  // gathers, so the loads of a group are in flight together.
-  float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j0 = 0; j0 < k; j0 += 8) {
-    int row[8];
-    float w[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int j = j0 + u;
-      row[u] = j < k ? tok_slot_row[(size_t)t * k + j] : -1;
-      w[u] = j < k ? topk_w[(size_t)t * k + j] : 0.f;
-    }
-    float4 y[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-      y[u] = row[u] >= 0 ? __ldg(reinterpret_cast<const float4*>(y_perm + (size_t)row[u] * H + h))
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      if (row[u] < 0) continue;
-      r.x = fmaf(w[u], y[u].x, r.x);
-      r.y = fmaf(w[u], y[u].y, r.y);
-      r.z = fmaf(w[u], y[u].z, r.z);
-      r.w = fmaf(w[u], y[u].w, r.w);
-    }
-  }
-  acc.x += r.x;
-  acc.y += r.y;
-  acc.z += r.z;
-  acc.w += r.w;
-  uint2 o;
-  o.x = pack_bf16x2(acc.x, acc.y);
-  o.y = pack_bf16x2(acc.z, acc.w);
-  *reinterpret_cast<uint2*>(out + (size_t)t * H + h) = o;
+  combine4(y_perm, tok_slot_row, topk_w, shared_y, t, h, H, k, out);
 }
 
 cudaError_t launch_combine(const float* y_perm, const int32_t* tok_slot_row, const float* topk_w,

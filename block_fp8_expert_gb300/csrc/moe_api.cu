@@ -1,6 +1,7 @@
 // The C ABI (include/moe_fp8.h): argument checks, workspace layout, launches.
 // Nothing here allocates device memory or synchronises the host, except
 // moe_read_device_status, whose job is to read a device word back.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -129,6 +130,9 @@ cudaError_t ensure_smem(const void* func, int bytes) {
   return e;
 }
 
+std::atomic<unsigned long long> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 int num_sms() {
   static int cached[64] = {};
   int dev = 0;
@@ -219,6 +223,8 @@ const char* moe_status_string(moe_status s) {
 const char* moe_last_error_message(void) { return g_last_error.c_str(); }
 
 const char* moe_version(void) { return "moe_fp8 0.1 sm_103a"; }
+
+unsigned long long moe_kernel_launches(void) { return moe::g_launches.load(); }
 
 moe_status moe_workspace_bytes(moe_dims d, size_t* bytes) {
   moe_status s = check_dims(d);

@@ -323,6 +323,53 @@ __device__ __forceinline__ void chunk_mma(const uint4& w_lo, const uint4& w_hi,
 // of each call clears all of them.
 constexpr int kStatusWords = 16;
 
+
+// ---------------------------------------------------------------------------
+// Combine of output columns h..h+3 of token t (h a multiple of 4):
+// out[t, h..h+3] = sum_j w[t,j] y_perm[tok_slot_row[t*k+j], h..] (+ shared_y),
+// summed in fp32 in slot order j (in groups of 8 slots, loads first), the
+// shared expert's row added last, rounded once to bf16.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void combine4(const float* __restrict__ y_perm,
+                                         const int32_t* __restrict__ tok_slot_row,
+                                         const float* __restrict__ topk_w,
+                                         const float* __restrict__ shared_y, int t, int h, int H,
+                                         int k, uint16_t* __restrict__ out) {
+  auto ld4 = [](const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); };
+  float4 acc = shared_y ? ld4(shared_y + (size_t)t * H + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j0 = 0; j0 < k; j0 += 8) {
+    int row[8];
+    float w[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = j0 + u;
+      row[u] = j < k ? tok_slot_row[(size_t)t * k + j] : -1;
+      w[u] = j < k ? topk_w[(size_t)t * k + j] : 0.f;
+    }
+    float4 y[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      y[u] = row[u] >= 0 ? ld4(y_perm + (size_t)row[u] * H + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (row[u] < 0) continue;
+      r.x = fmaf(w[u], y[u].x, r.x);
+      r.y = fmaf(w[u], y[u].y, r.y);
+      r.z = fmaf(w[u], y[u].z, r.z);
+      r.w = fmaf(w[u], y[u].w, r.w);
+    }
+  }
+  acc.x += r.x;
+  acc.y += r.y;
+  acc.z += r.z;
+  acc.w += r.w;
+  uint2 o;
+  o.x = pack_bf16x2(acc.x, acc.y);
+  o.y = pack_bf16x2(acc.z, acc.w);
+  *reinterpret_cast<uint2*>(out + (size_t)t * H + h) = o;
+}
+
 __device__ __forceinline__ void raise_status(int32_t* status, int32_t bits) {
   if (status) atomicOr(status, bits);
 }

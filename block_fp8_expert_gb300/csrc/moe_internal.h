@@ -21,9 +21,13 @@ void set_last_error(const char* msg);
 
 // Kernel launch on `s`, optionally with programmatic stream serialisation
 // (the kernel must begin with griddep_wait()).
+// Adds one to the process-wide launch counter (moe_kernel_launches).
+void count_launch();
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                      cudaStream_t s, bool pdl, Args&&... args) {
+  count_launch();
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;

@@ -33,7 +33,7 @@ k_router_mma(const uint16_t* __restrict__ x, const float* __restrict__ Wr, int T
   griddep_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
-  // The router runs first in a layer call: it clears the status word that
+  // The router runs first in a layer call: it clears the status words that
   // later kernels of the call may raise.
   if (status && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && tid < kStatusWords)
     status[tid] = 0;

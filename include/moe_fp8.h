@@ -97,6 +97,12 @@ const char* moe_last_error_message(void);
 /* Library version string, e.g. "moe_fp8 0.1 sm_103a". */
 const char* moe_version(void);
 
+/* Diagnostic: kernel launches this library has issued in this process (all
+ * host threads; a launch recorded into a CUDA graph counts once, at capture).
+ * No counterpart in the pages: it lets a caller count the kernels of one
+ * call, e.g. around the capture of one moe_layer_forward. */
+unsigned long long moe_kernel_launches(void);
+
 /* Workspace size in bytes that every call below needs for dims d. */
 moe_status moe_workspace_bytes(moe_dims d, size_t* bytes);
 
