@@ -494,6 +494,32 @@ def run_gpu(args):
     return 0
 
 
+def run_oracle_sweep(args):
+    """The fp64 oracle timed on this host's cores on every workload (one full
+    layer call each, after a small warm-up call); no GPU is used.  Prints one
+    JSON line."""
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", str(cores()))
+    plan = [("tiny", 8), ("qwen3moe_decode", 1), ("qwen3moe_decode", 8),
+            ("qwen3moe_decode", 64), ("qwen3moe_prefill", 4096), ("large_sparse", 1),
+            ("large_sparse", 256), ("skewed", 1), ("skewed", 16), ("skewed", 256),
+            ("skewed", 2048), ("skewed", 16384)]
+    rows, cache = [], {}
+    for nm, T in plan:
+        w = mi.WORKLOADS[nm]
+        key = (w.H, w.I, w.E, w.k, w.I_shared, w.zipf_s)
+        if key not in cache:
+            cache.clear()
+            cache[key] = mi.make_layer(w, seed=0)
+        layer = cache[key]
+        x_bits, _ = mi.make_tokens(layer, T, seed=0)
+        oracle_rate(layer, x_bits[:1])  # warm-up (first-call costs)
+        rate, dt = oracle_rate(layer, x_bits)
+        rows.append({"workload": f"{nm}_T{T}", "seconds": dt, "tokens_per_s": rate})
+    print(json.dumps({"oracle_sweep": rows, "cores": cores(), "kind": "oracle",
+                      "sample": "one full layer call per workload, fp64 NumPy oracle"}))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -505,9 +531,13 @@ def main(argv=None):
     ap.add_argument("--sweep-steps", type=int, default=10)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-sweep", action="store_true",
+                    help="time the fp64 oracle on every workload (host only) and exit")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.oracle_sweep:
+        return run_oracle_sweep(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

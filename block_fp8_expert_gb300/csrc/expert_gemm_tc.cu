@@ -189,7 +189,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
       mbar_init(&sh.b8_empty[s], kDecWarps);
     }
     for (int s = 0; s < NA; ++s) {
-      mbar_init(&sh.a_full[s], kLoadThreads);
+      mbar_init(&sh.a_full[s], kLoadWarps);
       mbar_init(&sh.a_empty[s], 1);
     }
     for (int s = 0; s < NC; ++s) {
@@ -280,18 +280,23 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
         // most kALag newer groups still pending, so kALag + 1 steps of
         // gathers stay in flight), then the proxy fence makes them visible
         // to tensor-core reads.
+        // One arrival per loader warp, after every lane's wait and fence.
         if (j >= kALag) {
           cp_async_wait<kALag>();
           tc::fence_proxy_async();
-          mbar_arrive(&sh.a_full[(j - kALag) % NA]);
-          if (lane == 0) reinterpret_cast<volatile int*>(sh.prog)[warp] = j - kALag + 1;
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&sh.a_full[(j - kALag) % NA]);
+            reinterpret_cast<volatile int*>(sh.prog)[warp] = j - kALag + 1;
+          }
         }
       }
     }
     // publish the last steps
     cp_async_wait<0>();
     tc::fence_proxy_async();
-    if (ok)
+    __syncwarp();
+    if (ok && lane == 0)
       for (int p = max(0, j - kALag); p < j; ++p) mbar_arrive(&sh.a_full[p % NA]);
   } else if (warp >= W_DEC0 && warp < W_DEC0 + kDecWarps) {
     // ------------------------------------------------ decode E4M3 -> fp16
