@@ -46,11 +46,17 @@ constexpr int B16_BYTES = BN * BK * 2;  // 32 KB
 constexpr int OFF_A = 0;
 constexpr int OFF_B8 = OFF_A + NA * A_BYTES;
 constexpr int OFF_B16 = OFF_B8 + NB * B8_BYTES;
-constexpr int SMEM_WS = OFF_B16 + NC * B16_BYTES + 1024;  // + alignment slack
-constexpr int kWarps = 16;
-constexpr int kThreadsWS = kWarps * 32;
+// down epilogue: per epilogue warp one 32-row x 32-column fp32 staging tile
+// (4 KB, 128-byte swizzled) that a TMA store writes out
+constexpr int EPI_BYTES = 4 * 4096;
+constexpr int OFF_EPI = OFF_B16 + NC * B16_BYTES;
+constexpr int SMEM_WS = OFF_EPI + EPI_BYTES + 1024;  // + alignment slack
 constexpr int kLoadWarps = 2, kDecWarps = 8;
-constexpr int W_TMA = 0, W_LOAD0 = 1, W_DEC0 = 3, W_MMA = 11;  // warps 12-15: epilogue
+// warp roles: TMA, activation loaders, decoders, MMA issue, 4 epilogue warps
+constexpr int W_TMA = 0, W_LOAD0 = 1, W_DEC0 = W_LOAD0 + kLoadWarps,
+              W_MMA = W_DEC0 + kDecWarps;
+constexpr int kWarps = W_MMA + 1 + 4;
+constexpr int kThreadsWS = kWarps * 32;
 constexpr int kLoadThreads = kLoadWarps * 32, kDecThreads = kDecWarps * 32;
 constexpr uint32_t TMEM_COLS = 512;  // two 256-column accumulators
 
@@ -77,11 +83,16 @@ struct WsShared {
   uint64_t acc_full[2], acc_empty[2];
   uint32_t tmem_base;
   int abort_flag;
-  // Steps each role has completed, for the timeout record: [0] codes
-  // issued, [1..2] activation steps published per loader warp, [3..10]
-  // steps decoded per decoder warp, [11] steps issued to the tensor core,
-  // [12] tiles started by it, [13] tiles finished by the epilogue.
-  int prog[14];
+  // Steps each role has completed, for the timeout record: [warp] for the
+  // TMA warp (codes issued), the loader warps (activation steps published)
+  // and the decoder warps (steps decoded); [kWarps] steps issued to the
+  // tensor core, [kWarps + 1] tiles started by it, [kWarps + 2] tiles
+  // finished by the epilogue.
+  int prog[kWarps + 3];
+  // copies of the per-expert tile prefix and row offsets (E + 1 entries),
+  // so that finding a tile's expert costs shared-memory reads only
+  int tile_off[kMaxExperts + 1];
+  int expert_off[kMaxExperts + 1];
 };
 
 // Warp-uniform bounded wait: every lane polls the barrier together (the
@@ -121,20 +132,27 @@ __device__ __forceinline__ bool warp_wait(WsShared& sh, uint64_t* bar, uint32_t 
       status[3] = step;
       status[4] = (int)parity;
       status[5] = (int)blockIdx.x;
+      // [6] codes issued, [7..8] min/max activation steps published,
+      // [9..10] min/max steps decoded, [11] steps issued to the tensor
+      // core, [12] tiles it started, [13] tiles the epilogue finished
       const volatile int* pg = sh.prog;
-      int dmin = pg[3], dmax = pg[3];
-      for (int i = 4; i < 11; ++i) {
-        dmin = min(dmin, pg[i]);
-        dmax = max(dmax, pg[i]);
+      int lmin = pg[W_LOAD0], lmax = pg[W_LOAD0], dmin = pg[W_DEC0], dmax = pg[W_DEC0];
+      for (int i = 1; i < kLoadWarps; ++i) {
+        lmin = min(lmin, pg[W_LOAD0 + i]);
+        lmax = max(lmax, pg[W_LOAD0 + i]);
       }
-      status[6] = pg[0];
-      status[7] = pg[1];
-      status[8] = pg[2];
+      for (int i = 1; i < kDecWarps; ++i) {
+        dmin = min(dmin, pg[W_DEC0 + i]);
+        dmax = max(dmax, pg[W_DEC0 + i]);
+      }
+      status[6] = pg[W_TMA];
+      status[7] = lmin;
+      status[8] = lmax;
       status[9] = dmin;
       status[10] = dmax;
-      status[11] = pg[11];
-      status[12] = pg[12];
-      status[13] = pg[13];
+      status[11] = pg[kWarps];
+      status[12] = pg[kWarps + 1];
+      status[13] = pg[kWarps + 2];
     }
   }
   __syncwarp();
@@ -145,18 +163,20 @@ struct TileInfo {
   int e, r0, mrows, m0, n0;
 };
 
-__device__ __forceinline__ TileInfo tile_info(const GemmArgs& a, int t, bool gateup) {
+// Tile t -> expert, rows and columns, from the shared-memory copies.
+__device__ __forceinline__ TileInfo tile_info(const WsShared& sh, const GemmArgs& a, int t,
+                                              bool gateup) {
   TileInfo ti;
   const int slot = t / a.n_ntiles, nt = t % a.n_ntiles;
   int lo = 0, hi = a.E;  // largest e with tile_off[e] <= slot
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (a.tile_off[mid] <= slot) lo = mid; else hi = mid;
+    if (sh.tile_off[mid] <= slot) lo = mid; else hi = mid;
   }
   ti.e = lo;
-  ti.r0 = a.expert_off[lo];
-  ti.m0 = (slot - a.tile_off[lo]) * BM;
-  ti.mrows = min(BM, a.expert_off[lo + 1] - ti.r0 - ti.m0);
+  ti.r0 = sh.expert_off[lo];
+  ti.m0 = (slot - sh.tile_off[lo]) * BM;
+  ti.mrows = min(BM, sh.expert_off[lo + 1] - ti.r0 - ti.m0);
   ti.n0 = nt * (gateup ? BN / 2 : BN);
   return ti;
 }
@@ -166,7 +186,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemmArgs& a, int t, bool gat
 template <bool GATEUP>
 __global__ void __launch_bounds__(kThreadsWS, 1)
 k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
-                 const GemmArgs args) {
+                 const __grid_constant__ CUtensorMap tm2, const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ WsShared sh;
   griddep_wait();
@@ -189,7 +209,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
       mbar_init(&sh.b8_empty[s], kDecWarps);
     }
     for (int s = 0; s < NA; ++s) {
-      mbar_init(&sh.a_full[s], kLoadWarps);
+      mbar_init(&sh.a_full[s], GATEUP ? kLoadWarps : 1);
       mbar_init(&sh.a_empty[s], 1);
     }
     for (int s = 0; s < NC; ++s) {
@@ -201,8 +221,12 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
       mbar_init(&sh.acc_empty[s], 4);
     }
     sh.abort_flag = 0;
-    for (int i = 0; i < 14; ++i) sh.prog[i] = 0;
+    for (int i = 0; i < kWarps + 3; ++i) sh.prog[i] = 0;
     fence_mbar_init();
+  }
+  for (int i = tid; i <= a.E; i += kThreadsWS) {
+    sh.tile_off[i] = a.tile_off[i];
+    sh.expert_off[i] = a.expert_off[i];
   }
   if (warp == 0) {
     tc::tmem_alloc(&sh.tmem_base, TMEM_COLS);
@@ -218,7 +242,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
     int j = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-      const TileInfo ti = tile_info(a, t, GATEUP);
+      const TileInfo ti = tile_info(sh, a, t, GATEUP);
       for (int ks = 0; ks < nK; ++ks, ++j) {
         const int sb = j % NB;
         if (j >= NB && !warp_wait(sh, &sh.b8_empty[sb], (uint32_t)(((j / NB) - 1) & 1), a.status, 1, j)) {
@@ -238,7 +262,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
           } else {
             tc::tma_load_2d(dst, &tm0, ks * BK, row, &sh.b8_full[sb]);
           }
-          reinterpret_cast<volatile int*>(sh.prog)[0] = j + 1;
+          reinterpret_cast<volatile int*>(sh.prog)[W_TMA] = j + 1;
         }
         __syncwarp();
       }
@@ -246,21 +270,59 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
     // drain: the copies of the last NB steps issued must have landed
     if (lane == 0)
       for (int i = max(0, j - NB); i < j; ++i) mbar_wait(&sh.b8_full[i % NB], (uint32_t)((i / NB) & 1));
-  } else if (warp >= W_LOAD0 && warp < W_LOAD0 + kLoadWarps) {
+  } else if (!GATEUP && warp > W_LOAD0 && warp < W_LOAD0 + kLoadWarps) {
+    // down: one TMA warp loads the rows; the other loader warps idle
+  } else if (!GATEUP && warp == W_LOAD0) {
+    // ------------------------------------------------ hid rows (TMA, down)
+    // The down projection's rows are consecutive permuted rows: one
+    // 128-byte-swizzled box of 64 columns x 128 rows per step (rows past the
+    // expert's segment are computed and never stored; rows past P read 0).
+    int j = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+      const TileInfo ti = tile_info(sh, a, t, GATEUP);
+      for (int ks = 0; ks < nK; ++ks, ++j) {
+        const int sa = j % NA;
+        if (j >= NA && !warp_wait(sh, &sh.a_empty[sa], (uint32_t)(((j / NA) - 1) & 1), a.status, 2, j)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&sh.a_full[sa], A_BYTES);
+          tc::tma_load_2d(smem + OFF_A + sa * A_BYTES, &tm1, ks * BK, ti.r0 + ti.m0, &sh.a_full[sa]);
+          reinterpret_cast<volatile int*>(sh.prog)[warp] = j + 1;
+        }
+        __syncwarp();
+      }
+    }
+    // drain: the copies of the last NA steps issued must have landed
+    if (lane == 0)
+      for (int i = max(0, j - NA); i < j; ++i) mbar_wait(&sh.a_full[i % NA], (uint32_t)((i / NA) & 1));
+    __syncwarp();
+  } else if (GATEUP && warp >= W_LOAD0 && warp < W_LOAD0 + kLoadWarps) {
     // ------------------------------------------------ activation rows (cp.async)
     constexpr int RPT = (BM * 8) / kLoadThreads;  // 16-byte chunks per thread per step
     const int lt = tid - W_LOAD0 * 32;
     const int jj = lt & 7, mb = lt >> 3;  // chunk in row; rows mb + (kLoadThreads/8) u
     int j = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-      const TileInfo ti = tile_info(a, t, GATEUP);
-      int src[RPT];
+    // source rows of a tile (token rows for gate/up)
+    auto rows_of = [&](int t, int (&src)[RPT]) {
+      const TileInfo ti = tile_info(sh, a, t, GATEUP);
 #pragma unroll
       for (int u = 0; u < RPT; ++u) {
         const int m = mb + (kLoadThreads / 8) * u;
-        src[u] = m < ti.mrows ? (GATEUP ? a.row_token[ti.r0 + ti.m0 + m] : ti.r0 + ti.m0 + m) : -1;
+        src[u] = m < ti.mrows ? a.row_token[ti.r0 + ti.m0 + m] : -1;
       }
+    };
+    int src_next[RPT];
+    if ((int)blockIdx.x < n_tiles) rows_of(blockIdx.x, src_next);
+    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+      int src[RPT];
+#pragma unroll
+      for (int u = 0; u < RPT; ++u) src[u] = src_next[u];
+      // the next tile's token rows load while this tile streams
+      if (t + (int)gridDim.x < n_tiles) rows_of(t + gridDim.x, src_next);
       for (int ks = 0; ks < nK; ++ks, ++j) {
         const int sa = j % NA;
         if (j >= NA && !warp_wait(sh, &sh.a_empty[sa], (uint32_t)(((j / NA) - 1) & 1), a.status, 2, j)) {
@@ -304,7 +366,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
     int j = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-      const TileInfo ti = tile_info(a, t, GATEUP);
+      const TileInfo ti = tile_info(sh, a, t, GATEUP);
       const size_t srow = (size_t)ti.e * nRb + ti.n0 / kScaleBlock;
       for (int ks = 0; ks < nK; ++ks, ++j) {
         const int sb = j % NB, c = j % NC;
@@ -351,7 +413,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
         if (lane == 0) {
           mbar_arrive(&sh.b16_full[c]);
           mbar_arrive(&sh.b8_empty[sb]);
-          reinterpret_cast<volatile int*>(sh.prog)[warp] = j + 1;  // warps 3-10
+          reinterpret_cast<volatile int*>(sh.prog)[warp] = j + 1;
         }
       }
     }
@@ -386,8 +448,8 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
           tc::commit(&sh.a_empty[sa]);
           tc::commit(&sh.b16_empty[c]);
           if (ks == nK - 1) tc::commit(&sh.acc_full[acc]);
-          reinterpret_cast<volatile int*>(sh.prog)[11] = j + 1;
-          reinterpret_cast<volatile int*>(sh.prog)[12] = tl + 1;
+          reinterpret_cast<volatile int*>(sh.prog)[kWarps] = j + 1;
+          reinterpret_cast<volatile int*>(sh.prog)[kWarps + 1] = tl + 1;
         }
         __syncwarp();
       }
@@ -403,7 +465,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
       const int acc = tl & 1;
       if (!warp_wait(sh, &sh.acc_full[acc], (uint32_t)((tl >> 1) & 1), a.status, 8, tl)) break;
       tc::fence_after_sync();
-      const TileInfo ti = tile_info(a, t, GATEUP);
+      const TileInfo ti = tile_info(sh, a, t, GATEUP);
       const uint32_t tl_addr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
       if (GATEUP) {
         uint16_t* hid = reinterpret_cast<uint16_t*>(a.out);
@@ -436,13 +498,31 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
         if (overflow) raise_status(a.status, MOE_DEV_FP16_RANGE);
       } else {
         float* y = reinterpret_cast<float*>(a.out);
+        // A warp whose 32 rows all belong to the tile's expert stages each
+        // 32-column chunk in shared memory and writes it with one TMA store
+        // (whole 128-byte row segments); a partial group stores directly.
+        const bool whole = quad * 32 + 32 <= ti.mrows;
+        uint8_t* stg = smem + OFF_EPI + quad * 4096;
 #pragma unroll 1
         for (int c8 = 0; c8 < 8; ++c8) {
           const int col = c8 * 32;
           uint32_t v[32];
           tc::ld_32x32b_x32(tl_addr + col, v);
           tc::wait_ld();
-          if (m < ti.mrows) {
+          if (whole) {
+            if (lane == 0) tc::bulk_wait_read_all();  // the previous store has read the tile
+            __syncwarp();
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              *reinterpret_cast<uint4*>(stg + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+                  make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            tc::fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+              tc::tma_store_2d(&tm2, ti.n0 + col, ti.r0 + ti.m0 + quad * 32, stg);
+              tc::bulk_commit();
+            }
+          } else if (m < ti.mrows) {
             float4* dst = reinterpret_cast<float4*>(
                 y + (size_t)(ti.r0 + ti.m0 + m) * a.out_ld + ti.n0 + col);
 #pragma unroll
@@ -455,8 +535,10 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap tm0, const __grid_constant_
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.acc_empty[acc]);
-      if (lane == 0 && quad == 0) reinterpret_cast<volatile int*>(sh.prog)[13] = tl + 1;
+      if (lane == 0 && quad == 0) reinterpret_cast<volatile int*>(sh.prog)[kWarps + 2] = tl + 1;
     }
+    if (!GATEUP && lane == 0) tc::bulk_wait_all();  // every TMA store is complete
+    __syncwarp();
   }
 
   // ---- all roles done: free TMEM
@@ -526,21 +608,32 @@ cudaError_t get_encoder(EncodeTiled* out) {
 }
 }  // namespace
 
-cudaError_t make_u8_tensor_map(CUtensorMap* map, const uint8_t* base, long long rows, int cols,
-                               int box_cols, int box_rows, bool swizzle128) {
+namespace {
+// 2-D map over a row-major matrix [rows, cols] of esize-byte elements.
+cudaError_t make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, int esize, const void* base,
+                        long long rows, int cols, int box_cols, int box_rows, int swizzle_bytes) {
   EncodeTiled enc;
   cudaError_t e = get_encoder(&enc);
   if (e != cudaSuccess) return e;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)cols};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * esize};
   const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r =
-      enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box,
-          estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+      enc(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE,
+          swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+          : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                : CU_TENSOR_MAP_SWIZZLE_NONE,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+}  // namespace
+
+cudaError_t make_u8_tensor_map(CUtensorMap* map, const uint8_t* base, long long rows, int cols,
+                               int box_cols, int box_rows, bool swizzle128) {
+  return make_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, rows, cols, box_cols, box_rows,
+                     swizzle128 ? 128 : 0);
 }
 
 namespace {
@@ -568,6 +661,16 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x16, const int32_t* expert_off
   if ((err = code_map(&gmap, w.gate.codes, (long long)E * I, H, 128)) != cudaSuccess) return err;
   if ((err = code_map(&umap, w.up.codes, (long long)E * I, H, 128)) != cudaSuccess) return err;
   if ((err = code_map(&dmap, w.down.codes, (long long)E * H, I, 256)) != cudaSuccess) return err;
+  // hid [P, I] fp16, read by the down projection: 64 columns x 128 rows,
+  // 128-byte swizzled (the K-major operand layout the MMA descriptors use)
+  CUtensorMap hmap, ymap;
+  if ((err = make_map_2d(&hmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, hid, P, I, BK, BM, 128)) !=
+      cudaSuccess)
+    return err;
+  // y [P, H] fp32, written by the down epilogue: 32 columns x 32 rows, swizzled
+  if ((err = make_map_2d(&ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, y, P, H, 32, 32, 128)) !=
+      cudaSuccess)
+    return err;
   err = launch_k(k_tile_offsets, dim3(1), dim3(1024), 0, s, pdl, expert_off, E, tile_off);
   if (err != cudaSuccess) return err;
   // Host bound on the tile count: each expert adds at most one partial tile.
@@ -577,12 +680,12 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x16, const int32_t* expert_off
   GemmArgs g{x16, H, I, expert_off, row_token, tile_off, E, w.gate.scales, w.up.scales,
              (void*)hid, I, I / (BN / 2), status};
   err = launch_k(k_expert_gemm_ws<true>, dim3(min(nsm, max_mtiles * g.n_ntiles)), blk,
-                 (size_t)SMEM_WS, s, pdl, gmap, umap, g);
+                 (size_t)SMEM_WS, s, pdl, gmap, umap, ymap, g);
   if (err != cudaSuccess) return err;
   GemmArgs d{(const uint16_t*)hid, I, H, expert_off, row_token, tile_off, E, w.down.scales,
              nullptr, (void*)y, H, H / BN, status};
   return launch_k(k_expert_gemm_ws<false>, dim3(min(nsm, max_mtiles * d.n_ntiles)), blk,
-                  (size_t)SMEM_WS, s, pdl, dmap, dmap, d);
+                  (size_t)SMEM_WS, s, pdl, dmap, hmap, ymap, d);
 }
 
 }  // namespace moe
