@@ -177,6 +177,7 @@ WsLayout ws_layout(const moe_dims& d) {
   L.sh_active = take(2 * 4);
   L.tile_off = take((E + 1) * 4);
   L.sh_tile_off = take(2 * 4);
+  L.x_perm = take(expert_gemm_tc_ok(d.H, d.I) ? P * H * 2 : 0);
   L.total = o;
   return L;
 }
@@ -301,9 +302,9 @@ moe_status moe_expert_ffn_fp8(const uint16_t* x, const int32_t* expert_off,
              "moe_expert_ffn_fp8");
   const int P = d.T * d.k;
   if (use_expert_gemm(P, d.E, d.H, d.I))
-    CUDA_CHECK(launch_expert_gemm_tc(x16, expert_off, row_token, d.E, P, w, d.H, d.I,
-                                     at<int32_t>(ws, L.tile_off), at<uint16_t>(ws, L.hid), y_perm,
-                                     status, st, true),
+    CUDA_CHECK(launch_expert_gemm_tc(x16, d.T, expert_off, row_token, at<uint16_t>(ws, L.x_perm),
+                                     d.E, P, w, d.H, d.I, at<int32_t>(ws, L.tile_off),
+                                     at<uint16_t>(ws, L.hid), y_perm, status, st, true),
                "moe_expert_ffn_fp8");
   else
     CUDA_CHECK(launch_expert_gemv(x16, expert_off, row_token, active, d.E < P ? d.E : P, w, d.H,
@@ -390,9 +391,9 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
                  "moe_layer_forward: shared");
   }
   if (use_expert_gemm(P, d.E, d.H, d.I))
-    CUDA_CHECK(launch_expert_gemm_tc(x16, off, row_token, d.E, P, routed, d.H, d.I,
-                                     at<int32_t>(ws, L.tile_off), at<uint16_t>(ws, L.hid), y_perm,
-                                     status, st, true),
+    CUDA_CHECK(launch_expert_gemm_tc(x16, d.T, off, row_token, at<uint16_t>(ws, L.x_perm), d.E, P,
+                                     routed, d.H, d.I, at<int32_t>(ws, L.tile_off),
+                                     at<uint16_t>(ws, L.hid), y_perm, status, st, true),
                "moe_layer_forward: experts");
   else
     CUDA_CHECK(launch_expert_gemv(x16, off, row_token, active, d.E < P ? d.E : P, routed, d.H,
@@ -403,7 +404,8 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
   if (has_shared) {
     shared_y = at<float>(ws, L.sh_y);
     if (use_expert_gemm(d.T, 1, d.H, d.I_shared))
-      CUDA_CHECK(launch_expert_gemm_tc(x16, soff, srows, 1, d.T, *shared, d.H, d.I_shared,
+      CUDA_CHECK(launch_expert_gemm_tc(x16, d.T, soff, srows, nullptr, 1, d.T, *shared, d.H,
+                                       d.I_shared,
                                        at<int32_t>(ws, L.sh_tile_off), at<uint16_t>(ws, L.sh_hid),
                                        shared_y, status, st, true),
                  "moe_layer_forward: shared expert");

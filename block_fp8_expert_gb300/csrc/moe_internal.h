@@ -44,10 +44,6 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
 // Raises `func`'s dynamic shared-memory limit to `bytes`, once per device
 // (host-side attribute; the first call on a device should precede capture).
 cudaError_t ensure_smem(const void* func, int bytes);
-// 2-D TMA map over a row-major uint8 matrix [rows, cols]: box = box_cols x
-// box_rows, optionally 128-byte swizzled; L2 256-byte promotion.
-cudaError_t make_u8_tensor_map(CUtensorMap* map, const uint8_t* base, long long rows, int cols,
-                               int box_cols, int box_rows, bool swizzle128);
 
 // Largest expert count the library accepts.
 constexpr int kMaxExperts = 1024;
@@ -59,7 +55,7 @@ int num_sms();
 struct WsLayout {
   size_t status, logits, rank, block_cnt, block_base, active, idx, w, off, row_token,
       tok_slot_row, row_pair, x16, hid, y_perm, sh_hid, sh_y, sh_off, sh_rows, sh_active,
-      tile_off, sh_tile_off, total;
+      tile_off, sh_tile_off, x_perm, total;
 };
 WsLayout ws_layout(const moe_dims& d);
 
@@ -107,12 +103,16 @@ cudaError_t launch_expert_gemv(const uint16_t* x16, const int32_t* expert_off,
 
 // Grouped GEMM on the tensor cores (tcgen05) for many tokens per expert:
 // gate/up + SwiGLU -> hid, then down -> y.  Needs H % 256 == 0 and
-// I % 128 == 0 (expert_gemm_tc_ok).  tile_off: E + 1 ints of scratch.
+// I % 128 == 0, H, I <= 4096 (expert_gemm_tc_ok).  tile_off: E + 1 ints of scratch.
 bool expert_gemm_tc_ok(int H, int I);
-cudaError_t launch_expert_gemm_tc(const uint16_t* x16, const int32_t* expert_off,
-                                  const int32_t* row_token, int E, int P, const moe_fp8_ffn& w,
-                                  int H, int I, int32_t* tile_off, uint16_t* hid, float* y,
-                                  int32_t* status, cudaStream_t s, bool pdl);
+// x16: [T, H] fp16.  x_perm: [P, H] fp16 scratch that receives the
+// activation rows in expert order (x16[row_token[p]]), or NULL when row_token
+// is the identity (the rows of x16 are then read in place).
+cudaError_t launch_expert_gemm_tc(const uint16_t* x16, int T, const int32_t* expert_off,
+                                  const int32_t* row_token, uint16_t* x_perm, int E, int P,
+                                  const moe_fp8_ffn& w, int H, int I, int32_t* tile_off,
+                                  uint16_t* hid, float* y, int32_t* status, cudaStream_t s,
+                                  bool pdl);
 
 // Regime: true -> tensor-core grouped GEMM, false -> streamed grouped GEMV.
 // Decided on the host from shapes only; MOE_FP8_EXPERT_PATH=gemm|gemv in the
