@@ -26,7 +26,9 @@
 //   warps 3-10  decode codes to fp16 times the block scale
 //               (fp16(dec * fp16(scale))) and store them into a TMEM stage;
 //               warp w serves TMEM lanes 32 (w % 4) .. + 31 of one block;
-//   warps 11-14 epilogue: tcgen05.ld from the accumulators, SwiGLU, stores.
+//   warps 11-18 epilogue: tcgen05.ld from the accumulators, SwiGLU, stores;
+//               warp w reads TMEM lanes 32 (w % 4) .. + 31, half of the
+//               tile's columns (gate/up) or one of the two blocks (down).
 // Every wait is bounded (about 2 s) and also gives up as soon as another
 // role has given up, recording MOE_DEV_WAIT_TIMEOUT; the CTA then drains its
 // copies and MMAs and frees its TMEM before it exits.
@@ -48,13 +50,15 @@ constexpr int T_BYTES = BT * BK * 2;    // 16 KB
 constexpr int C_BYTES = 2 * BW * BK;    // 16 KB: two code blocks of 8 KB
 constexpr int OFF_T = 0;
 constexpr int OFF_C = OFF_T + NT * T_BYTES;
-// gate/up epilogue: per epilogue warp a hid tile [128 tokens][32 features]
-// fp16 (8 KB), written to global memory one 64-byte row per bulk copy
-constexpr int STG_WARP_BYTES = BT * 32 * 2;
-constexpr int STG_BYTES = 4 * STG_WARP_BYTES;  // 32 KB
+// Epilogue staging, 4 KB per epilogue warp: gate/up stages its half of a hid
+// tile, [64 tokens][32 features] fp16, written one 64-byte row per bulk copy;
+// down stages one fp32 tile [32 tokens][32 features] (128-byte swizzled) at a
+// time, each written by one TMA store.
+constexpr int STG_WARP_BYTES = 4096;
 constexpr int OFF_STG = OFF_C + NCD * C_BYTES;
+constexpr int kDecWarps = 8, kEpiWarps = 8;
+constexpr int STG_BYTES = kEpiWarps * STG_WARP_BYTES;  // 32 KB
 constexpr int SMEM_WS = OFF_STG + STG_BYTES + 1024;  // + alignment slack
-constexpr int kDecWarps = 8, kEpiWarps = 4;
 // warp roles: code TMA, token TMA, MMA issue, decoders, epilogue
 constexpr int W_CODES = 0, W_TOK = 1, W_MMA = 2, W_DEC0 = 3, W_EPI0 = W_DEC0 + kDecWarps;
 constexpr int kWarps = W_EPI0 + kEpiWarps;
@@ -64,7 +68,7 @@ constexpr uint32_t COL_D1 = BT;       // D0 at column 0, D1 at 128
 constexpr uint32_t COL_A = 2 * BT;    // weight stages from column 256
 constexpr uint32_t A_STAGE_COLS = 64;  // two blocks x 32 columns (64 fp16 of K)
 static_assert(COL_A + NA * A_STAGE_COLS <= TMEM_COLS, "TMEM budget");
-static_assert(kDecWarps == 8 && kEpiWarps == 4, "two blocks x four lane quarters");
+static_assert(kDecWarps == 8 && kEpiWarps == 8, "two blocks (or halves) x four lane quarters");
 
 struct GemmArgs {
   const int32_t* expert_off;
@@ -202,7 +206,8 @@ __device__ __forceinline__ TileInfo tile_info(const WsShared& sh, const GemmArgs
 template <bool GATEUP>
 __global__ void __launch_bounds__(kThreadsWS, 1)
 k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant__ CUtensorMap cm1,
-                 const __grid_constant__ CUtensorMap tmap, const GemmArgs args) {
+                 const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_y,
+                 const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ WsShared sh;
   griddep_wait();
@@ -429,38 +434,38 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     if (lane == 0 && j > 0) mbar_wait(&sh.a_empty[(j - 1) % NA], (uint32_t)(((j - 1) / NA) & 1));
     __syncwarp();
   } else {
-    // ------------------------------------------------ epilogue (warps 11-14)
+    // ------------------------------------------------ epilogue (warps 11-18)
     // Lane quarter q of both accumulators: weight rows 32 q + lane; columns
-    // are the tile's tokens.
-    const int q = warp & 3;
+    // are the tile's tokens.  Half eh of the epilogue warps takes the 32-token
+    // chunks c = eh, eh + 2 (gate/up) or block eh (down).
+    const int q = warp & 3, eh = (warp - W_EPI0) >> 2;
     const uint32_t t_lane = tmem + ((uint32_t)(32 * q) << 16);
-    uint8_t* stg = smem + OFF_STG + q * STG_WARP_BYTES;
+    uint8_t* stg = smem + OFF_STG + (warp - W_EPI0) * STG_WARP_BYTES;
     int tl = 0;
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tl) {
       const TileInfo ti = tile_info(sh, a, t, GATEUP);
-      if (GATEUP) {
-        // this warp's row copies of the previous tile have read its staging
-        tc::bulk_wait_read_all();
-        __syncwarp();
-      }
+      // this warp's copies of the previous tile have read its staging
+      tc::bulk_wait_read_all();
+      __syncwarp();
       if (!warp_wait(sh, &sh.acc_full, (uint32_t)(tl & 1), a.status, 8, tl)) break;
       tc::fence_after_sync();
       const int nchunks = (ti.n + 31) >> 5;
       if (GATEUP) {
         bool overflow = false;
 #pragma unroll 1
-        for (int c = 0; c < nchunks; ++c) {
+        for (int c = eh; c < nchunks; c += 2) {
           uint32_t gr[32], ur[32];
           tc::ld_32x32b_x32(t_lane + 32 * c, gr);
           tc::ld_32x32b_x32(t_lane + COL_D1 + 32 * c, ur);
           tc::wait_ld();
           const int nv = ti.rows - 32 * c;  // columns of real tokens in this chunk
+          uint8_t* rows = stg + (c >> 1) * (32 * 64);
 #pragma unroll
           for (int v = 0; v < 32; ++v) {
             const float g = __uint_as_float(gr[v]), u = __uint_as_float(ur[v]);
             const float h = __fdividef(g, 1.f + __expf(-g)) * u;  // silu(g) * u
             overflow |= v < nv && !(fabsf(h) <= kF16Max);
-            *reinterpret_cast<uint16_t*>(stg + (32 * c + v) * 64 + lane * 2) = f32_to_f16_bits(h);
+            *reinterpret_cast<uint16_t*>(rows + v * 64 + lane * 2) = f32_to_f16_bits(h);
           }
         }
         if (overflow) raise_status(a.status, MOE_DEV_FP16_RANGE);
@@ -468,40 +473,62 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.acc_empty);
         // staged rows -> bulk copies (async proxy): features 32 q .. + 31 of
-        // each token row, 64 bytes
+        // each of this half's token rows, 64 bytes
         tc::fence_proxy_async();
         __syncwarp();
         uint16_t* hid = reinterpret_cast<uint16_t*>(a.out) + (size_t)(ti.r0 + ti.m0) * a.out_ld +
                         ti.n0 + 32 * q;
-        for (int m = lane; m < ti.rows; m += 32)
-          tc::bulk_store(hid + (size_t)m * a.out_ld, stg + m * 64, 64);
+        for (int i = lane; i < 64; i += 32) {
+          const int c = 2 * (i >> 5) + eh, m = 32 * c + (i & 31);  // token row of staged row i
+          if (m < ti.rows) tc::bulk_store(hid + (size_t)m * a.out_ld, stg + i * 64, 64);
+        }
         tc::bulk_commit();
       } else {
+        // Chunk c of block eh: features n0 + 128 eh + 32 q .. + 31 (this
+        // warp's lanes) x tokens 32 c .. 32 c + 31 (the chunk's columns).  A
+        // chunk of 32 real tokens is staged token-major (row = token, 128
+        // bytes, 16-byte groups swizzled by token % 8: conflict-free, one word
+        // per lane) and written by one TMA store; a ragged chunk is stored
+        // directly, its real tokens only.
         float* y = reinterpret_cast<float*>(a.out) + (size_t)(ti.r0 + ti.m0) * a.out_ld + ti.n0 +
-                   32 * q + lane;
+                   eh * BW + 32 * q + lane;
 #pragma unroll 1
-        for (int blk = 0; blk < 2; ++blk) {
-#pragma unroll 1
-          for (int c = 0; c < nchunks; ++c) {
-            uint32_t v[32];
-            tc::ld_32x32b_x32(t_lane + blk * COL_D1 + 32 * c, v);
-            tc::wait_ld();
-            if (blk == 1 && c == nchunks - 1) {
-              // every read of the accumulators is done: the next tile may start
-              tc::fence_before_sync();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&sh.acc_empty);
-            }
-            const int nv = min(32, ti.rows - 32 * c);
+        for (int c = 0; c < nchunks; ++c) {
+          uint32_t v[32];
+          tc::ld_32x32b_x32(t_lane + eh * COL_D1 + 32 * c, v);
+          tc::wait_ld();
+          if (c == nchunks - 1) {
+            // this warp's reads of the accumulators are done
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.acc_empty);
+          }
+          const int nv = ti.rows - 32 * c;
+          if (nv >= 32) {
+            // the previous store from the staging tile has read it
+            tc::bulk_wait_read_all();
+            __syncwarp();
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              if (i < nv) y[(size_t)(32 * c + i) * a.out_ld + blk * BW] = __uint_as_float(v[i]);
+              *reinterpret_cast<uint32_t*>(stg + i * 128 + (((lane >> 2) ^ (i & 7)) << 4) +
+                                           (lane & 3) * 4) = v[i];
+            tc::fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {  // bulk groups are per thread: always the same lane
+              tc::tma_store_2d(&tmap_y, ti.n0 + eh * BW + 32 * q, ti.r0 + ti.m0 + 32 * c, stg);
+              tc::bulk_commit();
+            }
+            __syncwarp();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < nv) y[(size_t)(32 * c + i) * a.out_ld] = __uint_as_float(v[i]);
           }
         }
       }
-      if (lane == 0 && q == 0) reinterpret_cast<volatile int*>(sh.prog)[kWarps + 2] = tl + 1;
+      if (lane == 0 && q == 0 && eh == 0) reinterpret_cast<volatile int*>(sh.prog)[kWarps + 2] = tl + 1;
     }
-    if (GATEUP) tc::bulk_wait_all();  // every row copy is complete
+    tc::bulk_wait_all();  // every bulk copy and TMA store of this warp is complete
     __syncwarp();
   }
 
@@ -634,7 +661,7 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x16, int T, const int32_t* exp
   cudaError_t err;
   if ((err = ensure_smem((const void*)k_expert_gemm_ws<true>, SMEM_WS)) != cudaSuccess) return err;
   if ((err = ensure_smem((const void*)k_expert_gemm_ws<false>, SMEM_WS)) != cudaSuccess) return err;
-  CUtensorMap gmap, umap, dmap, xmap, hmap;
+  CUtensorMap gmap, umap, dmap, xmap, hmap, ymap;
   if ((err = code_map(&gmap, w.gate.codes, (long long)E * I, H)) != cudaSuccess) return err;
   if ((err = code_map(&umap, w.up.codes, (long long)E * I, H)) != cudaSuccess) return err;
   if ((err = code_map(&dmap, w.down.codes, (long long)E * H, I)) != cudaSuccess) return err;
@@ -646,6 +673,10 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x16, int T, const int32_t* exp
       cudaSuccess)
     return err;
   if ((err = make_map_2d(&hmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, hid, P, I, BK, BT, 128)) !=
+      cudaSuccess)
+    return err;
+  // y [P, H] fp32, written by the down epilogue: 32 columns x 32 rows, swizzled
+  if ((err = make_map_2d(&ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, y, P, H, 32, 32, 128)) !=
       cudaSuccess)
     return err;
   if (x_perm) {
@@ -662,12 +693,12 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x16, int T, const int32_t* exp
   GemmArgs g{expert_off, tile_off, E, H, I, w.gate.scales, w.up.scales,
              (void*)hid, I, I / BW, status};
   err = launch_k(k_expert_gemm_ws<true>, dim3(min(nsm, max_ttiles * g.n_wblocks)), blk,
-                 (size_t)SMEM_WS, s, pdl, gmap, umap, xmap, g);
+                 (size_t)SMEM_WS, s, pdl, gmap, umap, xmap, ymap, g);
   if (err != cudaSuccess) return err;
   GemmArgs d{expert_off, tile_off, E, I, H, w.down.scales, nullptr, (void*)y, H,
              H / (2 * BW), status};
   return launch_k(k_expert_gemm_ws<false>, dim3(min(nsm, max_ttiles * d.n_wblocks)), blk,
-                  (size_t)SMEM_WS, s, pdl, dmap, dmap, hmap, d);
+                  (size_t)SMEM_WS, s, pdl, dmap, dmap, hmap, ymap, d);
 }
 
 }  // namespace moe
