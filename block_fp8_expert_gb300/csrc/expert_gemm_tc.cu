@@ -619,8 +619,10 @@ cudaError_t get_encoder(EncodeTiled* out) {
   return fn ? cudaSuccess : (err != cudaSuccess ? err : cudaErrorNotSupported);
 }
 
+}  // namespace
+
 // 2-D map over a row-major matrix [rows, cols] of esize-byte elements.
-cudaError_t make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, int esize, const void* base,
+cudaError_t make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, int esize, const void* base,
                         long long rows, int cols, int box_cols, int box_rows, int swizzle_bytes) {
   EncodeTiled enc;
   cudaError_t e = get_encoder(&enc);
@@ -639,11 +641,12 @@ cudaError_t make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, int esize, 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+namespace {
 // 2-D map over a stack of code matrices [rows_total, K] (uint8, row-major):
 // box = 64 bytes of K x 128 rows, 64-byte swizzle (conflict-free reads of a
 // row's four 16-byte chunks by the lanes that own consecutive rows).
 cudaError_t code_map(CUtensorMap* map, const uint8_t* codes, long long rows_total, int K) {
-  return make_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, codes, rows_total, K, BK, BW, 64);
+  return make_tensor_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, codes, rows_total, K, BK, BW, 64);
 }
 }  // namespace
 
@@ -669,14 +672,14 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x16, int T, const int32_t* exp
   // already in order) and hid [P, I] fp16: 64 columns x 128 rows per box,
   // 128-byte swizzled (the K-major operand layout of the MMA)
   const uint16_t* xrows = x_perm ? x_perm : x16;
-  if ((err = make_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xrows, P, H, BK, BT, 128)) !=
+  if ((err = make_tensor_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xrows, P, H, BK, BT, 128)) !=
       cudaSuccess)
     return err;
-  if ((err = make_map_2d(&hmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, hid, P, I, BK, BT, 128)) !=
+  if ((err = make_tensor_map_2d(&hmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, hid, P, I, BK, BT, 128)) !=
       cudaSuccess)
     return err;
   // y [P, H] fp32, written by the down epilogue: 32 columns x 32 rows, swizzled
-  if ((err = make_map_2d(&ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, y, P, H, 32, 32, 128)) !=
+  if ((err = make_tensor_map_2d(&ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, y, P, H, 32, 32, 128)) !=
       cudaSuccess)
     return err;
   if (x_perm) {

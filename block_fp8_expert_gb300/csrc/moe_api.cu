@@ -178,6 +178,7 @@ WsLayout ws_layout(const moe_dims& d) {
   L.tile_off = take((E + 1) * 4);
   L.sh_tile_off = take(2 * 4);
   L.x_perm = take(expert_gemm_tc_ok(d.H, d.I) ? P * H * 2 : 0);
+  L.wr_planes = take(router_tc_ok(d.T, d.H, d.E) ? 3 * E * H * 2 : 0);
   L.total = o;
   return L;
 }
@@ -248,9 +249,9 @@ moe_status moe_route(const uint16_t* x, const float* Wr, const float* bias, moe_
   REQUIRE_PTR(topk_w);
   if ((s = check_ws(d, ws, ws_bytes)) != MOE_OK) return s;
   const WsLayout L = ws_layout(d);
-  CUDA_CHECK(launch_route(x, Wr, bias, d.T, d.H, d.E, d.k, at<float>(ws, L.logits), topk_idx,
-                          topk_w, nullptr, at<int32_t>(ws, L.status), (cudaStream_t)stream,
-                          true),
+  CUDA_CHECK(launch_route(x, Wr, bias, d.T, d.H, d.E, d.k, at<float>(ws, L.logits),
+                          at<uint16_t>(ws, L.wr_planes), topk_idx, topk_w, nullptr,
+                          at<int32_t>(ws, L.status), (cudaStream_t)stream, true),
              "moe_route");
   return MOE_OK;
 }
@@ -372,14 +373,15 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
     // router logits, then top-k + permutation (+ the shared expert's identity
     // permutation) in one CTA
     CUDA_CHECK(launch_route_permute_small(
-                   x, Wr, bias, d.T, d.H, d.E, d.k, at<float>(ws, L.logits), idx, w, off,
+                   x, Wr, bias, d.T, d.H, d.E, d.k, at<float>(ws, L.logits),
+                   at<uint16_t>(ws, L.wr_planes), idx, w, off,
                    row_token, tok_slot_row, at<int32_t>(ws, L.row_pair), active,
                    has_shared ? soff : nullptr, has_shared ? srows : nullptr,
                    has_shared ? sact : nullptr, x16, status, st, true),
                "moe_layer_forward: route+permute");
   } else {
-    CUDA_CHECK(launch_route(x, Wr, bias, d.T, d.H, d.E, d.k, at<float>(ws, L.logits), idx, w,
-                            x16, status, st, true),
+    CUDA_CHECK(launch_route(x, Wr, bias, d.T, d.H, d.E, d.k, at<float>(ws, L.logits),
+                            at<uint16_t>(ws, L.wr_planes), idx, w, x16, status, st, true),
                "moe_layer_forward: route");
     CUDA_CHECK(launch_permute(idx, d.T, d.E, d.k, at<int32_t>(ws, L.rank),
                               at<int32_t>(ws, L.block_cnt), at<int32_t>(ws, L.block_base), off,

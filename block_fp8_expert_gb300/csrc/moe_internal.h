@@ -45,6 +45,13 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
 // (host-side attribute; the first call on a device should precede capture).
 cudaError_t ensure_smem(const void* func, int bytes);
 
+// 2-D TMA map over a row-major matrix [rows, cols] of esize-byte elements:
+// box = box_cols x box_rows, swizzle 0, 64 or 128 bytes, L2 256-byte
+// promotion, out-of-range elements read as zero.
+cudaError_t make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, int esize,
+                               const void* base, long long rows, int cols, int box_cols,
+                               int box_rows, int swizzle_bytes);
+
 // Largest expert count the library accepts.
 constexpr int kMaxExperts = 1024;
 
@@ -55,7 +62,7 @@ int num_sms();
 struct WsLayout {
   size_t status, logits, rank, block_cnt, block_base, active, idx, w, off, row_token,
       tok_slot_row, row_pair, x16, hid, y_perm, sh_hid, sh_y, sh_off, sh_rows, sh_active,
-      tile_off, sh_tile_off, x_perm, total;
+      tile_off, sh_tile_off, x_perm, wr_planes, total;
 };
 WsLayout ws_layout(const moe_dims& d);
 
@@ -63,17 +70,25 @@ WsLayout ws_layout(const moe_dims& d);
 // programmatic stream serialisation (each begins with griddep_wait()).
 
 // Router logits (+ optional fp16 copy of x) and top-k.  `part` holds up to 8
-// K-slices of partial logits, [8][T][E] floats.
+// K-slices of partial logits, [8][T][E] floats; `planes` is scratch for the
+// bf16 split of Wr, [3][E][H] (used from 128 tokens, router_tc_ok).
 cudaError_t launch_route(const uint16_t* x, const float* Wr, const float* bias, int T, int H,
-                         int E, int k, float* part, int32_t* topk_idx, float* topk_w,
-                         uint16_t* x16, int32_t* status, cudaStream_t s, bool pdl);
+                         int E, int k, float* part, uint16_t* planes, int32_t* topk_idx,
+                         float* topk_w, uint16_t* x16, int32_t* status, cudaStream_t s, bool pdl);
+
+// Router logits on the tensor cores (route_tc.cu): T >= 128, E % 128 == 0,
+// H % 64 == 0.  Writes KS slices of partial logits (KS from route_kslices).
+bool router_tc_ok(int T, int H, int E);
+cudaError_t launch_router_logits_tc(const uint16_t* x, const float* Wr, int T, int H, int E,
+                                    int KS, float* part, uint16_t* x16, uint16_t* planes,
+                                    int32_t* status, cudaStream_t s, bool pdl);
 
 // Router logits, then top-k and the full permutation in one CTA, for
 // T*k <= 4096 (small_route_permute_ok).  sh_* may be NULL (no shared expert).
 bool small_route_permute_ok(int T, int E, int k);
 cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const float* bias,
                                        int T, int H, int E, int k, float* part,
-                                       int32_t* topk_idx, float* topk_w, int32_t* expert_off,
+                                       uint16_t* planes, int32_t* topk_idx, float* topk_w, int32_t* expert_off,
                                        int32_t* row_token, int32_t* tok_slot_row,
                                        int32_t* row_pair, int32_t* active, int32_t* sh_off,
                                        int32_t* sh_rows, int32_t* sh_active, uint16_t* x16,

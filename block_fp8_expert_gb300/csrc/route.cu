@@ -412,6 +412,13 @@ k_topk_permute_small(const float* __restrict__ part, int KS, const float* __rest
 }
 
 int route_kslices(int T, int H, int E) {
+  if (router_tc_ok(T, H, E)) {
+    // tensor-core path: split K until the CTAs fill about one wave
+    const int tiles = cdiv(T, 128) * (E / 128);
+    int ks = 1;
+    while (ks < kMaxKSlices && tiles * ks * 2 <= num_sms() && (H / (2 * ks)) % 64 == 0) ks *= 2;
+    return ks;
+  }
   // Split K across CTAs when few tokens leave too few CTAs to stream Wr: with
   // 8 slices each of the 4 warps of a CTA owns one 64-column chunk (H = 2048).
   // The top-k lane sums every slice of its experts; slices x experts per lane
@@ -425,9 +432,11 @@ int route_kslices(int T, int H, int E) {
 }
 
 cudaError_t launch_router_logits(const uint16_t* x, const float* Wr, int T, int H, int E,
-                                 float* part, uint16_t* x16, int32_t* status, cudaStream_t s,
-                                 bool pdl) {
+                                 float* part, uint16_t* planes, uint16_t* x16, int32_t* status,
+                                 cudaStream_t s, bool pdl) {
   const int KS = route_kslices(T, H, E);
+  if (router_tc_ok(T, H, E))
+    return launch_router_logits_tc(x, Wr, T, H, E, KS, part, x16, planes, status, s, pdl);
   const int kslice = H / KS;
   const dim3 blk(kRouteWarps * 32);
   if (T <= 8)
@@ -441,10 +450,10 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* Wr, int T, int 
 }
 
 cudaError_t launch_route(const uint16_t* x, const float* Wr, const float* bias, int T, int H,
-                         int E, int k, float* part, int32_t* topk_idx, float* topk_w,
-                         uint16_t* x16, int32_t* status, cudaStream_t s, bool pdl) {
+                         int E, int k, float* part, uint16_t* planes, int32_t* topk_idx,
+                         float* topk_w, uint16_t* x16, int32_t* status, cudaStream_t s, bool pdl) {
   if (T == 0) return cudaSuccess;
-  cudaError_t err = launch_router_logits(x, Wr, T, H, E, part, x16, status, s, pdl);
+  cudaError_t err = launch_router_logits(x, Wr, T, H, E, part, planes, x16, status, s, pdl);
   if (err != cudaSuccess) return err;
   const int KS = route_kslices(T, H, E);
   const int epl = cdiv(E, 32);
@@ -466,12 +475,13 @@ bool small_route_permute_ok(int T, int E, int k) {
 
 cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const float* bias,
                                        int T, int H, int E, int k, float* part,
-                                       int32_t* topk_idx, float* topk_w, int32_t* expert_off,
+                                       uint16_t* planes, int32_t* topk_idx, float* topk_w,
+                                       int32_t* expert_off,
                                        int32_t* row_token, int32_t* tok_slot_row,
                                        int32_t* row_pair, int32_t* active, int32_t* sh_off,
                                        int32_t* sh_rows, int32_t* sh_active, uint16_t* x16,
                                        int32_t* status, cudaStream_t s, bool pdl) {
-  cudaError_t err = launch_router_logits(x, Wr, T, H, E, part, x16, status, s, pdl);
+  cudaError_t err = launch_router_logits(x, Wr, T, H, E, part, planes, x16, status, s, pdl);
   if (err != cudaSuccess) return err;
   const int KS = route_kslices(T, H, E);
   const size_t smem = small_route_smem(E);

@@ -7,6 +7,12 @@ import moe_inputs as mi
 
 # Per-element bound of the layer statement: |gpu - ref| <= 1e-2 (|ref| + rms(ref)).
 REL = 1e-2
+# The renormalised top-k weights are values under the same statement; they are
+# checked 100x tighter.  The logits behind them accumulate in fp32 inside the
+# tensor cores (three bf16 parts of Wr), which leaves errors of order 1e-5 of
+# the logit scale over K = 2048 -- well inside the 1e-4 top-k gap the inputs
+# keep, so the indices stay exact.
+W_REL = 1e-4
 
 _layers = {}
 

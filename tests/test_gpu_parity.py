@@ -6,7 +6,7 @@ import pytest
 
 import moe_inputs as mi
 import oracle
-from gpu_common import assert_within_tol, bf16_bits, host_layer, require_gpu
+from gpu_common import W_REL, assert_within_tol, bf16_bits, host_layer, require_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -67,7 +67,7 @@ def test_route(torch, name, T):
     x = oracle.bf16_to_f64(xb)
     ridx, rw = oracle.topk_renorm(oracle.softmax(oracle.router_logits(x, L.Wr, L.bias)), L.k)
     assert np.array_equal(idx.cpu().numpy(), ridx)
-    assert_within_tol(w.cpu().numpy(), rw, "topk_w", rel=1e-5)
+    assert_within_tol(w.cpu().numpy(), rw, "topk_w", rel=W_REL)
 
 
 @pytest.mark.parametrize("T,E,k", [(1, 16, 2), (8, 16, 2), (13, 128, 8), (300, 512, 10),
@@ -184,7 +184,7 @@ def test_layer_forward_full(torch, name, T):
     out, idx, w = _forward(torch, D, _x(torch, xb))
     ref = oracle.moe_layer(xb, L, keep_intermediates=False)
     assert np.array_equal(idx.cpu().numpy(), ref["topk_idx"])
-    assert_within_tol(w.cpu().numpy(), ref["topk_w"], "topk_w", rel=1e-5)
+    assert_within_tol(w.cpu().numpy(), ref["topk_w"], "topk_w", rel=W_REL)
     assert_within_tol(oracle.bf16_to_f64(bf16_bits(out)), ref["out"], f"out {name} T={T}")
 
 
@@ -201,7 +201,7 @@ def test_layer_forward_sampled(torch, name, T):
     toks = np.unique(np.concatenate([[0, T - 1], rng.choice(T, 30, replace=False)]))
     ref = oracle.moe_layer_sampled(xb, L, toks)
     assert np.array_equal(idx.cpu().numpy(), ref["topk_idx"])
-    assert_within_tol(w.cpu().numpy(), ref["topk_w"], "topk_w", rel=1e-5)
+    assert_within_tol(w.cpu().numpy(), ref["topk_w"], "topk_w", rel=W_REL)
     got = oracle.bf16_to_f64(bf16_bits(out))[toks]
     assert_within_tol(got, ref["out_sampled"], f"out {name} T={T} (sampled)")
 
