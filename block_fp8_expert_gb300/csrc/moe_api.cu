@@ -105,16 +105,21 @@ T* at(void* ws, size_t off) {
 
 void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
 
-// Average tokens per expert from which the tensor-core GEMM replaces the
-// streamed GEMV.
-constexpr int kGemmMinRowsPerExpert = 32;
+// Average rows per expert from which the tensor-core GEMM replaces the
+// streamed GEMV.  Routed experts: from 5 (measured: at 4 per expert the two
+// paths take the same time, and the GEMM pulls ahead as soon as a few experts
+// are hot, since the GEMV re-streams an expert's weights for every group of 8
+// or 16 rows).  One dense expert (the shared one) has only I / 128 weight
+// tiles per 128 rows to spread over the SMs: from 32 rows.
+constexpr int kGemmMinRowsPerRoutedExpert = 5;
+constexpr int kGemmMinRowsDense = 32;
 
 bool use_expert_gemm(int rows, int experts, int H, int I) {
   if (!expert_gemm_tc_ok(H, I)) return false;
   const char* f = getenv("MOE_FP8_EXPERT_PATH");
   if (f && strcmp(f, "gemm") == 0) return true;
   if (f && strcmp(f, "gemv") == 0) return false;
-  return rows >= kGemmMinRowsPerExpert * experts;
+  return experts > 1 ? rows >= kGemmMinRowsPerRoutedExpert * experts : rows >= kGemmMinRowsDense;
 }
 
 cudaError_t ensure_smem(const void* func, int bytes) {
