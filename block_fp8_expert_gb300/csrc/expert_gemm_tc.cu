@@ -81,6 +81,7 @@ struct GemmArgs {
   void* out;            // hid fp16 [P, I] or y fp32 [P, H]
   int out_ld;
   int n_wblocks;  // weight-block pairs per expert (tiles per token tile)
+  int all_wait;   // 1: the previous kernel wrote the tile offsets (every warp waits)
   int32_t* status;
 };
 
@@ -210,7 +211,12 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
                  const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ WsShared sh;
-  griddep_wait();
+  // Only the token warp waits for the previous kernel (it reads that
+  // kernel's output: the expert-order activation rows or hid).  Everything
+  // else reads data written two or more launches back (tile and row offsets,
+  // weights), so on SMs the previous kernel has already left the codes are
+  // fetched and decoded while its last tiles finish.
+  if (args.all_wait) griddep_wait();
   griddep_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const GemmArgs& a = args;
@@ -293,6 +299,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     __syncwarp();
   } else if (warp == W_TOK) {
     // ------------------------------------------------ token rows (TMA)
+    griddep_wait();
     // One box of 128 consecutive permuted rows per step (rows past the tile
     // are never stored; rows past the matrix read 0).
     int j = 0;
@@ -682,24 +689,26 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x16, int T, const int32_t* exp
   if ((err = make_tensor_map_2d(&ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, y, P, H, 32, 32, 128)) !=
       cudaSuccess)
     return err;
+  // Tile offsets first, then the gather: the GEMMs' warps other than the
+  // token warp read the offsets without waiting for their previous kernel.
+  err = launch_k(k_tile_offsets, dim3(1), dim3(1024), 0, s, pdl, expert_off, E, tile_off);
+  if (err != cudaSuccess) return err;
   if (x_perm) {
     err = launch_k(k_gather_rows, dim3(cdiv(P, 8)), dim3(256), 0, s, pdl, x16, T, row_token,
                    expert_off, E, P, H, x_perm);
     if (err != cudaSuccess) return err;
   }
-  err = launch_k(k_tile_offsets, dim3(1), dim3(1024), 0, s, pdl, expert_off, E, tile_off);
-  if (err != cudaSuccess) return err;
   // Host bound on the tile count: each expert adds at most one partial tile.
   const int max_ttiles = cdiv(P, BT) + min(E, P);
   const int nsm = num_sms();
   const dim3 blk(kThreadsWS);
   GemmArgs g{expert_off, tile_off, E, H, I, w.gate.scales, w.up.scales,
-             (void*)hid, I, I / BW, status};
+             (void*)hid, I, I / BW, x_perm ? 0 : 1, status};
   err = launch_k(k_expert_gemm_ws<true>, dim3(min(nsm, max_ttiles * g.n_wblocks)), blk,
                  (size_t)SMEM_WS, s, pdl, gmap, umap, xmap, ymap, g);
   if (err != cudaSuccess) return err;
   GemmArgs d{expert_off, tile_off, E, I, H, w.down.scales, nullptr, (void*)y, H,
-             H / (2 * BW), status};
+             H / (2 * BW), 0, status};
   return launch_k(k_expert_gemm_ws<false>, dim3(min(nsm, max_ttiles * d.n_wblocks)), blk,
                   (size_t)SMEM_WS, s, pdl, dmap, dmap, hmap, ymap, d);
 }

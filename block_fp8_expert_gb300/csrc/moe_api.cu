@@ -106,12 +106,13 @@ T* at(void* ws, size_t off) {
 void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
 
 // Average rows per expert from which the tensor-core GEMM replaces the
-// streamed GEMV.  Routed experts: from 5 (measured: at 4 per expert the two
-// paths take the same time, and the GEMM pulls ahead as soon as a few experts
-// are hot, since the GEMV re-streams an expert's weights for every group of 8
-// or 16 rows).  One dense expert (the shared one) has only I / 128 weight
-// tiles per 128 rows to spread over the SMs: from 32 rows.
-constexpr int kGemmMinRowsPerRoutedExpert = 5;
+// streamed GEMV.  Routed experts: from 4 (measured crossover: at 2 rows per
+// expert the GEMV is 2% faster, at 4 the GEMM is 1% faster, and it pulls
+// further ahead as soon as a few experts are hot, since the GEMV re-streams an
+// expert's weights for every group of 8 or 16 rows).  One dense expert (the
+// shared one) has only I / 128 weight tiles per 128 rows to spread over the
+// SMs: from 32 rows.
+constexpr int kGemmMinRowsPerRoutedExpert = 4;
 constexpr int kGemmMinRowsDense = 32;
 
 bool use_expert_gemm(int rows, int experts, int H, int I) {
