@@ -58,6 +58,7 @@ _SIGNATURES = {
     "moe_last_error_message": (ctypes.c_char_p, []),
     "moe_version": (ctypes.c_char_p, []),
     "moe_kernel_launches": (ctypes.c_ulonglong, []),
+    "moe_expert_uses_gemm": (ctypes.c_int, [Dims]),
     "moe_workspace_bytes": (_st, [Dims, ctypes.POINTER(_sz)]),
     "moe_route": (_st, [_vp, _vp, _vp, Dims, _vp, _vp, _vp, _sz, _vp]),
     "moe_permute": (_st, [_vp, Dims, _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -128,6 +129,15 @@ def version() -> str:
 def kernel_launches() -> int:
     """Kernel launches this library has issued in this process (diagnostic)."""
     return int(lib().moe_kernel_launches())
+
+
+def expert_uses_gemm(d) -> bool:
+    """True if a layer call with dims d runs its routed experts on the
+    tensor-core GEMM (diagnostic; raises on invalid dims)."""
+    r = int(lib().moe_expert_uses_gemm(d))
+    if r < 0:
+        raise ValueError("invalid moe_dims")
+    return r == 1
 
 
 def status_string(status: int) -> str:

@@ -234,6 +234,11 @@ const char* moe_version(void) { return "moe_fp8 0.1 sm_103a"; }
 
 unsigned long long moe_kernel_launches(void) { return moe::g_launches.load(); }
 
+int moe_expert_uses_gemm(moe_dims d) {
+  if (check_dims(d) != MOE_OK) return -1;
+  return use_expert_gemm(d.T * d.k, d.E, d.H, d.I) ? 1 : 0;
+}
+
 moe_status moe_workspace_bytes(moe_dims d, size_t* bytes) {
   moe_status s = check_dims(d);
   if (s != MOE_OK) return s;

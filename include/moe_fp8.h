@@ -103,6 +103,12 @@ const char* moe_version(void);
  * call, e.g. around the capture of one moe_layer_forward. */
 unsigned long long moe_kernel_launches(void);
 
+/* Diagnostic: 1 if the routed experts of a layer call with dimensions d run
+ * on the tensor-core grouped GEMM, 0 if on the streamed GEMV (the regime rule
+ * documented at moe_layer_forward, including the MOE_FP8_EXPERT_PATH
+ * override); -1 if d is invalid.  No GPU work, no counterpart in the pages. */
+int moe_expert_uses_gemm(moe_dims d);
+
 /* Workspace size in bytes that every call below needs for dims d. */
 moe_status moe_workspace_bytes(moe_dims d, size_t* bytes);
 
