@@ -78,8 +78,9 @@ struct GemmArgs {
   int rows_per_expert;  // I for gate/up, H for down
   const float* s0;      // gate (or down) scales
   const float* s1;      // up scales (gate/up only)
-  void* out;            // hid fp16 [P, I] or y fp32 [P, H]
+  void* out;            // hid fp16 [P, I] or y [P, H] (fp32, or fp16 when y_half)
   int out_ld;
+  int y_half;
   int n_wblocks;  // weight-block pairs per expert (tiles per token tile)
   int all_wait;   // 1: the previous kernel wrote the tile offsets (every warp waits)
   int32_t* status;
@@ -511,14 +512,29 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
             if (lane == 0) mbar_arrive(&sh.acc_empty);
           }
           const int nv = ti.rows - 32 * c;
+          if (a.y_half) {
+            bool overflow = false;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) overflow |= i < nv && !(fabsf(__uint_as_float(v[i])) <= kF16Max);
+            if (overflow) raise_status(a.status, MOE_DEV_FP16_RANGE);
+          }
           if (nv >= 32) {
             // the previous store from the staging tile has read it
             tc::bulk_wait_read_all();
             __syncwarp();
+            if (a.y_half) {
+              // rows of 32 fp16 (64 bytes), 16-byte groups swizzled by
+              // (token >> 1) & 3 (the 64-byte TMA swizzle)
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              *reinterpret_cast<uint32_t*>(stg + i * 128 + (((lane >> 2) ^ (i & 7)) << 4) +
-                                           (lane & 3) * 4) = v[i];
+              for (int i = 0; i < 32; ++i)
+                *reinterpret_cast<uint16_t*>(stg + i * 64 + ((((lane >> 3) ^ ((i >> 1) & 3))) << 4) +
+                                             (lane & 7) * 2) = f32_to_f16_bits(__uint_as_float(v[i]));
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                *reinterpret_cast<uint32_t*>(stg + i * 128 + (((lane >> 2) ^ (i & 7)) << 4) +
+                                             (lane & 3) * 4) = v[i];
+            }
             tc::fence_proxy_async();
             __syncwarp();
             if (lane == 0) {  // bulk groups are per thread: always the same lane
@@ -526,6 +542,12 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
               tc::bulk_commit();
             }
             __syncwarp();
+          } else if (a.y_half) {
+            uint16_t* yh = reinterpret_cast<uint16_t*>(a.out) + (size_t)(ti.r0 + ti.m0) * a.out_ld +
+                           ti.n0 + eh * BW + 32 * q + lane;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < nv) yh[(size_t)(32 * c + i) * a.out_ld] = f32_to_f16_bits(__uint_as_float(v[i]));
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
@@ -666,8 +688,8 @@ bool expert_gemm_tc_ok(int H, int I) {
 cudaError_t launch_expert_gemm_tc(const uint16_t* x16, int T, const int32_t* expert_off,
                                   const int32_t* row_token, uint16_t* x_perm, int E, int P,
                                   const moe_fp8_ffn& w, int H, int I, int32_t* tile_off,
-                                  uint16_t* hid, float* y, int32_t* status, cudaStream_t s,
-                                  bool pdl) {
+                                  uint16_t* hid, void* y, bool y_half, int32_t* status,
+                                  cudaStream_t s, bool pdl) {
   cudaError_t err;
   if ((err = ensure_smem((const void*)k_expert_gemm_ws<true>, SMEM_WS)) != cudaSuccess) return err;
   if ((err = ensure_smem((const void*)k_expert_gemm_ws<false>, SMEM_WS)) != cudaSuccess) return err;
@@ -685,9 +707,12 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x16, int T, const int32_t* exp
   if ((err = make_tensor_map_2d(&hmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, hid, P, I, BK, BT, 128)) !=
       cudaSuccess)
     return err;
-  // y [P, H] fp32, written by the down epilogue: 32 columns x 32 rows, swizzled
-  if ((err = make_tensor_map_2d(&ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, y, P, H, 32, 32, 128)) !=
-      cudaSuccess)
+  // y [P, H], written by the down epilogue: 32 columns x 32 rows; fp32 rows of
+  // 128 bytes (128-byte swizzle) or fp16 rows of 64 bytes (64-byte swizzle)
+  if ((err = y_half ? make_tensor_map_2d(&ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, y, P, H, 32,
+                                         32, 64)
+                    : make_tensor_map_2d(&ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, y, P, H, 32,
+                                         32, 128)) != cudaSuccess)
     return err;
   // Tile offsets first, then the gather: the GEMMs' warps other than the
   // token warp read the offsets without waiting for their previous kernel.
@@ -703,11 +728,11 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x16, int T, const int32_t* exp
   const int nsm = num_sms();
   const dim3 blk(kThreadsWS);
   GemmArgs g{expert_off, tile_off, E, H, I, w.gate.scales, w.up.scales,
-             (void*)hid, I, I / BW, x_perm ? 0 : 1, status};
+             (void*)hid, I, 0, I / BW, x_perm ? 0 : 1, status};
   err = launch_k(k_expert_gemm_ws<true>, dim3(min(nsm, max_ttiles * g.n_wblocks)), blk,
                  (size_t)SMEM_WS, s, pdl, gmap, umap, xmap, ymap, g);
   if (err != cudaSuccess) return err;
-  GemmArgs d{expert_off, tile_off, E, I, H, w.down.scales, nullptr, (void*)y, H,
+  GemmArgs d{expert_off, tile_off, E, I, H, w.down.scales, nullptr, y, H, y_half ? 1 : 0,
              H / (2 * BW), 0, status};
   return launch_k(k_expert_gemm_ws<false>, dim3(min(nsm, max_ttiles * d.n_wblocks)), blk,
                   (size_t)SMEM_WS, s, pdl, dmap, dmap, hmap, ymap, d);

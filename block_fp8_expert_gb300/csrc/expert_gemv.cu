@@ -183,17 +183,18 @@ k_gateup_stream(const uint16_t* __restrict__ x16, int H, int I,
 // down projection.  grid (H/32, max active experts).  A CTA owns 32 output
 // rows (two 16-row MMA tiles); warp w works on tile w & 1 and K-part w >> 1 of
 // 4 (chunks kp, kp+4, ...), kDnChunks per warp per K-group.
-// y[r, h] = sum_i hid[r, i] Wd[h, i] in fp32 for every row r of the expert.
+// y[r, h] = sum_i hid[r, i] Wd[h, i], summed in fp32, stored in fp32 or (YH)
+// fp16 for every row r of the expert.
 // ---------------------------------------------------------------------------
 constexpr int kDnChunks = 3;  // I <= 768 in one K-group
 constexpr size_t kDnSmem = sizeof(uint4) * kDnChunks * 2 * kThreads;  // 24 KB
 
-template <int NT>
+template <int NT, bool YH>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
 k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
               const int32_t* __restrict__ expert_off, const int32_t* __restrict__ active,
               const uint8_t* __restrict__ dcodes, const float* __restrict__ dscales,
-              float* __restrict__ y) {
+              void* __restrict__ y, int32_t* __restrict__ status) {
   extern __shared__ uint4 wbuf[];  // [kDnChunks * 2][kThreads]
   __shared__ float red[4][2][NT][4][32];
   griddep_wait();
@@ -290,7 +291,15 @@ k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
       for (int p = 0; p < 4; ++p) v += red[p][t2][nt][q][L];
       const int row = (L >> 2) + 8 * (q >> 1);
       const int n = n0 + nt * 8 + 2 * (L & 3) + (q & 1);
-      if (n < ne) y[(size_t)(r0 + n) * H + blockIdx.x * 32 + t2 * 16 + row] = v;
+      if (n < ne) {
+        const size_t at = (size_t)(r0 + n) * H + blockIdx.x * 32 + t2 * 16 + row;
+        if (YH) {
+          if (!(fabsf(v) <= kF16Max)) raise_status(status, MOE_DEV_FP16_RANGE);
+          static_cast<uint16_t*>(y)[at] = f32_to_f16_bits(v);
+        } else {
+          static_cast<float*>(y)[at] = v;
+        }
+      }
     }
     __syncthreads();
   }
@@ -299,30 +308,32 @@ k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
 cudaError_t launch_expert_gemv(const uint16_t* x16, const int32_t* expert_off,
                                const int32_t* row_token, const int32_t* active, int max_active,
                                const moe_fp8_ffn& w, int H, int I, int tokens_per_expert_hint,
-                               uint16_t* hid, float* y, int32_t* status, cudaStream_t s,
-                               bool pdl) {
+                               uint16_t* hid, void* y, bool y_half, int32_t* status,
+                               cudaStream_t s, bool pdl) {
   if (max_active <= 0) return cudaSuccess;
   cudaError_t e;
   const bool nt1 = tokens_per_expert_hint <= 8;
   const dim3 block(kThreads);
   const dim3 g1(I / 16, max_active), g2(H / 32, max_active);
+  auto down = [&](auto kern) -> cudaError_t {
+    cudaError_t err = ensure_smem((const void*)kern, kDnSmem);
+    if (err != cudaSuccess) return err;
+    return launch_k(kern, g2, block, kDnSmem, s, pdl, (const uint16_t*)hid, H, I, expert_off,
+                    active, w.down.codes, w.down.scales, y, status);
+  };
   if (nt1) {
     if ((e = ensure_smem((const void*)k_gateup_stream<1>, kGuSmem)) != cudaSuccess) return e;
-    if ((e = ensure_smem((const void*)k_down_stream<1>, kDnSmem)) != cudaSuccess) return e;
     e = launch_k(k_gateup_stream<1>, g1, block, kGuSmem, s, pdl, x16, H, I, expert_off,
                  row_token, active, w.gate.codes, w.gate.scales, w.up.codes, w.up.scales, hid,
                  status);
     if (e != cudaSuccess) return e;
-    return launch_k(k_down_stream<1>, g2, block, kDnSmem, s, pdl, (const uint16_t*)hid, H, I,
-                    expert_off, active, w.down.codes, w.down.scales, y);
+    return y_half ? down(k_down_stream<1, true>) : down(k_down_stream<1, false>);
   }
   if ((e = ensure_smem((const void*)k_gateup_stream<2>, kGuSmem)) != cudaSuccess) return e;
-  if ((e = ensure_smem((const void*)k_down_stream<2>, kDnSmem)) != cudaSuccess) return e;
   e = launch_k(k_gateup_stream<2>, g1, block, kGuSmem, s, pdl, x16, H, I, expert_off, row_token,
                active, w.gate.codes, w.gate.scales, w.up.codes, w.up.scales, hid, status);
   if (e != cudaSuccess) return e;
-  return launch_k(k_down_stream<2>, g2, block, kDnSmem, s, pdl, (const uint16_t*)hid, H, I,
-                  expert_off, active, w.down.codes, w.down.scales, y);
+  return y_half ? down(k_down_stream<2, true>) : down(k_down_stream<2, false>);
 }
 
 // x (bf16) -> x16 (fp16), flagging values beyond fp16 range; for callers of

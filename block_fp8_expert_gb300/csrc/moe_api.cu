@@ -175,9 +175,9 @@ WsLayout ws_layout(const moe_dims& d) {
   L.row_pair = take(P * 4);
   L.x16 = take(T * H * 2);
   L.hid = take(P * I * 2);
-  L.y_perm = take(P * H * 4);
+  L.y_perm = take(P * H * 2);  // fp16 expert outputs of moe_layer_forward
   L.sh_hid = take(Is ? T * Is * 2 : 0);
-  L.sh_y = take(Is ? T * H * 4 : 0);
+  L.sh_y = take(Is ? T * H * 2 : 0);
   L.sh_off = take(2 * 4);
   L.sh_rows = take(Is ? T * 4 : 0);
   L.sh_active = take(2 * 4);
@@ -316,12 +316,12 @@ moe_status moe_expert_ffn_fp8(const uint16_t* x, const int32_t* expert_off,
   if (use_expert_gemm(P, d.E, d.H, d.I))
     CUDA_CHECK(launch_expert_gemm_tc(x16, d.T, expert_off, row_token, at<uint16_t>(ws, L.x_perm),
                                      d.E, P, w, d.H, d.I, at<int32_t>(ws, L.tile_off),
-                                     at<uint16_t>(ws, L.hid), y_perm, status, st, true),
+                                     at<uint16_t>(ws, L.hid), y_perm, false, status, st, true),
                "moe_expert_ffn_fp8");
   else
     CUDA_CHECK(launch_expert_gemv(x16, expert_off, row_token, active, d.E < P ? d.E : P, w, d.H,
-                                  d.I, cdiv(P, d.E), at<uint16_t>(ws, L.hid), y_perm, status, st,
-                                  true),
+                                  d.I, cdiv(P, d.E), at<uint16_t>(ws, L.hid), y_perm, false,
+                                  status, st, true),
                "moe_expert_ffn_fp8");
   return MOE_OK;
 }
@@ -336,7 +336,7 @@ moe_status moe_combine(const float* y_perm, const int32_t* tok_slot_row, const f
   REQUIRE_PTR(topk_w);
   REQUIRE_OPT_PTR(shared_y);
   REQUIRE_PTR(out);
-  CUDA_CHECK(launch_combine(y_perm, tok_slot_row, topk_w, shared_y, d.T, d.H, d.k, out,
+  CUDA_CHECK(launch_combine(y_perm, false, tok_slot_row, topk_w, shared_y, d.T, d.H, d.k, out,
                             (cudaStream_t)stream, true),
              "moe_combine");
   return MOE_OK;
@@ -372,7 +372,7 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
   int32_t* row_token = at<int32_t>(ws, L.row_token);
   int32_t* tok_slot_row = at<int32_t>(ws, L.tok_slot_row);
   int32_t* active = at<int32_t>(ws, L.active);
-  float* y_perm = at<float>(ws, L.y_perm);
+  uint16_t* y_perm = at<uint16_t>(ws, L.y_perm);  // fp16 inside the layer call
 
   int32_t* status = at<int32_t>(ws, L.status);
   uint16_t* x16 = at<uint16_t>(ws, L.x16);
@@ -406,28 +406,28 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
   if (use_expert_gemm(P, d.E, d.H, d.I))
     CUDA_CHECK(launch_expert_gemm_tc(x16, d.T, off, row_token, at<uint16_t>(ws, L.x_perm), d.E, P,
                                      routed, d.H, d.I, at<int32_t>(ws, L.tile_off),
-                                     at<uint16_t>(ws, L.hid), y_perm, status, st, true),
+                                     at<uint16_t>(ws, L.hid), y_perm, true, status, st, true),
                "moe_layer_forward: experts");
   else
     CUDA_CHECK(launch_expert_gemv(x16, off, row_token, active, d.E < P ? d.E : P, routed, d.H,
-                                  d.I, cdiv(P, d.E), at<uint16_t>(ws, L.hid), y_perm, status, st,
-                                  true),
+                                  d.I, cdiv(P, d.E), at<uint16_t>(ws, L.hid), y_perm, true,
+                                  status, st, true),
                "moe_layer_forward: experts");
-  float* shared_y = nullptr;
+  uint16_t* shared_y = nullptr;
   if (has_shared) {
-    shared_y = at<float>(ws, L.sh_y);
+    shared_y = at<uint16_t>(ws, L.sh_y);
     if (use_expert_gemm(d.T, 1, d.H, d.I_shared))
       CUDA_CHECK(launch_expert_gemm_tc(x16, d.T, soff, srows, nullptr, 1, d.T, *shared, d.H,
                                        d.I_shared,
                                        at<int32_t>(ws, L.sh_tile_off), at<uint16_t>(ws, L.sh_hid),
-                                       shared_y, status, st, true),
+                                       shared_y, true, status, st, true),
                  "moe_layer_forward: shared expert");
     else
       CUDA_CHECK(launch_expert_gemv(x16, soff, srows, sact, 1, *shared, d.H, d.I_shared, d.T,
-                                    at<uint16_t>(ws, L.sh_hid), shared_y, status, st, true),
+                                    at<uint16_t>(ws, L.sh_hid), shared_y, true, status, st, true),
                  "moe_layer_forward: shared expert");
   }
-  CUDA_CHECK(launch_combine(y_perm, tok_slot_row, w, shared_y, d.T, d.H, d.k, out, st, true),
+  CUDA_CHECK(launch_combine(y_perm, true, tok_slot_row, w, shared_y, d.T, d.H, d.k, out, st, true),
              "moe_layer_forward: combine");
   return MOE_OK;
 }

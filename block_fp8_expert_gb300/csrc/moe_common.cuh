@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "moe_fp8.h"
@@ -330,12 +331,22 @@ constexpr int kStatusWords = 16;
 // summed in fp32 in slot order j (in groups of 8 slots, loads first), the
 // shared expert's row added last, rounded once to bf16.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void combine4(const float* __restrict__ y_perm,
+__device__ __forceinline__ float4 load4(const float* p) {
+  return __ldg(reinterpret_cast<const float4*>(p));
+}
+__device__ __forceinline__ float4 load4(const uint16_t* p) {  // four fp16
+  const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+template <typename YT>
+__device__ __forceinline__ void combine4(const YT* __restrict__ y_perm,
                                          const int32_t* __restrict__ tok_slot_row,
                                          const float* __restrict__ topk_w,
-                                         const float* __restrict__ shared_y, int t, int h, int H,
+                                         const YT* __restrict__ shared_y, int t, int h, int H,
                                          int k, uint16_t* __restrict__ out) {
-  auto ld4 = [](const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); };
+  auto ld4 = [](const YT* p) { return load4(p); };
   float4 acc = shared_y ? ld4(shared_y + (size_t)t * H + h) : make_float4(0.f, 0.f, 0.f, 0.f);
   float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int j0 = 0; j0 < k; j0 += 8) {

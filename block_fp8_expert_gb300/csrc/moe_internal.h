@@ -107,14 +107,14 @@ cudaError_t launch_x_to_f16(const uint16_t* x, long long n, uint16_t* x16, int32
                             cudaStream_t s, bool pdl);
 
 // Grouped GEMV over the experts listed in `active` (count, then ids), on the
-// fp16 activations x16.  max_active bounds the list length;
+// fp16 activations x16; y fp32 or (y_half) fp16.  max_active bounds the list length;
 // tokens_per_expert_hint (the expected rows per expert) picks the MMA's N
 // width; any segment length is handled.
 cudaError_t launch_expert_gemv(const uint16_t* x16, const int32_t* expert_off,
                                const int32_t* row_token, const int32_t* active, int max_active,
                                const moe_fp8_ffn& w, int H, int I, int tokens_per_expert_hint,
-                               uint16_t* hid, float* y, int32_t* status, cudaStream_t s,
-                               bool pdl);
+                               uint16_t* hid, void* y, bool y_half, int32_t* status,
+                               cudaStream_t s, bool pdl);
 
 // Grouped GEMM on the tensor cores (tcgen05) for many tokens per expert:
 // gate/up + SwiGLU -> hid, then down -> y.  Needs H % 256 == 0 and
@@ -122,21 +122,23 @@ cudaError_t launch_expert_gemv(const uint16_t* x16, const int32_t* expert_off,
 bool expert_gemm_tc_ok(int H, int I);
 // x16: [T, H] fp16.  x_perm: [P, H] fp16 scratch that receives the
 // activation rows in expert order (x16[row_token[p]]), or NULL when row_token
-// is the identity (the rows of x16 are then read in place).
+// is the identity (the rows of x16 are then read in place).  y: [P, H], fp32
+// or (y_half) fp16; an fp16 value beyond range raises MOE_DEV_FP16_RANGE.
 cudaError_t launch_expert_gemm_tc(const uint16_t* x16, int T, const int32_t* expert_off,
                                   const int32_t* row_token, uint16_t* x_perm, int E, int P,
                                   const moe_fp8_ffn& w, int H, int I, int32_t* tile_off,
-                                  uint16_t* hid, float* y, int32_t* status, cudaStream_t s,
-                                  bool pdl);
+                                  uint16_t* hid, void* y, bool y_half, int32_t* status,
+                                  cudaStream_t s, bool pdl);
 
 // Regime: true -> tensor-core grouped GEMM, false -> streamed grouped GEMV.
 // Decided on the host from shapes only; MOE_FP8_EXPERT_PATH=gemm|gemv in the
 // environment overrides it (when the GEMM supports the shapes).
 bool use_expert_gemm(int rows, int experts, int H, int I);
 
-cudaError_t launch_combine(const float* y_perm, const int32_t* tok_slot_row, const float* topk_w,
-                           const float* shared_y, int T, int H, int k, uint16_t* out,
-                           cudaStream_t s, bool pdl);
+// y_perm and shared_y (may be NULL): fp32, or fp16 when y_half.
+cudaError_t launch_combine(const void* y_perm, bool y_half, const int32_t* tok_slot_row,
+                           const float* topk_w, const void* shared_y, int T, int H, int k,
+                           uint16_t* out, cudaStream_t s, bool pdl);
 
 // Identity permutation of T tokens onto one expert (the shared expert):
 // off = {0, T}, rows = 0..T-1, active = {1, 0}.
