@@ -83,6 +83,12 @@ struct GemmArgs {
   int y_half;
   int n_wblocks;  // weight-block pairs per expert (tiles per token tile)
   int all_wait;   // 1: the previous kernel wrote the tile offsets (every warp waits)
+  // Per token tile ("slot") of the gate/up GEMM: completed epilogue-warp
+  // tiles.  gate/up adds kEpiWarps per weight-block tile once its hid rows are
+  // stored; down's token warp waits for slot_need before loading hid rows,
+  // instead of waiting for the whole gate/up grid.  NULL: whole-grid wait.
+  int32_t* slot_done;
+  int slot_need;
   int32_t* status;
 };
 
@@ -182,6 +188,7 @@ __device__ __forceinline__ bool warp_wait_all(WsShared& sh, uint64_t* const (&ba
 
 struct TileInfo {
   int e, r0, m0, rows, n, n0;  // n = rows rounded up to 16 (the MMA's N)
+  int slot;                    // token tile index (tile_off[e] + m0 / 128)
 };
 
 // Tile t -> expert, token rows and weight rows, from the shared-memory copies.
@@ -195,6 +202,7 @@ __device__ __forceinline__ TileInfo tile_info(const WsShared& sh, const GemmArgs
     if (sh.tile_off[mid] <= slot) lo = mid; else hi = mid;
   }
   ti.e = lo;
+  ti.slot = slot;
   ti.r0 = sh.expert_off[lo];
   ti.m0 = (slot - sh.tile_off[lo]) * BT;
   ti.rows = min(BT, sh.expert_off[lo + 1] - ti.r0 - ti.m0);
@@ -300,13 +308,38 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     __syncwarp();
   } else if (warp == W_TOK) {
     // ------------------------------------------------ token rows (TMA)
-    griddep_wait();
+    if (!a.slot_done || GATEUP) griddep_wait();
     // One box of 128 consecutive permuted rows per step (rows past the tile
     // are never stored; rows past the matrix read 0).
     int j = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
       const TileInfo ti = tile_info(sh, a, t, GATEUP);
+      if (!GATEUP && a.slot_done) {
+        // this token tile's hid rows: every gate/up weight-block tile of the
+        // slot has stored them (bounded warp-uniform poll, then the acquired
+        // data is ordered before the async-proxy loads below)
+        const WaitBudget b = wait_budget();
+        bool done = false;
+        for (uint32_t n = 0; !done; ++n) {
+          done = __all_sync(0xffffffffu, tc::ld_acquire_gpu(a.slot_done + ti.slot) >= a.slot_need);
+          if (!done && (n & 31) == 31) {
+            const bool give_up =
+                *reinterpret_cast<volatile int*>(&sh.abort_flag) != 0 || budget_spent(b);
+            if (__any_sync(0xffffffffu, give_up)) break;
+          }
+        }
+        if (!done) {
+          if (lane == 0 && !sh.abort_flag) {
+            sh.abort_flag = 1;
+            raise_status(a.status, MOE_DEV_WAIT_TIMEOUT);
+          }
+          __syncwarp();
+          ok = false;
+          break;
+        }
+        tc::fence_proxy_async_global();
+      }
       for (int ks = 0; ks < nK; ++ks, ++j) {
         const int st = j % NT;
         if (j >= NT && !warp_wait(sh, &sh.t_empty[st], (uint32_t)(((j / NT) - 1) & 1), a.status, 2, j)) {
@@ -491,6 +524,16 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
           if (m < ti.rows) tc::bulk_store(hid + (size_t)m * a.out_ld, stg + i * 64, 64);
         }
         tc::bulk_commit();
+        if (a.slot_done) {
+          // publish: this warp's hid rows of the tile are stored
+          tc::bulk_wait_all();
+          tc::fence_proxy_async_global();
+          __syncwarp();
+          if (lane == 0) {
+            __threadfence();
+            tc::red_release_gpu_add(a.slot_done + ti.slot, 1);
+          }
+        }
       } else {
         // Chunk c of block eh: features n0 + 128 eh + 32 q .. + 31 (this
         // warp's lanes) x tokens 32 c .. 32 c + 31 (the chunk's columns).  A
@@ -573,7 +616,8 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
 // Per-expert token-tile prefix: tile_off[e] = sum_{e' < e} ceil(cnt_e' / 128),
 // tile_off[E] = total.  One CTA, E <= 1024.
 __global__ void __launch_bounds__(1024)
-k_tile_offsets(const int32_t* __restrict__ expert_off, int E, int32_t* __restrict__ tile_off) {
+k_tile_offsets(const int32_t* __restrict__ expert_off, int E, int32_t* __restrict__ tile_off,
+               int32_t* __restrict__ slot_done, int max_slots) {
   __shared__ int32_t wsum[32];
   griddep_wait();
   griddep_trigger();
@@ -600,6 +644,9 @@ k_tile_offsets(const int32_t* __restrict__ expert_off, int E, int32_t* __restric
   const int before = warp ? wsum[warp - 1] : 0;
   if (tid < E) tile_off[tid] = before + incl - c;
   if (tid == E - 1) tile_off[E] = before + incl;
+  // the gate/up -> down completion counters of this call start at zero
+  if (slot_done)
+    for (int i = tid; i < max_slots; i += blockDim.x) slot_done[i] = 0;
 }
 
 // Activation rows in expert order: xp[p] = x[row_token[p]] (fp16, K columns,
@@ -688,8 +735,8 @@ bool expert_gemm_tc_ok(int H, int I) {
 cudaError_t launch_expert_gemm_tc(const uint16_t* x16, int T, const int32_t* expert_off,
                                   const int32_t* row_token, uint16_t* x_perm, int E, int P,
                                   const moe_fp8_ffn& w, int H, int I, int32_t* tile_off,
-                                  uint16_t* hid, void* y, bool y_half, int32_t* status,
-                                  cudaStream_t s, bool pdl) {
+                                  int32_t* slot_done, uint16_t* hid, void* y, bool y_half,
+                                  int32_t* status, cudaStream_t s, bool pdl) {
   cudaError_t err;
   if ((err = ensure_smem((const void*)k_expert_gemm_ws<true>, SMEM_WS)) != cudaSuccess) return err;
   if ((err = ensure_smem((const void*)k_expert_gemm_ws<false>, SMEM_WS)) != cudaSuccess) return err;
@@ -716,24 +763,25 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x16, int T, const int32_t* exp
     return err;
   // Tile offsets first, then the gather: the GEMMs' warps other than the
   // token warp read the offsets without waiting for their previous kernel.
-  err = launch_k(k_tile_offsets, dim3(1), dim3(1024), 0, s, pdl, expert_off, E, tile_off);
+  // Host bound on the tile count: each expert adds at most one partial tile.
+  const int max_ttiles = cdiv(P, BT) + min(E, P);
+  err = launch_k(k_tile_offsets, dim3(1), dim3(1024), 0, s, pdl, expert_off, E, tile_off,
+                 slot_done, max_ttiles);
   if (err != cudaSuccess) return err;
   if (x_perm) {
     err = launch_k(k_gather_rows, dim3(cdiv(P, 8)), dim3(256), 0, s, pdl, x16, T, row_token,
                    expert_off, E, P, H, x_perm);
     if (err != cudaSuccess) return err;
   }
-  // Host bound on the tile count: each expert adds at most one partial tile.
-  const int max_ttiles = cdiv(P, BT) + min(E, P);
   const int nsm = num_sms();
   const dim3 blk(kThreadsWS);
   GemmArgs g{expert_off, tile_off, E, H, I, w.gate.scales, w.up.scales,
-             (void*)hid, I, 0, I / BW, x_perm ? 0 : 1, status};
+             (void*)hid, I, 0, I / BW, x_perm ? 0 : 1, slot_done, 0, status};
   err = launch_k(k_expert_gemm_ws<true>, dim3(min(nsm, max_ttiles * g.n_wblocks)), blk,
                  (size_t)SMEM_WS, s, pdl, gmap, umap, xmap, ymap, g);
   if (err != cudaSuccess) return err;
   GemmArgs d{expert_off, tile_off, E, I, H, w.down.scales, nullptr, y, H, y_half ? 1 : 0,
-             H / (2 * BW), 0, status};
+             H / (2 * BW), 0, slot_done, (I / BW) * kEpiWarps, status};
   return launch_k(k_expert_gemm_ws<false>, dim3(min(nsm, max_ttiles * d.n_wblocks)), blk,
                   (size_t)SMEM_WS, s, pdl, dmap, dmap, hmap, ymap, d);
 }

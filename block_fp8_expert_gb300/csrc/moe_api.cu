@@ -1,6 +1,7 @@
 // The C ABI (include/moe_fp8.h): argument checks, workspace layout, launches.
 // Nothing here allocates device memory or synchronises the host, except
 // moe_read_device_status, whose job is to read a device word back.
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -185,6 +186,8 @@ WsLayout ws_layout(const moe_dims& d) {
   L.sh_tile_off = take(2 * 4);
   L.x_perm = take(expert_gemm_tc_ok(d.H, d.I) ? P * H * 2 : 0);
   L.wr_planes = take(router_tc_ok(d.T, d.H, d.E) ? 3 * E * H * 2 : 0);
+  L.slot_done = take(((P + 127) / 128 + std::min(E, P)) * 4);
+  L.sh_slot_done = take(Is ? ((T + 127) / 128 + 1) * 4 : 0);
   L.total = o;
   return L;
 }
@@ -316,7 +319,8 @@ moe_status moe_expert_ffn_fp8(const uint16_t* x, const int32_t* expert_off,
   if (use_expert_gemm(P, d.E, d.H, d.I))
     CUDA_CHECK(launch_expert_gemm_tc(x16, d.T, expert_off, row_token, at<uint16_t>(ws, L.x_perm),
                                      d.E, P, w, d.H, d.I, at<int32_t>(ws, L.tile_off),
-                                     at<uint16_t>(ws, L.hid), y_perm, false, status, st, true),
+                                     at<int32_t>(ws, L.slot_done), at<uint16_t>(ws, L.hid), y_perm,
+                                     false, status, st, true),
                "moe_expert_ffn_fp8");
   else
     CUDA_CHECK(launch_expert_gemv(x16, expert_off, row_token, active, d.E < P ? d.E : P, w, d.H,
@@ -406,7 +410,8 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
   if (use_expert_gemm(P, d.E, d.H, d.I))
     CUDA_CHECK(launch_expert_gemm_tc(x16, d.T, off, row_token, at<uint16_t>(ws, L.x_perm), d.E, P,
                                      routed, d.H, d.I, at<int32_t>(ws, L.tile_off),
-                                     at<uint16_t>(ws, L.hid), y_perm, true, status, st, true),
+                                     at<int32_t>(ws, L.slot_done), at<uint16_t>(ws, L.hid), y_perm,
+                                     true, status, st, true),
                "moe_layer_forward: experts");
   else
     CUDA_CHECK(launch_expert_gemv(x16, off, row_token, active, d.E < P ? d.E : P, routed, d.H,
@@ -419,7 +424,8 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
     if (use_expert_gemm(d.T, 1, d.H, d.I_shared))
       CUDA_CHECK(launch_expert_gemm_tc(x16, d.T, soff, srows, nullptr, 1, d.T, *shared, d.H,
                                        d.I_shared,
-                                       at<int32_t>(ws, L.sh_tile_off), at<uint16_t>(ws, L.sh_hid),
+                                       at<int32_t>(ws, L.sh_tile_off),
+                                       at<int32_t>(ws, L.sh_slot_done), at<uint16_t>(ws, L.sh_hid),
                                        shared_y, true, status, st, true),
                  "moe_layer_forward: shared expert");
     else

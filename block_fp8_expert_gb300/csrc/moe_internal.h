@@ -62,7 +62,7 @@ int num_sms();
 struct WsLayout {
   size_t status, logits, rank, block_cnt, block_base, active, idx, w, off, row_token,
       tok_slot_row, row_pair, x16, hid, y_perm, sh_hid, sh_y, sh_off, sh_rows, sh_active,
-      tile_off, sh_tile_off, x_perm, wr_planes, total;
+      tile_off, sh_tile_off, x_perm, wr_planes, slot_done, sh_slot_done, total;
 };
 WsLayout ws_layout(const moe_dims& d);
 
@@ -118,7 +118,9 @@ cudaError_t launch_expert_gemv(const uint16_t* x16, const int32_t* expert_off,
 
 // Grouped GEMM on the tensor cores (tcgen05) for many tokens per expert:
 // gate/up + SwiGLU -> hid, then down -> y.  Needs H % 256 == 0 and
-// I % 128 == 0, H, I <= 4096 (expert_gemm_tc_ok).  tile_off: E + 1 ints of scratch.
+// I % 128 == 0, H, I <= 4096 (expert_gemm_tc_ok).  tile_off: E + 1 ints of scratch;
+// slot_done: cdiv(P, 128) + min(E, P) ints of scratch (the down GEMM then
+// starts each token tile as soon as its hid rows are stored), or NULL.
 bool expert_gemm_tc_ok(int H, int I);
 // x16: [T, H] fp16.  x_perm: [P, H] fp16 scratch that receives the
 // activation rows in expert order (x16[row_token[p]]), or NULL when row_token
@@ -127,8 +129,8 @@ bool expert_gemm_tc_ok(int H, int I);
 cudaError_t launch_expert_gemm_tc(const uint16_t* x16, int T, const int32_t* expert_off,
                                   const int32_t* row_token, uint16_t* x_perm, int E, int P,
                                   const moe_fp8_ffn& w, int H, int I, int32_t* tile_off,
-                                  uint16_t* hid, void* y, bool y_half, int32_t* status,
-                                  cudaStream_t s, bool pdl);
+                                  int32_t* slot_done, uint16_t* hid, void* y, bool y_half,
+                                  int32_t* status, cudaStream_t s, bool pdl);
 
 // Regime: true -> tensor-core grouped GEMM, false -> streamed grouped GEMV.
 // Decided on the host from shapes only; MOE_FP8_EXPERT_PATH=gemm|gemv in the
