@@ -5,24 +5,27 @@
 
 namespace moe {
 
+// One thread per 16 bytes of each of a token's expert rows: 4 fp32 or 8 fp16
+// outputs.
 template <typename YT>
 __global__ void __launch_bounds__(256)
 k_combine(const YT* __restrict__ y_perm, const int32_t* __restrict__ tok_slot_row,
           const float* __restrict__ topk_w, const YT* __restrict__ shared_y, int T, int H,
           int k, uint16_t* __restrict__ out) {
+  constexpr int V = 16 / sizeof(YT);
   griddep_wait();
   griddep_trigger();
-  const int H4 = H / 4;
+  const int HV = H / V;
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (long long)T * H4) return;
-  const int t = (int)(i / H4), h = (int)(i % H4) * 4;
-  combine4(y_perm, tok_slot_row, topk_w, shared_y, t, h, H, k, out);
+  if (i >= (long long)T * HV) return;
+  const int t = (int)(i / HV), h = (int)(i % HV) * V;
+  combine_v<YT, V>(y_perm, tok_slot_row, topk_w, shared_y, t, h, H, k, out);
 }
 
 cudaError_t launch_combine(const void* y_perm, bool y_half, const int32_t* tok_slot_row,
                            const float* topk_w, const void* shared_y, int T, int H, int k,
                            uint16_t* out, cudaStream_t s, bool pdl) {
-  const long long n = (long long)T * (H / 4);
+  const long long n = (long long)T * (H / (y_half ? 8 : 4));
   if (n == 0) return cudaSuccess;
   const dim3 grid((unsigned)((n + 255) / 256));
   if (y_half)

@@ -331,24 +331,33 @@ constexpr int kStatusWords = 16;
 // summed in fp32 in slot order j (in groups of 8 slots, loads first), the
 // shared expert's row added last, rounded once to bf16.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float4 load4(const float* p) {
-  return __ldg(reinterpret_cast<const float4*>(p));
+// V consecutive expert outputs as fp32: V = 4 fp32 or V = 8 fp16 (16 bytes).
+__device__ __forceinline__ void load_v(const float* p, float (&v)[4]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
 }
-__device__ __forceinline__ float4 load4(const uint16_t* p) {  // four fp16
-  const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
-  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
-  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
-  return make_float4(a.x, a.y, b.x, b.y);
+__device__ __forceinline__ void load_v(const uint16_t* p, float (&v)[8]) {
+  const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
 }
-template <typename YT>
-__device__ __forceinline__ void combine4(const YT* __restrict__ y_perm,
-                                         const int32_t* __restrict__ tok_slot_row,
-                                         const float* __restrict__ topk_w,
-                                         const YT* __restrict__ shared_y, int t, int h, int H,
-                                         int k, uint16_t* __restrict__ out) {
-  auto ld4 = [](const YT* p) { return load4(p); };
-  float4 acc = shared_y ? ld4(shared_y + (size_t)t * H + h) : make_float4(0.f, 0.f, 0.f, 0.f);
-  float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+// out[t, h .. h + V) = sum_j w[t, j] y_perm[tok_slot_row[t k + j], ...]
+// (+ shared_y[t, ...]), summed in fp32 in slot order j, rounded once to bf16.
+template <typename YT, int V>
+__device__ __forceinline__ void combine_v(const YT* __restrict__ y_perm,
+                                          const int32_t* __restrict__ tok_slot_row,
+                                          const float* __restrict__ topk_w,
+                                          const YT* __restrict__ shared_y, int t, int h, int H,
+                                          int k, uint16_t* __restrict__ out) {
+  float acc[V], r[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i] = r[i] = 0.f;
+  if (shared_y) load_v(shared_y + (size_t)t * H + h, acc);
   for (int j0 = 0; j0 < k; j0 += 8) {
     int row[8];
     float w[8];
@@ -358,27 +367,30 @@ __device__ __forceinline__ void combine4(const YT* __restrict__ y_perm,
       row[u] = j < k ? tok_slot_row[(size_t)t * k + j] : -1;
       w[u] = j < k ? topk_w[(size_t)t * k + j] : 0.f;
     }
-    float4 y[8];
+    float y[8][V];
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-      y[u] = row[u] >= 0 ? ld4(y_perm + (size_t)row[u] * H + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < 8; ++u) {
+      if (row[u] >= 0) {
+        load_v(y_perm + (size_t)row[u] * H + h, y[u]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i) y[u][i] = 0.f;
+      }
+    }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       if (row[u] < 0) continue;
-      r.x = fmaf(w[u], y[u].x, r.x);
-      r.y = fmaf(w[u], y[u].y, r.y);
-      r.z = fmaf(w[u], y[u].z, r.z);
-      r.w = fmaf(w[u], y[u].w, r.w);
+#pragma unroll
+      for (int i = 0; i < V; ++i) r[i] = fmaf(w[u], y[u][i], r[i]);
     }
   }
-  acc.x += r.x;
-  acc.y += r.y;
-  acc.z += r.z;
-  acc.w += r.w;
-  uint2 o;
-  o.x = pack_bf16x2(acc.x, acc.y);
-  o.y = pack_bf16x2(acc.z, acc.w);
-  *reinterpret_cast<uint2*>(out + (size_t)t * H + h) = o;
+  uint32_t o[V / 2];
+#pragma unroll
+  for (int i = 0; i < V / 2; ++i) o[i] = pack_bf16x2(acc[2 * i] + r[2 * i], acc[2 * i + 1] + r[2 * i + 1]);
+  if (V == 8)
+    *reinterpret_cast<uint4*>(out + (size_t)t * H + h) = make_uint4(o[0], o[1], o[2], o[3]);
+  else
+    *reinterpret_cast<uint2*>(out + (size_t)t * H + h) = make_uint2(o[0], o[1]);
 }
 
 __device__ __forceinline__ void raise_status(int32_t* status, int32_t bits) {
