@@ -110,3 +110,19 @@ def test_decode_shapes_through_gemm(torch, force_gemm, name, T):
     ref = oracle.moe_layer(xb, L, keep_intermediates=False)
     assert np.array_equal(idx.cpu().numpy(), ref["topk_idx"])
     assert_within_tol(oracle.bf16_to_f64(bf16_bits(out)), ref["out"], f"{name} T={T} gemm")
+
+
+def test_largest_gemm_shape(torch):
+    """H = I = 4096, the largest shape the tensor-core GEMM takes (32 block
+    scales of K per weight row block); 2 experts, top-1, 100 tokens = 50 rows
+    per expert on average, so the GEMM is the natural regime (checked), each
+    expert's only token tile ragged."""
+    import block_fp8_expert_gb300 as m
+    w = mi.Workload("gemm_max", H=4096, I=4096, E=2, k=1)
+    L = mi.make_layer(w, seed=7)
+    T = 100
+    assert m.expert_uses_gemm(m.dims(T, w.H, w.I, w.E, w.k))
+    xb, out, idx, wts = _run(torch, L, T, seed=7)
+    ref = oracle.moe_layer(xb, L, keep_intermediates=False)
+    assert np.array_equal(idx.cpu().numpy(), ref["topk_idx"])
+    assert_within_tol(oracle.bf16_to_f64(bf16_bits(out)), ref["out"], "H = I = 4096 gemm")
