@@ -107,21 +107,30 @@ T* at(void* ws, size_t off) {
 void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
 
 // Average rows per expert from which the tensor-core GEMM replaces the
-// streamed GEMV.  Routed experts: from 4 (measured crossover: at 2 rows per
-// expert the GEMV is 2% faster, at 4 the GEMM is 1% faster, and it pulls
-// further ahead as soon as a few experts are hot, since the GEMV re-streams an
-// expert's weights for every group of 8 or 16 rows).  One dense expert (the
-// shared one) has only I / 128 weight tiles per 128 rows to spread over the
-// SMs: from 32 rows.
-constexpr int kGemmMinRowsPerRoutedExpert = 4;
+// streamed GEMV.  Routed experts: from 1 (measured crossover: at 1 row per
+// expert the two paths take the same time (Qwen3 T=16), from 2 the GEMM is
+// faster (T=32: 131 vs 134 us), and it pulls ahead as soon as a few experts
+// are hot, since the GEMV re-streams an expert's weights for every group of 8
+// or 16 rows).  One dense expert (the shared one) has only I / 128 weight
+// tiles per 128 rows to spread over the SMs: from 32 rows.  Small experts
+// (H * I < 2^20 codes per matrix) stream so few bytes that the GEMM path's
+// fixed costs (two more launches, the tile machinery) dominate: they keep the
+// GEMV up to 32 rows per expert (the 16-expert H 256 layer: GEMV 20 / 26 us
+// at 32 / 100 tokens, GEMM 30 / 32 us).
+constexpr int kGemmMinRowsPerRoutedExpert = 1;
+constexpr int kGemmMinRowsPerSmallExpert = 32;
 constexpr int kGemmMinRowsDense = 32;
+constexpr long long kSmallExpertCodes = 1ll << 20;
 
 bool use_expert_gemm(int rows, int experts, int H, int I) {
   if (!expert_gemm_tc_ok(H, I)) return false;
   const char* f = getenv("MOE_FP8_EXPERT_PATH");
   if (f && strcmp(f, "gemm") == 0) return true;
   if (f && strcmp(f, "gemv") == 0) return false;
-  return experts > 1 ? rows >= kGemmMinRowsPerRoutedExpert * experts : rows >= kGemmMinRowsDense;
+  if (experts == 1) return rows >= kGemmMinRowsDense;
+  const int per = (long long)H * I >= kSmallExpertCodes ? kGemmMinRowsPerRoutedExpert
+                                                        : kGemmMinRowsPerSmallExpert;
+  return (long long)rows >= (long long)per * experts;
 }
 
 cudaError_t ensure_smem(const void* func, int bytes) {

@@ -186,8 +186,9 @@ moe_status moe_combine(const float* y_perm, const int32_t* tok_slot_row,
  *   topk_w_out   float [T, k] or NULL
  * The regime (few tokens per expert: streamed grouped GEMV; many tokens per
  * expert: tensor-core grouped GEMM) is chosen on the host from T*k/E only:
- * the GEMM (tcgen05, needs H % 256 == 0, I % 128 == 0, H, I <= 4096) from 4
- * rows per routed expert on average (the shared expert: from 32 tokens).  The
+ * the GEMM (tcgen05, needs H % 256 == 0, I % 128 == 0, H, I <= 4096) from 1
+ * row per routed expert on average (T*k >= E) when H*I >= 2^20, else from
+ * 32 rows per expert; the shared expert: from 32 tokens.  The
  * environment variable MOE_FP8_EXPERT_PATH=gemm or =gemv overrides the choice
  * (diagnostics and tests; read on every call).
  */

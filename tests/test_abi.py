@@ -52,12 +52,13 @@ def test_expert_regime_query(L, monkeypatch):
     """Host-only: the regime rule of moe_layer_forward and its override."""
     monkeypatch.delenv("MOE_FP8_EXPERT_PATH", raising=False)
     q = _lib.expert_uses_gemm
-    assert q(_lib.dims(64, 2048, 768, 128, 8))          # 4 rows per expert
-    assert not q(_lib.dims(32, 2048, 768, 128, 8))      # 2 rows per expert
+    assert q(_lib.dims(16, 2048, 768, 128, 8))          # 1 row per expert
+    assert not q(_lib.dims(8, 2048, 768, 128, 8))       # 1/2 row per expert
     assert q(_lib.dims(4096, 2048, 768, 128, 8))
     assert q(_lib.dims(4096, 256, 128, 16, 2))          # H 256, I 128: smallest GEMM shapes
     assert not q(_lib.dims(4096, 2048 + 64, 768, 128, 8))  # H % 256 != 0
-    assert not q(_lib.dims(8, 256, 128, 16, 2))         # tiny: 1 row per expert
+    assert not q(_lib.dims(100, 256, 128, 16, 2))       # small experts: 12.5 rows each
+    assert q(_lib.dims(256, 256, 128, 16, 2))           # small experts: 32 rows each
     assert not q(_lib.dims(4096, 2048, 768 + 64, 128, 8))  # I % 128 != 0
     monkeypatch.setenv("MOE_FP8_EXPERT_PATH", "gemv")
     assert not q(_lib.dims(4096, 2048, 768, 128, 8))

@@ -188,6 +188,25 @@ def test_layer_forward_full(torch, name, T):
     assert_within_tol(oracle.bf16_to_f64(bf16_bits(out)), ref["out"], f"out {name} T={T}")
 
 
+# Shapes the regime rule sends to the tensor-core GEMM, forced through the
+# streamed GEMV (MOE_FP8_EXPERT_PATH=gemv): the GEMV's 16-token variant and its
+# hot-expert row loops stay covered.
+GEMV_FORCED = [("tiny", 100), ("qwen3moe_decode", 64), ("skewed", 256), ("large_sparse", 256)]
+
+
+@pytest.mark.parametrize("name,T", GEMV_FORCED)
+def test_layer_forward_full_through_gemv(torch, monkeypatch, name, T):
+    monkeypatch.setenv("MOE_FP8_EXPERT_PATH", "gemv")
+    L = host_layer(name)
+    D = dev_layer(name)
+    xb, _ = mi.make_tokens(L, T, seed=0)
+    out, idx, w = _forward(torch, D, _x(torch, xb))
+    ref = oracle.moe_layer(xb, L, keep_intermediates=False)
+    assert np.array_equal(idx.cpu().numpy(), ref["topk_idx"])
+    assert_within_tol(w.cpu().numpy(), ref["topk_w"], "topk_w", rel=W_REL)
+    assert_within_tol(oracle.bf16_to_f64(bf16_bits(out)), ref["out"], f"out {name} T={T} gemv")
+
+
 SAMPLED = [("qwen3moe_prefill", 4096), ("skewed", 2048), ("skewed", 16384)]
 
 
