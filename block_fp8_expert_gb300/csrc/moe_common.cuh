@@ -326,10 +326,11 @@ constexpr int kStatusWords = 16;
 
 
 // ---------------------------------------------------------------------------
-// Combine of output columns h..h+3 of token t (h a multiple of 4):
-// out[t, h..h+3] = sum_j w[t,j] y_perm[tok_slot_row[t*k+j], h..] (+ shared_y),
-// summed in fp32 in slot order j (in groups of 8 slots, loads first), the
-// shared expert's row added last, rounded once to bf16.
+// Combine of output columns h..h+V-1 of token t (V = 4 for fp32 expert
+// rows, 8 for fp16; h a multiple of V):
+// out[t, h..] = sum_j w[t,j] y_perm[tok_slot_row[t*k+j], h..] (+ shared_y),
+// the routed terms summed in fp32 in slot order j (in groups of 8 slots,
+// loads first), then added to the shared expert's row, rounded once to bf16.
 // ---------------------------------------------------------------------------
 // V consecutive expert outputs as fp32: V = 4 fp32 or V = 8 fp16 (16 bytes).
 __device__ __forceinline__ void load_v(const float* p, float (&v)[4]) {
