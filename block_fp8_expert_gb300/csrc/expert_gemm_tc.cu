@@ -736,7 +736,9 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x16, int T, const int32_t* exp
                                   const int32_t* row_token, uint16_t* x_perm, int E, int P,
                                   const moe_fp8_ffn& w, int H, int I, int32_t* tile_off,
                                   int32_t* slot_done, uint16_t* hid, void* y, bool y_half,
-                                  int32_t* status, cudaStream_t s, bool pdl) {
+                                  int32_t* status, cudaStream_t s, bool pdl,
+                                  bool tile_off_ready) {
+  static_assert(BT == kGemmTokenTile, "token tile of the permutation's tile prefix");
   cudaError_t err;
   if ((err = ensure_smem((const void*)k_expert_gemm_ws<true>, SMEM_WS)) != cudaSuccess) return err;
   if ((err = ensure_smem((const void*)k_expert_gemm_ws<false>, SMEM_WS)) != cudaSuccess) return err;
@@ -765,9 +767,11 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x16, int T, const int32_t* exp
   // token warp read the offsets without waiting for their previous kernel.
   // Host bound on the tile count: each expert adds at most one partial tile.
   const int max_ttiles = cdiv(P, BT) + min(E, P);
-  err = launch_k(k_tile_offsets, dim3(1), dim3(1024), 0, s, pdl, expert_off, E, tile_off,
-                 slot_done, max_ttiles);
-  if (err != cudaSuccess) return err;
+  if (!tile_off_ready) {
+    err = launch_k(k_tile_offsets, dim3(1), dim3(1024), 0, s, pdl, expert_off, E, tile_off,
+                   slot_done, max_ttiles);
+    if (err != cudaSuccess) return err;
+  }
   if (x_perm) {
     err = launch_k(k_gather_rows, dim3(cdiv(P, 8)), dim3(256), 0, s, pdl, x16, T, row_token,
                    expert_off, E, P, H, x_perm);

@@ -195,7 +195,7 @@ WsLayout ws_layout(const moe_dims& d) {
   L.sh_tile_off = take(2 * 4);
   L.x_perm = take(expert_gemm_tc_ok(d.H, d.I) ? P * H * 2 : 0);
   L.wr_planes = take(router_tc_ok(d.T, d.H, d.E) ? 3 * E * H * 2 : 0);
-  L.slot_done = take(((P + 127) / 128 + std::min(E, P)) * 4);
+  L.slot_done = take(expert_gemm_slots(P, E) * 4);
   L.sh_slot_done = take(Is ? ((T + 127) / 128 + 1) * 4 : 0);
   L.total = o;
   return L;
@@ -393,7 +393,9 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
   int32_t* srows = at<int32_t>(ws, L.sh_rows);
   int32_t* sact = at<int32_t>(ws, L.sh_active);
   const bool has_shared = d.I_shared > 0;
-  if (small_route_permute_ok(d.T, d.E, d.k)) {
+  const bool gemm = use_expert_gemm(P, d.E, d.H, d.I);
+  const bool small = small_route_permute_ok(d.T, d.E, d.k);
+  if (small) {
     // router logits, then top-k + permutation (+ the shared expert's identity
     // permutation) in one CTA
     CUDA_CHECK(launch_route_permute_small(
@@ -401,7 +403,10 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
                    at<uint16_t>(ws, L.wr_planes), idx, w, off,
                    row_token, tok_slot_row, at<int32_t>(ws, L.row_pair), active,
                    has_shared ? soff : nullptr, has_shared ? srows : nullptr,
-                   has_shared ? sact : nullptr, x16, status, st, true),
+                   has_shared ? sact : nullptr, x16,
+                   gemm ? at<int32_t>(ws, L.tile_off) : nullptr,
+                   gemm ? at<int32_t>(ws, L.slot_done) : nullptr, expert_gemm_slots(P, d.E),
+                   status, st, true),
                "moe_layer_forward: route+permute");
   } else {
     CUDA_CHECK(launch_route(x, Wr, bias, d.T, d.H, d.E, d.k, at<float>(ws, L.logits),
@@ -416,11 +421,11 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
       CUDA_CHECK(launch_identity_perm(d.T, soff, srows, sact, st, true),
                  "moe_layer_forward: shared");
   }
-  if (use_expert_gemm(P, d.E, d.H, d.I))
+  if (gemm)
     CUDA_CHECK(launch_expert_gemm_tc(x16, d.T, off, row_token, at<uint16_t>(ws, L.x_perm), d.E, P,
                                      routed, d.H, d.I, at<int32_t>(ws, L.tile_off),
                                      at<int32_t>(ws, L.slot_done), at<uint16_t>(ws, L.hid), y_perm,
-                                     true, status, st, true),
+                                     true, status, st, true, /*tile_off_ready=*/small),
                "moe_layer_forward: experts");
   else
     CUDA_CHECK(launch_expert_gemv(x16, off, row_token, active, d.E < P ? d.E : P, routed, d.H,

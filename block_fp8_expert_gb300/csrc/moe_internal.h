@@ -83,8 +83,13 @@ cudaError_t launch_router_logits_tc(const uint16_t* x, const float* Wr, int T, i
                                     int KS, float* part, uint16_t* x16, uint16_t* planes,
                                     int32_t* status, cudaStream_t s, bool pdl);
 
+// Token rows per tile of the tensor-core GEMM (its MMA N, at most).
+constexpr int kGemmTokenTile = 128;
+
 // Router logits, then top-k and the full permutation in one CTA, for
 // T*k <= 4096 (small_route_permute_ok).  sh_* may be NULL (no shared expert).
+// tile_off (E + 1 ints) may be NULL; else the permutation also writes the
+// GEMM's token-tile prefix there and zeroes slot_done[0, max_slots).
 bool small_route_permute_ok(int T, int E, int k);
 cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const float* bias,
                                        int T, int H, int E, int k, float* part,
@@ -92,6 +97,7 @@ cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const
                                        int32_t* row_token, int32_t* tok_slot_row,
                                        int32_t* row_pair, int32_t* active, int32_t* sh_off,
                                        int32_t* sh_rows, int32_t* sh_active, uint16_t* x16,
+                                       int32_t* tile_off, int32_t* slot_done, int max_slots,
                                        int32_t* status, cudaStream_t s, bool pdl);
 
 cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, int32_t* rank,
@@ -121,6 +127,8 @@ cudaError_t launch_expert_gemv(const uint16_t* x16, const int32_t* expert_off,
 // I % 128 == 0, H, I <= 4096 (expert_gemm_tc_ok).  tile_off: E + 1 ints of scratch;
 // slot_done: cdiv(P, 128) + min(E, P) ints of scratch (the down GEMM then
 // starts each token tile as soon as its hid rows are stored), or NULL.
+// tile_off_ready: the permutation already wrote tile_off and zeroed slot_done
+// (launch_route_permute_small), so the tile-offset kernel is skipped.
 bool expert_gemm_tc_ok(int H, int I);
 // x16: [T, H] fp16.  x_perm: [P, H] fp16 scratch that receives the
 // activation rows in expert order (x16[row_token[p]]), or NULL when row_token
@@ -130,7 +138,10 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x16, int T, const int32_t* exp
                                   const int32_t* row_token, uint16_t* x_perm, int E, int P,
                                   const moe_fp8_ffn& w, int H, int I, int32_t* tile_off,
                                   int32_t* slot_done, uint16_t* hid, void* y, bool y_half,
-                                  int32_t* status, cudaStream_t s, bool pdl);
+                                  int32_t* status, cudaStream_t s, bool pdl,
+                                  bool tile_off_ready = false);
+// slot_done entries the GEMM uses for P routed rows over E experts.
+inline int expert_gemm_slots(int P, int E) { return (P + 127) / 128 + (E < P ? E : P); }
 
 // Regime: true -> tensor-core grouped GEMM, false -> streamed grouped GEMV.
 // Decided on the host from shapes only; MOE_FP8_EXPERT_PATH=gemm|gemv in the

@@ -277,7 +277,7 @@ constexpr int kSmallPairs = 4096;
 constexpr int kSplitTopkTokens = 16;
 
 size_t small_route_smem(int E) {
-  return sizeof(int32_t) * (kSmallPairs + 3 * 1024 + 1 + 64) + sizeof(uint16_t) * 32 * (size_t)E;
+  return sizeof(int32_t) * (kSmallPairs + 3 * 1024 + 1 + 96) + sizeof(uint16_t) * 32 * (size_t)E;
 }
 
 template <int EPL>
@@ -288,7 +288,8 @@ k_topk_permute_small(const float* __restrict__ part, int KS, const float* __rest
                      int32_t* __restrict__ row_token, int32_t* __restrict__ tok_slot_row,
                      int32_t* __restrict__ row_pair, int32_t* __restrict__ active,
                      int32_t* __restrict__ sh_off, int32_t* __restrict__ sh_rows,
-                     int32_t* __restrict__ sh_active) {
+                     int32_t* __restrict__ sh_active, int32_t* __restrict__ tile_off,
+                     int32_t* __restrict__ slot_done, int max_slots) {
   extern __shared__ int32_t sm[];
   int32_t* s_idx = sm;                   // [kSmallPairs] expert of pair q
   int32_t* s_cnt = s_idx + kSmallPairs;  // [1024] counts, then rows taken so far
@@ -296,7 +297,8 @@ k_topk_permute_small(const float* __restrict__ part, int KS, const float* __rest
   int32_t* s_off = s_tot + 1024;         // [1025] expert offsets
   int32_t* s_wsum = s_off + 1025;        // [32]
   int32_t* s_wact = s_wsum + 32;         // [32]
-  uint16_t* s_cw = reinterpret_cast<uint16_t*>(s_wact + 32);  // [32][E] per-warp counts
+  int32_t* s_wtil = s_wact + 32;         // [32]
+  uint16_t* s_cw = reinterpret_cast<uint16_t*>(s_wtil + 32);  // [32][E] per-warp counts
   griddep_wait();
   griddep_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -331,52 +333,67 @@ k_topk_permute_small(const float* __restrict__ part, int KS, const float* __rest
   // 2. counts, offsets, active list
   for (int q = tid; q < P; q += 1024) atomicAdd(&s_cnt[s_idx[q]], 1);
   __syncthreads();
+  // (and, for the tensor-core GEMM, the token-tile prefix: tile_off[e] =
+  // sum over e' < e of ceil(count / kGemmTokenTile))
   const int c = tid < E ? s_cnt[tid] : 0;
-  int incl = c, act = c > 0 ? 1 : 0;
+  const int nt = cdiv(c, kGemmTokenTile);
+  int incl = c, act = c > 0 ? 1 : 0, tin = nt;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int v = __shfl_up_sync(0xffffffffu, incl, o);
     const int a = __shfl_up_sync(0xffffffffu, act, o);
+    const int b = __shfl_up_sync(0xffffffffu, tin, o);
     if (lane >= o) {
       incl += v;
       act += a;
+      tin += b;
     }
   }
   if (lane == 31) {
     s_wsum[warp] = incl;
     s_wact[warp] = act;
+    s_wtil[warp] = tin;
   }
   __syncthreads();
   if (warp == 0) {
-    int s = s_wsum[lane], a = s_wact[lane];
+    int s = s_wsum[lane], a = s_wact[lane], b = s_wtil[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int v = __shfl_up_sync(0xffffffffu, s, o);
       const int w = __shfl_up_sync(0xffffffffu, a, o);
+      const int u = __shfl_up_sync(0xffffffffu, b, o);
       if (lane >= o) {
         s += v;
         a += w;
+        b += u;
       }
     }
     s_wsum[lane] = s;
     s_wact[lane] = a;
+    s_wtil[lane] = b;
   }
   __syncthreads();
   {
     const int before = warp ? s_wsum[warp - 1] : 0;
     const int before_a = warp ? s_wact[warp - 1] : 0;
+    const int before_t = warp ? s_wtil[warp - 1] : 0;
     if (tid < E) {
       const int o = before + incl - c;
       s_off[tid] = o;
       expert_off[tid] = o;
       if (c > 0) active[1 + before_a + act - 1] = tid;
+      if (tile_off) tile_off[tid] = before_t + tin - nt;
     }
     if (tid == E - 1) {
       s_off[E] = before + incl;
       expert_off[E] = before + incl;
       active[0] = before_a + act;
+      if (tile_off) tile_off[E] = before_t + tin;
     }
   }
+  // the GEMM's gate/up -> down completion counters of this call start at zero
+  if (slot_done)
+    for (int i = tid; i < max_slots; i += 1024) slot_done[i] = 0;
   __syncthreads();
   s_cnt[tid] = 0;  // rows of each expert placed by earlier rounds
   // 3. rank rounds of 1024 pairs
@@ -480,6 +497,7 @@ cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const
                                        int32_t* row_token, int32_t* tok_slot_row,
                                        int32_t* row_pair, int32_t* active, int32_t* sh_off,
                                        int32_t* sh_rows, int32_t* sh_active, uint16_t* x16,
+                                       int32_t* tile_off, int32_t* slot_done, int max_slots,
                                        int32_t* status, cudaStream_t s, bool pdl) {
   cudaError_t err = launch_router_logits(x, Wr, T, H, E, part, planes, x16, status, s, pdl);
   if (err != cudaSuccess) return err;
@@ -501,7 +519,7 @@ cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const
     if (err != cudaSuccess) return err;
     return launch_k(k_topk_permute_small<0>, dim3(1), dim3(1024), smem, s, pdl, part, KS, bias,
                     T, E, k, topk_idx, topk_w, expert_off, row_token, tok_slot_row, row_pair,
-                    active, sh_off, sh_rows, sh_active);
+                    active, sh_off, sh_rows, sh_active, tile_off, slot_done, max_slots);
   }
 #define MOE_SMALL(EPLV)                                                                      \
   do {                                                                                       \
@@ -509,7 +527,8 @@ cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const
     if (err != cudaSuccess) return err;                                                      \
     return launch_k(k_topk_permute_small<EPLV>, dim3(1), dim3(1024), smem, s, pdl, part, KS, \
                     bias, T, E, k, topk_idx, topk_w, expert_off, row_token, tok_slot_row,    \
-                    row_pair, active, sh_off, sh_rows, sh_active);                           \
+                    row_pair, active, sh_off, sh_rows, sh_active, tile_off, slot_done,       \
+                    max_slots);                                                              \
   } while (0)
   if (epl <= 1) MOE_SMALL(1);
   if (epl <= 2) MOE_SMALL(2);
