@@ -185,18 +185,26 @@ k_gateup_stream(const uint16_t* __restrict__ x16, int H, int I,
 // 4 (chunks kp, kp+4, ...), kDnChunks per warp per K-group.
 // y[r, h] = sum_i hid[r, i] Wd[h, i], summed in fp32, stored in fp32 or (YH)
 // fp16 for every row r of the expert.
+// FUSE (cmb.ticket set; YH only; T <= 64, k <= 8): the last CTA of each 32-row
+// slice of h — one ticket per slice, counted up to the number of active
+// experts — also combines that slice for every token, with the combine
+// kernel's arithmetic (fp32 fmaf over the slots in order j, rounded once to
+// bf16), so no combine launch follows.  A thread per (token, 8 columns)
+// loads its token's slot rows and weights before the ticket, leaving one
+// round trip (the y rows) after it.
 // ---------------------------------------------------------------------------
 constexpr int kDnChunks = 3;  // I <= 768 in one K-group
 constexpr size_t kDnSmem = sizeof(uint4) * kDnChunks * 2 * kThreads;  // 24 KB
 
-template <int NT, bool YH>
+template <int NT, bool YH, bool FUSE = false>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
 k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
               const int32_t* __restrict__ expert_off, const int32_t* __restrict__ active,
               const uint8_t* __restrict__ dcodes, const float* __restrict__ dscales,
-              void* __restrict__ y, int32_t* __restrict__ status) {
+              void* __restrict__ y, int32_t* __restrict__ status, const FusedCombine cmb) {
   extern __shared__ uint4 wbuf[];  // [kDnChunks * 2][kThreads]
   __shared__ float red[4][2][NT][4][32];
+  __shared__ int is_last;
   griddep_wait();
   griddep_trigger();
   const int a = blockIdx.y;
@@ -303,14 +311,72 @@ k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
     }
     __syncthreads();
   }
+  if constexpr (YH && FUSE) {
+    {
+      const int t = tid >> 2, h = blockIdx.x * 32 + (tid & 3) * 8;
+      const bool mine = t < cmb.T;
+      int row[8];
+      float wt[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const bool ok = mine && j < cmb.k;
+        row[j] = ok ? cmb.tok_slot_row[t * cmb.k + j] : -1;
+        wt[j] = ok ? cmb.topk_w[t * cmb.k + j] : 0.f;
+      }
+      // the CTA's y stores (ordered by the barrier) are released device-wide
+      // before its ticket counts; the last ticket acquires everyone's
+      __syncthreads();
+      if (tid == 0) {
+        __threadfence();
+        is_last = atomicAdd(&cmb.ticket[blockIdx.x], 1) == active[0] - 1;
+        __threadfence();
+      }
+      __syncthreads();
+      if (is_last && mine) {
+        float yv[8][8], r[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (row[j] >= 0) {
+            load_v_cg(static_cast<const uint16_t*>(y) + (size_t)row[j] * H + h, yv[j]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) yv[j][i] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) r[i] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (row[j] < 0) continue;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) r[i] = fmaf(wt[j], yv[j][i], r[i]);
+        }
+        uint32_t o4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o4[i] = pack_bf16x2(0.f + r[2 * i], 0.f + r[2 * i + 1]);
+        *reinterpret_cast<uint4*>(cmb.out + (size_t)t * H + h) =
+            make_uint4(o4[0], o4[1], o4[2], o4[3]);
+      }
+    }
+  }
+}
+
+bool fused_combine_ok(int T, int k, int H, int max_active) {
+  // a thread per (token, 8 columns of the slice), at most 8 slots, and the
+  // down grid in one wave (a fenced ticket per CTA costs a round trip that
+  // later waves would queue behind)
+  const long long ctas = (long long)(H / 32) * max_active;
+  return T >= 1 && T * 4 <= kThreads && k >= 1 && k <= 8 && H % 32 == 0 &&
+         ctas <= (long long)num_sms() * 4;
 }
 
 cudaError_t launch_expert_gemv(const uint16_t* x16, const int32_t* expert_off,
                                const int32_t* row_token, const int32_t* active, int max_active,
                                const moe_fp8_ffn& w, int H, int I, int tokens_per_expert_hint,
                                uint16_t* hid, void* y, bool y_half, int32_t* status,
-                               cudaStream_t s, bool pdl) {
+                               cudaStream_t s, bool pdl, const FusedCombine& cmb) {
   if (max_active <= 0) return cudaSuccess;
+  if (cmb.ticket && !fused_combine_ok(cmb.T, cmb.k, H, max_active)) return cudaErrorInvalidValue;
   cudaError_t e;
   const bool nt1 = tokens_per_expert_hint <= 8;
   const dim3 block(kThreads);
@@ -319,7 +385,7 @@ cudaError_t launch_expert_gemv(const uint16_t* x16, const int32_t* expert_off,
     cudaError_t err = ensure_smem((const void*)kern, kDnSmem);
     if (err != cudaSuccess) return err;
     return launch_k(kern, g2, block, kDnSmem, s, pdl, (const uint16_t*)hid, H, I, expert_off,
-                    active, w.down.codes, w.down.scales, y, status);
+                    active, w.down.codes, w.down.scales, y, status, cmb);
   };
   if (nt1) {
     if ((e = ensure_smem((const void*)k_gateup_stream<1>, kGuSmem)) != cudaSuccess) return e;
@@ -327,8 +393,10 @@ cudaError_t launch_expert_gemv(const uint16_t* x16, const int32_t* expert_off,
                  row_token, active, w.gate.codes, w.gate.scales, w.up.codes, w.up.scales, hid,
                  status);
     if (e != cudaSuccess) return e;
+    if (cmb.ticket) return down(k_down_stream<1, true, true>);
     return y_half ? down(k_down_stream<1, true>) : down(k_down_stream<1, false>);
   }
+  if (cmb.ticket) return down(k_down_stream<2, true, true>);
   if ((e = ensure_smem((const void*)k_gateup_stream<2>, kGuSmem)) != cudaSuccess) return e;
   e = launch_k(k_gateup_stream<2>, g1, block, kGuSmem, s, pdl, x16, H, I, expert_off, row_token,
                active, w.gate.codes, w.gate.scales, w.up.codes, w.up.scales, hid, status);

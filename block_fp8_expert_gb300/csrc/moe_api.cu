@@ -196,6 +196,7 @@ WsLayout ws_layout(const moe_dims& d) {
   L.x_perm = take(expert_gemm_tc_ok(d.H, d.I) ? P * H * 2 : 0);
   L.wr_planes = take(router_tc_ok(d.T, d.H, d.E) ? 3 * E * H * 2 : 0);
   L.slot_done = take(expert_gemm_slots(P, E) * 4);
+  L.ticket = take(((size_t)d.H / 32) * 4);  // fused combine: one per 32 columns of H
   L.sh_slot_done = take(Is ? ((T + 127) / 128 + 1) * 4 : 0);
   L.total = o;
   return L;
@@ -395,6 +396,10 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
   const bool has_shared = d.I_shared > 0;
   const bool gemm = use_expert_gemm(P, d.E, d.H, d.I);
   const bool small = small_route_permute_ok(d.T, d.E, d.k);
+  // streamed GEMV, one-CTA permutation, no shared expert: the down kernel
+  // also combines (its tickets cleared by the permutation)
+  const bool fuse_combine =
+      !gemm && small && !has_shared && fused_combine_ok(d.T, d.k, d.H, d.E < P ? d.E : P);
   if (small) {
     // router logits, then top-k + permutation (+ the shared expert's identity
     // permutation) in one CTA
@@ -405,7 +410,9 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
                    has_shared ? soff : nullptr, has_shared ? srows : nullptr,
                    has_shared ? sact : nullptr, x16,
                    gemm ? at<int32_t>(ws, L.tile_off) : nullptr,
-                   gemm ? at<int32_t>(ws, L.slot_done) : nullptr, expert_gemm_slots(P, d.E),
+                   gemm ? at<int32_t>(ws, L.slot_done)
+                        : (fuse_combine ? at<int32_t>(ws, L.ticket) : nullptr),
+                   gemm ? expert_gemm_slots(P, d.E) : d.H / 32,
                    status, st, true),
                "moe_layer_forward: route+permute");
   } else {
@@ -421,17 +428,27 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
       CUDA_CHECK(launch_identity_perm(d.T, soff, srows, sact, st, true),
                  "moe_layer_forward: shared");
   }
-  if (gemm)
+  if (gemm) {
     CUDA_CHECK(launch_expert_gemm_tc(x16, d.T, off, row_token, at<uint16_t>(ws, L.x_perm), d.E, P,
                                      routed, d.H, d.I, at<int32_t>(ws, L.tile_off),
                                      at<int32_t>(ws, L.slot_done), at<uint16_t>(ws, L.hid), y_perm,
                                      true, status, st, true, /*tile_off_ready=*/small),
                "moe_layer_forward: experts");
-  else
+  } else {
+    FusedCombine cmb;
+    if (fuse_combine) {
+      cmb.ticket = at<int32_t>(ws, L.ticket);
+      cmb.tok_slot_row = tok_slot_row;
+      cmb.topk_w = w;
+      cmb.T = d.T;
+      cmb.k = d.k;
+      cmb.out = out;
+    }
     CUDA_CHECK(launch_expert_gemv(x16, off, row_token, active, d.E < P ? d.E : P, routed, d.H,
                                   d.I, cdiv(P, d.E), at<uint16_t>(ws, L.hid), y_perm, true,
-                                  status, st, true),
+                                  status, st, true, cmb),
                "moe_layer_forward: experts");
+  }
   uint16_t* shared_y = nullptr;
   if (has_shared) {
     shared_y = at<uint16_t>(ws, L.sh_y);
@@ -447,8 +464,10 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
                                     at<uint16_t>(ws, L.sh_hid), shared_y, true, status, st, true),
                  "moe_layer_forward: shared expert");
   }
-  CUDA_CHECK(launch_combine(y_perm, true, tok_slot_row, w, shared_y, d.T, d.H, d.k, out, st, true),
-             "moe_layer_forward: combine");
+  if (!fuse_combine)
+    CUDA_CHECK(launch_combine(y_perm, true, tok_slot_row, w, shared_y, d.T, d.H, d.k, out, st,
+                              true),
+               "moe_layer_forward: combine");
   return MOE_OK;
 }
 

@@ -347,6 +347,18 @@ __device__ __forceinline__ void load_v(const uint16_t* p, float (&v)[8]) {
     v[2 * i + 1] = f.y;
   }
 }
+// L2-coherent load (ld.global.cg) of 8 fp16, for rows that other CTAs of the
+// running kernel wrote.
+__device__ __forceinline__ void load_v_cg(const uint16_t* p, float (&v)[8]) {
+  const uint4 a = __ldcg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
 // out[t, h .. h + V) = sum_j w[t, j] y_perm[tok_slot_row[t k + j], ...]
 // (+ shared_y[t, ...]), summed in fp32 in slot order j, rounded once to bf16.
 template <typename YT, int V>

@@ -62,7 +62,7 @@ int num_sms();
 struct WsLayout {
   size_t status, logits, rank, block_cnt, block_base, active, idx, w, off, row_token,
       tok_slot_row, row_pair, x16, hid, y_perm, sh_hid, sh_y, sh_off, sh_rows, sh_active,
-      tile_off, sh_tile_off, x_perm, wr_planes, slot_done, sh_slot_done, total;
+      tile_off, sh_tile_off, x_perm, wr_planes, slot_done, sh_slot_done, ticket, total;
 };
 WsLayout ws_layout(const moe_dims& d);
 
@@ -89,7 +89,8 @@ constexpr int kGemmTokenTile = 128;
 // Router logits, then top-k and the full permutation in one CTA, for
 // T*k <= 4096 (small_route_permute_ok).  sh_* may be NULL (no shared expert).
 // tile_off (E + 1 ints) may be NULL; else the permutation also writes the
-// GEMM's token-tile prefix there and zeroes slot_done[0, max_slots).
+// GEMM's token-tile prefix there.  counters[0, n_counters) (may be NULL) are
+// zeroed: the GEMM's completion counters or the fused combine's tickets.
 bool small_route_permute_ok(int T, int E, int k);
 cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const float* bias,
                                        int T, int H, int E, int k, float* part,
@@ -97,7 +98,7 @@ cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const
                                        int32_t* row_token, int32_t* tok_slot_row,
                                        int32_t* row_pair, int32_t* active, int32_t* sh_off,
                                        int32_t* sh_rows, int32_t* sh_active, uint16_t* x16,
-                                       int32_t* tile_off, int32_t* slot_done, int max_slots,
+                                       int32_t* tile_off, int32_t* counters, int n_counters,
                                        int32_t* status, cudaStream_t s, bool pdl);
 
 cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, int32_t* rank,
@@ -116,11 +117,25 @@ cudaError_t launch_x_to_f16(const uint16_t* x, long long n, uint16_t* x16, int32
 // fp16 activations x16; y fp32 or (y_half) fp16.  max_active bounds the list length;
 // tokens_per_expert_hint (the expected rows per expert) picks the MMA's N
 // width; any segment length is handled.
+// The combine folded into the streamed down projection (fp16 y only): the
+// last down CTA of each 32-row slice of H writes out[t, slice] for every
+// token.  ticket: H / 32 ints that are zero when the down kernel starts (the
+// one-CTA permutation clears them); NULL = no fused combine.  Only for
+// shapes fused_combine_ok accepts (T <= 64, k <= 8, the down grid of
+// H / 32 x max_active CTAs in one wave).
+bool fused_combine_ok(int T, int k, int H, int max_active);
+struct FusedCombine {
+  int32_t* ticket = nullptr;
+  const int32_t* tok_slot_row = nullptr;
+  const float* topk_w = nullptr;
+  int T = 0, k = 0;
+  uint16_t* out = nullptr;
+};
 cudaError_t launch_expert_gemv(const uint16_t* x16, const int32_t* expert_off,
                                const int32_t* row_token, const int32_t* active, int max_active,
                                const moe_fp8_ffn& w, int H, int I, int tokens_per_expert_hint,
                                uint16_t* hid, void* y, bool y_half, int32_t* status,
-                               cudaStream_t s, bool pdl);
+                               cudaStream_t s, bool pdl, const FusedCombine& cmb = FusedCombine{});
 
 // Grouped GEMM on the tensor cores (tcgen05) for many tokens per expert:
 // gate/up + SwiGLU -> hid, then down -> y.  Needs H % 256 == 0 and

@@ -289,7 +289,7 @@ k_topk_permute_small(const float* __restrict__ part, int KS, const float* __rest
                      int32_t* __restrict__ row_pair, int32_t* __restrict__ active,
                      int32_t* __restrict__ sh_off, int32_t* __restrict__ sh_rows,
                      int32_t* __restrict__ sh_active, int32_t* __restrict__ tile_off,
-                     int32_t* __restrict__ slot_done, int max_slots) {
+                     int32_t* __restrict__ counters, int n_counters) {
   extern __shared__ int32_t sm[];
   int32_t* s_idx = sm;                   // [kSmallPairs] expert of pair q
   int32_t* s_cnt = s_idx + kSmallPairs;  // [1024] counts, then rows taken so far
@@ -391,9 +391,10 @@ k_topk_permute_small(const float* __restrict__ part, int KS, const float* __rest
       if (tile_off) tile_off[E] = before_t + tin;
     }
   }
-  // the GEMM's gate/up -> down completion counters of this call start at zero
-  if (slot_done)
-    for (int i = tid; i < max_slots; i += 1024) slot_done[i] = 0;
+  // the expert kernels' counters of this call (the GEMM's gate/up -> down
+  // completion counters, or the fused combine's tickets) start at zero
+  if (counters)
+    for (int i = tid; i < n_counters; i += 1024) counters[i] = 0;
   __syncthreads();
   s_cnt[tid] = 0;  // rows of each expert placed by earlier rounds
   // 3. rank rounds of 1024 pairs
@@ -497,7 +498,7 @@ cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const
                                        int32_t* row_token, int32_t* tok_slot_row,
                                        int32_t* row_pair, int32_t* active, int32_t* sh_off,
                                        int32_t* sh_rows, int32_t* sh_active, uint16_t* x16,
-                                       int32_t* tile_off, int32_t* slot_done, int max_slots,
+                                       int32_t* tile_off, int32_t* counters, int n_counters,
                                        int32_t* status, cudaStream_t s, bool pdl) {
   cudaError_t err = launch_router_logits(x, Wr, T, H, E, part, planes, x16, status, s, pdl);
   if (err != cudaSuccess) return err;
@@ -519,7 +520,7 @@ cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const
     if (err != cudaSuccess) return err;
     return launch_k(k_topk_permute_small<0>, dim3(1), dim3(1024), smem, s, pdl, part, KS, bias,
                     T, E, k, topk_idx, topk_w, expert_off, row_token, tok_slot_row, row_pair,
-                    active, sh_off, sh_rows, sh_active, tile_off, slot_done, max_slots);
+                    active, sh_off, sh_rows, sh_active, tile_off, counters, n_counters);
   }
 #define MOE_SMALL(EPLV)                                                                      \
   do {                                                                                       \
@@ -527,8 +528,8 @@ cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const
     if (err != cudaSuccess) return err;                                                      \
     return launch_k(k_topk_permute_small<EPLV>, dim3(1), dim3(1024), smem, s, pdl, part, KS, \
                     bias, T, E, k, topk_idx, topk_w, expert_off, row_token, tok_slot_row,    \
-                    row_pair, active, sh_off, sh_rows, sh_active, tile_off, slot_done,       \
-                    max_slots);                                                              \
+                    row_pair, active, sh_off, sh_rows, sh_active, tile_off, counters,        \
+                    n_counters);                                                             \
   } while (0)
   if (epl <= 1) MOE_SMALL(1);
   if (epl <= 2) MOE_SMALL(2);

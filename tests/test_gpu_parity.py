@@ -237,6 +237,28 @@ def test_layer_forward_is_deterministic(torch):
                            v.view(torch.uint8) if v.dtype == torch.bfloat16 else v)
 
 
+@pytest.mark.parametrize("name,T", [("tiny", 8), ("qwen3moe_decode", 1), ("qwen3moe_decode", 8),
+                                    ("qwen3moe_decode", 64), ("large_sparse", 1)])
+def test_layer_forward_dirty_workspace(torch, name, T):
+    """Every counter a call relies on (the fused combine's tickets, the GEMM's
+    completion counters, the status words) is cleared by the call itself: a
+    workspace full of stale bytes gives the same output, twice in a row."""
+    L = host_layer(name)
+    D = dev_layer(name)
+    xb, _ = mi.make_tokens(L, T, seed=3)
+    xd = _x(torch, xb)
+    ws = D.workspace(T)
+    outs = []
+    for fill in (0x5A, 0xFF):
+        ws.fill_(fill)
+        outs.append(D.forward(xd, ws=ws))
+        torch.cuda.synchronize()
+        assert ws[:4].view(torch.int32).item() == 0
+    assert torch.equal(outs[0].view(torch.uint8), outs[1].view(torch.uint8))
+    ref = oracle.moe_layer(xb, L, keep_intermediates=False)
+    assert_within_tol(oracle.bf16_to_f64(bf16_bits(outs[0])), ref["out"], f"out {name} T={T}")
+
+
 def test_layer_forward_empty_batch(torch):
     D = dev_layer("tiny")
     x = torch.empty((0, D.H), dtype=torch.bfloat16, device="cuda")
