@@ -205,8 +205,11 @@ k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
   extern __shared__ uint4 wbuf[];  // [kDnChunks * 2][kThreads]
   __shared__ float red[4][2][NT][4][32];
   __shared__ int is_last;
-  griddep_wait();
-  griddep_trigger();
+  // The active list and the offsets come from the permutation, which had
+  // completed before the previous kernel (gate/up) passed its own
+  // griddep_wait; they and the weights are read before this kernel waits for
+  // gate/up, so the first K-group's weights stream while gate/up finishes.
+  // Everything gate/up writes (hid) is read after the wait.
   const int a = blockIdx.y;
   if (a >= active[0]) return;
   const int e = active[1 + a];
@@ -234,6 +237,8 @@ k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
   // The first K-group's weights depend only on the expert: start them before
   // the expert's rows are read.
   issue(0);
+  griddep_wait();
+  griddep_trigger();
   const int r0 = expert_off[e];
   const int ne = expert_off[e + 1] - r0;
   bool issued = true;
