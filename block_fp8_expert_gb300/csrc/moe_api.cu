@@ -465,8 +465,8 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
                  "moe_layer_forward: shared expert");
   }
   if (!fuse_combine)
-    CUDA_CHECK(launch_combine(y_perm, true, tok_slot_row, w, shared_y, d.T, d.H, d.k, out, st,
-                              true),
+    CUDA_CHECK(launch_combine_layer(y_perm, true, tok_slot_row, w, shared_y, d.T, d.H, d.k, out,
+                                    st),
                "moe_layer_forward: combine");
   return MOE_OK;
 }
