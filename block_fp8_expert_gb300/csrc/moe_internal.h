@@ -168,8 +168,9 @@ cudaError_t launch_combine(const void* y_perm, bool y_half, const int32_t* tok_s
                            const float* topk_w, const void* shared_y, int T, int H, int k,
                            uint16_t* out, cudaStream_t s, bool pdl);
 // The same inside moe_layer_forward (programmatic dependent launch): for
-// k <= 8 the slot rows and weights, which the routing wrote before any expert
-// kernel ran, are loaded before the kernel waits for the expert outputs.
+// k <= 16 the slot rows and weights, which the routing wrote before any
+// expert kernel ran, are loaded before the kernel waits for the expert
+// outputs.
 cudaError_t launch_combine_layer(const void* y_perm, bool y_half, const int32_t* tok_slot_row,
                                  const float* topk_w, const void* shared_y, int T, int H, int k,
                                  uint16_t* out, cudaStream_t s);
