@@ -90,6 +90,9 @@ struct GemmArgs {
   int32_t* slot_done;
   int slot_need;
   int32_t* status;
+  // down only: the gate/up launch's grid and weight blocks per token tile
+  // when both GEMMs run one CTA per SM (0: no stride adjustment)
+  int gu_grid, gu_wblocks;
 };
 
 struct WsShared {
@@ -191,6 +194,28 @@ struct TileInfo {
   int slot;                    // token tile index (tile_off[e] + m0 / 128)
 };
 
+// CTAs that take tiles, each taking every stride-th one.  All of them, except
+// in this case: the down GEMM's CTAs can only start on SMs that gate/up CTAs
+// have left, and when gate/up's tiles do not divide evenly over its grid, r of
+// its CTAs run one tile longer, so the last r down CTAs (dispatched in order)
+// start one gate/up tile late.  If leaving those r CTAs without tiles ends
+// the launch sooner, in units of down tiles (a gate/up tile is H / I of one:
+// the same 256 x K x N shape with K = H rather than I), the stride is G - r.
+__device__ __forceinline__ int tile_stride(const GemmArgs& a, int n_tiles) {
+  const int G = (int)gridDim.x;
+  if (a.gu_grid != G || a.gu_grid <= 0) return G;
+  const long long gu_tiles = (long long)a.tile_off[a.E] * a.gu_wblocks;
+  if (gu_tiles <= a.gu_grid) return G;
+  const int r = (int)(gu_tiles % a.gu_grid);
+  if (r == 0 || n_tiles <= G) return G;
+  const float rho = (float)a.rows_per_expert / (float)a.K;
+  const int c_first = cdiv(n_tiles, G);                // tiles of CTA 0
+  const int c_late = cdiv(n_tiles - (G - r), G);       // tiles of the first late CTA
+  const float end_all = fmaxf((float)c_first, rho + (float)c_late);
+  const float end_early = (float)cdiv(n_tiles, G - r);
+  return end_early < end_all ? G - r : G;
+}
+
 // Tile t -> expert, token rows and weight rows, from the shared-memory copies.
 __device__ __forceinline__ TileInfo tile_info(const WsShared& sh, const GemmArgs& a, int t,
                                               bool gateup) {
@@ -230,7 +255,9 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const GemmArgs& a = args;
   const int n_tiles = a.tile_off[a.E] * a.n_wblocks;
-  if ((int)blockIdx.x >= n_tiles) return;  // uniform per CTA, before any barrier
+  const int tstride = GATEUP ? (int)gridDim.x : tile_stride(a, n_tiles);
+  // uniform per CTA, before any barrier
+  if ((int)blockIdx.x >= n_tiles || (int)blockIdx.x >= tstride) return;
   const int nK = a.K / BK;
   const int nKb = cdiv(a.K, kScaleBlock);
   const int nRb = cdiv(a.rows_per_expert, kScaleBlock);
@@ -275,7 +302,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     // ------------------------------------------------ E4M3 code blocks (TMA)
     int j = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+    for (int t = blockIdx.x; t < n_tiles && ok; t += tstride) {
       const TileInfo ti = tile_info(sh, a, t, GATEUP);
       const int row = ti.e * a.rows_per_expert + ti.n0;
       for (int ks = 0; ks < nK; ++ks, ++j) {
@@ -313,7 +340,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     // are never stored; rows past the matrix read 0).
     int j = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+    for (int t = blockIdx.x; t < n_tiles && ok; t += tstride) {
       const TileInfo ti = tile_info(sh, a, t, GATEUP);
       if (!GATEUP && a.slot_done) {
         // this token tile's hid rows: every gate/up weight-block tile of the
@@ -381,9 +408,9 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     float scale_next = scale_of(blockIdx.x);
     int j = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+    for (int t = blockIdx.x; t < n_tiles && ok; t += tstride) {
       const float scale_tile = scale_next;
-      if (t + (int)gridDim.x < n_tiles) scale_next = scale_of(t + gridDim.x);
+      if (t + tstride < n_tiles) scale_next = scale_of(t + tstride);
       for (int ks = 0; ks < nK; ++ks, ++j) {
         const int sc = j % NCD, sa = j % NA;
         const float scale = __shfl_sync(0xffffffffu, scale_tile, ks * BK / kScaleBlock);
@@ -425,7 +452,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     // ------------------------------------------------ tcgen05.mma issue
     int j = 0, tl = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++tl) {
+    for (int t = blockIdx.x; t < n_tiles && ok; t += tstride, ++tl) {
       const TileInfo ti = tile_info(sh, a, t, GATEUP);
       const uint32_t idesc = tc::idesc_f16_f32(BW, ti.n);
       if (tl >= 1 && !warp_wait(sh, &sh.acc_empty, (uint32_t)((tl - 1) & 1), a.status, 5, tl)) {
@@ -483,7 +510,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     const uint32_t t_lane = tmem + ((uint32_t)(32 * q) << 16);
     uint8_t* stg = smem + OFF_STG + (warp - W_EPI0) * STG_WARP_BYTES;
     int tl = 0;
-    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tl) {
+    for (int t = blockIdx.x; t < n_tiles; t += tstride, ++tl) {
       const TileInfo ti = tile_info(sh, a, t, GATEUP);
       // this warp's copies of the previous tile have read its staging
       tc::bulk_wait_read_all();
@@ -786,6 +813,11 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x16, int T, const int32_t* exp
   if (err != cudaSuccess) return err;
   GemmArgs d{expert_off, tile_off, E, I, H, w.down.scales, nullptr, y, H, y_half ? 1 : 0,
              H / (2 * BW), 0, slot_done, (I / BW) * kEpiWarps, status};
+  const int gu_grid = min(nsm, max_ttiles * g.n_wblocks);
+  if (gu_grid == nsm && min(nsm, max_ttiles * d.n_wblocks) == nsm) {
+    d.gu_grid = gu_grid;
+    d.gu_wblocks = g.n_wblocks;
+  }
   return launch_k(k_expert_gemm_ws<false>, dim3(min(nsm, max_ttiles * d.n_wblocks)), blk,
                   (size_t)SMEM_WS, s, pdl, dmap, dmap, hmap, ymap, d);
 }
