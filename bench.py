@@ -470,7 +470,7 @@ def run_gpu(args):
                 ("tiny", 8)]
         for nm, tt_ in plan:
             try:
-                r, *_ = measure_workload(torch, nm, tt_, args.sweep_steps, 2, flush, pk, dev_cache)
+                r, *_ = measure_workload(torch, nm, tt_, args.sweep_steps, 3, flush, pk, dev_cache)
                 sweep.append(r)
             except Exception as ex:  # report, do not hide
                 sweep.append({"workload": f"{nm}_T{tt_}", "error": repr(ex)[:200]})
