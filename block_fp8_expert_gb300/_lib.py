@@ -24,6 +24,8 @@ MOE_ERR_TIMEOUT = 6
 MOE_ERR_NOT_IMPLEMENTED = 7
 MOE_DEV_BAD_EXPERT_INDEX = 1
 MOE_DEV_WAIT_TIMEOUT = 2
+MOE_DEV_FP16_RANGE = 4
+MOE_DEV_NONFINITE = 8
 
 
 class MoeError(RuntimeError):
@@ -195,7 +197,8 @@ def moe_layer_forward(x, Wr, bias, routed: Fp8Ffn, shared: Optional[Fp8Ffn], d: 
 
 
 def moe_read_device_status(ws, stream=None) -> int:
-    """The workspace's device status bits; raises MoeError when any is set."""
+    """The workspace's device status bits; raises MoeError when any is set.
+    ws=None reads the status word of moe_permute_static_scratch's fixed array."""
     v = ctypes.c_int32(0)
     st = lib().moe_read_device_status(_ptr(ws), ctypes.byref(v), _stream(stream))
     if st not in (MOE_OK, MOE_ERR_DEVICE_STATUS):

@@ -8,7 +8,20 @@
 //   gate/up: the gate rows n0..n0+127 and the same up rows, K = H; the
 //            epilogue writes hid = silu(g) * u in fp16;
 //   down:    output rows n0..n0+255 as two blocks of 128, K = I; the epilogue
-//            writes y in fp32.
+//            writes y in fp32, or fp16 with one exponent per 32 columns.
+// Range: every operand and intermediate is normalised by an exact power of
+// two, so the fp16 formats hold any block-scale and activation magnitude:
+//   x'  = x 2^-a per token row (a = floor(log2 rms(x)), by the gather);
+//   W'  = dec(code) * (S / 2^p), p = floor(log2) of the largest scale of the
+//         expert's gate (or up) matrix, or of the down row block;
+//   hid'= silu(g) u / 2^(a + pg + a + pu + c), c = floor(log2 H) + 4: the
+//         accumulators give it as sigma(g) D0 D1 2^-c, independent of every
+//         scale and of the activations' magnitude;
+//   y   = D 2^(pd + pg + pu + c + 2a).
+// A hid' value beyond fp16's range, or a token whose 32 features of one
+// epilogue warp all fall below 2^-12 (where fp16's spacing would cost
+// precision), raises MOE_DEV_FP16_RANGE; a non-finite scale, activation or
+// result raises MOE_DEV_NONFINITE.
 // Two accumulators D0, D1 (128 lanes = weight rows x N columns = tokens, fp32)
 // use TMEM columns 0..255; columns 256..511 hold four stages of decoded
 // weights (two 128 x 64 fp16 blocks per 64-wide K step).  N is the tile's row
@@ -78,9 +91,8 @@ struct GemmArgs {
   int rows_per_expert;  // I for gate/up, H for down
   const float* s0;      // gate (or down) scales
   const float* s1;      // up scales (gate/up only)
-  void* out;            // hid fp16 [P, I] or y [P, H] (fp32, or fp16 when y_half)
+  void* out;            // hid fp16 [P, I] or y [P, H] (fp32, or fp16 when yexp is set)
   int out_ld;
-  int y_half;
   int n_wblocks;  // weight-block pairs per expert (tiles per token tile)
   int all_wait;   // 1: the previous kernel wrote the tile offsets (every warp waits)
   // Per token tile ("slot") of the gate/up GEMM: completed epilogue-warp
@@ -93,6 +105,16 @@ struct GemmArgs {
   // down only: the gate/up launch's grid and weight blocks per token tile
   // when both GEMMs run one CTA per SM (0: no stride adjustment)
   int gu_grid, gu_wblocks;
+  // Range normalisation (see the top of this file)
+  const int32_t* xexp;  // a of each permuted row: its activations are x' 2^a
+  const float* gs;      // down only: the gate and up scales, for pg and pu
+  const float* us;
+  int n_gu_scales;      // scales per expert of one gate/up matrix
+  int hid_shift;        // c
+  // down, fp16 y only: exponent s per 32 columns and row (y = y'' 2^s),
+  // [rows_per_expert / 32][yexp_rows]; NULL: y is fp32
+  int16_t* yexp;
+  int yexp_rows;
 };
 
 struct WsShared {
@@ -399,11 +421,19 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     // Block scales: lane i holds the scale of K block i of the tile's weight
     // row block (nKb <= 32), loaded one tile ahead so that no step waits for
     // global memory.
+    // The scale is divided by the power of two 2^p of the expert matrix's
+    // (gate/up) or the row block's (down) largest scale, so the fp16 operand
+    // fp16(dec * fp16(S / 2^p)) stays in range for any scale magnitude; the
+    // epilogue multiplies 2^p back in fp32.
     const float* sp = (GATEUP && blk) ? a.s1 : a.s0;
+    bool bad = false;
     auto scale_of = [&](int t) -> float {
       const TileInfo ti = tile_info(sh, a, t, GATEUP);
       const size_t srow = (size_t)ti.e * nRb + ti.n0 / kScaleBlock + (GATEUP ? 0 : blk);
-      return lane < nKb ? sp[srow * nKb + lane] : 0.f;
+      const float sc = lane < nKb ? sp[srow * nKb + lane] : 0.f;
+      const int p = GATEUP ? warp_max_exp_of(sp + (size_t)ti.e * nRb * nKb, nRb * nKb, lane, bad)
+                           : warp_max_exp(__float_as_uint(sc) & 0x7fffffffu, bad);
+      return sc * pow2f(-p);
     };
     float scale_next = scale_of(blockIdx.x);
     int j = 0;
@@ -448,6 +478,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
         }
       }
     }
+    if (bad && lane == 0) raise_status(a.status, MOE_DEV_NONFINITE);
   } else if (warp == W_MMA) {
     // ------------------------------------------------ tcgen05.mma issue
     int j = 0, tl = 0;
@@ -509,9 +540,24 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     const int q = warp & 3, eh = (warp - W_EPI0) >> 2;
     const uint32_t t_lane = tmem + ((uint32_t)(32 * q) << 16);
     uint8_t* stg = smem + OFF_STG + (warp - W_EPI0) * STG_WARP_BYTES;
+    const int nKb = cdiv(a.K, kScaleBlock), nRb = cdiv(a.rows_per_expert, kScaleBlock);
+    const float inv_c = pow2f(-a.hid_shift);
+    bool bad = false;
     int tl = 0;
     for (int t = blockIdx.x; t < n_tiles; t += tstride, ++tl) {
       const TileInfo ti = tile_info(sh, a, t, GATEUP);
+      // the tile's powers of two (scales only: computed before the wait)
+      int p0 = 0;  // gate/up: pg; down: pd + pg + pu + c
+      if (GATEUP) {
+        p0 = warp_max_exp_of(a.s0 + (size_t)ti.e * nRb * nKb, nRb * nKb, lane, bad);
+      } else {
+        const size_t srow = (size_t)ti.e * nRb + ti.n0 / kScaleBlock + eh;
+        const float sc = lane < nKb ? a.s0[srow * nKb + lane] : 0.f;
+        p0 = warp_max_exp(__float_as_uint(sc) & 0x7fffffffu, bad) +
+             warp_max_exp_of(a.gs + (size_t)ti.e * a.n_gu_scales, a.n_gu_scales, lane, bad) +
+             warp_max_exp_of(a.us + (size_t)ti.e * a.n_gu_scales, a.n_gu_scales, lane, bad) +
+             a.hid_shift;
+      }
       // this warp's copies of the previous tile have read its staging
       tc::bulk_wait_read_all();
       __syncwarp();
@@ -519,24 +565,39 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
       tc::fence_after_sync();
       const int nchunks = (ti.n + 31) >> 5;
       if (GATEUP) {
-        bool overflow = false;
+        bool overflow = false, underflow = false;
 #pragma unroll 1
         for (int c = eh; c < nchunks; c += 2) {
           uint32_t gr[32], ur[32];
           tc::ld_32x32b_x32(t_lane + 32 * c, gr);
           tc::ld_32x32b_x32(t_lane + COL_D1 + 32 * c, ur);
-          tc::wait_ld();
+          // a of this chunk's tokens: lane i holds token 32 c + i's
           const int nv = ti.rows - 32 * c;  // columns of real tokens in this chunk
+          const int ax = lane < nv ? __ldg(a.xexp + ti.r0 + ti.m0 + 32 * c + lane) : 0;
+          tc::wait_ld();
           uint8_t* rows = stg + (c >> 1) * (32 * 64);
+          uint32_t small = 0, nonzero = 0;
 #pragma unroll
           for (int v = 0; v < 32; ++v) {
-            const float g = __uint_as_float(gr[v]), u = __uint_as_float(ur[v]);
-            const float h = __fdividef(g, 1.f + __expf(-g)) * u;  // silu(g) * u
+            const float d0 = __uint_as_float(gr[v]), d1 = __uint_as_float(ur[v]);
+            // g = d0 2^(pg + a) decides the gate; the rest is normalised:
+            // hid' = sigma(g) d0 d1 2^-c
+            const int av = __shfl_sync(0xffffffffu, ax, v);
+            const float g = d0 * pow2f(min(max(p0 + av, -126), 127));
+            const float sig = __fdividef(1.f, 1.f + __expf(-fminf(fmaxf(g, -80.f), 80.f)));
+            const float h = sig * d0 * d1 * inv_c;
             overflow |= v < nv && !(fabsf(h) <= kF16Max);
+            small |= (uint32_t)(fabsf(h) < 0x1p-12f) << v;
+            nonzero |= (uint32_t)(h != 0.f) << v;
             *reinterpret_cast<uint16_t*>(rows + v * 64 + lane * 2) = f32_to_f16_bits(h);
           }
+          // a token (column) whose 32 features here are all tiny but not all
+          // zero would lose precision to fp16's subnormal spacing
+          const uint32_t valid = nv >= 32 ? 0xffffffffu : ((1u << nv) - 1u);
+          if (__reduce_and_sync(0xffffffffu, small) & __reduce_or_sync(0xffffffffu, nonzero) & valid)
+            underflow = true;
         }
-        if (overflow) raise_status(a.status, MOE_DEV_FP16_RANGE);
+        if (overflow || underflow) raise_status(a.status, MOE_DEV_FP16_RANGE);
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.acc_empty);
@@ -568,12 +629,15 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
         // bytes, 16-byte groups swizzled by token % 8: conflict-free, one word
         // per lane) and written by one TMA store; a ragged chunk is stored
         // directly, its real tokens only.
-        float* y = reinterpret_cast<float*>(a.out) + (size_t)(ti.r0 + ti.m0) * a.out_ld + ti.n0 +
-                   eh * BW + 32 * q + lane;
+        const int col0 = ti.n0 + eh * BW + 32 * q;  // first of this warp's 32 columns
+        float* y = reinterpret_cast<float*>(a.out) + (size_t)(ti.r0 + ti.m0) * a.out_ld + col0 +
+                   lane;
 #pragma unroll 1
         for (int c = 0; c < nchunks; ++c) {
           uint32_t v[32];
           tc::ld_32x32b_x32(t_lane + eh * COL_D1 + 32 * c, v);
+          const int nv = ti.rows - 32 * c;
+          const int ax = lane < nv ? __ldg(a.xexp + ti.r0 + ti.m0 + 32 * c + lane) : 0;
           tc::wait_ld();
           if (c == nchunks - 1) {
             // this warp's reads of the accumulators are done
@@ -581,52 +645,78 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.acc_empty);
           }
-          const int nv = ti.rows - 32 * c;
-          if (a.y_half) {
-            bool overflow = false;
+          if (a.yexp) {
+            // fp16 y'' per token: the token's 32 columns here share one
+            // exponent s (y = y'' 2^s), held by lane = token.  A chunk of 32
+            // real tokens is staged (rows of 32 fp16 = 64 bytes, 16-byte
+            // groups swizzled by (token >> 1) & 3, the 64-byte TMA swizzle)
+            // and written by one TMA store; a ragged chunk is stored
+            // directly, its real tokens only.  Each value is converted and
+            // staged as soon as its token's exponent is known.
+            if (nv >= 32) {
+              tc::bulk_wait_read_all();  // the previous store has read the staging
+              __syncwarp();
+            }
+            uint16_t* yh = reinterpret_cast<uint16_t*>(a.out) + (size_t)(ti.r0 + ti.m0) * a.out_ld +
+                           col0 + lane;
+            int my_e = 0;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) overflow |= i < nv && !(fabsf(__uint_as_float(v[i])) <= kF16Max);
-            if (overflow) raise_status(a.status, MOE_DEV_FP16_RANGE);
-          }
-          if (nv >= 32) {
-            // the previous store from the staging tile has read it
-            tc::bulk_wait_read_all();
-            __syncwarp();
-            if (a.y_half) {
-              // rows of 32 fp16 (64 bytes), 16-byte groups swizzled by
-              // (token >> 1) & 3 (the 64-byte TMA swizzle)
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
+            for (int i = 0; i < 32; ++i) {
+              const uint32_t m = __reduce_max_sync(0xffffffffu, v[i] & 0x7fffffffu);
+              if (i < nv && m >= 0x7f800000u) bad = true;
+              const int E = min(exp_of_bits(m), 127);
+              if (lane == i) my_e = E;
+              const uint16_t hv = f32_to_f16_bits(__uint_as_float(v[i]) * pow2f(kGroupTop - E));
+              if (nv >= 32)
                 *reinterpret_cast<uint16_t*>(stg + i * 64 + ((((lane >> 3) ^ ((i >> 1) & 3))) << 4) +
-                                             (lane & 7) * 2) = f32_to_f16_bits(__uint_as_float(v[i]));
-            } else {
+                                             (lane & 7) * 2) = hv;
+              else if (i < nv)
+                yh[(size_t)(32 * c + i) * a.out_ld] = hv;
+            }
+            if (lane < nv)
+              a.yexp[(size_t)(col0 >> 5) * a.yexp_rows + ti.r0 + ti.m0 + 32 * c + lane] =
+                  (int16_t)(my_e - kGroupTop + p0 + 2 * ax);
+            if (nv >= 32) {
+              tc::fence_proxy_async();
+              __syncwarp();
+              if (lane == 0) {  // bulk groups are per thread: always the same lane
+                tc::tma_store_2d(&tmap_y, col0, ti.r0 + ti.m0 + 32 * c, stg);
+                tc::bulk_commit();
+              }
+              __syncwarp();
+            }
+          } else {
+            // fp32 y = D 2^(pd + pg + pu + c + 2a)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              v[i] = __float_as_uint(
+                  ldexp2f(__uint_as_float(v[i]), p0 + 2 * __shfl_sync(0xffffffffu, ax, i)));
+            if (nv >= 32) {
+              // the previous store from the staging tile has read it
+              tc::bulk_wait_read_all();
+              __syncwarp();
 #pragma unroll
               for (int i = 0; i < 32; ++i)
                 *reinterpret_cast<uint32_t*>(stg + i * 128 + (((lane >> 2) ^ (i & 7)) << 4) +
                                              (lane & 3) * 4) = v[i];
-            }
-            tc::fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) {  // bulk groups are per thread: always the same lane
-              tc::tma_store_2d(&tmap_y, ti.n0 + eh * BW + 32 * q, ti.r0 + ti.m0 + 32 * c, stg);
-              tc::bulk_commit();
-            }
-            __syncwarp();
-          } else if (a.y_half) {
-            uint16_t* yh = reinterpret_cast<uint16_t*>(a.out) + (size_t)(ti.r0 + ti.m0) * a.out_ld +
-                           ti.n0 + eh * BW + 32 * q + lane;
+              tc::fence_proxy_async();
+              __syncwarp();
+              if (lane == 0) {  // bulk groups are per thread: always the same lane
+                tc::tma_store_2d(&tmap_y, col0, ti.r0 + ti.m0 + 32 * c, stg);
+                tc::bulk_commit();
+              }
+              __syncwarp();
+            } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i < nv) yh[(size_t)(32 * c + i) * a.out_ld] = f32_to_f16_bits(__uint_as_float(v[i]));
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i < nv) y[(size_t)(32 * c + i) * a.out_ld] = __uint_as_float(v[i]);
+              for (int i = 0; i < 32; ++i)
+                if (i < nv) y[(size_t)(32 * c + i) * a.out_ld] = __uint_as_float(v[i]);
+            }
           }
         }
       }
       if (lane == 0 && q == 0 && eh == 0) reinterpret_cast<volatile int*>(sh.prog)[kWarps + 2] = tl + 1;
     }
+    if (bad && lane == 0) raise_status(a.status, MOE_DEV_NONFINITE);
     tc::bulk_wait_all();  // every bulk copy and TMA store of this warp is complete
     __syncwarp();
   }
@@ -676,25 +766,84 @@ k_tile_offsets(const int32_t* __restrict__ expert_off, int E, int32_t* __restric
     for (int i = tid; i < max_slots; i += blockDim.x) slot_done[i] = 0;
 }
 
-// Activation rows in expert order: xp[p] = x[row_token[p]] (fp16, K columns,
-// K % 8 == 0) for the routed rows p < expert_off[E]; a token index outside
-// [0, T) gives a zero row.  One warp per row, 16-byte copies.
+// Activation rows in expert order, normalised: for each routed row
+// p < expert_off[E], with t = row_token[p],
+//   xexp[p] = a = floor(log2 rms(x[t]))  (0 for an all-zero row),
+//   xp[p]   = fp16(x[t] 2^-a),
+// exact (bf16 has fewer mantissa bits than fp16; |x'| < 2 sqrt(K) <= 128,
+// and only values under 2^-14 rms lose bits).  a is computed from x[t]
+// alone, so every row of a token gets the same a.  A token index outside
+// [0, T) gives a zero row with a = 0; an infinite or NaN activation raises
+// MOE_DEV_NONFINITE.  One warp per row; K % 256 == 0, K <= 4096.
+constexpr int kGatherMaxPieces = 16;  // 16-byte pieces per lane: K <= 4096
 __global__ void __launch_bounds__(256)
 k_gather_rows(const uint16_t* __restrict__ x, int T, const int32_t* __restrict__ row_token,
               const int32_t* __restrict__ expert_off, int E, int P, int K,
-              uint16_t* __restrict__ xp) {
+              uint16_t* __restrict__ xp, int32_t* __restrict__ xexp,
+              int32_t* __restrict__ status) {
   griddep_wait();
   griddep_trigger();
   const int p = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (p >= min(P, expert_off[E])) return;
+  if (p >= min(P, expert_off[E])) return;  // warp-uniform
   const int t = row_token[p];
+  const int np = K / 256;  // 16-byte pieces per lane
   uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)p * K);
   if (t < 0 || t >= T) {
-    for (int c = lane; c < K / 8; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < np; ++i) dst[lane + 32 * i] = make_uint4(0, 0, 0, 0);
+    if (lane == 0) xexp[p] = 0;
     return;
   }
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * K);
-  for (int c = lane; c < K / 8; c += 32) dst[c] = __ldg(src + c);
+  uint4 v[kGatherMaxPieces];
+  uint32_t m = 0;  // largest bf16 magnitude bits
+#pragma unroll
+  for (int i = 0; i < kGatherMaxPieces; ++i) {
+    if (i < np) {
+      v[i] = __ldg(src + lane + 32 * i);
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) m = max(m, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+    }
+  }
+  m = __reduce_max_sync(0xffffffffu, m);
+  if (m >= 0x7F80u && lane == 0) raise_status(status, MOE_DEV_NONFINITE);
+  // sum of squares of x / 2^ea (no overflow: every term is below 4), in a
+  // fixed order; lane 0's total decides a for the whole row
+  const int ea = min(exp_of_bits(m << 16), 126);
+  const float fa = pow2f(-ea);
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < kGatherMaxPieces; ++i) {
+    if (i < np) {
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float lo = bf16_lo(w[j]) * fa, hi = bf16_hi(w[j]) * fa;
+        ss = fmaf(lo, lo, ss);
+        ss = fmaf(hi, hi, ss);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  int ae = 0;
+  if (m != 0 && m < 0x7F80u) {
+    const float rms = sqrtf(ss / (float)K);  // in [2^-6, 2]: a normal float
+    ae = min(max(ea + (int)(__float_as_uint(rms) >> 23) - 127, -126), 126);
+  }
+  ae = __shfl_sync(0xffffffffu, ae, 0);
+  const float f = pow2f(-ae);
+#pragma unroll
+  for (int i = 0; i < kGatherMaxPieces; ++i) {
+    if (i < np) {
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+      dst[lane + 32 * i] = make_uint4(pack_f16x2(bf16_lo(w[0]) * f, bf16_hi(w[0]) * f),
+                                      pack_f16x2(bf16_lo(w[1]) * f, bf16_hi(w[1]) * f),
+                                      pack_f16x2(bf16_lo(w[2]) * f, bf16_hi(w[2]) * f),
+                                      pack_f16x2(bf16_lo(w[3]) * f, bf16_hi(w[3]) * f));
+    }
+  }
+  if (lane == 0) xexp[p] = ae;
 }
 
 // ---------------------------------------------------------------------------
@@ -759,13 +908,14 @@ bool expert_gemm_tc_ok(int H, int I) {
          I <= 32 * kScaleBlock;
 }
 
-cudaError_t launch_expert_gemm_tc(const uint16_t* x16, int T, const int32_t* expert_off,
-                                  const int32_t* row_token, uint16_t* x_perm, int E, int P,
-                                  const moe_fp8_ffn& w, int H, int I, int32_t* tile_off,
-                                  int32_t* slot_done, uint16_t* hid, void* y, bool y_half,
-                                  int32_t* status, cudaStream_t s, bool pdl,
-                                  bool tile_off_ready) {
+cudaError_t launch_expert_gemm_tc(const uint16_t* x, int T, const int32_t* expert_off,
+                                  const int32_t* row_token, uint16_t* x_perm, int32_t* xexp,
+                                  int E, int P, const moe_fp8_ffn& w, int H, int I,
+                                  int32_t* tile_off, int32_t* slot_done, uint16_t* hid, void* y,
+                                  int16_t* yexp, int yexp_rows, int32_t* status, cudaStream_t s,
+                                  bool pdl, bool tile_off_ready) {
   static_assert(BT == kGemmTokenTile, "token tile of the permutation's tile prefix");
+  if (!x_perm || !xexp) return cudaErrorInvalidValue;
   cudaError_t err;
   if ((err = ensure_smem((const void*)k_expert_gemm_ws<true>, SMEM_WS)) != cudaSuccess) return err;
   if ((err = ensure_smem((const void*)k_expert_gemm_ws<false>, SMEM_WS)) != cudaSuccess) return err;
@@ -773,22 +923,21 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x16, int T, const int32_t* exp
   if ((err = code_map(&gmap, w.gate.codes, (long long)E * I, H)) != cudaSuccess) return err;
   if ((err = code_map(&umap, w.up.codes, (long long)E * I, H)) != cudaSuccess) return err;
   if ((err = code_map(&dmap, w.down.codes, (long long)E * H, I)) != cudaSuccess) return err;
-  // Activations in expert order [P, H] fp16 (gathered unless the rows are
-  // already in order) and hid [P, I] fp16: 64 columns x 128 rows per box,
-  // 128-byte swizzled (the K-major operand layout of the MMA)
-  const uint16_t* xrows = x_perm ? x_perm : x16;
-  if ((err = make_tensor_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xrows, P, H, BK, BT, 128)) !=
-      cudaSuccess)
+  // Normalised activations in expert order [P, H] fp16 and hid [P, I] fp16:
+  // 64 columns x 128 rows per box, 128-byte swizzled (the K-major operand
+  // layout of the MMA)
+  if ((err = make_tensor_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x_perm, P, H, BK, BT,
+                                128)) != cudaSuccess)
     return err;
   if ((err = make_tensor_map_2d(&hmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, hid, P, I, BK, BT, 128)) !=
       cudaSuccess)
     return err;
   // y [P, H], written by the down epilogue: 32 columns x 32 rows; fp32 rows of
   // 128 bytes (128-byte swizzle) or fp16 rows of 64 bytes (64-byte swizzle)
-  if ((err = y_half ? make_tensor_map_2d(&ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, y, P, H, 32,
-                                         32, 64)
-                    : make_tensor_map_2d(&ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, y, P, H, 32,
-                                         32, 128)) != cudaSuccess)
+  if ((err = yexp ? make_tensor_map_2d(&ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, y, P, H, 32, 32,
+                                       64)
+                  : make_tensor_map_2d(&ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, y, P, H, 32, 32,
+                                       128)) != cudaSuccess)
     return err;
   // Tile offsets first, then the gather: the GEMMs' warps other than the
   // token warp read the offsets without waiting for their previous kernel.
@@ -799,20 +948,55 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x16, int T, const int32_t* exp
                    slot_done, max_ttiles);
     if (err != cudaSuccess) return err;
   }
-  if (x_perm) {
-    err = launch_k(k_gather_rows, dim3(cdiv(P, 8)), dim3(256), 0, s, pdl, x16, T, row_token,
-                   expert_off, E, P, H, x_perm);
-    if (err != cudaSuccess) return err;
-  }
+  err = launch_k(k_gather_rows, dim3(cdiv(P, 8)), dim3(256), 0, s, pdl, x, T, row_token,
+                 expert_off, E, P, H, x_perm, xexp, status);
+  if (err != cudaSuccess) return err;
+  int log2H = 0;
+  while ((2 << log2H) <= H) ++log2H;
   const int nsm = num_sms();
   const dim3 blk(kThreadsWS);
-  GemmArgs g{expert_off, tile_off, E, H, I, w.gate.scales, w.up.scales,
-             (void*)hid, I, 0, I / BW, x_perm ? 0 : 1, slot_done, 0, status};
+  GemmArgs g{};
+  g.expert_off = expert_off;
+  g.tile_off = tile_off;
+  g.E = E;
+  g.K = H;
+  g.rows_per_expert = I;
+  g.s0 = w.gate.scales;
+  g.s1 = w.up.scales;
+  g.out = hid;
+  g.out_ld = I;
+  g.n_wblocks = I / BW;
+  g.all_wait = 0;  // the gather ran between the tile offsets and this GEMM
+  g.slot_done = slot_done;
+  g.slot_need = 0;
+  g.status = status;
+  g.xexp = xexp;
+  g.hid_shift = log2H + 4;
   err = launch_k(k_expert_gemm_ws<true>, dim3(min(nsm, max_ttiles * g.n_wblocks)), blk,
                  (size_t)SMEM_WS, s, pdl, gmap, umap, xmap, ymap, g);
   if (err != cudaSuccess) return err;
-  GemmArgs d{expert_off, tile_off, E, I, H, w.down.scales, nullptr, y, H, y_half ? 1 : 0,
-             H / (2 * BW), 0, slot_done, (I / BW) * kEpiWarps, status};
+  GemmArgs d{};
+  d.expert_off = expert_off;
+  d.tile_off = tile_off;
+  d.E = E;
+  d.K = I;
+  d.rows_per_expert = H;
+  d.s0 = w.down.scales;
+  d.s1 = nullptr;
+  d.out = y;
+  d.out_ld = H;
+  d.n_wblocks = H / (2 * BW);
+  d.all_wait = 0;
+  d.slot_done = slot_done;
+  d.slot_need = (I / BW) * kEpiWarps;
+  d.status = status;
+  d.xexp = xexp;
+  d.gs = w.gate.scales;
+  d.us = w.up.scales;
+  d.n_gu_scales = cdiv(I, kScaleBlock) * cdiv(H, kScaleBlock);
+  d.hid_shift = g.hid_shift;
+  d.yexp = yexp;
+  d.yexp_rows = yexp_rows;
   const int gu_grid = min(nsm, max_ttiles * g.n_wblocks);
   if (gu_grid == nsm && min(nsm, max_ttiles * d.n_wblocks) == nsm) {
     d.gu_grid = gu_grid;

@@ -21,11 +21,17 @@
 // 16c + 4s + {0,1} and 16c + 4s + {2,3}.  The activations use the same map,
 // so every product pairs the right weight with the right activation.
 //
-// Block scale: each 64-column chunk lies inside one 128x128 scale block, so
-// the chunk's MMA sum is multiplied by its scale in fp32 and added to an fp32
-// accumulator.  Both projections multiply fp16 activations (x16, the fp16
-// copy of x written by the router, and hid) by dec(code) decoded exactly to
-// fp16 with one cvt per pair; the scale is applied in fp32.
+// Block scale and range: each 64-column chunk lies inside one 128x128 scale
+// block, so the chunk's MMA sum is multiplied by its scale in fp32 and added
+// to an fp32 accumulator.  The activations are brought into fp16 per
+// (token, chunk) by a power of two: the bf16 activations x are scaled so the
+// largest of the token's 64 values lands in [2^14, 2^15) (exact: bf16 has
+// fewer mantissa bits than fp16) and the power of two rejoins the scale in
+// fp32.  The SwiGLU output hid is stored as fp16 with one exponent per 16
+// features of a row, the down kernel aligns a chunk's four exponents and
+// again moves the power of two into the fp32 scale.  So the expert FFN has no
+// range limit beyond fp32's: block scales, activations and weights of any
+// magnitude keep fp16's relative precision (2^-11) at every rounding.
 #include "moe_internal.h"
 
 namespace moe {
@@ -36,19 +42,22 @@ constexpr int kThreads = 256;
 // gate/up + SwiGLU.  grid (I/16, max active experts).  A CTA owns 16 rows of
 // the expert's gate and up matrices; its 8 warps split K = H into 64-column
 // chunks (warp w: chunks w, w+8, ...), kGuChunks per warp per K-group.
-// hid[r, i] = silu(g) * u in fp16 for every row r of the expert.
+// hid[r, i] = silu(g) * u for every row r of the expert, stored as fp16 hid''
+// with hid = hid'' 2^(hexp - 14), one exponent per row and 16 features (the
+// CTA's 16): hexp[r, i0 / 16].
 // ---------------------------------------------------------------------------
 constexpr int kGuChunks = 4;  // chunks per warp per K-group: H <= 2048 in one group
 constexpr size_t kGuSmem = sizeof(uint4) * kGuChunks * 4 * kThreads;  // 64 KB
 
 template <int NT>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2)
-k_gateup_stream(const uint16_t* __restrict__ x16, int H, int I,
+k_gateup_stream(const uint16_t* __restrict__ x, int H, int I,
                 const int32_t* __restrict__ expert_off, const int32_t* __restrict__ row_token,
                 const int32_t* __restrict__ active,
                 const uint8_t* __restrict__ gcodes, const float* __restrict__ gscales,
                 const uint8_t* __restrict__ ucodes, const float* __restrict__ uscales,
-                uint16_t* __restrict__ hid, int32_t* __restrict__ status) {
+                uint16_t* __restrict__ hid, int8_t* __restrict__ hexp,
+                int32_t* __restrict__ status) {
   extern __shared__ uint4 wbuf[];  // [kGuChunks * 4][kThreads]
   __shared__ float red[8][NT][2][4][32];
   __shared__ int tok[NT * 8];
@@ -68,6 +77,7 @@ k_gateup_stream(const uint16_t* __restrict__ x16, int H, int I,
   const size_t r8 = (size_t)8 * H;
   const float* gs = gscales + ((size_t)e * cdiv(I, kScaleBlock) + i0 / kScaleBlock) * nHb;
   const float* us = uscales + ((size_t)e * cdiv(I, kScaleBlock) + i0 / kScaleBlock) * nHb;
+  bool bad = false;  // an infinite or NaN input or result
   // All weight copies of one K-group (2048 columns of H).
   auto issue = [&](int kg) {
 #pragma unroll
@@ -106,7 +116,7 @@ k_gateup_stream(const uint16_t* __restrict__ x16, int H, int I,
       // 1. all weight copies of this K-group (unless already in flight)
       if (!issued) issue(kg);
       issued = false;
-      // 2. block scales and activations, straight into registers
+      // 2. block scales and activations (bf16), straight into registers
       float sg[kGuChunks], su[kGuChunks];
       uint4 xa[kGuChunks][NT][2];
 #pragma unroll
@@ -117,7 +127,7 @@ k_gateup_stream(const uint16_t* __restrict__ x16, int H, int I,
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           if (ch < nch && trow[nt] >= 0) {
-            const uint16_t* xp = x16 + (size_t)trow[nt] * H + ch * 64 + 16 * c;
+            const uint16_t* xp = x + (size_t)trow[nt] * H + ch * 64 + 16 * c;
             xa[j][nt][0] = ldg16(xp);
             xa[j][nt][1] = ldg16(xp + 8);
           } else {
@@ -125,12 +135,26 @@ k_gateup_stream(const uint16_t* __restrict__ x16, int H, int I,
           }
         }
       }
-      // 3. decode + MMA per chunk as its copies land, block scale in fp32
+      // 3. per chunk as its copies land: activations to fp16 by a power of
+      // two per token, decode + MMA, then scale and power of two in fp32
 #pragma unroll
       for (int j = 0; j < kGuChunks; ++j) {
-        const int ch = kg + warp + 8 * j;
+        const int ch = kg + warp + 8 * j;  // warp-uniform
         cp_async_wait_n(kGuChunks - 1 - j);
         if (ch < nch) {
+          if (!(fabsf(sg[j]) <= FLT_MAX) || !(fabsf(su[j]) <= FLT_MAX)) bad = true;
+          // factors of the accumulator columns (tokens 2c, 2c + 1 of 8)
+          float fg[NT][2], fu[NT][2];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const int ex = bf16x16_to_f16_norm(xa[j][nt], bad);
+            const int e0 = min(__shfl_sync(0xffffffffu, ex, 8 * c), 127) - kGroupTop;
+            const int e1 = min(__shfl_sync(0xffffffffu, ex, 8 * c + 4), 127) - kGroupTop;
+            fg[nt][0] = sg[j] * pow2f(e0);
+            fg[nt][1] = sg[j] * pow2f(e1);
+            fu[nt][0] = su[j] * pow2f(e0);
+            fu[nt][1] = su[j] * pow2f(e1);
+          }
           float pg[NT][4], pu[NT][4];
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
@@ -144,8 +168,8 @@ k_gateup_stream(const uint16_t* __restrict__ x16, int H, int I,
           for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              accg[nt][q] = fmaf(pg[nt][q], sg[j], accg[nt][q]);
-              accu[nt][q] = fmaf(pu[nt][q], su[j], accu[nt][q]);
+              accg[nt][q] = fmaf(pg[nt][q], fg[nt][q & 1], accg[nt][q]);
+              accu[nt][q] = fmaf(pu[nt][q], fu[nt][q & 1], accu[nt][q]);
             }
         }
       }
@@ -158,33 +182,45 @@ k_gateup_stream(const uint16_t* __restrict__ x16, int H, int I,
         red[warp][nt][1][q][lane] = accu[nt][q];
       }
     __syncthreads();
-    // One output (row, token) per thread: tid = nt*128 + q*32 + L.
+    // One output per thread: half-warp h = tid / 16 is token n0 + h, lane f
+    // of it feature i0 + f (accumulator element: row f = (L >> 2) + 8 (q >> 1),
+    // token 2 (L & 3) + (q & 1) of group nt).
     if (tid < NT * 128) {
-      const int nt = tid >> 7, q = (tid >> 5) & 3, L = tid & 31;
+      const int nl = tid >> 4, f = tid & 15;
+      const int nt = nl >> 3, nn = nl & 7;
+      const int q = ((f >> 3) << 1) | (nn & 1), L = ((f & 7) << 2) | (nn >> 1);
       float gv = 0.f, uv = 0.f;
 #pragma unroll
       for (int w = 0; w < 8; ++w) {
         gv += red[w][nt][0][q][L];
         uv += red[w][nt][1][q][L];
       }
-      const int row = (L >> 2) + 8 * (q >> 1);
-      const int n = n0 + nt * 8 + 2 * (L & 3) + (q & 1);
+      const int n = n0 + nl;
+      const float hv = gv / (1.f + expf(-gv)) * uv;
+      // the token's 16 features: largest magnitude over the half-warp
+      uint32_t m = __float_as_uint(hv) & 0x7fffffffu;
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+      const int E = min(exp_of_bits(m), 127);
       if (n < ne) {
-        const float hv = gv / (1.f + expf(-gv)) * uv;
-        if (!(fabsf(hv) <= kF16Max)) raise_status(status, MOE_DEV_FP16_RANGE);
-        hid[(size_t)(r0 + n) * I + i0 + row] = f32_to_f16_bits(hv);
+        if (m >= 0x7f800000u) bad = true;
+        hid[(size_t)(r0 + n) * I + i0 + f] = f32_to_f16_bits(hv * pow2f(kGroupTop - E));
+        if (f == 0) hexp[(size_t)(r0 + n) * (I / 16) + i0 / 16] = (int8_t)E;
       }
     }
     __syncthreads();
   }
+  if (bad) raise_status(status, MOE_DEV_NONFINITE);
 }
 
 // ---------------------------------------------------------------------------
 // down projection.  grid (H/32, max active experts).  A CTA owns 32 output
 // rows (two 16-row MMA tiles); warp w works on tile w & 1 and K-part w >> 1 of
 // 4 (chunks kp, kp+4, ...), kDnChunks per warp per K-group.
-// y[r, h] = sum_i hid[r, i] Wd[h, i], summed in fp32, stored in fp32 or (YH)
-// fp16 for every row r of the expert.
+// y[r, h] = sum_i hid[r, i] Wd[h, i], summed in fp32, for every row r of the
+// expert; stored in fp32, or (YH) as fp16 y'' with y = y'' 2^s and one
+// exponent s per row and 32 columns (the CTA's 32): yexp[h / 32][r], the
+// table being [H / 32][y_rows].
 // FUSE (cmb.ticket set; YH only; T <= 64, k <= 8): the last CTA of each 32-row
 // slice of h — one ticket per slice, counted up to the number of active
 // experts — also combines that slice for every token, with the combine
@@ -198,10 +234,11 @@ constexpr size_t kDnSmem = sizeof(uint4) * kDnChunks * 2 * kThreads;  // 24 KB
 
 template <int NT, bool YH, bool FUSE = false>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
-k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
+k_down_stream(const uint16_t* __restrict__ hid, const int8_t* __restrict__ hexp, int H, int I,
               const int32_t* __restrict__ expert_off, const int32_t* __restrict__ active,
               const uint8_t* __restrict__ dcodes, const float* __restrict__ dscales,
-              void* __restrict__ y, int32_t* __restrict__ status, const FusedCombine cmb) {
+              void* __restrict__ y, int16_t* __restrict__ yexp, int y_rows,
+              int32_t* __restrict__ status, const FusedCombine cmb) {
   extern __shared__ uint4 wbuf[];  // [kDnChunks * 2][kThreads]
   __shared__ float red[4][2][NT][4][32];
   __shared__ int is_last;
@@ -209,7 +246,7 @@ k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
   // completed before the previous kernel (gate/up) passed its own
   // griddep_wait; they and the weights are read before this kernel waits for
   // gate/up, so the first K-group's weights stream while gate/up finishes.
-  // Everything gate/up writes (hid) is read after the wait.
+  // Everything gate/up writes (hid and its exponents) is read after the wait.
   const int a = blockIdx.y;
   if (a >= active[0]) return;
   const int e = active[1 + a];
@@ -222,6 +259,7 @@ k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
   const uint8_t* dp = dcodes + ((size_t)e * H + h0 + g) * I + 16 * c;
   const size_t r8 = (size_t)8 * I;
   const float* ds = dscales + ((size_t)e * cdiv(H, kScaleBlock) + h0 / kScaleBlock) * nIb;
+  bool bad = false;
   // All weight copies of one K-group (768 columns of I).
   auto issue = [&](int kg) {
 #pragma unroll
@@ -257,6 +295,7 @@ k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
       issued = false;
       float sd[kDnChunks];
       uint4 xa[kDnChunks][NT][2];
+      int hx[kDnChunks][NT];
 #pragma unroll
       for (int j = 0; j < kDnChunks; ++j) {
         const int ch = kg + kp + 4 * j;
@@ -264,19 +303,31 @@ k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           if (ch < nch && valid[nt]) {
-            const uint16_t* hp = hid + (size_t)(r0 + n0 + nt * 8 + g) * I + ch * 64 + 16 * c;
+            // this thread's 16 features are exactly one exponent group
+            const size_t row = (size_t)(r0 + n0 + nt * 8 + g);
+            const uint16_t* hp = hid + row * I + ch * 64 + 16 * c;
             xa[j][nt][0] = ldg16(hp);
             xa[j][nt][1] = ldg16(hp + 8);
+            hx[j][nt] = hexp[row * (I / 16) + ch * 4 + c];
           } else {
             xa[j][nt][0] = xa[j][nt][1] = make_uint4(0, 0, 0, 0);
+            hx[j][nt] = kExpFloor;
           }
         }
       }
 #pragma unroll
       for (int j = 0; j < kDnChunks; ++j) {
-        const int ch = kg + kp + 4 * j;
+        const int ch = kg + kp + 4 * j;  // warp-uniform
         cp_async_wait_n(kDnChunks - 1 - j);
         if (ch < nch) {
+          if (!(fabsf(sd[j]) <= FLT_MAX)) bad = true;
+          float fd[NT][2];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const int m = f16x16_align(xa[j][nt], hx[j][nt]);
+            fd[nt][0] = sd[j] * pow2f(__shfl_sync(0xffffffffu, m, 8 * c) - kGroupTop);
+            fd[nt][1] = sd[j] * pow2f(__shfl_sync(0xffffffffu, m, 8 * c + 4) - kGroupTop);
+          }
           float p[NT][4];
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
@@ -287,7 +338,7 @@ k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) acc[nt][q] = fmaf(p[nt][q], sd[j], acc[nt][q]);
+            for (int q = 0; q < 4; ++q) acc[nt][q] = fmaf(p[nt][q], fd[nt][q & 1], acc[nt][q]);
         }
       }
     }
@@ -296,19 +347,25 @@ k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
 #pragma unroll
       for (int q = 0; q < 4; ++q) red[kp][mt][nt][q][lane] = acc[nt][q];
     __syncthreads();
-    // outputs: (tile, nt, q, L) -> one per thread per round
-    for (int o = tid; o < 2 * NT * 128; o += kThreads) {
-      const int t2 = o / (NT * 128), nt = (o >> 7) % NT, q = (o >> 5) & 3, L = o & 31;
+    // outputs: warp (o / 32) is token n0 + o / 32, lane f of it column
+    // 32 blockIdx.x + f (accumulator element: tile f / 16, row (L >> 2) +
+    // 8 (q >> 1) = f % 16, token 2 (L & 3) + (q & 1) of group nt)
+    for (int o = tid; o < NT * 256; o += kThreads) {
+      const int nl = o >> 5, f = o & 31;
+      const int t2 = f >> 4, row = f & 15, nt = nl >> 3, nn = nl & 7;
+      const int q = ((row >> 3) << 1) | (nn & 1), L = ((row & 7) << 2) | (nn >> 1);
       float v = 0.f;
 #pragma unroll
       for (int p = 0; p < 4; ++p) v += red[p][t2][nt][q][L];
-      const int row = (L >> 2) + 8 * (q >> 1);
-      const int n = n0 + nt * 8 + 2 * (L & 3) + (q & 1);
-      if (n < ne) {
-        const size_t at = (size_t)(r0 + n) * H + blockIdx.x * 32 + t2 * 16 + row;
+      const int n = n0 + nl;
+      if (n < ne) {  // warp-uniform
+        const size_t at = (size_t)(r0 + n) * H + blockIdx.x * 32 + f;
         if (YH) {
-          if (!(fabsf(v) <= kF16Max)) raise_status(status, MOE_DEV_FP16_RANGE);
-          static_cast<uint16_t*>(y)[at] = f32_to_f16_bits(v);
+          const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(v) & 0x7fffffffu);
+          if (m >= 0x7f800000u) bad = true;
+          const int E = min(exp_of_bits(m), 127);
+          static_cast<uint16_t*>(y)[at] = f32_to_f16_bits(v * pow2f(kGroupTop - E));
+          if (f == 0) yexp[(size_t)blockIdx.x * y_rows + r0 + n] = (int16_t)(E - kGroupTop);
         } else {
           static_cast<float*>(y)[at] = v;
         }
@@ -316,6 +373,7 @@ k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
     }
     __syncthreads();
   }
+  if (bad) raise_status(status, MOE_DEV_NONFINITE);
   if constexpr (YH && FUSE) {
     {
       const int t = tid >> 2, h = blockIdx.x * 32 + (tid & 3) * 8;
@@ -338,23 +396,32 @@ k_down_stream(const uint16_t* __restrict__ hid, int H, int I,
       }
       __syncthreads();
       if (is_last && mine) {
-        float yv[8][8], r[8];
+        // the slot rows stay packed (8 fp16 in 16 bytes) until they are used
+        uint4 yr[8];
+        int ys[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           if (row[j] >= 0) {
-            load_v_cg(static_cast<const uint16_t*>(y) + (size_t)row[j] * H + h, yv[j]);
+            yr[j] = __ldcg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(y) +
+                                                          (size_t)row[j] * H + h));
+            ys[j] = __ldcg(yexp + (size_t)blockIdx.x * y_rows + row[j]);
           } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) yv[j][i] = 0.f;
+            yr[j] = make_uint4(0, 0, 0, 0);
+            ys[j] = 0;
           }
         }
+        float r[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) r[i] = 0.f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           if (row[j] < 0) continue;
+          // w 2^s is exact, so fmaf(w 2^s, y'', r) rounds w y + r once
+          const float wf = ldexp2f(wt[j], ys[j]);
+          float yv[8];
+          unpack_f16x8(yr[j], yv);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) r[i] = fmaf(wt[j], yv[j][i], r[i]);
+          for (int i = 0; i < 8; ++i) r[i] = fmaf(wf, yv[i], r[i]);
         }
         uint32_t o4[4];
 #pragma unroll
@@ -375,13 +442,15 @@ bool fused_combine_ok(int T, int k, int H, int max_active) {
          ctas <= (long long)num_sms() * 4;
 }
 
-cudaError_t launch_expert_gemv(const uint16_t* x16, const int32_t* expert_off,
+cudaError_t launch_expert_gemv(const uint16_t* x, const int32_t* expert_off,
                                const int32_t* row_token, const int32_t* active, int max_active,
                                const moe_fp8_ffn& w, int H, int I, int tokens_per_expert_hint,
-                               uint16_t* hid, void* y, bool y_half, int32_t* status,
-                               cudaStream_t s, bool pdl, const FusedCombine& cmb) {
+                               uint16_t* hid, int8_t* hexp, void* y, int16_t* yexp, int y_rows,
+                               int32_t* status, cudaStream_t s, bool pdl,
+                               const FusedCombine& cmb) {
   if (max_active <= 0) return cudaSuccess;
-  if (cmb.ticket && !fused_combine_ok(cmb.T, cmb.k, H, max_active)) return cudaErrorInvalidValue;
+  if (cmb.ticket && (!yexp || !fused_combine_ok(cmb.T, cmb.k, H, max_active)))
+    return cudaErrorInvalidValue;
   cudaError_t e;
   const bool nt1 = tokens_per_expert_hint <= 8;
   const dim3 block(kThreads);
@@ -389,55 +458,25 @@ cudaError_t launch_expert_gemv(const uint16_t* x16, const int32_t* expert_off,
   auto down = [&](auto kern) -> cudaError_t {
     cudaError_t err = ensure_smem((const void*)kern, kDnSmem);
     if (err != cudaSuccess) return err;
-    return launch_k(kern, g2, block, kDnSmem, s, pdl, (const uint16_t*)hid, H, I, expert_off,
-                    active, w.down.codes, w.down.scales, y, status, cmb);
+    return launch_k(kern, g2, block, kDnSmem, s, pdl, (const uint16_t*)hid, (const int8_t*)hexp,
+                    H, I, expert_off, active, w.down.codes, w.down.scales, y, yexp, y_rows,
+                    status, cmb);
   };
   if (nt1) {
     if ((e = ensure_smem((const void*)k_gateup_stream<1>, kGuSmem)) != cudaSuccess) return e;
-    e = launch_k(k_gateup_stream<1>, g1, block, kGuSmem, s, pdl, x16, H, I, expert_off,
+    e = launch_k(k_gateup_stream<1>, g1, block, kGuSmem, s, pdl, x, H, I, expert_off,
                  row_token, active, w.gate.codes, w.gate.scales, w.up.codes, w.up.scales, hid,
-                 status);
+                 hexp, status);
     if (e != cudaSuccess) return e;
     if (cmb.ticket) return down(k_down_stream<1, true, true>);
-    return y_half ? down(k_down_stream<1, true>) : down(k_down_stream<1, false>);
+    return yexp ? down(k_down_stream<1, true>) : down(k_down_stream<1, false>);
   }
-  if (cmb.ticket) return down(k_down_stream<2, true, true>);
   if ((e = ensure_smem((const void*)k_gateup_stream<2>, kGuSmem)) != cudaSuccess) return e;
-  e = launch_k(k_gateup_stream<2>, g1, block, kGuSmem, s, pdl, x16, H, I, expert_off, row_token,
-               active, w.gate.codes, w.gate.scales, w.up.codes, w.up.scales, hid, status);
+  e = launch_k(k_gateup_stream<2>, g1, block, kGuSmem, s, pdl, x, H, I, expert_off, row_token,
+               active, w.gate.codes, w.gate.scales, w.up.codes, w.up.scales, hid, hexp, status);
   if (e != cudaSuccess) return e;
-  return y_half ? down(k_down_stream<2, true>) : down(k_down_stream<2, false>);
-}
-
-// x (bf16) -> x16 (fp16), flagging values beyond fp16 range; for callers of
-// the expert FFN that did not run the router here.
-__global__ void __launch_bounds__(256)
-k_x_to_f16(const uint16_t* __restrict__ x, long long n8, uint16_t* __restrict__ x16,
-           int32_t* __restrict__ status) {
-  griddep_wait();
-  griddep_trigger();
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n8) return;
-  const uint4 v = ldg16(x + 8 * i);
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t h[4];
-  bool overflow = false;
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    const float lo = bf16_lo(w[m]), hi = bf16_hi(w[m]);
-    overflow |= !(fabsf(lo) <= kF16Max) || !(fabsf(hi) <= kF16Max);
-    h[m] = (uint32_t)f32_to_f16_bits(lo) | ((uint32_t)f32_to_f16_bits(hi) << 16);
-  }
-  if (overflow) raise_status(status, MOE_DEV_FP16_RANGE);
-  *reinterpret_cast<uint4*>(x16 + 8 * i) = make_uint4(h[0], h[1], h[2], h[3]);
-}
-
-cudaError_t launch_x_to_f16(const uint16_t* x, long long n, uint16_t* x16, int32_t* status,
-                            cudaStream_t s, bool pdl) {
-  const long long n8 = n / 8;
-  if (n8 == 0) return cudaSuccess;
-  return launch_k(k_x_to_f16, dim3((unsigned)((n8 + 255) / 256)), dim3(256), 0, s, pdl, x, n8,
-                  x16, status);
+  if (cmb.ticket) return down(k_down_stream<2, true, true>);
+  return yexp ? down(k_down_stream<2, true>) : down(k_down_stream<2, false>);
 }
 
 }  // namespace moe

@@ -183,17 +183,28 @@ WsLayout ws_layout(const moe_dims& d) {
   L.row_token = take(P * 4);
   L.tok_slot_row = take(P * 4);
   L.row_pair = take(P * 4);
-  L.x16 = take(T * H * 2);
+  // hid and y rows in fp16 with power-of-two exponents: hid per 16 features
+  // (streamed GEMV), y per 32 columns, the exponent tables [H / 32][rows]
   L.hid = take(P * I * 2);
-  L.y_perm = take(P * H * 2);  // fp16 expert outputs of moe_layer_forward
+  L.hexp = take(P * (I / 16));
+  L.y_perm = take(P * H * 2);
+  L.yexp = take((H / 32) * P * 2);
   L.sh_hid = take(Is ? T * Is * 2 : 0);
+  L.sh_hexp = take(Is ? T * (Is / 16) : 0);
   L.sh_y = take(Is ? T * H * 2 : 0);
+  L.sh_yexp = take(Is ? (H / 32) * T * 2 : 0);
   L.sh_off = take(2 * 4);
   L.sh_rows = take(Is ? T * 4 : 0);
   L.sh_active = take(2 * 4);
   L.tile_off = take((E + 1) * 4);
   L.sh_tile_off = take(2 * 4);
-  L.x_perm = take(expert_gemm_tc_ok(d.H, d.I) ? P * H * 2 : 0);
+  // the tensor-core GEMM's normalised activation rows in expert order
+  const bool gemm_ok = expert_gemm_tc_ok(d.H, d.I);
+  const bool sh_gemm_ok = Is && expert_gemm_tc_ok(d.H, d.I_shared);
+  L.x_perm = take(gemm_ok ? P * H * 2 : 0);
+  L.xexp = take(gemm_ok ? P * 4 : 0);
+  L.sh_x = take(sh_gemm_ok ? T * H * 2 : 0);
+  L.sh_xexp = take(sh_gemm_ok ? T * 4 : 0);
   L.wr_planes = take(router_tc_ok(d.T, d.H, d.E) ? 3 * E * H * 2 : 0);
   L.slot_done = take(expert_gemm_slots(P, E) * 4);
   L.ticket = take(((size_t)d.H / 32) * 4);  // fused combine: one per 32 columns of H
@@ -274,8 +285,8 @@ moe_status moe_route(const uint16_t* x, const float* Wr, const float* bias, moe_
   if ((s = check_ws(d, ws, ws_bytes)) != MOE_OK) return s;
   const WsLayout L = ws_layout(d);
   CUDA_CHECK(launch_route(x, Wr, bias, d.T, d.H, d.E, d.k, at<float>(ws, L.logits),
-                          at<uint16_t>(ws, L.wr_planes), topk_idx, topk_w, nullptr,
-                          at<int32_t>(ws, L.status), (cudaStream_t)stream, true),
+                          at<uint16_t>(ws, L.wr_planes), topk_idx, topk_w, at<int32_t>(ws, L.status),
+                          (cudaStream_t)stream, true),
              "moe_route");
   return MOE_OK;
 }
@@ -320,22 +331,20 @@ moe_status moe_expert_ffn_fp8(const uint16_t* x, const int32_t* expert_off,
   cudaStream_t st = (cudaStream_t)stream;
   int32_t* active = at<int32_t>(ws, L.active);
   int32_t* status = at<int32_t>(ws, L.status);
-  uint16_t* x16 = at<uint16_t>(ws, L.x16);
   CUDA_CHECK(launch_active_from_offsets(expert_off, d.E, active, status, st, true),
-             "moe_expert_ffn_fp8");
-  CUDA_CHECK(launch_x_to_f16(x, (long long)d.T * d.H, x16, status, st, true),
              "moe_expert_ffn_fp8");
   const int P = d.T * d.k;
   if (use_expert_gemm(P, d.E, d.H, d.I))
-    CUDA_CHECK(launch_expert_gemm_tc(x16, d.T, expert_off, row_token, at<uint16_t>(ws, L.x_perm),
-                                     d.E, P, w, d.H, d.I, at<int32_t>(ws, L.tile_off),
-                                     at<int32_t>(ws, L.slot_done), at<uint16_t>(ws, L.hid), y_perm,
-                                     false, status, st, true),
+    CUDA_CHECK(launch_expert_gemm_tc(x, d.T, expert_off, row_token, at<uint16_t>(ws, L.x_perm),
+                                     at<int32_t>(ws, L.xexp), d.E, P, w, d.H, d.I,
+                                     at<int32_t>(ws, L.tile_off), at<int32_t>(ws, L.slot_done),
+                                     at<uint16_t>(ws, L.hid), y_perm, nullptr, 0, status, st,
+                                     true),
                "moe_expert_ffn_fp8");
   else
-    CUDA_CHECK(launch_expert_gemv(x16, expert_off, row_token, active, d.E < P ? d.E : P, w, d.H,
-                                  d.I, cdiv(P, d.E), at<uint16_t>(ws, L.hid), y_perm, false,
-                                  status, st, true),
+    CUDA_CHECK(launch_expert_gemv(x, expert_off, row_token, active, d.E < P ? d.E : P, w, d.H,
+                                  d.I, cdiv(P, d.E), at<uint16_t>(ws, L.hid),
+                                  at<int8_t>(ws, L.hexp), y_perm, nullptr, 0, status, st, true),
                "moe_expert_ffn_fp8");
   return MOE_OK;
 }
@@ -350,7 +359,7 @@ moe_status moe_combine(const float* y_perm, const int32_t* tok_slot_row, const f
   REQUIRE_PTR(topk_w);
   REQUIRE_OPT_PTR(shared_y);
   REQUIRE_PTR(out);
-  CUDA_CHECK(launch_combine(y_perm, false, tok_slot_row, topk_w, shared_y, d.T, d.H, d.k, out,
+  CUDA_CHECK(launch_combine(y_perm, tok_slot_row, topk_w, shared_y, d.T, d.H, d.k, out,
                             (cudaStream_t)stream, true),
              "moe_combine");
   return MOE_OK;
@@ -386,10 +395,11 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
   int32_t* row_token = at<int32_t>(ws, L.row_token);
   int32_t* tok_slot_row = at<int32_t>(ws, L.tok_slot_row);
   int32_t* active = at<int32_t>(ws, L.active);
-  uint16_t* y_perm = at<uint16_t>(ws, L.y_perm);  // fp16 inside the layer call
+  // expert outputs inside the layer call: fp16 rows, exponent per 32 columns
+  uint16_t* y_perm = at<uint16_t>(ws, L.y_perm);
+  int16_t* yexp = at<int16_t>(ws, L.yexp);
 
   int32_t* status = at<int32_t>(ws, L.status);
-  uint16_t* x16 = at<uint16_t>(ws, L.x16);
   int32_t* soff = at<int32_t>(ws, L.sh_off);
   int32_t* srows = at<int32_t>(ws, L.sh_rows);
   int32_t* sact = at<int32_t>(ws, L.sh_active);
@@ -408,7 +418,7 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
                    at<uint16_t>(ws, L.wr_planes), idx, w, off,
                    row_token, tok_slot_row, at<int32_t>(ws, L.row_pair), active,
                    has_shared ? soff : nullptr, has_shared ? srows : nullptr,
-                   has_shared ? sact : nullptr, x16,
+                   has_shared ? sact : nullptr,
                    gemm ? at<int32_t>(ws, L.tile_off) : nullptr,
                    gemm ? at<int32_t>(ws, L.slot_done)
                         : (fuse_combine ? at<int32_t>(ws, L.ticket) : nullptr),
@@ -417,7 +427,7 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
                "moe_layer_forward: route+permute");
   } else {
     CUDA_CHECK(launch_route(x, Wr, bias, d.T, d.H, d.E, d.k, at<float>(ws, L.logits),
-                            at<uint16_t>(ws, L.wr_planes), idx, w, x16, status, st, true),
+                            at<uint16_t>(ws, L.wr_planes), idx, w, status, st, true),
                "moe_layer_forward: route");
     CUDA_CHECK(launch_permute(idx, d.T, d.E, d.k, at<int32_t>(ws, L.rank),
                               at<int32_t>(ws, L.block_cnt), at<int32_t>(ws, L.block_base), off,
@@ -429,10 +439,11 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
                  "moe_layer_forward: shared");
   }
   if (gemm) {
-    CUDA_CHECK(launch_expert_gemm_tc(x16, d.T, off, row_token, at<uint16_t>(ws, L.x_perm), d.E, P,
-                                     routed, d.H, d.I, at<int32_t>(ws, L.tile_off),
-                                     at<int32_t>(ws, L.slot_done), at<uint16_t>(ws, L.hid), y_perm,
-                                     true, status, st, true, /*tile_off_ready=*/small),
+    CUDA_CHECK(launch_expert_gemm_tc(x, d.T, off, row_token, at<uint16_t>(ws, L.x_perm),
+                                     at<int32_t>(ws, L.xexp), d.E, P, routed, d.H, d.I,
+                                     at<int32_t>(ws, L.tile_off), at<int32_t>(ws, L.slot_done),
+                                     at<uint16_t>(ws, L.hid), y_perm, yexp, P, status, st, true,
+                                     /*tile_off_ready=*/small),
                "moe_layer_forward: experts");
   } else {
     FusedCombine cmb;
@@ -444,39 +455,50 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
       cmb.k = d.k;
       cmb.out = out;
     }
-    CUDA_CHECK(launch_expert_gemv(x16, off, row_token, active, d.E < P ? d.E : P, routed, d.H,
-                                  d.I, cdiv(P, d.E), at<uint16_t>(ws, L.hid), y_perm, true,
-                                  status, st, true, cmb),
+    CUDA_CHECK(launch_expert_gemv(x, off, row_token, active, d.E < P ? d.E : P, routed, d.H,
+                                  d.I, cdiv(P, d.E), at<uint16_t>(ws, L.hid),
+                                  at<int8_t>(ws, L.hexp), y_perm, yexp, P, status, st, true,
+                                  cmb),
                "moe_layer_forward: experts");
   }
   uint16_t* shared_y = nullptr;
+  int16_t* shared_yexp = nullptr;
   if (has_shared) {
     shared_y = at<uint16_t>(ws, L.sh_y);
+    shared_yexp = at<int16_t>(ws, L.sh_yexp);
     if (use_expert_gemm(d.T, 1, d.H, d.I_shared))
-      CUDA_CHECK(launch_expert_gemm_tc(x16, d.T, soff, srows, nullptr, 1, d.T, *shared, d.H,
-                                       d.I_shared,
-                                       at<int32_t>(ws, L.sh_tile_off),
+      CUDA_CHECK(launch_expert_gemm_tc(x, d.T, soff, srows, at<uint16_t>(ws, L.sh_x),
+                                       at<int32_t>(ws, L.sh_xexp), 1, d.T, *shared, d.H,
+                                       d.I_shared, at<int32_t>(ws, L.sh_tile_off),
                                        at<int32_t>(ws, L.sh_slot_done), at<uint16_t>(ws, L.sh_hid),
-                                       shared_y, true, status, st, true),
+                                       shared_y, shared_yexp, d.T, status, st, true),
                  "moe_layer_forward: shared expert");
     else
-      CUDA_CHECK(launch_expert_gemv(x16, soff, srows, sact, 1, *shared, d.H, d.I_shared, d.T,
-                                    at<uint16_t>(ws, L.sh_hid), shared_y, true, status, st, true),
+      CUDA_CHECK(launch_expert_gemv(x, soff, srows, sact, 1, *shared, d.H, d.I_shared, d.T,
+                                    at<uint16_t>(ws, L.sh_hid), at<int8_t>(ws, L.sh_hexp),
+                                    shared_y, shared_yexp, d.T, status, st, true),
                  "moe_layer_forward: shared expert");
   }
   if (!fuse_combine)
-    CUDA_CHECK(launch_combine_layer(y_perm, true, tok_slot_row, w, shared_y, d.T, d.H, d.k, out,
-                                    st),
+    CUDA_CHECK(launch_combine_layer(y_perm, yexp, P, tok_slot_row, w, shared_y, shared_yexp, d.T,
+                                    d.H, d.k, out, st),
                "moe_layer_forward: combine");
   return MOE_OK;
 }
 
 moe_status moe_read_device_status(const void* ws, int32_t* status, void* stream) {
-  REQUIRE_PTR(ws);
+  REQUIRE_OPT_PTR(ws);
   if (!status) return fail(MOE_ERR_INVALID_ARG, "status is NULL");
   cudaStream_t st = (cudaStream_t)stream;
+  const void* word = ws;
+  if (!word) {
+    // no workspace: the fixed array of moe_permute_static_scratch
+    int32_t* p = nullptr;
+    CUDA_CHECK(static_scratch_status(&p), "moe_read_device_status");
+    word = p;
+  }
   int32_t v = 0;
-  CUDA_CHECK(cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, st),
+  CUDA_CHECK(cudaMemcpyAsync(&v, word, sizeof v, cudaMemcpyDeviceToHost, st),
              "moe_read_device_status");
   CUDA_CHECK(cudaStreamSynchronize(st), "moe_read_device_status");
   *status = v;

@@ -1,6 +1,7 @@
 // Device helpers shared by the kernels of the block-FP8 MoE layer (sm_103a).
 #pragma once
 
+#include <cfloat>
 #include <cstdint>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -81,6 +82,111 @@ __device__ __forceinline__ uint16_t f32_to_f16_bits(float v) {
 }
 
 constexpr float kF16Max = 65504.f;
+
+// Two floats -> f16x2 (lo in bits 0..15), round to nearest even.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// Power-of-two range normalisation of the fp16 intermediates
+// ---------------------------------------------------------------------------
+// A group of values v is stored as fp16 v'' with v = v'' 2^(E - kGroupTop),
+// E = floor(log2) of the group's largest magnitude: that magnitude lands in
+// [2^14, 2^15), so every member within 2^-28 of it keeps fp16's full 11-bit
+// precision whatever the group's own magnitude.  Multiplying by a power of
+// two is exact, so only the one fp16 rounding remains.
+constexpr int kGroupTop = 14;
+// E is clamped below at kExpFloor (a group whose largest magnitude is under
+// 2^-100 is scaled as if it were 2^-100; its members stay representable).
+constexpr int kExpFloor = -100;
+
+// 2^n as a float for n in [-126, 127].
+__device__ __forceinline__ float pow2f(int n) { return __int_as_float((n + 127) << 23); }
+
+// v 2^n for any int n, in two exact power-of-two steps (each within fp32's
+// normal exponents): the result rounds only where it leaves fp32's normal
+// range, where it becomes subnormal, zero or infinite as v 2^n would.
+__device__ __forceinline__ float ldexp2f(float v, int n) {
+  n = min(max(n, -252), 252);
+  const int h = n / 2;
+  return v * pow2f(h) * pow2f(n - h);
+}
+
+// floor(log2 |v|) from the magnitude bits of a float, clamped to
+// [kExpFloor, 128] (128: infinity or NaN).
+__device__ __forceinline__ int exp_of_bits(uint32_t absbits) {
+  return max((int)(absbits >> 23) - 127, kExpFloor);
+}
+
+// fp16 bits of 2^d for d <= 0: subnormal below 2^-14, zero below 2^-24.
+__device__ __forceinline__ uint32_t f16_pow2_bits(int d) {
+  if (d >= -14) return (uint32_t)(d + 15) << 10;
+  if (d >= -24) return 1u << (d + 24);
+  return 0u;
+}
+
+// floor(log2) of the largest magnitude among the warp's values (magnitude
+// bits, one per lane), clamped to [-126, 126]; 0 when every value is zero or
+// fp32-subnormal.  Sets `bad` when one is infinite or NaN.  Warp-uniform; all
+// 32 lanes must call it.
+__device__ __forceinline__ int warp_max_exp(uint32_t absbits, bool& bad) {
+  const uint32_t m = __reduce_max_sync(0xffffffffu, absbits);
+  if (m >= 0x7f800000u) bad = true;
+  if (m < 0x00800000u) return 0;
+  return min(max((int)(m >> 23) - 127, -126), 126);
+}
+
+// The same over n floats at p (lane i reads p[i], p[i + 32], ...).
+__device__ __forceinline__ int warp_max_exp_of(const float* __restrict__ p, int n, int lane,
+                                               bool& bad) {
+  uint32_t m = 0;
+  for (int i = lane; i < n; i += 32) m = max(m, __float_as_uint(__ldg(p + i)) & 0x7fffffffu);
+  return warp_max_exp(m, bad);
+}
+
+// 16 bf16 activations of one token (two 16-byte registers, 8 bf16x2) turned
+// in place into f16x2 holding x 2^(kGroupTop - E), E = floor(log2) of the
+// largest magnitude over the quad of lanes 4g .. 4g + 3 that holds the
+// token's 64 columns of a chunk (the MMA's B fragment).  Returns E (the same
+// in the four lanes); sets `bad` when a value is infinite or NaN.
+__device__ __forceinline__ int bf16x16_to_f16_norm(uint4 (&v)[2], bool& bad) {
+  uint32_t w[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = max(m, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+  m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+  m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+  if (m >= 0x7F80u) bad = true;
+  const int E = exp_of_bits(m << 16);
+  const float f = pow2f(kGroupTop - min(E, 127));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = pack_f16x2(bf16_lo(w[i]) * f, bf16_hi(w[i]) * f);
+  v[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  v[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  return E;
+}
+
+// 16 fp16 values of one token (two 16-byte registers) stored as v'' with
+// v = v'' 2^(e - kGroupTop), aligned to the quad's largest e (returned):
+// lanes with a smaller e scale their values by 2^(e - max) in place (exact
+// down to fp16's subnormal range; values under 2^-24 of the quad's scale
+// vanish).
+__device__ __forceinline__ int f16x16_align(uint4 (&v)[2], int e) {
+  int m = max(e, __shfl_xor_sync(0xffffffffu, e, 1));
+  m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+  if (e != m) {
+    const uint32_t f = f16_pow2_bits(e - m) * 0x10001u;
+    uint32_t w[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(w[i]) : "r"(w[i]), "r"(f));
+    v[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    v[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+  return m;
+}
 
 // ---------------------------------------------------------------------------
 // Warp-level bf16 tensor-core MMA: D(16x8 f32) += A(16x16 bf16) B(16x8 bf16)
@@ -339,6 +445,16 @@ __device__ __forceinline__ void load_v(const float* p, float (&v)[4]) {
 }
 __device__ __forceinline__ void load_v(const uint16_t* p, float (&v)[8]) {
   const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+// 8 fp16 (one 16-byte register group) -> 8 floats.
+__device__ __forceinline__ void unpack_f16x8(const uint4& a, float (&v)[8]) {
   const uint32_t w[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {

@@ -61,27 +61,28 @@ int num_sms();
 // Workspace layout for one set of dims (byte offsets, each 256-aligned).
 struct WsLayout {
   size_t status, logits, rank, block_cnt, block_base, active, idx, w, off, row_token,
-      tok_slot_row, row_pair, x16, hid, y_perm, sh_hid, sh_y, sh_off, sh_rows, sh_active,
-      tile_off, sh_tile_off, x_perm, wr_planes, slot_done, sh_slot_done, ticket, total;
+      tok_slot_row, row_pair, hid, hexp, y_perm, yexp, sh_hid, sh_hexp, sh_y, sh_yexp, sh_off,
+      sh_rows, sh_active, tile_off, sh_tile_off, x_perm, xexp, sh_x, sh_xexp, wr_planes,
+      slot_done, sh_slot_done, ticket, total;
 };
 WsLayout ws_layout(const moe_dims& d);
 
 // All launchers enqueue on `s`; with pdl the kernels are launched with
 // programmatic stream serialisation (each begins with griddep_wait()).
 
-// Router logits (+ optional fp16 copy of x) and top-k.  `part` holds up to 8
-// K-slices of partial logits, [8][T][E] floats; `planes` is scratch for the
-// bf16 split of Wr, [3][E][H] (used from 128 tokens, router_tc_ok).
+// Router logits and top-k.  `part` holds up to 8 K-slices of partial
+// logits, [8][T][E] floats; `planes` is scratch for the bf16 split of Wr,
+// [3][E][H] (used from 128 tokens, router_tc_ok).
 cudaError_t launch_route(const uint16_t* x, const float* Wr, const float* bias, int T, int H,
                          int E, int k, float* part, uint16_t* planes, int32_t* topk_idx,
-                         float* topk_w, uint16_t* x16, int32_t* status, cudaStream_t s, bool pdl);
+                         float* topk_w, int32_t* status, cudaStream_t s, bool pdl);
 
 // Router logits on the tensor cores (route_tc.cu): T >= 128, E % 128 == 0,
 // H % 64 == 0.  Writes KS slices of partial logits (KS from route_kslices).
 bool router_tc_ok(int T, int H, int E);
 cudaError_t launch_router_logits_tc(const uint16_t* x, const float* Wr, int T, int H, int E,
-                                    int KS, float* part, uint16_t* x16, uint16_t* planes,
-                                    int32_t* status, cudaStream_t s, bool pdl);
+                                    int KS, float* part, uint16_t* planes, int32_t* status,
+                                    cudaStream_t s, bool pdl);
 
 // Token rows per tile of the tensor-core GEMM (its MMA N, at most).
 constexpr int kGemmTokenTile = 128;
@@ -97,7 +98,7 @@ cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const
                                        uint16_t* planes, int32_t* topk_idx, float* topk_w, int32_t* expert_off,
                                        int32_t* row_token, int32_t* tok_slot_row,
                                        int32_t* row_pair, int32_t* active, int32_t* sh_off,
-                                       int32_t* sh_rows, int32_t* sh_active, uint16_t* x16,
+                                       int32_t* sh_rows, int32_t* sh_active,
                                        int32_t* tile_off, int32_t* counters, int n_counters,
                                        int32_t* status, cudaStream_t s, bool pdl);
 
@@ -109,14 +110,12 @@ cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, int32_t
 cudaError_t launch_active_from_offsets(const int32_t* expert_off, int E, int32_t* active,
                                        int32_t* status, cudaStream_t s, bool pdl);
 
-// bf16 x -> fp16 x16 (n elements, a multiple of 8), flagging fp16 overflow.
-cudaError_t launch_x_to_f16(const uint16_t* x, long long n, uint16_t* x16, int32_t* status,
-                            cudaStream_t s, bool pdl);
-
 // Grouped GEMV over the experts listed in `active` (count, then ids), on the
-// fp16 activations x16; y fp32 or (y_half) fp16.  max_active bounds the list length;
-// tokens_per_expert_hint (the expected rows per expert) picks the MMA's N
-// width; any segment length is handled.
+// bf16 activations x [T, H].  hid: [P, I] fp16 scratch with hexp [P, I/16]
+// int8 exponents.  y: [P, H] fp32 when yexp is NULL, else fp16 with yexp
+// [H/32][y_rows] int16 exponents (y = y'' 2^s).  max_active bounds the list
+// length; tokens_per_expert_hint (the expected rows per expert) picks the
+// MMA's N width; any segment length is handled.
 // The combine folded into the streamed down projection (fp16 y only): the
 // last down CTA of each 32-row slice of H writes out[t, slice] for every
 // token.  ticket: H / 32 ints that are zero when the down kernel starts (the
@@ -131,11 +130,12 @@ struct FusedCombine {
   int T = 0, k = 0;
   uint16_t* out = nullptr;
 };
-cudaError_t launch_expert_gemv(const uint16_t* x16, const int32_t* expert_off,
+cudaError_t launch_expert_gemv(const uint16_t* x, const int32_t* expert_off,
                                const int32_t* row_token, const int32_t* active, int max_active,
                                const moe_fp8_ffn& w, int H, int I, int tokens_per_expert_hint,
-                               uint16_t* hid, void* y, bool y_half, int32_t* status,
-                               cudaStream_t s, bool pdl, const FusedCombine& cmb = FusedCombine{});
+                               uint16_t* hid, int8_t* hexp, void* y, int16_t* yexp, int y_rows,
+                               int32_t* status, cudaStream_t s, bool pdl,
+                               const FusedCombine& cmb = FusedCombine{});
 
 // Grouped GEMM on the tensor cores (tcgen05) for many tokens per expert:
 // gate/up + SwiGLU -> hid, then down -> y.  Needs H % 256 == 0 and
@@ -145,16 +145,17 @@ cudaError_t launch_expert_gemv(const uint16_t* x16, const int32_t* expert_off,
 // tile_off_ready: the permutation already wrote tile_off and zeroed slot_done
 // (launch_route_permute_small), so the tile-offset kernel is skipped.
 bool expert_gemm_tc_ok(int H, int I);
-// x16: [T, H] fp16.  x_perm: [P, H] fp16 scratch that receives the
-// activation rows in expert order (x16[row_token[p]]), or NULL when row_token
-// is the identity (the rows of x16 are then read in place).  y: [P, H], fp32
-// or (y_half) fp16; an fp16 value beyond range raises MOE_DEV_FP16_RANGE.
-cudaError_t launch_expert_gemm_tc(const uint16_t* x16, int T, const int32_t* expert_off,
-                                  const int32_t* row_token, uint16_t* x_perm, int E, int P,
-                                  const moe_fp8_ffn& w, int H, int I, int32_t* tile_off,
-                                  int32_t* slot_done, uint16_t* hid, void* y, bool y_half,
-                                  int32_t* status, cudaStream_t s, bool pdl,
-                                  bool tile_off_ready = false);
+// x: [T, H] bf16.  x_perm: [P, H] fp16 and xexp: [P] int32 scratch that
+// receive the activation rows in expert order, normalised by a power of two
+// (x[row_token[p]] = x_perm[p] 2^xexp[p]).  hid: [P, I] fp16 scratch.  y:
+// [P, H] fp32 when yexp is NULL, else fp16 with yexp [H/32][yexp_rows] int16
+// exponents (y = y'' 2^s).
+cudaError_t launch_expert_gemm_tc(const uint16_t* x, int T, const int32_t* expert_off,
+                                  const int32_t* row_token, uint16_t* x_perm, int32_t* xexp,
+                                  int E, int P, const moe_fp8_ffn& w, int H, int I,
+                                  int32_t* tile_off, int32_t* slot_done, uint16_t* hid, void* y,
+                                  int16_t* yexp, int yexp_rows, int32_t* status, cudaStream_t s,
+                                  bool pdl, bool tile_off_ready = false);
 // slot_done entries the GEMM uses for P routed rows over E experts.
 inline int expert_gemm_slots(int P, int E) { return (P + 127) / 128 + (E < P ? E : P); }
 
@@ -163,17 +164,23 @@ inline int expert_gemm_slots(int P, int E) { return (P + 127) / 128 + (E < P ? E
 // environment overrides it (when the GEMM supports the shapes).
 bool use_expert_gemm(int rows, int experts, int H, int I);
 
-// y_perm and shared_y (may be NULL): fp32, or fp16 when y_half.
-cudaError_t launch_combine(const void* y_perm, bool y_half, const int32_t* tok_slot_row,
-                           const float* topk_w, const void* shared_y, int T, int H, int k,
-                           uint16_t* out, cudaStream_t s, bool pdl);
-// The same inside moe_layer_forward (programmatic dependent launch): for
-// k <= 16 the slot rows and weights, which the routing wrote before any
-// expert kernel ran, are loaded before the kernel waits for the expert
-// outputs.
-cudaError_t launch_combine_layer(const void* y_perm, bool y_half, const int32_t* tok_slot_row,
-                                 const float* topk_w, const void* shared_y, int T, int H, int k,
+// fp32 y_perm and shared_y (may be NULL), the C ABI's moe_combine.
+cudaError_t launch_combine(const float* y_perm, const int32_t* tok_slot_row, const float* topk_w,
+                           const float* shared_y, int T, int H, int k, uint16_t* out,
+                           cudaStream_t s, bool pdl);
+// The same inside moe_layer_forward (programmatic dependent launch) on fp16
+// rows with power-of-two exponents: y [P, H] with yexp [H/32][P], the shared
+// rows sy [T, H] with syexp [H/32][T] (both NULL without a shared expert).
+// The slot rows and weights, which the routing wrote before any expert
+// kernel ran, are loaded before the kernel waits for the expert outputs.
+cudaError_t launch_combine_layer(const uint16_t* y, const int16_t* yexp, int P,
+                                 const int32_t* tok_slot_row, const float* topk_w,
+                                 const uint16_t* sy, const int16_t* syexp, int T, int H, int k,
                                  uint16_t* out, cudaStream_t s);
+
+// Device address of the status word of moe_permute_static_scratch's fixed
+// array on the current device.
+cudaError_t static_scratch_status(int32_t** out);
 
 // Identity permutation of T tokens onto one expert (the shared expert):
 // off = {0, T}, rows = 0..T-1, active = {1, 0}.

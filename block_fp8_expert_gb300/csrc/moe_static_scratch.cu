@@ -18,7 +18,8 @@
 //    GPU (different streams, no ordering between them) race and both results
 //    are undefined; order such calls on one stream or with events;
 //  - the array keeps the previous call's contents; the kernels overwrite every
-//    value they read except the status word, which each call clears first.
+//    value they read except the status word, which each call clears first
+//    and moe_read_device_status reads back when it is given no workspace.
 #include <mutex>
 
 #include "moe_internal.h"
@@ -69,6 +70,17 @@ cudaError_t scratch_address(void** out) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+// The fixed array's status word on the current device (read by
+// moe_read_device_status when it is given no workspace).
+cudaError_t static_scratch_status(int32_t** out) {
+  void* base = nullptr;
+  const cudaError_t e = scratch_address(&base);
+  if (e != cudaSuccess) return e;
+  *out = reinterpret_cast<int32_t*>(static_cast<char*>(base) + kOffStatus);
+  return cudaSuccess;
+}
+
 }  // namespace moe
 
 using namespace moe;

@@ -17,8 +17,6 @@ namespace moe {
 // slices of K = H and 8*NT tokens; its 4 warps take the slice's 64-column
 // chunks round-robin.  Partial sums go to part[ks][t][e]; the top-k kernels
 // add the KS slices in a fixed order (deterministic).
-// The CTAs of expert tile 0 also write x16, the fp16 copy of x that the
-// expert kernels use, and flag values beyond fp16 range.
 // ---------------------------------------------------------------------------
 constexpr int kRouteWarps = 4;
 constexpr int kMaxKSlices = 8;  // K-slices of the router logits (route_kslices)
@@ -26,8 +24,7 @@ constexpr int kMaxKSlices = 8;  // K-slices of the router logits (route_kslices)
 template <int NT>
 __global__ void __launch_bounds__(kRouteWarps * 32)
 k_router_mma(const uint16_t* __restrict__ x, const float* __restrict__ Wr, int T, int H, int E,
-             int kslice, float* __restrict__ part, uint16_t* __restrict__ x16,
-             int32_t* __restrict__ status) {
+             int kslice, float* __restrict__ part, int32_t* __restrict__ status) {
   __shared__ float red[kRouteWarps][NT][4][32];
   griddep_wait();
   griddep_trigger();
@@ -41,8 +38,6 @@ k_router_mma(const uint16_t* __restrict__ x, const float* __restrict__ Wr, int T
   const int t0 = blockIdx.z * NT * 8;
   const int kbeg = blockIdx.y * kslice, kend = min(H, kbeg + kslice);
   const int ea = e0 + g, eb = e0 + g + 8;
-  const bool write_x16 = x16 != nullptr && blockIdx.x == 0;
-  bool overflow = false;
   int trow[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) trow[nt] = (t0 + nt * 8 + g < T) ? t0 + nt * 8 + g : -1;
@@ -71,21 +66,6 @@ k_router_mma(const uint16_t* __restrict__ x, const float* __restrict__ Wr, int T
         const uint16_t* xp = x + (size_t)trow[nt] * H + kk;
         xa[nt][0] = ldg16(xp);
         xa[nt][1] = ldg16(xp + 8);
-        if (write_x16) {
-          // 16 bf16 -> 16 fp16 (round to nearest even), two 16-byte stores
-          uint32_t h[8];
-          const uint32_t v[8] = {xa[nt][0].x, xa[nt][0].y, xa[nt][0].z, xa[nt][0].w,
-                                 xa[nt][1].x, xa[nt][1].y, xa[nt][1].z, xa[nt][1].w};
-#pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            const float lo = bf16_lo(v[m]), hi = bf16_hi(v[m]);
-            overflow |= !(fabsf(lo) <= kF16Max) || !(fabsf(hi) <= kF16Max);
-            h[m] = (uint32_t)f32_to_f16_bits(lo) | ((uint32_t)f32_to_f16_bits(hi) << 16);
-          }
-          uint4* dst = reinterpret_cast<uint4*>(x16 + (size_t)trow[nt] * H + kk);
-          dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
-          dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
-        }
       } else {
         xa[nt][0] = xa[nt][1] = make_uint4(0, 0, 0, 0);
       }
@@ -118,7 +98,6 @@ k_router_mma(const uint16_t* __restrict__ x, const float* __restrict__ Wr, int T
       }
     }
   }
-  if (overflow) raise_status(status, MOE_DEV_FP16_RANGE);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -450,28 +429,28 @@ int route_kslices(int T, int H, int E) {
 }
 
 cudaError_t launch_router_logits(const uint16_t* x, const float* Wr, int T, int H, int E,
-                                 float* part, uint16_t* planes, uint16_t* x16, int32_t* status,
-                                 cudaStream_t s, bool pdl) {
+                                 float* part, uint16_t* planes, int32_t* status, cudaStream_t s,
+                                 bool pdl) {
   const int KS = route_kslices(T, H, E);
   if (router_tc_ok(T, H, E))
-    return launch_router_logits_tc(x, Wr, T, H, E, KS, part, x16, planes, status, s, pdl);
+    return launch_router_logits_tc(x, Wr, T, H, E, KS, part, planes, status, s, pdl);
   const int kslice = H / KS;
   const dim3 blk(kRouteWarps * 32);
   if (T <= 8)
     return launch_k(k_router_mma<1>, dim3(cdiv(E, 16), KS, cdiv(T, 8)), blk, 0, s, pdl, x, Wr,
-                    T, H, E, kslice, part, x16, status);
+                    T, H, E, kslice, part, status);
   if (T <= 64)
     return launch_k(k_router_mma<2>, dim3(cdiv(E, 16), KS, cdiv(T, 16)), blk, 0, s, pdl, x, Wr,
-                    T, H, E, kslice, part, x16, status);
+                    T, H, E, kslice, part, status);
   return launch_k(k_router_mma<4>, dim3(cdiv(E, 16), KS, cdiv(T, 32)), blk, 0, s, pdl, x, Wr,
-                  T, H, E, kslice, part, x16, status);
+                  T, H, E, kslice, part, status);
 }
 
 cudaError_t launch_route(const uint16_t* x, const float* Wr, const float* bias, int T, int H,
                          int E, int k, float* part, uint16_t* planes, int32_t* topk_idx,
-                         float* topk_w, uint16_t* x16, int32_t* status, cudaStream_t s, bool pdl) {
+                         float* topk_w, int32_t* status, cudaStream_t s, bool pdl) {
   if (T == 0) return cudaSuccess;
-  cudaError_t err = launch_router_logits(x, Wr, T, H, E, part, planes, x16, status, s, pdl);
+  cudaError_t err = launch_router_logits(x, Wr, T, H, E, part, planes, status, s, pdl);
   if (err != cudaSuccess) return err;
   const int KS = route_kslices(T, H, E);
   const int epl = cdiv(E, 32);
@@ -497,10 +476,10 @@ cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const
                                        int32_t* expert_off,
                                        int32_t* row_token, int32_t* tok_slot_row,
                                        int32_t* row_pair, int32_t* active, int32_t* sh_off,
-                                       int32_t* sh_rows, int32_t* sh_active, uint16_t* x16,
+                                       int32_t* sh_rows, int32_t* sh_active,
                                        int32_t* tile_off, int32_t* counters, int n_counters,
                                        int32_t* status, cudaStream_t s, bool pdl) {
-  cudaError_t err = launch_router_logits(x, Wr, T, H, E, part, planes, x16, status, s, pdl);
+  cudaError_t err = launch_router_logits(x, Wr, T, H, E, part, planes, status, s, pdl);
   if (err != cudaSuccess) return err;
   const int KS = route_kslices(T, H, E);
   const size_t smem = small_route_smem(E);

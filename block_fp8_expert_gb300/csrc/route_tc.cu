@@ -11,9 +11,7 @@
 //   warp 0      TMA: the step's x tile and its three weight tiles;
 //   warp 1      one elected thread issues tcgen05.mma (lo, mid, hi per
 //               16-wide K step) into one TMEM accumulator [128 x 128] fp32;
-//   warps 2-5   convert the step's x tile to the fp16 copy x16 that the
-//               expert kernels read (CTAs of the first expert tile), then
-//               write the slice's partial logits part[ks][t][e].
+//   warps 2-5   write the slice's partial logits part[ks][t][e].
 // The top-k kernel adds the KS slices in a fixed order (deterministic).
 #include <cuda.h>
 
@@ -96,7 +94,7 @@ k_router_split(const float* __restrict__ Wr, long long n, uint16_t* __restrict__
 
 __global__ void __launch_bounds__(kRWarps * 32, 1)
 k_router_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
-            int T, int H, int E, int kslice, float* __restrict__ part, uint16_t* __restrict__ x16,
+            int T, int H, int E, int kslice, float* __restrict__ part,
             int32_t* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ RouterShared sh;
@@ -105,14 +103,13 @@ k_router_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int t0 = blockIdx.x * RT, ks = blockIdx.y, e0 = blockIdx.z * RE;
   const int k0 = ks * kslice, nsteps = kslice / RBK;
-  const bool convert = x16 != nullptr && blockIdx.z == 0;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t smem_base = smem_u32(smem);
   if (tid == 0) {
     for (int s = 0; s < RNS; ++s) {
       mbar_init(&sh.full[s], 1);
-      mbar_init(&sh.empty[s], convert ? 5 : 1);  // MMA commit (+ 4 converter warps)
+      mbar_init(&sh.empty[s], 1);  // the MMA's commit
     }
     mbar_init(&sh.done, 1);
     sh.abort_flag = 0;
@@ -133,9 +130,6 @@ k_router_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
     for (; s < nsteps; ++s) {
       const int st = s % RNS;
       if (s >= RNS && !rwait(sh, &sh.empty[st], (uint32_t)(((s / RNS) - 1) & 1), status)) break;
-      // the converters' reads of this slot (generic proxy) are ordered
-      // before the copies that overwrite it (async proxy)
-      tc::fence_proxy_async();
       if (tc::elect_one()) {
         uint8_t* dst = smem + st * R_STAGE;
         const int kx = k0 + s * RBK;
@@ -179,42 +173,9 @@ k_router_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
     if (lane == 0 && s > 0) mbar_wait(&sh.empty[(s - 1) % RNS], (uint32_t)(((s - 1) / RNS) & 1));
     __syncwarp();
   } else {
-    // ------------------------------------------------ x16 copy, then logits
+    // ------------------------------------------------ partial logits
     const int q = warp & 3;  // TMEM lane quarter: experts e0 + 32 q + lane
-    bool ok = true;
-    if (convert) {
-      // row r = 32 (warp - 2) + lane of each x tile: 64 bf16 -> fp16
-      const int r = 32 * (warp - 2) + lane;
-      bool overflow = false;
-      for (int s = 0; s < nsteps; ++s) {
-        const int st = s % RNS;
-        if (!rwait(sh, &sh.full[st], (uint32_t)((s / RNS) & 1), status)) {
-          ok = false;
-          break;
-        }
-        if (t0 + r < T) {
-          const uint8_t* row = smem + st * R_STAGE + r * 128;
-          uint4* dst = reinterpret_cast<uint4*>(x16 + (size_t)(t0 + r) * H + k0 + s * RBK);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint4 v = *reinterpret_cast<const uint4*>(row + ((j ^ (r & 7)) << 4));
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            uint32_t h[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              const float lo = bf16_lo(w[m]), hi = bf16_hi(w[m]);
-              overflow |= !(fabsf(lo) <= kF16Max) || !(fabsf(hi) <= kF16Max);
-              h[m] = (uint32_t)f32_to_f16_bits(lo) | ((uint32_t)f32_to_f16_bits(hi) << 16);
-            }
-            dst[j] = make_uint4(h[0], h[1], h[2], h[3]);
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.empty[st]);
-      }
-      if (overflow) raise_status(status, MOE_DEV_FP16_RANGE);
-    }
-    if (ok && rwait(sh, &sh.done, 0, status)) {
+    if (rwait(sh, &sh.done, 0, status)) {
       tc::fence_after_sync();
       const uint32_t t_lane = tmem + ((uint32_t)(32 * q) << 16);
       const int e = e0 + 32 * q + lane;
@@ -248,8 +209,8 @@ bool router_tc_ok(int T, int H, int E) {
 }
 
 cudaError_t launch_router_logits_tc(const uint16_t* x, const float* Wr, int T, int H, int E,
-                                    int KS, float* part, uint16_t* x16, uint16_t* planes,
-                                    int32_t* status, cudaStream_t s, bool pdl) {
+                                    int KS, float* part, uint16_t* planes, int32_t* status,
+                                    cudaStream_t s, bool pdl) {
   cudaError_t err = ensure_smem((const void*)k_router_tc, R_SMEM);
   if (err != cudaSuccess) return err;
   CUtensorMap xmap, wmap;
@@ -267,7 +228,7 @@ cudaError_t launch_router_logits_tc(const uint16_t* x, const float* Wr, int T, i
                  status);
   if (err != cudaSuccess) return err;
   return launch_k(k_router_tc, dim3(cdiv(T, RT), KS, E / RE), dim3(kRWarps * 32), (size_t)R_SMEM,
-                  s, pdl, xmap, wmap, T, H, E, H / KS, part, x16, status);
+                  s, pdl, xmap, wmap, T, H, E, H / KS, part, status);
 }
 
 }  // namespace moe

@@ -65,7 +65,9 @@ typedef int32_t moe_status;
 /* Device status bits (moe_read_device_status). */
 #define MOE_DEV_BAD_EXPERT_INDEX 1 /* moe_permute saw idx < 0 or idx >= E   */
 #define MOE_DEV_WAIT_TIMEOUT 2     /* a kernel's bounded wait ran out       */
-#define MOE_DEV_FP16_RANGE 4       /* an intermediate exceeded fp16 range   */
+#define MOE_DEV_FP16_RANGE 4       /* an fp16 intermediate left its range   */
+#define MOE_DEV_NONFINITE 8        /* an input (x, a block scale) or an
+                                      intermediate was infinite or NaN      */
 
 /* Layer dimensions. T tokens, hidden size H, routed-expert intermediate I,
  * E routed experts, top-k, shared-expert intermediate I_shared (0 = none). */
@@ -113,7 +115,9 @@ int moe_expert_uses_gemm(moe_dims d);
 moe_status moe_workspace_bytes(moe_dims d, size_t* bytes);
 
 /*
- * Router: logits, softmax over experts, top-k with renormalisation.
+ * Router: logits, softmax over experts, top-k with renormalisation (colizig
+ * README, model table under "What this project is trying to prove": 128
+ * experts top-8, or 512 experts top-10, per MoE layer).
  *   x        bf16  [T, H]
  *   Wr       float [E, H]
  *   bias     float [E] or NULL
@@ -129,7 +133,9 @@ moe_status moe_route(const uint16_t* x, const float* Wr, const float* bias,
                      size_t ws_bytes, void* stream);
 
 /*
- * Permutation of the T*k (token, slot) pairs into expert-contiguous rows.
+ * Permutation of the T*k (token, slot) pairs into expert-contiguous rows, so
+ * that each selected expert is evaluated once over all of its tokens
+ * (colizig README, "Features": MoE per-expert evaluation).
  *   topk_idx     int32 [T, k]   in
  *   expert_off   int32 [E + 1]  out: segment e is rows [off[e], off[e+1]),
  *                               off[0] = 0, off[E] = T*k
@@ -148,16 +154,27 @@ moe_status moe_permute(const int32_t* topk_idx, moe_dims d,
 /*
  * Routed experts: for every permuted row r of expert e,
  *   y_perm[r] = (silu(x[row_token[r]] Wg_e^T) * (x[row_token[r]] Wu_e^T)) Wd_e^T
- * with W = dec(codes) * block scale.
+ * with W = dec(codes) * block scale (colizig README, "Features": block-FP8
+ * E4M3 weights dequantised inside a fused decode+FMA dot product, MoE
+ * per-expert evaluation).
  *   x          bf16  [T, H]
  *   expert_off int32 [E + 1], row_token int32 [T*k]  (from moe_permute)
  *   w          the E routed experts
  *   y_perm     float [T*k, H] out (rows past off[E] are left untouched)
  * d.T and d.k size the row space; d.I_shared is ignored.
- * Precision: gate/up products are exact (bf16 activations times decoded
- * E4M3 weights, fp32 accumulation, block scale applied in fp32); the SwiGLU
- * output hid is rounded to fp16 for the down projection.  |hid| above 65504
- * sets MOE_DEV_FP16_RANGE.  Clears the device status word first.
+ * Precision and range: the products run on fp16 operands with fp32
+ * accumulation.  Every fp16 operand and intermediate (activations, scaled
+ * weights, the SwiGLU output hid) is normalised by an exact power of two
+ * that the fp32 side undoes, so block scales and activations of any
+ * magnitude keep fp16's relative precision; the remaining roundings are
+ * one fp16 rounding of each scaled weight (tensor-core GEMM) and of hid.
+ * Flags: MOE_DEV_NONFINITE for an infinite or NaN activation, block scale
+ * or result; on the tensor-core GEMM (many rows per expert), whose hid uses
+ * a fixed power of two per expert, MOE_DEV_FP16_RANGE when a hid value
+ * exceeds fp16's range or a token's values of 32 features all fall below
+ * 2^-12 of the normalised scale (weights whose codes are far smaller or
+ * larger than their block scale suggests).  Clears the device status word
+ * first.
  */
 moe_status moe_expert_ffn_fp8(const uint16_t* x, const int32_t* expert_off,
                               const int32_t* row_token, moe_fp8_ffn w,
@@ -165,7 +182,10 @@ moe_status moe_expert_ffn_fp8(const uint16_t* x, const int32_t* expert_off,
                               size_t ws_bytes, void* stream);
 
 /*
- * Combine: out[t] = sum_j topk_w[t,j] y_perm[tok_slot_row[t*k+j]]
+ * Combine of the expert outputs back to token order, weighted by the
+ * renormalised routing weights (colizig README, model table: top-k routed
+ * experts plus, for the 512-expert family, one shared expert):
+ * out[t] = sum_j topk_w[t,j] y_perm[tok_slot_row[t*k+j]]
  *                   (+ shared_y[t] when shared_y is not NULL),
  * summed in fp32 in slot order and rounded once to bf16 (nearest-even).
  * Pairs with tok_slot_row < 0 contribute nothing.
@@ -177,8 +197,13 @@ moe_status moe_combine(const float* y_perm, const int32_t* tok_slot_row,
                        uint16_t* out, void* stream);
 
 /*
- * The whole layer: route, permute, routed experts, the shared expert when
- * d.I_shared > 0 (applied to every token with weight 1), combine.
+ * The whole layer (colizig README, model table under "What this project is
+ * trying to prove" and "Status": MoE (+shared expert) with block-FP8
+ * weights): route, permute, routed experts, the shared expert when
+ * d.I_shared > 0 (applied to every token with weight 1), combine.  The
+ * expert outputs stay in the workspace as fp16 with one power-of-two
+ * exponent per row and 32 columns, so they too have no range limit; the
+ * precision and flags are those of moe_expert_ffn_fp8.
  *   shared       NULL when d.I_shared == 0, else one expert (n = 1) with
  *                gate/up [I_shared, H] and down [H, I_shared]
  *   out          bf16 [T, H]
@@ -203,8 +228,7 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr,
  * moe_permute without a workspace, for callers that cannot allocate device
  * memory: for example a plugin whose host framework passes it only the input
  * and output buffers of each call, or a serving loop whose device memory is
- * fixed at start-up.  The pages describe no such call; it has no counterpart
- * there.
+ * fixed at start-up.  The paper has no counterpart to this call.
  *
  * Same arguments, results and determinism as moe_permute, minus ws/ws_bytes.
  * Its scratch is one array compiled into the library (about 1.3 MB, held on
@@ -220,8 +244,8 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr,
  *    the status word it uses before its kernels run; every other scratch
  *    value is written before it is read.
  *  - An expert index outside [0, E) gives its pair tok_slot_row = -1 and no
- *    row, as in moe_permute; the status bit is kept in the fixed array and is
- *    not readable through moe_read_device_status.
+ *    row, as in moe_permute, and sets MOE_DEV_BAD_EXPERT_INDEX in the fixed
+ *    array's status word: moe_read_device_status(NULL, ...) reads it.
  */
 moe_status moe_permute_static_scratch(const int32_t* topk_idx, moe_dims d,
                                       int32_t* expert_off, int32_t* row_token,
@@ -231,7 +255,13 @@ moe_status moe_permute_static_scratch(const int32_t* topk_idx, moe_dims d,
  * Copy the workspace's device status word to *status (MOE_DEV_* bits) after
  * synchronising `stream`.  Returns MOE_ERR_DEVICE_STATUS when any bit is set.
  * The word is cleared at the start of moe_route, moe_permute,
- * moe_expert_ffn_fp8 and moe_layer_forward.
+ * moe_expert_ffn_fp8 and moe_layer_forward.  With ws == NULL it reads the
+ * status word of moe_permute_static_scratch's fixed array on the current
+ * device instead (this does no allocation; on a device where that call has
+ * not run yet it looks up the array's address first).  An unfinished or
+ * invalid result is reported here rather than returned as a plausible
+ * number (colizig README, "What this project is trying to prove" and
+ * "Status": an incomplete subsystem returns an error, not a wrong number).
  */
 moe_status moe_read_device_status(const void* ws, int32_t* status,
                                   void* stream);

@@ -17,7 +17,8 @@ shared expert):
   gate/up [E, I, H] and down [E, H, I], uint8;
 * one float32 scale per 128x128 block, ~ U(0.005, 0.02), layouts
   [E, ceil(I/128), ceil(H/128)] (gate/up) and [E, ceil(H/128), ceil(I/128)]
-  (down);
+  (down); other scale distributions and a code gain can be asked for, to
+  cover the scale range of real block-FP8 checkpoints;
 * for the skewed workload, a router bias b[e] = ln q_{pi(e)} with
   q_r proportional to r^-1.2 (Zipf, s = 1.2) and pi a seeded permutation.
 
@@ -155,25 +156,42 @@ def e4m3_encode(z: np.ndarray) -> np.ndarray:
 # drawing
 # --------------------------------------------------------------------------
 
-def _draw_codes(seed: int, tag: str, e: int, rows: int, cols: int) -> np.ndarray:
+SCALE_RANGE = (0.005, 0.02)
+
+
+def _draw_codes(seed: int, tag: str, e: int, rows: int, cols: int,
+                code_gain: float = 1.0) -> np.ndarray:
     z = _rng(seed, tag, e).standard_normal((rows, cols), dtype=np.float32)
+    if code_gain != 1.0:
+        z = z * np.float32(code_gain)
     return e4m3_encode(z)
 
 
-def _draw_scales(seed: int, tag: str, E: int, rows: int, cols: int) -> np.ndarray:
+def _draw_scales(seed: int, tag: str, E: int, rows: int, cols: int,
+                 scale_range=SCALE_RANGE, scale_dist: str = "uniform") -> np.ndarray:
+    """One float32 scale per 128x128 block: U(lo, hi), or ("loguniform")
+    exp(U(ln lo, ln hi)), which mixes magnitudes across the blocks of one
+    row block."""
     shape = (E, _cdiv(rows, BLOCK), _cdiv(cols, BLOCK))
-    return _rng(seed, tag).uniform(0.005, 0.02, size=shape).astype(np.float32)
+    lo, hi = scale_range
+    rng = _rng(seed, tag)
+    if scale_dist == "uniform":
+        return rng.uniform(lo, hi, size=shape).astype(np.float32)
+    if scale_dist == "loguniform":
+        return np.exp(rng.uniform(math.log(lo), math.log(hi), size=shape)).astype(np.float32)
+    raise ValueError(f"unknown scale distribution {scale_dist!r}")
 
 
 def _draw_fp8(seed: int, tag: str, stag: str, E: int, rows: int, cols: int,
-              pool: ThreadPoolExecutor) -> Fp8Mat:
+              pool: ThreadPoolExecutor, code_gain: float = 1.0, scale_range=SCALE_RANGE,
+              scale_dist: str = "uniform") -> Fp8Mat:
     codes = np.empty((E, rows, cols), dtype=np.uint8)
 
     def one(e):
-        codes[e] = _draw_codes(seed, tag, e, rows, cols)
+        codes[e] = _draw_codes(seed, tag, e, rows, cols, code_gain)
 
     list(pool.map(one, range(E)))
-    return Fp8Mat(codes, _draw_scales(seed, stag, E, rows, cols))
+    return Fp8Mat(codes, _draw_scales(seed, stag, E, rows, cols, scale_range, scale_dist))
 
 
 def zipf_bias(E: int, s: float, seed: int) -> np.ndarray:
@@ -186,27 +204,50 @@ def zipf_bias(E: int, s: float, seed: int) -> np.ndarray:
 
 
 def make_layer(workload: str | Workload, seed: int = 0,
-               threads: Optional[int] = None) -> LayerWeights:
-    """Draw every weight of one layer of the named workload."""
+               threads: Optional[int] = None, code_gain: float = 1.0,
+               scale_range=SCALE_RANGE, scale_dist: str = "uniform") -> LayerWeights:
+    """Draw every weight of one layer of the named workload.
+
+    The defaults are the workloads' distributions.  code_gain multiplies the
+    N(0, 1) draw before it is encoded (100 gives codes spread over the whole
+    E4M3 range, as an amax-scaled checkpoint has); scale_range and scale_dist
+    choose the block scales' distribution (see _draw_scales)."""
     w = WORKLOADS[workload] if isinstance(workload, str) else workload
     H, I, E = w.H, w.I, w.E
     threads = threads or min(32, os.cpu_count() or 1)
     Wr = (_rng(seed, "wr").standard_normal((E, H), dtype=np.float32)
           * np.float32(0.02))
     bias = zipf_bias(E, w.zipf_s, seed) if w.zipf_s else None
+    kw = dict(code_gain=code_gain, scale_range=scale_range, scale_dist=scale_dist)
     with ThreadPoolExecutor(threads) as pool:
-        gate = _draw_fp8(seed, "gate", "gate_s", E, I, H, pool)
-        up = _draw_fp8(seed, "up", "up_s", E, I, H, pool)
-        down = _draw_fp8(seed, "down", "down_s", E, H, I, pool)
+        gate = _draw_fp8(seed, "gate", "gate_s", E, I, H, pool, **kw)
+        up = _draw_fp8(seed, "up", "up_s", E, I, H, pool, **kw)
+        down = _draw_fp8(seed, "down", "down_s", E, H, I, pool, **kw)
         sg = su = sd = None
         if w.I_shared:
             Is = w.I_shared
-            sg = _draw_fp8(seed, "sh_gate", "sh_gate_s", 1, Is, H, pool)
-            su = _draw_fp8(seed, "sh_up", "sh_up_s", 1, Is, H, pool)
-            sd = _draw_fp8(seed, "sh_down", "sh_down_s", 1, H, Is, pool)
+            sg = _draw_fp8(seed, "sh_gate", "sh_gate_s", 1, Is, H, pool, **kw)
+            su = _draw_fp8(seed, "sh_up", "sh_up_s", 1, Is, H, pool, **kw)
+            sd = _draw_fp8(seed, "sh_down", "sh_down_s", 1, H, Is, pool, **kw)
     return LayerWeights(H=H, I=I, E=E, k=w.k, I_shared=w.I_shared, Wr=Wr,
                         bias=bias, gate=gate, up=up, down=down,
                         shared_gate=sg, shared_up=su, shared_down=sd)
+
+
+def with_scales(layer: LayerWeights, seed: int, scale_range,
+                scale_dist: str = "uniform") -> LayerWeights:
+    """The same layer (same codes, router and bias arrays, shared not
+    copied) with every block scale redrawn from another distribution."""
+    def re(m: Optional[Fp8Mat], tag: str) -> Optional[Fp8Mat]:
+        if m is None:
+            return None
+        E, nr, nc = m.scales.shape
+        return Fp8Mat(m.codes, _draw_scales(seed, tag, E, nr * BLOCK, nc * BLOCK,
+                                            scale_range, scale_dist))
+    return dataclasses.replace(
+        layer, gate=re(layer.gate, "gate_s"), up=re(layer.up, "up_s"),
+        down=re(layer.down, "down_s"), shared_gate=re(layer.shared_gate, "sh_gate_s"),
+        shared_up=re(layer.shared_up, "sh_up_s"), shared_down=re(layer.shared_down, "sh_down_s"))
 
 
 def _bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:

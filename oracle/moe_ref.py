@@ -17,7 +17,7 @@ Sources, cited by page title and section:
   optional always-on shared expert, and a weighted combine back to token
   order.
 
-Readings where the pages are silent (each is also listed in the design doc):
+Readings where the pages are silent:
 
 R1  "E4M3" is the OCP FP8 E4M3 variant without infinities (bias 7, codes
     0x7F/0xFF are NaN, largest finite 448), the format of block-FP8
@@ -155,7 +155,9 @@ def permute(topk_idx, E: int):
 
 def silu(z) -> np.ndarray:
     z = np.asarray(z, dtype=np.float64)
-    return z / (1.0 + np.exp(-z))
+    # exp(-z) overflows to inf for z < -709; z / inf is then the limit 0
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
 
 
 def expert_ffn(xp, Wg, Wu, Wd) -> np.ndarray:

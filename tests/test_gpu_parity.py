@@ -207,22 +207,21 @@ def test_layer_forward_full_through_gemv(torch, monkeypatch, name, T):
     assert_within_tol(oracle.bf16_to_f64(bf16_bits(out)), ref["out"], f"out {name} T={T} gemv")
 
 
-SAMPLED = [("qwen3moe_prefill", 4096), ("skewed", 2048), ("skewed", 16384)]
+# Full-size batches of the tensor-core GEMM regime, every output element
+# compared (the fp64 oracle takes a few seconds per call on the host).
+LARGE = [("qwen3moe_prefill", 4096), ("skewed", 2048), ("skewed", 16384)]
 
 
-@pytest.mark.parametrize("name,T", SAMPLED)
-def test_layer_forward_sampled(torch, name, T):
+@pytest.mark.parametrize("name,T", LARGE)
+def test_layer_forward_large(torch, name, T):
     L = host_layer(name if name != "qwen3moe_prefill" else "qwen3moe_decode")
     D = dev_layer(name if name != "qwen3moe_prefill" else "qwen3moe_decode")
     xb, _ = mi.make_tokens(L, T, seed=0)
     out, idx, w = _forward(torch, D, _x(torch, xb))
-    rng = np.random.default_rng(T)
-    toks = np.unique(np.concatenate([[0, T - 1], rng.choice(T, 30, replace=False)]))
-    ref = oracle.moe_layer_sampled(xb, L, toks)
+    ref = oracle.moe_layer(xb, L, keep_intermediates=False)
     assert np.array_equal(idx.cpu().numpy(), ref["topk_idx"])
     assert_within_tol(w.cpu().numpy(), ref["topk_w"], "topk_w", rel=W_REL)
-    got = oracle.bf16_to_f64(bf16_bits(out))[toks]
-    assert_within_tol(got, ref["out_sampled"], f"out {name} T={T} (sampled)")
+    assert_within_tol(oracle.bf16_to_f64(bf16_bits(out)), ref["out"], f"out {name} T={T}")
 
 
 def test_layer_forward_is_deterministic(torch):
@@ -304,24 +303,3 @@ def test_identity_expert_closed_form(torch):
     expect = c ** 3 * x ** 2 / (1 + np.exp(-c * x))
     assert idx.cpu().numpy().ravel().tolist() == [0] * 5
     assert_within_tol(oracle.bf16_to_f64(bf16_bits(out)), expect, "identity expert")
-
-
-def test_fp16_range_is_flagged(torch):
-    """A SwiGLU output beyond fp16 range raises MOE_DEV_FP16_RANGE instead of
-    passing silently."""
-    import block_fp8_expert_gb300 as m
-    from block_fp8_expert_gb300.device import DeviceLayer
-    L = mi.make_layer("tiny", seed=6)
-    L.gate.scales[:] = 300.0
-    L.up.scales[:] = 300.0
-    D = DeviceLayer.from_host(L)
-    xb, _ = mi.make_tokens(L, 4, seed=6)
-    ws = D.workspace(4)
-    D.forward(_x(torch, xb), ws=ws)
-    with pytest.raises(m.MoeError) as ei:
-        m.moe_read_device_status(ws)
-    assert "0x4" in str(ei.value)
-    # the next normal call clears the word
-    D2 = dev_layer("tiny")
-    D2.forward(_x(torch, xb), ws=ws)
-    assert m.moe_read_device_status(ws) == 0

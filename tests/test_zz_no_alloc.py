@@ -62,3 +62,32 @@ def test_static_scratch_permute_refuses_sizes_beyond_its_limit():
         assert st == _lib.MOE_ERR_UNSUPPORTED
         assert b"use moe_permute" in L.moe_last_error_message() or b"E <= 512" in \
             L.moe_last_error_message()
+
+
+def test_static_scratch_bad_index_is_readable():
+    """An expert index outside [0, E) gives its pair no row, as moe_permute
+    does, and its status bit in the fixed array is read back through
+    moe_read_device_status with no workspace; a clean call clears it."""
+    torch = require_gpu()
+    from block_fp8_expert_gb300 import _lib
+    L = _lib.lib()
+    T, E, k = 4, 16, 2
+    d = _lib.dims(T, 256, 128, E, k)
+    off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    rt = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    tsr = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    for idx, expect in (([[0, 1], [2, 16], [-1, 3], [4, 5]], _lib.MOE_DEV_BAD_EXPERT_INDEX),
+                        ([[0, 1], [2, 3], [4, 5], [6, 7]], 0)):
+        ti = torch.tensor(idx, dtype=torch.int32, device="cuda")
+        st = L.moe_permute_static_scratch(ti.data_ptr(), d, off.data_ptr(), rt.data_ptr(),
+                                          tsr.data_ptr(), stream)
+        assert st == _lib.MOE_OK, L.moe_last_error_message()
+        v = ctypes.c_int32(-1)
+        st = L.moe_read_device_status(None, ctypes.byref(v), stream)
+        assert v.value == expect
+        assert st == (_lib.MOE_ERR_DEVICE_STATUS if expect else _lib.MOE_OK)
+        if expect:
+            t = tsr.cpu().numpy()
+            assert t[3] == -1 and t[4] == -1
+            assert off.cpu().numpy()[-1] == 6
