@@ -1,16 +1,22 @@
 """Benchmark of the block-FP8 MoE FFN layer on GB300.
 
-One step = one full layer forward (router, softmax/top-k, permutation,
-gate/up + SwiGLU, down projection, combine) over one batch of synthetic tokens,
-replayed from a CUDA graph.  The headline workload is the Qwen3-MoE-shaped
-decode layer (hidden 2048, expert intermediate 768, 128 experts, top-8,
-block-FP8 E4M3 weights with 128x128 fp32 scales) at a batch of 64 tokens.
+One pass = one full layer forward (router, softmax/top-k, permutation,
+gate/up + SwiGLU, down projection, combine) over one batch of synthetic tokens;
+one step = M passes replayed from a CUDA graph (below).  The headline workload
+is the Qwen3-MoE-shaped decode layer (hidden 2048, expert intermediate 768,
+128 experts, top-8, block-FP8 E4M3 weights with 128x128 fp32 scales) at a
+batch of 64 tokens.
 
-Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the
-launching stream; L2 is flushed (a 512 MiB write) before every timed step,
-outside the events.  Max over ranks; under torchrun each rank runs its own
-replica of the layer on its own tokens (weak scaling, no collective in the
-data path).
+Timing: each step replays one CUDA graph of M layer passes (each pass the
+whole hot path over the batch) that rotate over R device copies of the layer,
+R chosen so that R copies span at least 4x the L2 (a pass never finds the
+previous passes' weights in L2, as when stepping through a model's layers);
+M is chosen so the K timed steps last about 1.5 s, long enough for the
+nvidia-smi clock samples taken meanwhile.  W warm-up steps, then K steps, each
+bracketed by CUDA events on the launching stream; L2 is also flushed (a
+512 MiB write) before every step, outside the events.  Max over ranks; under
+torchrun each rank runs its own replica of the layer on its own tokens (weak
+scaling, no collective in the data path).
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
 on a bounded token sample instead.
@@ -269,6 +275,64 @@ class LayerRun:
         return self.ws[:24].view(self.torch.int32).cpu().numpy()[:6].tolist()
 
 
+class PassGraph:
+    """M layer passes rotating over R device copies of one layer, captured as
+    one CUDA graph (one replay = one timed step).  The copies hold the same
+    weights at different addresses, so a pass reads its weights from HBM
+    whenever R copies exceed the L2."""
+
+    def __init__(self, torch, D, host, x_bits, R, M):
+        from block_fp8_expert_gb300 import _lib
+        from block_fp8_expert_gb300.device import DeviceLayer
+        self.torch = torch
+        self.R, self.M = R, M
+        self.runs = [LayerRun(torch, D, x_bits, graph=False)]
+        for _ in range(R - 1):
+            self.runs.append(LayerRun(torch, DeviceLayer.from_host(host), x_bits, graph=False))
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for r in self.runs:
+                r.fwd()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        n0 = _lib.kernel_launches()
+        with torch.cuda.graph(self.graph):
+            for p in range(M):
+                self.runs[p % R].fwd()
+        torch.cuda.synchronize()
+        self.launches_per_pass = (_lib.kernel_launches() - n0) / M
+
+    def step(self):
+        self.graph.replay()
+
+    def device_status(self):
+        return max((r.device_status() for r in self.runs), key=lambda v: v[0] != 0)
+
+
+def copies_for_l2(torch, bytes_per_pass, most=64):
+    """Device copies of a layer so that a rotation over them touches at least
+    4x the L2 between two visits of the same copy (at least 2, at most
+    `most`: a layer of under 4x L2 / most bytes stays partly L2-resident)."""
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    return min(most, max(2, -(-4 * l2 // max(1, bytes_per_pass))))
+
+
+def single_pass_time(torch, run, flush, n=5):
+    """Mean time of one graph-replayed pass (L2 flushed before each)."""
+    return sum(time_steps(torch, run.step, n, 3, flush)) / n
+
+
+def passes_per_step(t_pass, steps, R, target_s, max_passes=4096):
+    """M, a multiple of R, so that `steps` steps of M passes last about
+    target_s."""
+    m = int(target_s / max(steps * t_pass, 1e-9))
+    m = max(R, min(max_passes, m))
+    return -(-m // R) * R
+
+
 def aggregate(t_rank: float, world: int, tokens_per_rank: int, steps: int, dist=None,
               device=None):
     """Whole-job throughput from each rank's summed step time: the slowest
@@ -338,7 +402,10 @@ def phase_times(torch, D, run, steps, flush):
     return {k: sum(v) / len(v) for k, v in res.items()}
 
 
-def measure_workload(torch, name, T, steps, warmup, flush, pk, dev_cache, seed=0):
+def measure_workload(torch, name, T, steps, warmup, flush, pk, dev_cache, seed=0,
+                     target_s=0.4):
+    """One sweep entry: `steps` steps of M passes over rotating copies (about
+    target_s of timed work), with its own clock record."""
     from block_fp8_expert_gb300.device import DeviceLayer
     w = mi.WORKLOADS[name]
     key = (w.H, w.I, w.E, w.k, w.I_shared, w.zipf_s)
@@ -350,18 +417,28 @@ def measure_workload(torch, name, T, steps, warmup, flush, pk, dev_cache, seed=0
     host, D = dev_cache[key]
     x_bits, _ = mi.make_tokens(host, T, seed=seed)
     run = LayerRun(torch, D, x_bits)
-    times = time_steps(torch, run.step, steps, warmup, flush)
-    t = sum(times) / len(times)
     Dn = run.distinct_experts()
     B, F, _ = algorithmic(w, T, Dn)
+    R = copies_for_l2(torch, B)
+    M = passes_per_step(single_pass_time(torch, run, flush), steps, R, target_s)
+    pg = PassGraph(torch, D, host, x_bits, R, M)
+    for _ in range(warmup):
+        pg.step()
+    torch.cuda.synchronize()
+    with Clocks(torch.cuda.current_device()) as clk:
+        times = time_steps(torch, pg.step, steps, 0, flush)
+    t = sum(times) / (len(times) * M)  # per pass
     t_hbm = B / (pk["hbm_gbs"] * 1e9)
     t_tc = F / (pk["bf16_tflops"] * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
+    ck = clk.summary()
     res = {"workload": f"{name}_T{T}", "T": T, "ms": t * 1e3, "tokens_per_s": T / t,
-           "ms_max": max(times) * 1e3, "device_status": run.device_status(),
-           "distinct_experts": Dn, "bytes": B, "flops": F,
-           "hbm_gbs": B / t / 1e9, "tflops": F / t / 1e12, "bound": bound,
-           "roofline_frac": max(t_hbm, t_tc) / t}
+           "passes": len(times) * M, "layer_copies": R,
+           "device_status": pg.device_status(), "distinct_experts": Dn, "bytes": B,
+           "flops": F, "hbm_gbs": B / t / 1e9, "tflops": F / t / 1e12, "bound": bound,
+           "roofline_frac": max(t_hbm, t_tc) / t, "clocks": ck,
+           "kcycles": t * ck["sm_mhz"] * 1e3 if ck["sm_mhz"] else None}
+    del pg
     return res, run, D, host
 
 
@@ -396,21 +473,34 @@ def run_gpu(args):
     dev_cache[(w.H, w.I, w.E, w.k, w.I_shared, w.zipf_s)] = (host, D)
     x_bits, _ = mi.make_tokens(host, T, seed=rank)
     run = LayerRun(torch, D, x_bits)
+    Dn = run.distinct_experts()
+    B, F, expert_B = algorithmic(w, T, Dn)
+    # M passes per step over R rotating copies: the K steps last ~1.5 s
+    R = copies_for_l2(torch, B)
+    M = passes_per_step(single_pass_time(torch, run, flush), args.steps, R, 1.5)
+    if dist:  # every rank runs the same number of passes
+        import torch.distributed as _d
+        mt = torch.tensor([M], dtype=torch.int64, device="cuda")
+        _d.all_reduce(mt, op=_d.ReduceOp.MAX)
+        M = -(-int(mt.item()) // R) * R
+    pg = PassGraph(torch, D, host, x_bits, R, M)
     for _ in range(args.warmup):
-        run.step()
+        pg.step()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     with Clocks(local) as clk:
-        times = time_steps(torch, run.step, args.steps, 0, flush)
+        times = time_steps(torch, pg.step, args.steps, 0, flush)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    value, t_all = aggregate(sum(times), world, T, args.steps, dist, "cuda")
+    value, t_all = aggregate(sum(times), world, T * M, args.steps, dist, "cuda")
     ms_per_step = t_all / args.steps * 1e3
-    Dn = run.distinct_experts()
-    B, F, expert_B = algorithmic(w, T, Dn)
+    ms_per_pass = ms_per_step / M
+    headline_status = pg.device_status()
+    launches_per_pass = pg.launches_per_pass
+    del pg
 
     # phase table and the dominant unit's roofline: the expert FFN call, on
     # whichever path the library takes for this workload
@@ -459,8 +549,8 @@ def run_gpu(args):
     e2e_t = sum(e2e_times) / len(e2e_times)
 
     # this library's kernels per layer call, counted by the library itself
-    # while the call was captured into the replayed graph
-    launches_per_step = run.launches
+    # while the passes were captured into the replayed graph
+    launches_per_step = int(round(launches_per_pass * M))
 
     sweep = []
     if not args.no_sweep and rank == 0:
@@ -470,7 +560,8 @@ def run_gpu(args):
                 ("tiny", 8)]
         for nm, tt_ in plan:
             try:
-                r, *_ = measure_workload(torch, nm, tt_, args.sweep_steps, 3, flush, pk, dev_cache)
+                r, *_ = measure_workload(torch, nm, tt_, args.sweep_steps, 3, flush, pk,
+                                         dev_cache)
                 sweep.append(r)
             except Exception as ex:  # report, do not hide
                 sweep.append({"workload": f"{nm}_T{tt_}", "error": repr(ex)[:200]})
@@ -484,27 +575,36 @@ def run_gpu(args):
                          "fp64 NumPy oracle"}
 
     if rank == 0:
+        ck = clk.summary()
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic",
+            "dtype": "bf16 activations in and out, E4M3 weights; fp16 MMA operands, "
+                     "fp32 accumulation",
+            "data": "synthetic",
             "config": {"workload": f"{name}_T{T}", "H": w.H, "I": w.I, "E": w.E, "k": w.k,
                        "T": T, "weights": "E4M3 codes + fp32 scale per 128x128 block",
-                       "distinct_experts": Dn, "l2": "flushed before every timed step "
-                       "(512 MiB write)", "graph": "CUDA graph replay per step",
+                       "distinct_experts": Dn,
+                       "passes_per_step": M, "layer_copies": R,
+                       "l2": f"each step replays {M} layer passes rotating over {R} device "
+                             f"copies of the layer (>= 4x L2 apart); L2 also flushed before "
+                             f"every step (512 MiB write)",
+                       "graph": "one CUDA graph replay per step",
                        "parallelism": f"replicas{world}"},
-            "layer_roofline": {"bytes": B, "flops": F, "achieved_gbs": B / (t_all / args.steps) / 1e9,
-                               "frac_hbm": B / (t_all / args.steps) / 1e9 / pk["hbm_gbs"]},
+            "ms_per_pass": ms_per_pass,
+            "kcycles_per_pass": ms_per_pass * ck["sm_mhz"] if ck["sm_mhz"] else None,
+            "layer_roofline": {"bytes": B, "flops": F, "achieved_gbs": B / (ms_per_pass * 1e-3) / 1e9,
+                               "frac_hbm": B / (ms_per_pass * 1e-3) / 1e9 / pk["hbm_gbs"]},
             "roofline": roof,
             "phases_us": {k: v * 1e6 for k, v in ph.items()},
             "cpu_baseline": cpu,
             "e2e": {"value": world * T / e2e_t, "unit": "tokens/s",
                     "h2d_bytes_per_step": T * w.H * 2, "d2h_bytes_per_step": T * w.H * 2},
             "gpu_launches": launches_per_step * args.steps,
-            "device_status": run.device_status(),
+            "device_status": headline_status,
             "ms_step_max": max(times) * 1e3,
-            "clocks": clk.summary(),
+            "clocks": ck,
             "sweep": sweep,
         }
         print(json.dumps(line), flush=True)

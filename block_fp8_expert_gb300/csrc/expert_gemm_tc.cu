@@ -623,21 +623,22 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
           }
         }
       } else {
-        // Chunk c of block eh: features n0 + 128 eh + 32 q .. + 31 (this
-        // warp's lanes) x tokens 32 c .. 32 c + 31 (the chunk's columns).  A
-        // chunk of 32 real tokens is staged token-major (row = token, 128
-        // bytes, 16-byte groups swizzled by token % 8: conflict-free, one word
-        // per lane) and written by one TMA store; a ragged chunk is stored
-        // directly, its real tokens only.
+        // Chunk c of block eh: features col0 .. col0 + 31 (this warp's
+        // lanes) x tokens 32 c .. 32 c + 31 (the chunk's columns).  The chunk
+        // is staged in fp32 token-major (row = token, 128 bytes, 16-byte
+        // groups swizzled by token % 8: conflict-free both ways), then lane r
+        // reads back token 32 c + r's 32 values, so the token's power of two
+        // and the group exponent of its 32 values are lane-local.  A chunk of
+        // 32 real tokens leaves by one TMA store from the staging tile; a
+        // ragged chunk's real rows by plain stores.
         const int col0 = ti.n0 + eh * BW + 32 * q;  // first of this warp's 32 columns
-        float* y = reinterpret_cast<float*>(a.out) + (size_t)(ti.r0 + ti.m0) * a.out_ld + col0 +
-                   lane;
 #pragma unroll 1
         for (int c = 0; c < nchunks; ++c) {
           uint32_t v[32];
           tc::ld_32x32b_x32(t_lane + eh * COL_D1 + 32 * c, v);
           const int nv = ti.rows - 32 * c;
-          const int ax = lane < nv ? __ldg(a.xexp + ti.r0 + ti.m0 + 32 * c + lane) : 0;
+          const size_t row = (size_t)(ti.r0 + ti.m0 + 32 * c + lane);  // this lane's token row
+          const int ax = lane < nv ? __ldg(a.xexp + row) : 0;
           tc::wait_ld();
           if (c == nchunks - 1) {
             // this warp's reads of the accumulators are done
@@ -645,37 +646,50 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.acc_empty);
           }
-          if (a.yexp) {
-            // fp16 y'' per token: the token's 32 columns here share one
-            // exponent s (y = y'' 2^s), held by lane = token.  A chunk of 32
-            // real tokens is staged (rows of 32 fp16 = 64 bytes, 16-byte
-            // groups swizzled by (token >> 1) & 3, the 64-byte TMA swizzle)
-            // and written by one TMA store; a ragged chunk is stored
-            // directly, its real tokens only.  Each value is converted and
-            // staged as soon as its token's exponent is known.
-            if (nv >= 32) {
-              tc::bulk_wait_read_all();  // the previous store has read the staging
-              __syncwarp();
-            }
-            uint16_t* yh = reinterpret_cast<uint16_t*>(a.out) + (size_t)(ti.r0 + ti.m0) * a.out_ld +
-                           col0 + lane;
-            int my_e = 0;
+          // the previous store from the staging tile has read it
+          tc::bulk_wait_read_all();
+          __syncwarp();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const uint32_t m = __reduce_max_sync(0xffffffffu, v[i] & 0x7fffffffu);
-              if (i < nv && m >= 0x7f800000u) bad = true;
-              const int E = min(exp_of_bits(m), 127);
-              if (lane == i) my_e = E;
-              const uint16_t hv = f32_to_f16_bits(__uint_as_float(v[i]) * pow2f(kGroupTop - E));
-              if (nv >= 32)
-                *reinterpret_cast<uint16_t*>(stg + i * 64 + ((((lane >> 3) ^ ((i >> 1) & 3))) << 4) +
-                                             (lane & 7) * 2) = hv;
-              else if (i < nv)
-                yh[(size_t)(32 * c + i) * a.out_ld] = hv;
-            }
+          for (int i = 0; i < 32; ++i)
+            *reinterpret_cast<uint32_t*>(stg + i * 128 + (((lane >> 2) ^ (i & 7)) << 4) +
+                                         (lane & 3) * 4) = v[i];
+          __syncwarp();
+          float f[32];  // token 32 c + lane: its features col0 .. col0 + 31
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 g = *reinterpret_cast<const float4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4));
+            f[4 * j] = g.x;
+            f[4 * j + 1] = g.y;
+            f[4 * j + 2] = g.z;
+            f[4 * j + 3] = g.w;
+          }
+          __syncwarp();  // every lane has read its row before the tile is reused
+          if (a.yexp) {
+            // fp16 y'' with y = y'' 2^s, s per token and 32 columns
+            uint32_t m = 0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) m = max(m, __float_as_uint(f[i]) & 0x7fffffffu);
+            if (lane < nv && m >= 0x7f800000u) bad = true;
+            const int E = min(exp_of_bits(m), 127);
+            const float sc = pow2f(kGroupTop - E);
             if (lane < nv)
-              a.yexp[(size_t)(col0 >> 5) * a.yexp_rows + ti.r0 + ti.m0 + 32 * c + lane] =
-                  (int16_t)(my_e - kGroupTop + p0 + 2 * ax);
+              a.yexp[(size_t)(col0 >> 5) * a.yexp_rows + row] = (int16_t)(E - kGroupTop + p0 + 2 * ax);
+            // row r of 32 fp16 (64 bytes): into the staging tile at r * 64,
+            // 16-byte groups swizzled by (r >> 1) & 3 (the 64-byte TMA
+            // swizzle), or straight to its row when the chunk is ragged
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) +
+                                                  row * a.out_ld + col0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint4 w4 = make_uint4(pack_f16x2(f[8 * j] * sc, f[8 * j + 1] * sc),
+                                          pack_f16x2(f[8 * j + 2] * sc, f[8 * j + 3] * sc),
+                                          pack_f16x2(f[8 * j + 4] * sc, f[8 * j + 5] * sc),
+                                          pack_f16x2(f[8 * j + 6] * sc, f[8 * j + 7] * sc));
+              if (nv >= 32)
+                *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = w4;
+              else if (lane < nv)
+                dst[j] = w4;
+            }
             if (nv >= 32) {
               tc::fence_proxy_async();
               __syncwarp();
@@ -686,30 +700,28 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
               __syncwarp();
             }
           } else {
-            // fp32 y = D 2^(pd + pg + pu + c + 2a)
+            // fp32 y = D 2^(pd + pg + pu + c + 2a), in two exact steps
+            const int n = min(max(p0 + 2 * ax, -252), 252), h1 = n / 2;
+            const float s1 = pow2f(h1), s2 = pow2f(n - h1);
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) +
+                                                    row * a.out_ld + col0);
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              v[i] = __float_as_uint(
-                  ldexp2f(__uint_as_float(v[i]), p0 + 2 * __shfl_sync(0xffffffffu, ax, i)));
+            for (int j = 0; j < 8; ++j) {
+              const float4 w4 = make_float4(f[4 * j] * s1 * s2, f[4 * j + 1] * s1 * s2,
+                                            f[4 * j + 2] * s1 * s2, f[4 * j + 3] * s1 * s2);
+              if (nv >= 32)
+                *reinterpret_cast<float4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) = w4;
+              else if (lane < nv)
+                dst[j] = w4;
+            }
             if (nv >= 32) {
-              // the previous store from the staging tile has read it
-              tc::bulk_wait_read_all();
-              __syncwarp();
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                *reinterpret_cast<uint32_t*>(stg + i * 128 + (((lane >> 2) ^ (i & 7)) << 4) +
-                                             (lane & 3) * 4) = v[i];
               tc::fence_proxy_async();
               __syncwarp();
-              if (lane == 0) {  // bulk groups are per thread: always the same lane
+              if (lane == 0) {
                 tc::tma_store_2d(&tmap_y, col0, ti.r0 + ti.m0 + 32 * c, stg);
                 tc::bulk_commit();
               }
               __syncwarp();
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (i < nv) y[(size_t)(32 * c + i) * a.out_ld] = __uint_as_float(v[i]);
             }
           }
         }
@@ -766,35 +778,22 @@ k_tile_offsets(const int32_t* __restrict__ expert_off, int E, int32_t* __restric
     for (int i = tid; i < max_slots; i += blockDim.x) slot_done[i] = 0;
 }
 
-// Activation rows in expert order, normalised: for each routed row
-// p < expert_off[E], with t = row_token[p],
-//   xexp[p] = a = floor(log2 rms(x[t]))  (0 for an all-zero row),
-//   xp[p]   = fp16(x[t] 2^-a),
+// Activation rows normalised for the GEMM: a row of x becomes
+//   a  = floor(log2 rms(x[t]))  (0 for an all-zero row),
+//   x' = fp16(x[t] 2^-a),
 // exact (bf16 has fewer mantissa bits than fp16; |x'| < 2 sqrt(K) <= 128,
-// and only values under 2^-14 rms lose bits).  a is computed from x[t]
-// alone, so every row of a token gets the same a.  A token index outside
-// [0, T) gives a zero row with a = 0; an infinite or NaN activation raises
-// MOE_DEV_NONFINITE.  One warp per row; K % 256 == 0, K <= 4096.
-constexpr int kGatherMaxPieces = 16;  // 16-byte pieces per lane: K <= 4096
-__global__ void __launch_bounds__(256)
-k_gather_rows(const uint16_t* __restrict__ x, int T, const int32_t* __restrict__ row_token,
-              const int32_t* __restrict__ expert_off, int E, int P, int K,
-              uint16_t* __restrict__ xp, int32_t* __restrict__ xexp,
-              int32_t* __restrict__ status) {
-  griddep_wait();
-  griddep_trigger();
-  const int p = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (p >= min(P, expert_off[E])) return;  // warp-uniform
-  const int t = row_token[p];
-  const int np = K / 256;  // 16-byte pieces per lane
-  uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)p * K);
-  if (t < 0 || t >= T) {
-    for (int i = 0; i < np; ++i) dst[lane + 32 * i] = make_uint4(0, 0, 0, 0);
-    if (lane == 0) xexp[p] = 0;
-    return;
-  }
+// and only values under 2^-14 rms lose bits).  a depends on x[t] alone, so
+// every copy of a token's row gets the same a.  An infinite or NaN activation
+// raises MOE_DEV_NONFINITE.  K % 256 == 0, K <= 4096: one warp holds a row in
+// registers, kGatherMaxPieces 16-byte pieces per lane at most.
+constexpr int kGatherMaxPieces = 16;
+
+// One warp: x[t] -> v (fp16 x', in place) and returns a (warp-uniform).
+__device__ __forceinline__ int normalise_row(const uint16_t* __restrict__ x, int t, int K, int lane,
+                                             uint4 (&v)[kGatherMaxPieces],
+                                             int32_t* __restrict__ status) {
+  const int np = K / 256;
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * K);
-  uint4 v[kGatherMaxPieces];
   uint32_t m = 0;  // largest bf16 magnitude bits
 #pragma unroll
   for (int i = 0; i < kGatherMaxPieces; ++i) {
@@ -837,13 +836,75 @@ k_gather_rows(const uint16_t* __restrict__ x, int T, const int32_t* __restrict__
   for (int i = 0; i < kGatherMaxPieces; ++i) {
     if (i < np) {
       const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-      dst[lane + 32 * i] = make_uint4(pack_f16x2(bf16_lo(w[0]) * f, bf16_hi(w[0]) * f),
-                                      pack_f16x2(bf16_lo(w[1]) * f, bf16_hi(w[1]) * f),
-                                      pack_f16x2(bf16_lo(w[2]) * f, bf16_hi(w[2]) * f),
-                                      pack_f16x2(bf16_lo(w[3]) * f, bf16_hi(w[3]) * f));
+      v[i] = make_uint4(pack_f16x2(bf16_lo(w[0]) * f, bf16_hi(w[0]) * f),
+                        pack_f16x2(bf16_lo(w[1]) * f, bf16_hi(w[1]) * f),
+                        pack_f16x2(bf16_lo(w[2]) * f, bf16_hi(w[2]) * f),
+                        pack_f16x2(bf16_lo(w[3]) * f, bf16_hi(w[3]) * f));
     }
   }
-  if (lane == 0) xexp[p] = ae;
+  return ae;
+}
+
+__device__ __forceinline__ void store_row(uint16_t* __restrict__ dst_row, int K, int lane,
+                                          const uint4 (&v)[kGatherMaxPieces]) {
+  uint4* dst = reinterpret_cast<uint4*>(dst_row);
+#pragma unroll
+  for (int i = 0; i < kGatherMaxPieces; ++i)
+    if (i < K / 256) dst[lane + 32 * i] = v[i];
+}
+
+// Rows in expert order from the permutation's row -> token map: xp[p] = x'
+// of token row_token[p], xexp[p] = its a, for the routed rows p <
+// expert_off[E]; a token index outside [0, T) gives a zero row with a = 0.
+// One warp per row.
+__global__ void __launch_bounds__(256)
+k_gather_rows(const uint16_t* __restrict__ x, int T, const int32_t* __restrict__ row_token,
+              const int32_t* __restrict__ expert_off, int E, int P, int K,
+              uint16_t* __restrict__ xp, int32_t* __restrict__ xexp,
+              int32_t* __restrict__ status) {
+  griddep_wait();
+  griddep_trigger();
+  const int p = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (p >= min(P, expert_off[E])) return;  // warp-uniform
+  const int t = row_token[p];
+  uint4 v[kGatherMaxPieces];
+  int a = 0;
+  if (t < 0 || t >= T) {
+#pragma unroll
+    for (int i = 0; i < kGatherMaxPieces; ++i) v[i] = make_uint4(0, 0, 0, 0);
+  } else {
+    a = normalise_row(x, t, K, lane, v, status);
+  }
+  store_row(xp + (size_t)p * K, K, lane, v);
+  if (lane == 0) xexp[p] = a;
+}
+
+// The same from the token side (the layer call, which has the permutation's
+// token -> row map): one warp per token normalises x[t] once and writes it
+// to each of its rows tok_slot_row[t k + j] >= 0 and, when xs is set, to
+// row t of xs (the shared expert's rows, in token order).
+__global__ void __launch_bounds__(256)
+k_gather_tokens(const uint16_t* __restrict__ x, int T, int K,
+                const int32_t* __restrict__ tok_slot_row, int k, uint16_t* __restrict__ xp,
+                int32_t* __restrict__ xexp, uint16_t* __restrict__ xs,
+                int32_t* __restrict__ sxexp, int32_t* __restrict__ status) {
+  griddep_wait();
+  griddep_trigger();
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (t >= T) return;  // warp-uniform
+  uint4 v[kGatherMaxPieces];
+  const int a = normalise_row(x, t, K, lane, v, status);
+  const int my_row = lane < k ? tok_slot_row[(size_t)t * k + lane] : -1;
+  for (int j = 0; j < k; ++j) {
+    const int row = __shfl_sync(0xffffffffu, my_row, j);
+    if (row < 0) continue;  // warp-uniform
+    store_row(xp + (size_t)row * K, K, lane, v);
+    if (lane == 0) xexp[row] = a;
+  }
+  if (xs) {
+    store_row(xs + (size_t)t * K, K, lane, v);
+    if (lane == 0) sxexp[t] = a;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -913,9 +974,9 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x, int T, const int32_t* exper
                                   int E, int P, const moe_fp8_ffn& w, int H, int I,
                                   int32_t* tile_off, int32_t* slot_done, uint16_t* hid, void* y,
                                   int16_t* yexp, int yexp_rows, int32_t* status, cudaStream_t s,
-                                  bool pdl, bool tile_off_ready) {
+                                  bool pdl, bool tile_off_ready, const GemmGather& gather) {
   static_assert(BT == kGemmTokenTile, "token tile of the permutation's tile prefix");
-  if (!x_perm || !xexp) return cudaErrorInvalidValue;
+  if (!x_perm || !xexp || H > kGatherMaxPieces * 256) return cudaErrorInvalidValue;
   cudaError_t err;
   if ((err = ensure_smem((const void*)k_expert_gemm_ws<true>, SMEM_WS)) != cudaSuccess) return err;
   if ((err = ensure_smem((const void*)k_expert_gemm_ws<false>, SMEM_WS)) != cudaSuccess) return err;
@@ -948,8 +1009,17 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x, int T, const int32_t* exper
                    slot_done, max_ttiles);
     if (err != cudaSuccess) return err;
   }
-  err = launch_k(k_gather_rows, dim3(cdiv(P, 8)), dim3(256), 0, s, pdl, x, T, row_token,
-                 expert_off, E, P, H, x_perm, xexp, status);
+  bool prev_wrote_offsets = !tile_off_ready;  // the GEMM's previous kernel
+  if (gather.tok_slot_row) {
+    err = launch_k(k_gather_tokens, dim3(cdiv(T, 8)), dim3(256), 0, s, pdl, x, T, H,
+                   gather.tok_slot_row, gather.k, x_perm, xexp, gather.shared_rows,
+                   gather.shared_xexp, status);
+    prev_wrote_offsets = false;
+  } else if (!gather.rows_ready) {
+    err = launch_k(k_gather_rows, dim3(cdiv(P, 8)), dim3(256), 0, s, pdl, x, T, row_token,
+                   expert_off, E, P, H, x_perm, xexp, status);
+    prev_wrote_offsets = false;
+  }
   if (err != cudaSuccess) return err;
   int log2H = 0;
   while ((2 << log2H) <= H) ++log2H;
@@ -966,7 +1036,8 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x, int T, const int32_t* exper
   g.out = hid;
   g.out_ld = I;
   g.n_wblocks = I / BW;
-  g.all_wait = 0;  // the gather ran between the tile offsets and this GEMM
+  // every warp waits when the previous kernel wrote the tile offsets
+  g.all_wait = prev_wrote_offsets ? 1 : 0;
   g.slot_done = slot_done;
   g.slot_need = 0;
   g.status = status;

@@ -23,11 +23,12 @@
 //
 // Block scale and range: each 64-column chunk lies inside one 128x128 scale
 // block, so the chunk's MMA sum is multiplied by its scale in fp32 and added
-// to an fp32 accumulator.  The activations are brought into fp16 per
-// (token, chunk) by a power of two: the bf16 activations x are scaled so the
-// largest of the token's 64 values lands in [2^14, 2^15) (exact: bf16 has
-// fewer mantissa bits than fp16) and the power of two rejoins the scale in
-// fp32.  The SwiGLU output hid is stored as fp16 with one exponent per 16
+// to an fp32 accumulator.  The activations arrive in fp16 scaled per
+// (token, chunk) by a power of two (xn = x 2^(14 - e), written once per call
+// by the router or launch_x_norm: the largest of the token's 64 values lands
+// in [2^14, 2^15), exact because bf16 has fewer mantissa bits than fp16) and
+// 2^(e - 14) rejoins the scale in fp32.  The SwiGLU output hid is stored as
+// fp16 with one exponent per 16
 // features of a row, the down kernel aligns a chunk's four exponents and
 // again moves the power of two into the fp32 scale.  So the expert FFN has no
 // range limit beyond fp32's: block scales, activations and weights of any
@@ -51,7 +52,7 @@ constexpr size_t kGuSmem = sizeof(uint4) * kGuChunks * 4 * kThreads;  // 64 KB
 
 template <int NT>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2)
-k_gateup_stream(const uint16_t* __restrict__ x, int H, int I,
+k_gateup_stream(const uint16_t* __restrict__ xn, const int8_t* __restrict__ xe, int H, int I,
                 const int32_t* __restrict__ expert_off, const int32_t* __restrict__ row_token,
                 const int32_t* __restrict__ active,
                 const uint8_t* __restrict__ gcodes, const float* __restrict__ gscales,
@@ -116,9 +117,11 @@ k_gateup_stream(const uint16_t* __restrict__ x, int H, int I,
       // 1. all weight copies of this K-group (unless already in flight)
       if (!issued) issue(kg);
       issued = false;
-      // 2. block scales and activations (bf16), straight into registers
+      // 2. block scales and activations (fp16 and their exponents), straight
+      // into registers
       float sg[kGuChunks], su[kGuChunks];
       uint4 xa[kGuChunks][NT][2];
+      int xx[kGuChunks][NT];
 #pragma unroll
       for (int j = 0; j < kGuChunks; ++j) {
         const int ch = kg + warp + 8 * j;
@@ -127,16 +130,18 @@ k_gateup_stream(const uint16_t* __restrict__ x, int H, int I,
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           if (ch < nch && trow[nt] >= 0) {
-            const uint16_t* xp = x + (size_t)trow[nt] * H + ch * 64 + 16 * c;
+            const uint16_t* xp = xn + (size_t)trow[nt] * H + ch * 64 + 16 * c;
             xa[j][nt][0] = ldg16(xp);
             xa[j][nt][1] = ldg16(xp + 8);
+            xx[j][nt] = xe[(size_t)trow[nt] * nch + ch];
           } else {
             xa[j][nt][0] = xa[j][nt][1] = make_uint4(0, 0, 0, 0);
+            xx[j][nt] = kExpFloor;
           }
         }
       }
-      // 3. per chunk as its copies land: activations to fp16 by a power of
-      // two per token, decode + MMA, then scale and power of two in fp32
+      // 3. per chunk as its copies land: decode + MMA, then block scale and
+      // the activations' power of two in fp32
 #pragma unroll
       for (int j = 0; j < kGuChunks; ++j) {
         const int ch = kg + warp + 8 * j;  // warp-uniform
@@ -147,9 +152,8 @@ k_gateup_stream(const uint16_t* __restrict__ x, int H, int I,
           float fg[NT][2], fu[NT][2];
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            const int ex = bf16x16_to_f16_norm(xa[j][nt], bad);
-            const int e0 = min(__shfl_sync(0xffffffffu, ex, 8 * c), 127) - kGroupTop;
-            const int e1 = min(__shfl_sync(0xffffffffu, ex, 8 * c + 4), 127) - kGroupTop;
+            const int e0 = __shfl_sync(0xffffffffu, xx[j][nt], 8 * c) - kGroupTop;
+            const int e1 = __shfl_sync(0xffffffffu, xx[j][nt], 8 * c + 4) - kGroupTop;
             fg[nt][0] = sg[j] * pow2f(e0);
             fg[nt][1] = sg[j] * pow2f(e1);
             fu[nt][0] = su[j] * pow2f(e0);
@@ -442,7 +446,39 @@ bool fused_combine_ok(int T, int k, int H, int max_active) {
          ctas <= (long long)num_sms() * 4;
 }
 
-cudaError_t launch_expert_gemv(const uint16_t* x, const int32_t* expert_off,
+// xn = x 2^(14 - e), xe = e per (token, 64 columns): thread 16 values,
+// the quad of lanes 4g .. 4g + 3 one chunk (T H / 16 threads, launched as
+// whole warps: threads past the end take part in the shuffles with zeros).
+__global__ void __launch_bounds__(256)
+k_x_norm(const uint16_t* __restrict__ x, long long n16, int H, uint16_t* __restrict__ xn,
+         int8_t* __restrict__ xe) {
+  griddep_wait();
+  griddep_trigger();
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const bool in = i < n16;
+  uint4 v[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+  if (in) {
+    v[0] = ldg16(x + 16 * i);
+    v[1] = ldg16(x + 16 * i + 8);
+  }
+  bool bad = false;  // a non-finite x shows in the expert kernels' results
+  const int e = bf16x16_to_f16_norm(v, bad);
+  if (!in) return;
+  uint4* dst = reinterpret_cast<uint4*>(xn + 16 * i);
+  dst[0] = v[0];
+  dst[1] = v[1];
+  if ((i & 3) == 0) xe[i >> 2] = (int8_t)min(e, 127);  // chunk (16 i) / 64 of the row-major array
+}
+
+cudaError_t launch_x_norm(const uint16_t* x, int T, int H, uint16_t* xn, int8_t* xe,
+                          cudaStream_t s, bool pdl) {
+  const long long n16 = (long long)T * H / 16;
+  if (n16 == 0) return cudaSuccess;
+  return launch_k(k_x_norm, dim3((unsigned)((n16 + 255) / 256)), dim3(256), 0, s, pdl, x, n16, H,
+                  xn, xe);
+}
+
+cudaError_t launch_expert_gemv(const uint16_t* xn, const int8_t* xe, const int32_t* expert_off,
                                const int32_t* row_token, const int32_t* active, int max_active,
                                const moe_fp8_ffn& w, int H, int I, int tokens_per_expert_hint,
                                uint16_t* hid, int8_t* hexp, void* y, int16_t* yexp, int y_rows,
@@ -464,7 +500,7 @@ cudaError_t launch_expert_gemv(const uint16_t* x, const int32_t* expert_off,
   };
   if (nt1) {
     if ((e = ensure_smem((const void*)k_gateup_stream<1>, kGuSmem)) != cudaSuccess) return e;
-    e = launch_k(k_gateup_stream<1>, g1, block, kGuSmem, s, pdl, x, H, I, expert_off,
+    e = launch_k(k_gateup_stream<1>, g1, block, kGuSmem, s, pdl, xn, xe, H, I, expert_off,
                  row_token, active, w.gate.codes, w.gate.scales, w.up.codes, w.up.scales, hid,
                  hexp, status);
     if (e != cudaSuccess) return e;
@@ -472,8 +508,9 @@ cudaError_t launch_expert_gemv(const uint16_t* x, const int32_t* expert_off,
     return yexp ? down(k_down_stream<1, true>) : down(k_down_stream<1, false>);
   }
   if ((e = ensure_smem((const void*)k_gateup_stream<2>, kGuSmem)) != cudaSuccess) return e;
-  e = launch_k(k_gateup_stream<2>, g1, block, kGuSmem, s, pdl, x, H, I, expert_off, row_token,
-               active, w.gate.codes, w.gate.scales, w.up.codes, w.up.scales, hid, hexp, status);
+  e = launch_k(k_gateup_stream<2>, g1, block, kGuSmem, s, pdl, xn, xe, H, I, expert_off,
+               row_token, active, w.gate.codes, w.gate.scales, w.up.codes, w.up.scales, hid, hexp,
+               status);
   if (e != cudaSuccess) return e;
   if (cmb.ticket) return down(k_down_stream<2, true, true>);
   return yexp ? down(k_down_stream<2, true>) : down(k_down_stream<2, false>);

@@ -118,6 +118,9 @@ void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
 // GEMV up to 32 rows per expert (the 16-expert H 256 layer: GEMV 20 / 26 us
 // at 32 / 100 tokens, GEMM 30 / 32 us).
 constexpr int kGemmMinRowsPerRoutedExpert = 1;
+// Tokens from which the layer call gathers the GEMM's rows token-major
+// (about one wave of its 8-token CTAs).
+constexpr int kTokenGatherMin = 1024;
 constexpr int kGemmMinRowsPerSmallExpert = 32;
 constexpr int kGemmMinRowsDense = 32;
 constexpr long long kSmallExpertCodes = 1ll << 20;
@@ -183,6 +186,9 @@ WsLayout ws_layout(const moe_dims& d) {
   L.row_token = take(P * 4);
   L.tok_slot_row = take(P * 4);
   L.row_pair = take(P * 4);
+  // the streamed expert kernels' activations: fp16, exponent per 64 columns
+  L.xn = take(T * H * 2);
+  L.xe = take(T * (H / 64));
   // hid and y rows in fp16 with power-of-two exponents: hid per 16 features
   // (streamed GEMV), y per 32 columns, the exponent tables [H / 32][rows]
   L.hid = take(P * I * 2);
@@ -285,8 +291,8 @@ moe_status moe_route(const uint16_t* x, const float* Wr, const float* bias, moe_
   if ((s = check_ws(d, ws, ws_bytes)) != MOE_OK) return s;
   const WsLayout L = ws_layout(d);
   CUDA_CHECK(launch_route(x, Wr, bias, d.T, d.H, d.E, d.k, at<float>(ws, L.logits),
-                          at<uint16_t>(ws, L.wr_planes), topk_idx, topk_w, at<int32_t>(ws, L.status),
-                          (cudaStream_t)stream, true),
+                          at<uint16_t>(ws, L.wr_planes), topk_idx, topk_w, nullptr, nullptr,
+                          at<int32_t>(ws, L.status), (cudaStream_t)stream, true),
              "moe_route");
   return MOE_OK;
 }
@@ -334,7 +340,11 @@ moe_status moe_expert_ffn_fp8(const uint16_t* x, const int32_t* expert_off,
   CUDA_CHECK(launch_active_from_offsets(expert_off, d.E, active, status, st, true),
              "moe_expert_ffn_fp8");
   const int P = d.T * d.k;
-  if (use_expert_gemm(P, d.E, d.H, d.I))
+  const bool gemm = use_expert_gemm(P, d.E, d.H, d.I);
+  if (!gemm)
+    CUDA_CHECK(launch_x_norm(x, d.T, d.H, at<uint16_t>(ws, L.xn), at<int8_t>(ws, L.xe), st, true),
+               "moe_expert_ffn_fp8");
+  if (gemm)
     CUDA_CHECK(launch_expert_gemm_tc(x, d.T, expert_off, row_token, at<uint16_t>(ws, L.x_perm),
                                      at<int32_t>(ws, L.xexp), d.E, P, w, d.H, d.I,
                                      at<int32_t>(ws, L.tile_off), at<int32_t>(ws, L.slot_done),
@@ -342,9 +352,10 @@ moe_status moe_expert_ffn_fp8(const uint16_t* x, const int32_t* expert_off,
                                      true),
                "moe_expert_ffn_fp8");
   else
-    CUDA_CHECK(launch_expert_gemv(x, expert_off, row_token, active, d.E < P ? d.E : P, w, d.H,
-                                  d.I, cdiv(P, d.E), at<uint16_t>(ws, L.hid),
-                                  at<int8_t>(ws, L.hexp), y_perm, nullptr, 0, status, st, true),
+    CUDA_CHECK(launch_expert_gemv(at<uint16_t>(ws, L.xn), at<int8_t>(ws, L.xe), expert_off,
+                                  row_token, active, d.E < P ? d.E : P, w, d.H, d.I,
+                                  cdiv(P, d.E), at<uint16_t>(ws, L.hid), at<int8_t>(ws, L.hexp),
+                                  y_perm, nullptr, 0, status, st, true),
                "moe_expert_ffn_fp8");
   return MOE_OK;
 }
@@ -410,6 +421,11 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
   // also combines (its tickets cleared by the permutation)
   const bool fuse_combine =
       !gemm && small && !has_shared && fused_combine_ok(d.T, d.k, d.H, d.E < P ? d.E : P);
+  const bool shared_gemm = has_shared && use_expert_gemm(d.T, 1, d.H, d.I_shared);
+  // the router writes the streamed kernels' activations when one runs
+  const bool need_xn = !gemm || (has_shared && !shared_gemm);
+  uint16_t* xn = need_xn ? at<uint16_t>(ws, L.xn) : nullptr;
+  int8_t* xe = need_xn ? at<int8_t>(ws, L.xe) : nullptr;
   if (small) {
     // router logits, then top-k + permutation (+ the shared expert's identity
     // permutation) in one CTA
@@ -418,7 +434,7 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
                    at<uint16_t>(ws, L.wr_planes), idx, w, off,
                    row_token, tok_slot_row, at<int32_t>(ws, L.row_pair), active,
                    has_shared ? soff : nullptr, has_shared ? srows : nullptr,
-                   has_shared ? sact : nullptr,
+                   has_shared ? sact : nullptr, xn, xe,
                    gemm ? at<int32_t>(ws, L.tile_off) : nullptr,
                    gemm ? at<int32_t>(ws, L.slot_done)
                         : (fuse_combine ? at<int32_t>(ws, L.ticket) : nullptr),
@@ -427,7 +443,7 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
                "moe_layer_forward: route+permute");
   } else {
     CUDA_CHECK(launch_route(x, Wr, bias, d.T, d.H, d.E, d.k, at<float>(ws, L.logits),
-                            at<uint16_t>(ws, L.wr_planes), idx, w, status, st, true),
+                            at<uint16_t>(ws, L.wr_planes), idx, w, xn, xe, status, st, true),
                "moe_layer_forward: route");
     CUDA_CHECK(launch_permute(idx, d.T, d.E, d.k, at<int32_t>(ws, L.rank),
                               at<int32_t>(ws, L.block_cnt), at<int32_t>(ws, L.block_base), off,
@@ -438,12 +454,26 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
       CUDA_CHECK(launch_identity_perm(d.T, soff, srows, sact, st, true),
                  "moe_layer_forward: shared");
   }
+  // From kTokenGatherMin tokens one warp per token normalises its row once
+  // and writes its k routed rows (and its shared-expert row when that expert
+  // also runs on the GEMM); below, one warp per routed row keeps more CTAs
+  // in flight (8 tokens per CTA would leave most SMs idle).
+  const bool token_gather = gemm && d.T >= kTokenGatherMin;
   if (gemm) {
+    GemmGather gth;
+    if (token_gather) {
+      gth.tok_slot_row = tok_slot_row;
+      gth.k = d.k;
+      if (shared_gemm) {
+        gth.shared_rows = at<uint16_t>(ws, L.sh_x);
+        gth.shared_xexp = at<int32_t>(ws, L.sh_xexp);
+      }
+    }
     CUDA_CHECK(launch_expert_gemm_tc(x, d.T, off, row_token, at<uint16_t>(ws, L.x_perm),
                                      at<int32_t>(ws, L.xexp), d.E, P, routed, d.H, d.I,
                                      at<int32_t>(ws, L.tile_off), at<int32_t>(ws, L.slot_done),
                                      at<uint16_t>(ws, L.hid), y_perm, yexp, P, status, st, true,
-                                     /*tile_off_ready=*/small),
+                                     /*tile_off_ready=*/small, gth),
                "moe_layer_forward: experts");
   } else {
     FusedCombine cmb;
@@ -455,8 +485,8 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
       cmb.k = d.k;
       cmb.out = out;
     }
-    CUDA_CHECK(launch_expert_gemv(x, off, row_token, active, d.E < P ? d.E : P, routed, d.H,
-                                  d.I, cdiv(P, d.E), at<uint16_t>(ws, L.hid),
+    CUDA_CHECK(launch_expert_gemv(xn, xe, off, row_token, active, d.E < P ? d.E : P, routed,
+                                  d.H, d.I, cdiv(P, d.E), at<uint16_t>(ws, L.hid),
                                   at<int8_t>(ws, L.hexp), y_perm, yexp, P, status, st, true,
                                   cmb),
                "moe_layer_forward: experts");
@@ -466,15 +496,18 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
   if (has_shared) {
     shared_y = at<uint16_t>(ws, L.sh_y);
     shared_yexp = at<int16_t>(ws, L.sh_yexp);
-    if (use_expert_gemm(d.T, 1, d.H, d.I_shared))
+    if (shared_gemm) {
+      GemmGather gth;
+      gth.rows_ready = token_gather;  // the routed gather wrote the shared rows
       CUDA_CHECK(launch_expert_gemm_tc(x, d.T, soff, srows, at<uint16_t>(ws, L.sh_x),
                                        at<int32_t>(ws, L.sh_xexp), 1, d.T, *shared, d.H,
                                        d.I_shared, at<int32_t>(ws, L.sh_tile_off),
                                        at<int32_t>(ws, L.sh_slot_done), at<uint16_t>(ws, L.sh_hid),
-                                       shared_y, shared_yexp, d.T, status, st, true),
+                                       shared_y, shared_yexp, d.T, status, st, true, false, gth),
                  "moe_layer_forward: shared expert");
+    }
     else
-      CUDA_CHECK(launch_expert_gemv(x, soff, srows, sact, 1, *shared, d.H, d.I_shared, d.T,
+      CUDA_CHECK(launch_expert_gemv(xn, xe, soff, srows, sact, 1, *shared, d.H, d.I_shared, d.T,
                                     at<uint16_t>(ws, L.sh_hid), at<int8_t>(ws, L.sh_hexp),
                                     shared_y, shared_yexp, d.T, status, st, true),
                  "moe_layer_forward: shared expert");

@@ -139,12 +139,45 @@ __device__ __forceinline__ int warp_max_exp(uint32_t absbits, bool& bad) {
   return min(max((int)(m >> 23) - 127, -126), 126);
 }
 
-// The same over n floats at p (lane i reads p[i], p[i + 32], ...).
+// Largest magnitude bits among n floats at p, this lane's share (lane i
+// reads p[i], p[i + 32], ...), four independent loads per round so that one
+// memory round trip covers up to 128 floats.
+__device__ __forceinline__ uint32_t lane_max_bits(const float* __restrict__ p, int n, int lane) {
+  uint32_t m = 0;
+  for (int i = lane; i < n; i += 128) {
+    uint32_t v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      v[u] = i + 32 * u < n ? __float_as_uint(__ldg(p + i + 32 * u)) & 0x7fffffffu : 0u;
+    m = max(m, max(max(v[0], v[1]), max(v[2], v[3])));
+  }
+  return m;
+}
+
+// warp_max_exp over n floats at p.
 __device__ __forceinline__ int warp_max_exp_of(const float* __restrict__ p, int n, int lane,
                                                bool& bad) {
-  uint32_t m = 0;
-  for (int i = lane; i < n; i += 32) m = max(m, __float_as_uint(__ldg(p + i)) & 0x7fffffffu);
-  return warp_max_exp(m, bad);
+  return warp_max_exp(lane_max_bits(p, n, lane), bad);
+}
+
+// Column exponents of a 32 x 32 tile held one row per lane (v[i] = column
+// i of this lane's row): on return every lane's ex[k] holds, in byte j, the
+// largest biased fp32 exponent of column 4k + j over the 32 rows (255: an
+// infinite or NaN value).  The exponent of a column's largest magnitude is
+// the largest of its exponents, so this is exact.  Eight words of four
+// bytes, five butterfly rounds of shuffles and byte-wise maxima.
+__device__ __forceinline__ void column_max_exponents(const uint32_t (&v)[32], uint32_t (&ex)[8]) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    // the biased exponent is byte 3 of (bits << 1)
+    const uint32_t ab = __byte_perm(v[4 * k] << 1, v[4 * k + 1] << 1, 0x0073);
+    const uint32_t cd = __byte_perm(v[4 * k + 2] << 1, v[4 * k + 3] << 1, 0x0073);
+    ex[k] = __byte_perm(ab, cd, 0x5410);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) ex[k] = __vmaxu4(ex[k], __shfl_xor_sync(0xffffffffu, ex[k], o));
 }
 
 // 16 bf16 activations of one token (two 16-byte registers, 8 bf16x2) turned

@@ -61,7 +61,7 @@ int num_sms();
 // Workspace layout for one set of dims (byte offsets, each 256-aligned).
 struct WsLayout {
   size_t status, logits, rank, block_cnt, block_base, active, idx, w, off, row_token,
-      tok_slot_row, row_pair, hid, hexp, y_perm, yexp, sh_hid, sh_hexp, sh_y, sh_yexp, sh_off,
+      tok_slot_row, row_pair, xn, xe, hid, hexp, y_perm, yexp, sh_hid, sh_hexp, sh_y, sh_yexp, sh_off,
       sh_rows, sh_active, tile_off, sh_tile_off, x_perm, xexp, sh_x, sh_xexp, wr_planes,
       slot_done, sh_slot_done, ticket, total;
 };
@@ -72,17 +72,20 @@ WsLayout ws_layout(const moe_dims& d);
 
 // Router logits and top-k.  `part` holds up to 8 K-slices of partial
 // logits, [8][T][E] floats; `planes` is scratch for the bf16 split of Wr,
-// [3][E][H] (used from 128 tokens, router_tc_ok).
+// [3][E][H] (used from 128 tokens, router_tc_ok).  xn / xe (may be NULL):
+// the streamed expert kernels' activations, written on the way
+// (xn [T, H] fp16 = x 2^(14 - e), xe [T, H / 64] int8 = e per 64 columns).
 cudaError_t launch_route(const uint16_t* x, const float* Wr, const float* bias, int T, int H,
                          int E, int k, float* part, uint16_t* planes, int32_t* topk_idx,
-                         float* topk_w, int32_t* status, cudaStream_t s, bool pdl);
+                         float* topk_w, uint16_t* xn, int8_t* xe, int32_t* status,
+                         cudaStream_t s, bool pdl);
 
 // Router logits on the tensor cores (route_tc.cu): T >= 128, E % 128 == 0,
 // H % 64 == 0.  Writes KS slices of partial logits (KS from route_kslices).
 bool router_tc_ok(int T, int H, int E);
 cudaError_t launch_router_logits_tc(const uint16_t* x, const float* Wr, int T, int H, int E,
-                                    int KS, float* part, uint16_t* planes, int32_t* status,
-                                    cudaStream_t s, bool pdl);
+                                    int KS, float* part, uint16_t* planes, uint16_t* xn,
+                                    int8_t* xe, int32_t* status, cudaStream_t s, bool pdl);
 
 // Token rows per tile of the tensor-core GEMM (its MMA N, at most).
 constexpr int kGemmTokenTile = 128;
@@ -98,8 +101,9 @@ cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const
                                        uint16_t* planes, int32_t* topk_idx, float* topk_w, int32_t* expert_off,
                                        int32_t* row_token, int32_t* tok_slot_row,
                                        int32_t* row_pair, int32_t* active, int32_t* sh_off,
-                                       int32_t* sh_rows, int32_t* sh_active,
-                                       int32_t* tile_off, int32_t* counters, int n_counters,
+                                       int32_t* sh_rows, int32_t* sh_active, uint16_t* xn,
+                                       int8_t* xe, int32_t* tile_off, int32_t* counters,
+                                       int n_counters,
                                        int32_t* status, cudaStream_t s, bool pdl);
 
 cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, int32_t* rank,
@@ -110,8 +114,14 @@ cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, int32_t
 cudaError_t launch_active_from_offsets(const int32_t* expert_off, int E, int32_t* active,
                                        int32_t* status, cudaStream_t s, bool pdl);
 
+// The streamed expert kernels' activations from bf16 x [T, H] (n = T H):
+// xn [T, H] fp16 = x 2^(14 - e), xe [T, H / 64] int8 = e per 64 columns.
+cudaError_t launch_x_norm(const uint16_t* x, int T, int H, uint16_t* xn, int8_t* xe,
+                          cudaStream_t s, bool pdl);
+
 // Grouped GEMV over the experts listed in `active` (count, then ids), on the
-// bf16 activations x [T, H].  hid: [P, I] fp16 scratch with hexp [P, I/16]
+// normalised activations xn / xe (launch_x_norm or the router).  hid: [P, I]
+// fp16 scratch with hexp [P, I/16]
 // int8 exponents.  y: [P, H] fp32 when yexp is NULL, else fp16 with yexp
 // [H/32][y_rows] int16 exponents (y = y'' 2^s).  max_active bounds the list
 // length; tokens_per_expert_hint (the expected rows per expert) picks the
@@ -130,7 +140,7 @@ struct FusedCombine {
   int T = 0, k = 0;
   uint16_t* out = nullptr;
 };
-cudaError_t launch_expert_gemv(const uint16_t* x, const int32_t* expert_off,
+cudaError_t launch_expert_gemv(const uint16_t* xn, const int8_t* xe, const int32_t* expert_off,
                                const int32_t* row_token, const int32_t* active, int max_active,
                                const moe_fp8_ffn& w, int H, int I, int tokens_per_expert_hint,
                                uint16_t* hid, int8_t* hexp, void* y, int16_t* yexp, int y_rows,
@@ -145,6 +155,19 @@ cudaError_t launch_expert_gemv(const uint16_t* x, const int32_t* expert_off,
 // tile_off_ready: the permutation already wrote tile_off and zeroed slot_done
 // (launch_route_permute_small), so the tile-offset kernel is skipped.
 bool expert_gemm_tc_ok(int H, int I);
+// How the GEMM's activation rows are gathered.  Default: one warp per row
+// from row_token.  tok_slot_row set (the layer call): one warp per token,
+// written to the token's k rows and, when shared_rows is set, also to row t
+// of shared_rows / shared_xexp (the shared expert's rows, which a later GEMM
+// call then uses with rows_ready).  rows_ready: x_perm / xexp already hold
+// the rows; no gather is launched.
+struct GemmGather {
+  const int32_t* tok_slot_row = nullptr;
+  int k = 0;
+  uint16_t* shared_rows = nullptr;
+  int32_t* shared_xexp = nullptr;
+  bool rows_ready = false;
+};
 // x: [T, H] bf16.  x_perm: [P, H] fp16 and xexp: [P] int32 scratch that
 // receive the activation rows in expert order, normalised by a power of two
 // (x[row_token[p]] = x_perm[p] 2^xexp[p]).  hid: [P, I] fp16 scratch.  y:
@@ -155,7 +178,8 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x, int T, const int32_t* exper
                                   int E, int P, const moe_fp8_ffn& w, int H, int I,
                                   int32_t* tile_off, int32_t* slot_done, uint16_t* hid, void* y,
                                   int16_t* yexp, int yexp_rows, int32_t* status, cudaStream_t s,
-                                  bool pdl, bool tile_off_ready = false);
+                                  bool pdl, bool tile_off_ready = false,
+                                  const GemmGather& gather = GemmGather{});
 // slot_done entries the GEMM uses for P routed rows over E experts.
 inline int expert_gemm_slots(int P, int E) { return (P + 127) / 128 + (E < P ? E : P); }
 

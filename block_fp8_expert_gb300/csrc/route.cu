@@ -17,6 +17,10 @@ namespace moe {
 // slices of K = H and 8*NT tokens; its 4 warps take the slice's 64-column
 // chunks round-robin.  Partial sums go to part[ks][t][e]; the top-k kernels
 // add the KS slices in a fixed order (deterministic).
+// When xn is set, the CTAs of expert tile 0 also write the activations for
+// the streamed expert kernels: xn = fp16(x 2^(14 - e)) and xe = e, one e per
+// token and 64 columns (the largest magnitude of the 64 lands in
+// [2^14, 2^15); exact, see bf16x16_to_f16_norm).
 // ---------------------------------------------------------------------------
 constexpr int kRouteWarps = 4;
 constexpr int kMaxKSlices = 8;  // K-slices of the router logits (route_kslices)
@@ -24,7 +28,8 @@ constexpr int kMaxKSlices = 8;  // K-slices of the router logits (route_kslices)
 template <int NT>
 __global__ void __launch_bounds__(kRouteWarps * 32)
 k_router_mma(const uint16_t* __restrict__ x, const float* __restrict__ Wr, int T, int H, int E,
-             int kslice, float* __restrict__ part, int32_t* __restrict__ status) {
+             int kslice, float* __restrict__ part, uint16_t* __restrict__ xn,
+             int8_t* __restrict__ xe, int32_t* __restrict__ status) {
   __shared__ float red[kRouteWarps][NT][4][32];
   griddep_wait();
   griddep_trigger();
@@ -38,6 +43,7 @@ k_router_mma(const uint16_t* __restrict__ x, const float* __restrict__ Wr, int T
   const int t0 = blockIdx.z * NT * 8;
   const int kbeg = blockIdx.y * kslice, kend = min(H, kbeg + kslice);
   const int ea = e0 + g, eb = e0 + g + 8;
+  const bool write_xn = xn != nullptr && blockIdx.x == 0;  // CTA-uniform
   int trow[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) trow[nt] = (t0 + nt * 8 + g < T) ? t0 + nt * 8 + g : -1;
@@ -68,6 +74,22 @@ k_router_mma(const uint16_t* __restrict__ x, const float* __restrict__ Wr, int T
         xa[nt][1] = ldg16(xp + 8);
       } else {
         xa[nt][0] = xa[nt][1] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    if (write_xn) {
+      // the quad of lanes 4g .. 4g + 3 holds token trow's 64 columns k0 ..
+      // k0 + 63 (all lanes take part in the quad's shuffles)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        uint4 v[2] = {xa[nt][0], xa[nt][1]};
+        bool bad = false;  // a non-finite x shows in the expert kernels' results
+        const int ex = bf16x16_to_f16_norm(v, bad);
+        if (trow[nt] >= 0) {
+          uint4* dst = reinterpret_cast<uint4*>(xn + (size_t)trow[nt] * H + kk);
+          dst[0] = v[0];
+          dst[1] = v[1];
+          if (c == 0) xe[(size_t)trow[nt] * (H / 64) + k0 / 64] = (int8_t)min(ex, 127);
+        }
       }
     }
     // bf16x2 registers of the three parts, element pairs (2m, 2m+1)
@@ -429,28 +451,29 @@ int route_kslices(int T, int H, int E) {
 }
 
 cudaError_t launch_router_logits(const uint16_t* x, const float* Wr, int T, int H, int E,
-                                 float* part, uint16_t* planes, int32_t* status, cudaStream_t s,
-                                 bool pdl) {
+                                 float* part, uint16_t* planes, uint16_t* xn, int8_t* xe,
+                                 int32_t* status, cudaStream_t s, bool pdl) {
   const int KS = route_kslices(T, H, E);
   if (router_tc_ok(T, H, E))
-    return launch_router_logits_tc(x, Wr, T, H, E, KS, part, planes, status, s, pdl);
+    return launch_router_logits_tc(x, Wr, T, H, E, KS, part, planes, xn, xe, status, s, pdl);
   const int kslice = H / KS;
   const dim3 blk(kRouteWarps * 32);
   if (T <= 8)
     return launch_k(k_router_mma<1>, dim3(cdiv(E, 16), KS, cdiv(T, 8)), blk, 0, s, pdl, x, Wr,
-                    T, H, E, kslice, part, status);
+                    T, H, E, kslice, part, xn, xe, status);
   if (T <= 64)
     return launch_k(k_router_mma<2>, dim3(cdiv(E, 16), KS, cdiv(T, 16)), blk, 0, s, pdl, x, Wr,
-                    T, H, E, kslice, part, status);
+                    T, H, E, kslice, part, xn, xe, status);
   return launch_k(k_router_mma<4>, dim3(cdiv(E, 16), KS, cdiv(T, 32)), blk, 0, s, pdl, x, Wr,
-                  T, H, E, kslice, part, status);
+                  T, H, E, kslice, part, xn, xe, status);
 }
 
 cudaError_t launch_route(const uint16_t* x, const float* Wr, const float* bias, int T, int H,
                          int E, int k, float* part, uint16_t* planes, int32_t* topk_idx,
-                         float* topk_w, int32_t* status, cudaStream_t s, bool pdl) {
+                         float* topk_w, uint16_t* xn, int8_t* xe, int32_t* status,
+                         cudaStream_t s, bool pdl) {
   if (T == 0) return cudaSuccess;
-  cudaError_t err = launch_router_logits(x, Wr, T, H, E, part, planes, status, s, pdl);
+  cudaError_t err = launch_router_logits(x, Wr, T, H, E, part, planes, xn, xe, status, s, pdl);
   if (err != cudaSuccess) return err;
   const int KS = route_kslices(T, H, E);
   const int epl = cdiv(E, 32);
@@ -476,10 +499,10 @@ cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const
                                        int32_t* expert_off,
                                        int32_t* row_token, int32_t* tok_slot_row,
                                        int32_t* row_pair, int32_t* active, int32_t* sh_off,
-                                       int32_t* sh_rows, int32_t* sh_active,
-                                       int32_t* tile_off, int32_t* counters, int n_counters,
-                                       int32_t* status, cudaStream_t s, bool pdl) {
-  cudaError_t err = launch_router_logits(x, Wr, T, H, E, part, planes, status, s, pdl);
+                                       int32_t* sh_rows, int32_t* sh_active, uint16_t* xn,
+                                       int8_t* xe, int32_t* tile_off, int32_t* counters,
+                                       int n_counters, int32_t* status, cudaStream_t s, bool pdl) {
+  cudaError_t err = launch_router_logits(x, Wr, T, H, E, part, planes, xn, xe, status, s, pdl);
   if (err != cudaSuccess) return err;
   const int KS = route_kslices(T, H, E);
   const size_t smem = small_route_smem(E);

@@ -11,7 +11,11 @@
 //   warp 0      TMA: the step's x tile and its three weight tiles;
 //   warp 1      one elected thread issues tcgen05.mma (lo, mid, hi per
 //               16-wide K step) into one TMEM accumulator [128 x 128] fp32;
-//   warps 2-5   write the slice's partial logits part[ks][t][e].
+//   warps 2-5   when xn is set (CTAs of the first expert tile): turn the
+//               step's x tile into the streamed expert kernels' activations
+//               (xn = fp16(x 2^(14 - e)), one e = xe per token and 64
+//               columns); then write the slice's partial logits
+//               part[ks][t][e].
 // The top-k kernel adds the KS slices in a fixed order (deterministic).
 #include <cuda.h>
 
@@ -95,7 +99,7 @@ k_router_split(const float* __restrict__ Wr, long long n, uint16_t* __restrict__
 __global__ void __launch_bounds__(kRWarps * 32, 1)
 k_router_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
             int T, int H, int E, int kslice, float* __restrict__ part,
-            int32_t* __restrict__ status) {
+            uint16_t* __restrict__ xn, int8_t* __restrict__ xe, int32_t* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ RouterShared sh;
   griddep_wait();
@@ -103,13 +107,14 @@ k_router_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int t0 = blockIdx.x * RT, ks = blockIdx.y, e0 = blockIdx.z * RE;
   const int k0 = ks * kslice, nsteps = kslice / RBK;
+  const bool convert = xn != nullptr && blockIdx.z == 0;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t smem_base = smem_u32(smem);
   if (tid == 0) {
     for (int s = 0; s < RNS; ++s) {
       mbar_init(&sh.full[s], 1);
-      mbar_init(&sh.empty[s], 1);  // the MMA's commit
+      mbar_init(&sh.empty[s], convert ? 5 : 1);  // the MMA's commit (+ 4 converter warps)
     }
     mbar_init(&sh.done, 1);
     sh.abort_flag = 0;
@@ -130,6 +135,9 @@ k_router_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
     for (; s < nsteps; ++s) {
       const int st = s % RNS;
       if (s >= RNS && !rwait(sh, &sh.empty[st], (uint32_t)(((s / RNS) - 1) & 1), status)) break;
+      // the converters' reads of this slot (generic proxy) are ordered
+      // before the copies that overwrite it (async proxy)
+      tc::fence_proxy_async();
       if (tc::elect_one()) {
         uint8_t* dst = smem + st * R_STAGE;
         const int kx = k0 + s * RBK;
@@ -173,9 +181,48 @@ k_router_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
     if (lane == 0 && s > 0) mbar_wait(&sh.empty[(s - 1) % RNS], (uint32_t)(((s - 1) / RNS) & 1));
     __syncwarp();
   } else {
-    // ------------------------------------------------ partial logits
+    // ------------------------------------------------ activations, then logits
     const int q = warp & 3;  // TMEM lane quarter: experts e0 + 32 q + lane
-    if (rwait(sh, &sh.done, 0, status)) {
+    bool ok = true;
+    if (convert) {
+      // row r = 32 (warp - 2) + lane of each x tile: its 64 bf16 values
+      const int r = 32 * (warp - 2) + lane;
+      for (int s = 0; s < nsteps; ++s) {
+        const int st = s % RNS;
+        if (!rwait(sh, &sh.full[st], (uint32_t)((s / RNS) & 1), status)) {
+          ok = false;
+          break;
+        }
+        if (t0 + r < T) {
+          const uint8_t* row = smem + st * R_STAGE + r * 128;
+          uint4 v[8];
+          uint32_t m = 0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            v[j] = *reinterpret_cast<const uint4*>(row + ((j ^ (r & 7)) << 4));
+            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) m = max(m, max(w[u] & 0x7FFFu, (w[u] >> 16) & 0x7FFFu));
+          }
+          // a non-finite x shows in the expert kernels' results
+          const int ex = min(exp_of_bits(m << 16), 127);
+          const float f = pow2f(kGroupTop - ex);
+          uint4* dst = reinterpret_cast<uint4*>(xn + (size_t)(t0 + r) * H + k0 + s * RBK);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+            dst[j] = make_uint4(pack_f16x2(bf16_lo(w[0]) * f, bf16_hi(w[0]) * f),
+                                pack_f16x2(bf16_lo(w[1]) * f, bf16_hi(w[1]) * f),
+                                pack_f16x2(bf16_lo(w[2]) * f, bf16_hi(w[2]) * f),
+                                pack_f16x2(bf16_lo(w[3]) * f, bf16_hi(w[3]) * f));
+          }
+          xe[(size_t)(t0 + r) * (H / 64) + (k0 + s * RBK) / 64] = (int8_t)ex;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.empty[st]);
+      }
+    }
+    if (ok && rwait(sh, &sh.done, 0, status)) {
       tc::fence_after_sync();
       const uint32_t t_lane = tmem + ((uint32_t)(32 * q) << 16);
       const int e = e0 + 32 * q + lane;
@@ -209,8 +256,8 @@ bool router_tc_ok(int T, int H, int E) {
 }
 
 cudaError_t launch_router_logits_tc(const uint16_t* x, const float* Wr, int T, int H, int E,
-                                    int KS, float* part, uint16_t* planes, int32_t* status,
-                                    cudaStream_t s, bool pdl) {
+                                    int KS, float* part, uint16_t* planes, uint16_t* xn,
+                                    int8_t* xe, int32_t* status, cudaStream_t s, bool pdl) {
   cudaError_t err = ensure_smem((const void*)k_router_tc, R_SMEM);
   if (err != cudaSuccess) return err;
   CUtensorMap xmap, wmap;
@@ -228,7 +275,7 @@ cudaError_t launch_router_logits_tc(const uint16_t* x, const float* Wr, int T, i
                  status);
   if (err != cudaSuccess) return err;
   return launch_k(k_router_tc, dim3(cdiv(T, RT), KS, E / RE), dim3(kRWarps * 32), (size_t)R_SMEM,
-                  s, pdl, xmap, wmap, T, H, E, H / KS, part, status);
+                  s, pdl, xmap, wmap, T, H, E, H / KS, part, xn, xe, status);
 }
 
 }  // namespace moe
