@@ -47,6 +47,8 @@
 // copies and MMAs and frees its TMEM before it exits.
 #include <cuda.h>
 
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "moe_internal.h"
@@ -115,6 +117,9 @@ struct GemmArgs {
   // [rows_per_expert / 32][yexp_rows]; NULL: y is fp32
   int16_t* yexp;
   int yexp_rows;
+  // bounded waits give up after this many nanoseconds (0: the default);
+  // a diagnostic setting (MOE_FP8_WAIT_LIMIT_US)
+  uint64_t wait_ns;
 };
 
 struct WsShared {
@@ -124,6 +129,7 @@ struct WsShared {
   uint64_t acc_full, acc_empty;
   uint32_t tmem_base;
   int abort_flag;
+  uint64_t wait_ns;  // the role waits' budget (GemmArgs::wait_ns)
   // Steps each role has completed, for the timeout record: [warp] for the
   // TMA warps (steps issued) and the decoder warps (steps decoded),
   // [kWarps] steps issued to the tensor core, [kWarps + 1] tiles started by
@@ -148,7 +154,7 @@ __device__ __forceinline__ bool warp_wait(WsShared& sh, uint64_t* bar, uint32_t 
   constexpr unsigned kAll = 0xffffffffu;
   bool done = mbar_try_wait(bar, parity);
   if (__all_sync(kAll, done)) return true;
-  const WaitBudget b = wait_budget();
+  const WaitBudget b = wait_budget(sh.wait_ns);
   for (uint32_t n = 1;; ++n) {
     if (__any_sync(kAll, done)) {
       // the phase is complete: lanes that polled just before it completed
@@ -304,6 +310,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     mbar_init(&sh.acc_full, 1);
     mbar_init(&sh.acc_empty, kEpiWarps);
     sh.abort_flag = 0;
+    sh.wait_ns = a.wait_ns;
     for (int i = 0; i < kWarps + 3; ++i) sh.prog[i] = 0;
     fence_mbar_init();
   }
@@ -368,7 +375,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
         // this token tile's hid rows: every gate/up weight-block tile of the
         // slot has stored them (bounded warp-uniform poll, then the acquired
         // data is ordered before the async-proxy loads below)
-        const WaitBudget b = wait_budget();
+        const WaitBudget b = wait_budget(sh.wait_ns);
         bool done = false;
         for (uint32_t n = 0; !done; ++n) {
           done = __all_sync(0xffffffffu, tc::ld_acquire_gpu(a.slot_done + ti.slot) >= a.slot_need);
@@ -382,6 +389,14 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
           if (lane == 0 && !sh.abort_flag) {
             sh.abort_flag = 1;
             raise_status(a.status, MOE_DEV_WAIT_TIMEOUT);
+            // where: the token warp's wait for a token tile's hid rows
+            // (barrier id 9), the tile's slot and its completion count
+            if (a.status && atomicCAS(a.status + 1, 0, 1 + W_TOK) == 0) {
+              a.status[2] = 9;
+              a.status[3] = ti.slot;
+              a.status[4] = tc::ld_acquire_gpu(a.slot_done + ti.slot);
+              a.status[5] = (int)blockIdx.x;
+            }
           }
           __syncwarp();
           ok = false;
@@ -1023,6 +1038,17 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x, int T, const int32_t* exper
   if (err != cudaSuccess) return err;
   int log2H = 0;
   while ((2 << log2H) <= H) ++log2H;
+  // Diagnostics (read on every call): a shorter limit for the bounded waits
+  // (MOE_FP8_WAIT_LIMIT_US), and a down GEMM that waits for one more
+  // completed gate/up tile per token tile than exist, so that its wait runs
+  // out (MOE_FP8_TEST_STALL=down; the failure-path test).
+  uint64_t wait_ns = 0;
+  if (const char* lim = getenv("MOE_FP8_WAIT_LIMIT_US")) {
+    const long long us = atoll(lim);
+    if (us > 0) wait_ns = (uint64_t)us * 1000ull;
+  }
+  const char* stall = getenv("MOE_FP8_TEST_STALL");
+  const bool stall_down = stall && strcmp(stall, "down") == 0 && slot_done;
   const int nsm = num_sms();
   const dim3 blk(kThreadsWS);
   GemmArgs g{};
@@ -1043,6 +1069,7 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x, int T, const int32_t* exper
   g.status = status;
   g.xexp = xexp;
   g.hid_shift = log2H + 4;
+  g.wait_ns = wait_ns;
   err = launch_k(k_expert_gemm_ws<true>, dim3(min(nsm, max_ttiles * g.n_wblocks)), blk,
                  (size_t)SMEM_WS, s, pdl, gmap, umap, xmap, ymap, g);
   if (err != cudaSuccess) return err;
@@ -1068,6 +1095,8 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x, int T, const int32_t* exper
   d.hid_shift = g.hid_shift;
   d.yexp = yexp;
   d.yexp_rows = yexp_rows;
+  d.wait_ns = wait_ns;
+  if (stall_down) d.slot_need += 1;
   const int gu_grid = min(nsm, max_ttiles * g.n_wblocks);
   if (gu_grid == nsm && min(nsm, max_ttiles * d.n_wblocks) == nsm) {
     d.gu_grid = gu_grid;

@@ -371,19 +371,21 @@ __device__ __forceinline__ uint64_t global_ns() {
 // say the budget is spent, so a timer step cannot end a wait early and the
 // wait stays bounded either way.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;       // 2 s
-constexpr long long kWaitLimitCycles = 4000000000ll;   // about 2 s at 2 GHz
+constexpr long long kCyclesPerNs = 2;                  // about 2 GHz
 struct WaitBudget {
-  uint64_t t0;
+  uint64_t t0, ns;
   long long c0;
 };
-__device__ __forceinline__ WaitBudget wait_budget() {
+// A budget of limit_ns nanoseconds (0: the default kWaitLimitNs).
+__device__ __forceinline__ WaitBudget wait_budget(uint64_t limit_ns = 0) {
   WaitBudget b;
   b.t0 = global_ns();
   b.c0 = clock64();
+  b.ns = limit_ns ? limit_ns : kWaitLimitNs;
   return b;
 }
 __device__ __forceinline__ bool budget_spent(const WaitBudget& b) {
-  return clock64() - b.c0 > kWaitLimitCycles && global_ns() - b.t0 > kWaitLimitNs;
+  return clock64() - b.c0 > (long long)b.ns * kCyclesPerNs && global_ns() - b.t0 > b.ns;
 }
 // Bounded wait for the phase with the given parity by a single thread (the
 // rest of its warp may be elsewhere): it polls with the non-suspending probe

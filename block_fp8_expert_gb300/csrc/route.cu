@@ -430,6 +430,120 @@ k_topk_permute_small(const float* __restrict__ part, int KS, const float* __rest
   }
 }
 
+// ---------------------------------------------------------------------------
+// Tiny batches (T*k <= 64, T < kSplitTopkTokens): warp t does token t's
+// top-k as above, then warp 0 alone builds the whole permutation with
+// shuffles: every pair (q = t k + j) is ranked by (expert, q) against all
+// others, which is the expert-major, ascending-token order; the per-expert
+// counts (shared-memory atomics, order-free) give the offsets, the active
+// list and the GEMM's token-tile prefix (an expert has at most 64 rows here:
+// one token tile).  Same results as k_topk_permute_small.
+// ---------------------------------------------------------------------------
+constexpr int kTinyPairs = 64;
+
+template <int EPL>
+__global__ void __launch_bounds__(512, 1)
+k_topk_permute_tiny(const float* __restrict__ part, int KS, const float* __restrict__ bias,
+                    int T, int E, int k, int32_t* __restrict__ topk_idx,
+                    float* __restrict__ topk_w, int32_t* __restrict__ expert_off,
+                    int32_t* __restrict__ row_token, int32_t* __restrict__ tok_slot_row,
+                    int32_t* __restrict__ row_pair, int32_t* __restrict__ active,
+                    int32_t* __restrict__ sh_off, int32_t* __restrict__ sh_rows,
+                    int32_t* __restrict__ sh_active, int32_t* __restrict__ tile_off,
+                    int32_t* __restrict__ counters, int n_counters) {
+  __shared__ int32_t s_idx[kTinyPairs];
+  __shared__ int32_t s_cnt[kMaxExperts];
+  griddep_wait();
+  griddep_trigger();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int P = T * k;
+  for (int t = warp; t < T; t += (int)(blockDim.x >> 5)) {
+    int idx;
+    float w;
+    warp_topk<EPL>(part, KS, bias, T, E, k, t, lane, idx, w);
+    if (lane < k) {
+      topk_idx[(size_t)t * k + lane] = idx;
+      topk_w[(size_t)t * k + lane] = w;
+      s_idx[t * k + lane] = idx;
+    }
+  }
+  for (int e = tid; e < E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  if (warp != 0) return;  // no block-wide barrier follows
+  constexpr unsigned kAll = 0xffffffffu;
+  // this lane's pairs: q = lane and lane + 32; key (expert, q) is unique
+  const int q0 = lane, q1 = lane + 32;
+  const int e0 = q0 < P ? s_idx[q0] : -1, e1 = q1 < P ? s_idx[q1] : -1;
+  const int key0 = e0 >= 0 ? e0 * kTinyPairs + q0 : INT_MAX;
+  const int key1 = e1 >= 0 ? e1 * kTinyPairs + q1 : INT_MAX;
+  int r0 = 0, r1 = 0;
+#pragma unroll 4
+  for (int src = 0; src < 32; ++src) {
+    const int a = __shfl_sync(kAll, key0, src), b = __shfl_sync(kAll, key1, src);
+    r0 += (a < key0) + (b < key0);
+    r1 += (a < key1) + (b < key1);
+  }
+  if (e0 >= 0) {
+    atomicAdd(&s_cnt[e0], 1);
+    row_token[r0] = q0 / k;
+    tok_slot_row[q0] = r0;
+    if (row_pair) row_pair[r0] = q0;
+  }
+  if (e1 >= 0) {
+    atomicAdd(&s_cnt[e1], 1);
+    row_token[r1] = q1 / k;
+    tok_slot_row[q1] = r1;
+    if (row_pair) row_pair[r1] = q1;
+  }
+  __syncwarp();
+  // lane l owns experts [l B, l B + B): sums, then exclusive scans over lanes
+  const int B = (E + 31) / 32;
+  int tot = 0, act = 0;
+  for (int i = 0; i < B; ++i) {
+    const int e = lane * B + i;
+    if (e < E) {
+      tot += s_cnt[e];
+      act += s_cnt[e] > 0 ? 1 : 0;
+    }
+  }
+  int it = tot, ia = act;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int vt = __shfl_up_sync(kAll, it, o), va = __shfl_up_sync(kAll, ia, o);
+    if (lane >= o) {
+      it += vt;
+      ia += va;
+    }
+  }
+  int off = it - tot, ai = ia - act;
+  for (int i = 0; i < B; ++i) {
+    const int e = lane * B + i;
+    if (e < E) {
+      expert_off[e] = off;
+      if (tile_off) tile_off[e] = ai;  // one token tile per hit expert
+      if (s_cnt[e] > 0) active[1 + ai++] = e;
+      off += s_cnt[e];
+    }
+  }
+  if (lane == 31) {
+    expert_off[E] = it;
+    active[0] = ia;
+    if (tile_off) tile_off[E] = ia;
+  }
+  if (sh_rows) {  // shared expert: every token, in order
+    for (int t = lane; t < T; t += 32) sh_rows[t] = t;
+    if (lane == 0) {
+      sh_off[0] = 0;
+      sh_off[1] = T;
+      sh_active[0] = T > 0 ? 1 : 0;
+      sh_active[1] = 0;
+    }
+  }
+  // the expert kernels' counters of this call start at zero
+  if (counters)
+    for (int i = lane; i < n_counters; i += 32) counters[i] = 0;
+}
+
 int route_kslices(int T, int H, int E) {
   if (router_tc_ok(T, H, E)) {
     // tensor-core path: split K until the CTAs fill about one wave
@@ -523,6 +637,20 @@ cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const
     return launch_k(k_topk_permute_small<0>, dim3(1), dim3(1024), smem, s, pdl, part, KS, bias,
                     T, E, k, topk_idx, topk_w, expert_off, row_token, tok_slot_row, row_pair,
                     active, sh_off, sh_rows, sh_active, tile_off, counters, n_counters);
+  }
+  if ((long long)T * k <= kTinyPairs) {
+    const dim3 blk(32 * T);  // T < kSplitTopkTokens: at most 480 threads
+#define MOE_TINY(EPLV)                                                                        \
+  return launch_k(k_topk_permute_tiny<EPLV>, dim3(1), blk, 0, s, pdl, part, KS, bias, T, E, k, \
+                  topk_idx, topk_w, expert_off, row_token, tok_slot_row, row_pair, active,     \
+                  sh_off, sh_rows, sh_active, tile_off, counters, n_counters)
+    if (epl <= 1) MOE_TINY(1);
+    if (epl <= 2) MOE_TINY(2);
+    if (epl <= 4) MOE_TINY(4);
+    if (epl <= 8) MOE_TINY(8);
+    if (epl <= 16) MOE_TINY(16);
+    MOE_TINY(32);
+#undef MOE_TINY
   }
 #define MOE_SMALL(EPLV)                                                                      \
   do {                                                                                       \

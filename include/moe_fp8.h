@@ -215,7 +215,12 @@ moe_status moe_combine(const float* y_perm, const int32_t* tok_slot_row,
  * row per routed expert on average (T*k >= E) when H*I >= 2^20, else from
  * 32 rows per expert; the shared expert: from 32 tokens.  The
  * environment variable MOE_FP8_EXPERT_PATH=gemm or =gemv overrides the choice
- * (diagnostics and tests; read on every call).
+ * (diagnostics and tests; read on every call).  Two more diagnostic
+ * variables, read on every call of the tensor-core GEMM, exist to test the
+ * failure path: MOE_FP8_WAIT_LIMIT_US shortens its bounded device waits
+ * (default 2 s), and MOE_FP8_TEST_STALL=down makes its down projection wait
+ * for one more finished gate/up tile than exists, so that the wait runs out
+ * and MOE_DEV_WAIT_TIMEOUT is set (the output is then not valid).
  */
 moe_status moe_layer_forward(const uint16_t* x, const float* Wr,
                              const float* bias, moe_fp8_ffn routed,
