@@ -68,6 +68,8 @@ _SIGNATURES = {
     "moe_combine": (_st, [_vp, _vp, _vp, _vp, Dims, _vp, _vp]),
     "moe_layer_forward": (_st, [_vp, _vp, _vp, Fp8Ffn, ctypes.POINTER(Fp8Ffn), Dims, _vp, _vp,
                                 _vp, _vp, _sz, _vp]),
+    "moe_layer_forward_gated": (_st, [_vp, _vp, _vp, Fp8Ffn, ctypes.POINTER(Fp8Ffn), _vp, Dims,
+                                      _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_read_device_status": (_st, [_vp, ctypes.POINTER(ctypes.c_int32), _vp]),
     "moe_permute_static_scratch": (_st, [_vp, Dims, _vp, _vp, _vp, _vp]),
 }
@@ -194,6 +196,14 @@ def moe_layer_forward(x, Wr, bias, routed: Fp8Ffn, shared: Optional[Fp8Ffn], d: 
     _check(lib().moe_layer_forward(_ptr(x), _ptr(Wr), _ptr(bias), routed, sh, d, _ptr(out),
                                    _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(ws), _nbytes(ws),
                                    _stream(stream)), "moe_layer_forward")
+
+
+def moe_layer_forward_gated(x, Wr, bias, routed: Fp8Ffn, shared: Fp8Ffn, shared_gate, d: Dims,
+                            out, topk_idx_out, topk_w_out, ws, stream=None) -> None:
+    _check(lib().moe_layer_forward_gated(_ptr(x), _ptr(Wr), _ptr(bias), routed,
+                                         ctypes.byref(shared), _ptr(shared_gate), d, _ptr(out),
+                                         _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(ws),
+                                         _nbytes(ws), _stream(stream)), "moe_layer_forward_gated")
 
 
 def moe_read_device_status(ws, stream=None) -> int:

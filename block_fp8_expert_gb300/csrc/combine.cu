@@ -27,13 +27,14 @@ k_combine(const float* __restrict__ y_perm, const int32_t* __restrict__ tok_slot
 // fmaf(w 2^s, y'', r): w 2^s is exact, so this rounds w y + r once, the
 // same arithmetic as an fp32 y; the shared row (y''_s 2^s_s, exact) comes
 // first, then the slots in order j, eight rows in flight at a time, one bf16
-// rounding.  yexp is [H / 32][P], syexp [H / 32][T].
+// rounding.  yexp is [H / 32][P], syexp [H / 32][sstride].
 template <int KMAX>
 __global__ void __launch_bounds__(256)
 k_combine_layer(const uint16_t* __restrict__ y, const int16_t* __restrict__ yexp, int P,
                 const int32_t* __restrict__ tok_slot_row, const float* __restrict__ topk_w,
-                const uint16_t* __restrict__ sy, const int16_t* __restrict__ syexp, int T, int H,
-                int k, uint16_t* __restrict__ out) {
+                const uint16_t* __restrict__ sy, const int16_t* __restrict__ syexp, int sstride,
+                const float* __restrict__ sgate, int T, int H, int k,
+                uint16_t* __restrict__ out) {
   const int HV = H / 8;
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long long)T * HV) return;
@@ -52,7 +53,8 @@ k_combine_layer(const uint16_t* __restrict__ y, const int16_t* __restrict__ yexp
   for (int v = 0; v < 8; ++v) acc[v] = r[v] = 0.f;
   if (sy) {
     load_v(sy + (size_t)t * H + h, acc);
-    const float f = ldexp2f(1.f, syexp[(size_t)grp * T + t]);
+    float f = ldexp2f(1.f, syexp[(size_t)grp * sstride + t]);
+    if (sgate) f *= sgate[t];  // gated shared expert
 #pragma unroll
     for (int v = 0; v < 8; ++v) acc[v] *= f;  // exact unless it leaves fp32's range
   }
@@ -89,19 +91,20 @@ k_combine_layer(const uint16_t* __restrict__ y, const int16_t* __restrict__ yexp
 
 cudaError_t launch_combine_layer(const uint16_t* y, const int16_t* yexp, int P,
                                  const int32_t* tok_slot_row, const float* topk_w,
-                                 const uint16_t* sy, const int16_t* syexp, int T, int H, int k,
-                                 uint16_t* out, cudaStream_t s) {
+                                 const uint16_t* sy, const int16_t* syexp, int sstride,
+                                 const float* sgate, int T, int H, int k, uint16_t* out,
+                                 cudaStream_t s) {
   const long long n = (long long)T * (H / 8);
   if (n == 0) return cudaSuccess;
   const dim3 grid((unsigned)((n + 255) / 256)), blk(256);
   if (k <= 8)
     return launch_k(k_combine_layer<8>, grid, blk, 0, s, true, y, yexp, P, tok_slot_row, topk_w,
-                    sy, syexp, T, H, k, out);
+                    sy, syexp, sstride, sgate, T, H, k, out);
   if (k <= 16)
     return launch_k(k_combine_layer<16>, grid, blk, 0, s, true, y, yexp, P, tok_slot_row, topk_w,
-                    sy, syexp, T, H, k, out);
+                    sy, syexp, sstride, sgate, T, H, k, out);
   return launch_k(k_combine_layer<32>, grid, blk, 0, s, true, y, yexp, P, tok_slot_row, topk_w, sy,
-                  syexp, T, H, k, out);
+                  syexp, sstride, sgate, T, H, k, out);
 }
 
 cudaError_t launch_combine(const float* y_perm, const int32_t* tok_slot_row, const float* topk_w,

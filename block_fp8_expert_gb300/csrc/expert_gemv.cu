@@ -58,26 +58,32 @@ k_gateup_stream(const uint16_t* __restrict__ xn, const int8_t* __restrict__ xe, 
                 const uint8_t* __restrict__ gcodes, const float* __restrict__ gscales,
                 const uint8_t* __restrict__ ucodes, const float* __restrict__ uscales,
                 uint16_t* __restrict__ hid, int8_t* __restrict__ hexp,
-                int32_t* __restrict__ status) {
+                int32_t* __restrict__ status, const SharedExpert sx) {
   extern __shared__ uint4 wbuf[];  // [kGuChunks * 4][kThreads]
   __shared__ float red[8][NT][2][4][32];
   __shared__ int tok[NT * 8];
   griddep_wait();
   griddep_trigger();
-  const int a = blockIdx.y;
-  if (a >= active[0]) return;
-  const int e = active[1 + a];
+  // the last CTA column is the shared expert when there is one
+  const bool shared = sx.gc != nullptr && blockIdx.y == gridDim.y - 1;
+  int e = 0;
+  if (!shared) {
+    const int a = blockIdx.y;
+    if (a >= active[0]) return;
+    e = active[1 + a];
+  }
   const int i0 = blockIdx.x * 16;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
   const int nch = H / 64;
   const int nHb = cdiv(H, kScaleBlock);
   const size_t wrow = ((size_t)e * I + i0 + g) * H;
-  const uint8_t* gp = gcodes + wrow + 16 * c;
-  const uint8_t* up = ucodes + wrow + 16 * c;
+  const uint8_t* gp = (shared ? sx.gc : gcodes) + wrow + 16 * c;
+  const uint8_t* up = (shared ? sx.uc : ucodes) + wrow + 16 * c;
   const size_t r8 = (size_t)8 * H;
-  const float* gs = gscales + ((size_t)e * cdiv(I, kScaleBlock) + i0 / kScaleBlock) * nHb;
-  const float* us = uscales + ((size_t)e * cdiv(I, kScaleBlock) + i0 / kScaleBlock) * nHb;
+  const size_t srow = ((size_t)e * cdiv(I, kScaleBlock) + i0 / kScaleBlock) * nHb;
+  const float* gs = (shared ? sx.gs : gscales) + srow;
+  const float* us = (shared ? sx.us : uscales) + srow;
   bool bad = false;  // an infinite or NaN input or result
   // All weight copies of one K-group (2048 columns of H).
   auto issue = [&](int kg) {
@@ -97,12 +103,13 @@ k_gateup_stream(const uint16_t* __restrict__ xn, const int8_t* __restrict__ xe, 
   // The first K-group's weights depend only on the expert: start them before
   // the expert's rows and tokens are read.
   issue(0);
-  const int r0 = expert_off[e];
-  const int ne = expert_off[e + 1] - r0;
+  const int r0 = shared ? sx.row0 : expert_off[e];
+  const int ne = shared ? sx.T : expert_off[e + 1] - r0;
   bool issued = true;
 
   for (int n0 = 0; n0 < ne; n0 += NT * 8) {
-    if (tid < NT * 8) tok[tid] = (n0 + tid < ne) ? row_token[r0 + n0 + tid] : -1;
+    if (tid < NT * 8)
+      tok[tid] = (n0 + tid < ne) ? (shared ? n0 + tid : row_token[r0 + n0 + tid]) : -1;
     __syncthreads();
     int trow[NT];
 #pragma unroll
@@ -242,7 +249,7 @@ k_down_stream(const uint16_t* __restrict__ hid, const int8_t* __restrict__ hexp,
               const int32_t* __restrict__ expert_off, const int32_t* __restrict__ active,
               const uint8_t* __restrict__ dcodes, const float* __restrict__ dscales,
               void* __restrict__ y, int16_t* __restrict__ yexp, int y_rows,
-              int32_t* __restrict__ status, const FusedCombine cmb) {
+              int32_t* __restrict__ status, const FusedCombine cmb, const SharedExpert sx) {
   extern __shared__ uint4 wbuf[];  // [kDnChunks * 2][kThreads]
   __shared__ float red[4][2][NT][4][32];
   __shared__ int is_last;
@@ -251,18 +258,24 @@ k_down_stream(const uint16_t* __restrict__ hid, const int8_t* __restrict__ hexp,
   // griddep_wait; they and the weights are read before this kernel waits for
   // gate/up, so the first K-group's weights stream while gate/up finishes.
   // Everything gate/up writes (hid and its exponents) is read after the wait.
-  const int a = blockIdx.y;
-  if (a >= active[0]) return;
-  const int e = active[1 + a];
+  // the last CTA column is the shared expert when there is one
+  const bool shared = sx.gc != nullptr && blockIdx.y == gridDim.y - 1;
+  int e = 0;
+  if (!shared) {
+    const int a = blockIdx.y;
+    if (a >= active[0]) return;
+    e = active[1 + a];
+  }
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
   const int mt = warp & 1, kp = warp >> 1;
   const int h0 = blockIdx.x * 32 + mt * 16;
   const int nch = I / 64;
   const int nIb = cdiv(I, kScaleBlock);
-  const uint8_t* dp = dcodes + ((size_t)e * H + h0 + g) * I + 16 * c;
+  const uint8_t* dp = (shared ? sx.dc : dcodes) + ((size_t)e * H + h0 + g) * I + 16 * c;
   const size_t r8 = (size_t)8 * I;
-  const float* ds = dscales + ((size_t)e * cdiv(H, kScaleBlock) + h0 / kScaleBlock) * nIb;
+  const float* ds = (shared ? sx.ds : dscales) +
+                    ((size_t)e * cdiv(H, kScaleBlock) + h0 / kScaleBlock) * nIb;
   bool bad = false;
   // All weight copies of one K-group (768 columns of I).
   auto issue = [&](int kg) {
@@ -281,8 +294,8 @@ k_down_stream(const uint16_t* __restrict__ hid, const int8_t* __restrict__ hexp,
   issue(0);
   griddep_wait();
   griddep_trigger();
-  const int r0 = expert_off[e];
-  const int ne = expert_off[e + 1] - r0;
+  const int r0 = shared ? sx.row0 : expert_off[e];
+  const int ne = shared ? sx.T : expert_off[e + 1] - r0;
   bool issued = true;
 
   for (int n0 = 0; n0 < ne; n0 += NT * 8) {
@@ -395,7 +408,8 @@ k_down_stream(const uint16_t* __restrict__ hid, const int8_t* __restrict__ hexp,
       __syncthreads();
       if (tid == 0) {
         __threadfence();
-        is_last = atomicAdd(&cmb.ticket[blockIdx.x], 1) == active[0] - 1;
+        const int ctas = active[0] + (sx.gc ? 1 : 0);  // the slice's CTAs of this launch
+        is_last = atomicAdd(&cmb.ticket[blockIdx.x], 1) == ctas - 1;
         __threadfence();
       }
       __syncthreads();
@@ -414,9 +428,20 @@ k_down_stream(const uint16_t* __restrict__ hid, const int8_t* __restrict__ hexp,
             ys[j] = 0;
           }
         }
-        float r[8];
+        float r[8], acc[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) r[i] = 0.f;
+        for (int i = 0; i < 8; ++i) r[i] = acc[i] = 0.f;
+        if (sx.gc) {
+          // the shared expert's row (weight 1, exact), first
+          const size_t srow = (size_t)sx.row0 + t;
+          const uint4 sr = __ldcg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(y) +
+                                                                 srow * H + h));
+          float f = ldexp2f(1.f, __ldcg(yexp + (size_t)blockIdx.x * y_rows + srow));
+          if (cmb.sgate) f *= cmb.sgate[t];  // gated shared expert
+          unpack_f16x8(sr, acc);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] *= f;
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           if (row[j] < 0) continue;
@@ -429,7 +454,8 @@ k_down_stream(const uint16_t* __restrict__ hid, const int8_t* __restrict__ hexp,
         }
         uint32_t o4[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) o4[i] = pack_bf16x2(0.f + r[2 * i], 0.f + r[2 * i + 1]);
+        for (int i = 0; i < 4; ++i)
+          o4[i] = pack_bf16x2(acc[2 * i] + r[2 * i], acc[2 * i + 1] + r[2 * i + 1]);
         *reinterpret_cast<uint4*>(cmb.out + (size_t)t * H + h) =
             make_uint4(o4[0], o4[1], o4[2], o4[3]);
       }
@@ -483,26 +509,27 @@ cudaError_t launch_expert_gemv(const uint16_t* xn, const int8_t* xe, const int32
                                const moe_fp8_ffn& w, int H, int I, int tokens_per_expert_hint,
                                uint16_t* hid, int8_t* hexp, void* y, int16_t* yexp, int y_rows,
                                int32_t* status, cudaStream_t s, bool pdl,
-                               const FusedCombine& cmb) {
-  if (max_active <= 0) return cudaSuccess;
-  if (cmb.ticket && (!yexp || !fused_combine_ok(cmb.T, cmb.k, H, max_active)))
+                               const FusedCombine& cmb, const SharedExpert& sx) {
+  const int cols = max_active + (sx.gc ? 1 : 0);  // CTA columns: experts (+ the shared one)
+  if (cols <= 0) return cudaSuccess;
+  if (cmb.ticket && (!yexp || !fused_combine_ok(cmb.T, cmb.k, H, cols)))
     return cudaErrorInvalidValue;
   cudaError_t e;
   const bool nt1 = tokens_per_expert_hint <= 8;
   const dim3 block(kThreads);
-  const dim3 g1(I / 16, max_active), g2(H / 32, max_active);
+  const dim3 g1(I / 16, cols), g2(H / 32, cols);
   auto down = [&](auto kern) -> cudaError_t {
     cudaError_t err = ensure_smem((const void*)kern, kDnSmem);
     if (err != cudaSuccess) return err;
     return launch_k(kern, g2, block, kDnSmem, s, pdl, (const uint16_t*)hid, (const int8_t*)hexp,
                     H, I, expert_off, active, w.down.codes, w.down.scales, y, yexp, y_rows,
-                    status, cmb);
+                    status, cmb, sx);
   };
   if (nt1) {
     if ((e = ensure_smem((const void*)k_gateup_stream<1>, kGuSmem)) != cudaSuccess) return e;
     e = launch_k(k_gateup_stream<1>, g1, block, kGuSmem, s, pdl, xn, xe, H, I, expert_off,
                  row_token, active, w.gate.codes, w.gate.scales, w.up.codes, w.up.scales, hid,
-                 hexp, status);
+                 hexp, status, sx);
     if (e != cudaSuccess) return e;
     if (cmb.ticket) return down(k_down_stream<1, true, true>);
     return yexp ? down(k_down_stream<1, true>) : down(k_down_stream<1, false>);
@@ -510,7 +537,7 @@ cudaError_t launch_expert_gemv(const uint16_t* xn, const int8_t* xe, const int32
   if ((e = ensure_smem((const void*)k_gateup_stream<2>, kGuSmem)) != cudaSuccess) return e;
   e = launch_k(k_gateup_stream<2>, g1, block, kGuSmem, s, pdl, xn, xe, H, I, expert_off,
                row_token, active, w.gate.codes, w.gate.scales, w.up.codes, w.up.scales, hid, hexp,
-               status);
+               status, sx);
   if (e != cudaSuccess) return e;
   if (cmb.ticket) return down(k_down_stream<2, true, true>);
   return yexp ? down(k_down_stream<2, true>) : down(k_down_stream<2, false>);

@@ -191,14 +191,18 @@ WsLayout ws_layout(const moe_dims& d) {
   L.xe = take(T * (H / 64));
   // hid and y rows in fp16 with power-of-two exponents: hid per 16 features
   // (streamed GEMV), y per 32 columns, the exponent tables [H / 32][rows]
-  L.hid = take(P * I * 2);
-  L.hexp = take(P * (I / 16));
-  L.y_perm = take(P * H * 2);
-  L.yexp = take((H / 32) * P * 2);
+  // (P + T rows with a shared expert: the streamed GEMV may run it as one
+  // more expert of the same launches, rows P .. P + T - 1)
+  const size_t R = P + (Is ? T : 0);
+  L.hid = take(R * I * 2);
+  L.hexp = take(R * (I / 16));
+  L.y_perm = take(R * H * 2);
+  L.yexp = take((H / 32) * R * 2);
   L.sh_hid = take(Is ? T * Is * 2 : 0);
   L.sh_hexp = take(Is ? T * (Is / 16) : 0);
   L.sh_y = take(Is ? T * H * 2 : 0);
   L.sh_yexp = take(Is ? (H / 32) * T * 2 : 0);
+  L.sgate = take(Is ? T * 4 : 0);  // gated shared expert: sigmoid(x . g) per token
   L.sh_off = take(2 * 4);
   L.sh_rows = take(Is ? T * 4 : 0);
   L.sh_active = take(2 * 4);
@@ -376,10 +380,16 @@ moe_status moe_combine(const float* y_perm, const int32_t* tok_slot_row, const f
   return MOE_OK;
 }
 
-moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bias,
-                             moe_fp8_ffn routed, const moe_fp8_ffn* shared, moe_dims d,
-                             uint16_t* out, int32_t* topk_idx_out, float* topk_w_out, void* ws,
-                             size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace moe {
+namespace {
+// The layer call, with an optional gate vector for the shared expert.
+moe_status layer_forward(const uint16_t* x, const float* Wr, const float* bias,
+                         moe_fp8_ffn routed, const moe_fp8_ffn* shared,
+                         const float* shared_gate, moe_dims d, uint16_t* out,
+                         int32_t* topk_idx_out, float* topk_w_out, void* ws, size_t ws_bytes,
+                         void* stream) {
   moe_status s;
   if ((s = check_dims(d)) != MOE_OK) return s;
   if (d.T == 0) return MOE_OK;  // no token: nothing is read or written
@@ -396,6 +406,7 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
   } else if (shared) {
     return fail(MOE_ERR_INVALID_ARG, "shared given but I_shared == 0");
   }
+  REQUIRE_OPT_PTR(shared_gate);
   if ((s = check_ws(d, ws, ws_bytes)) != MOE_OK) return s;
   const WsLayout L = ws_layout(d);
   cudaStream_t st = (cudaStream_t)stream;
@@ -419,13 +430,20 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
   const bool small = small_route_permute_ok(d.T, d.E, d.k);
   // streamed GEMV, one-CTA permutation, no shared expert: the down kernel
   // also combines (its tickets cleared by the permutation)
-  const bool fuse_combine =
-      !gemm && small && !has_shared && fused_combine_ok(d.T, d.k, d.H, d.E < P ? d.E : P);
   const bool shared_gemm = has_shared && use_expert_gemm(d.T, 1, d.H, d.I_shared);
+  // The shared expert as one more expert of the routed GEMV launches (rows
+  // P .. P + T - 1), when both run on the GEMV and their I match.
+  const bool fused_shared = has_shared && !gemm && !shared_gemm && d.I_shared == d.I;
+  const bool sep_shared = has_shared && !fused_shared;  // its own launches
+  const int y_rows = P + (has_shared ? d.T : 0);  // rows of y_perm / yexp
+  const int max_active = d.E < P ? d.E : P;
+  const bool fuse_combine = !gemm && small && (!has_shared || fused_shared) &&
+                            fused_combine_ok(d.T, d.k, d.H, max_active + (fused_shared ? 1 : 0));
   // the router writes the streamed kernels' activations when one runs
   const bool need_xn = !gemm || (has_shared && !shared_gemm);
   uint16_t* xn = need_xn ? at<uint16_t>(ws, L.xn) : nullptr;
   int8_t* xe = need_xn ? at<int8_t>(ws, L.xe) : nullptr;
+  float* sgate = shared_gate ? at<float>(ws, L.sgate) : nullptr;
   if (small) {
     // router logits, then top-k + permutation (+ the shared expert's identity
     // permutation) in one CTA
@@ -433,24 +451,25 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
                    x, Wr, bias, d.T, d.H, d.E, d.k, at<float>(ws, L.logits),
                    at<uint16_t>(ws, L.wr_planes), idx, w, off,
                    row_token, tok_slot_row, at<int32_t>(ws, L.row_pair), active,
-                   has_shared ? soff : nullptr, has_shared ? srows : nullptr,
-                   has_shared ? sact : nullptr, xn, xe,
+                   sep_shared ? soff : nullptr, sep_shared ? srows : nullptr,
+                   sep_shared ? sact : nullptr, xn, xe,
                    gemm ? at<int32_t>(ws, L.tile_off) : nullptr,
                    gemm ? at<int32_t>(ws, L.slot_done)
                         : (fuse_combine ? at<int32_t>(ws, L.ticket) : nullptr),
                    gemm ? expert_gemm_slots(P, d.E) : d.H / 32,
-                   status, st, true),
+                   status, st, true, shared_gate, sgate),
                "moe_layer_forward: route+permute");
   } else {
     CUDA_CHECK(launch_route(x, Wr, bias, d.T, d.H, d.E, d.k, at<float>(ws, L.logits),
-                            at<uint16_t>(ws, L.wr_planes), idx, w, xn, xe, status, st, true),
+                            at<uint16_t>(ws, L.wr_planes), idx, w, xn, xe, status, st, true,
+                            shared_gate, sgate),
                "moe_layer_forward: route");
     CUDA_CHECK(launch_permute(idx, d.T, d.E, d.k, at<int32_t>(ws, L.rank),
                               at<int32_t>(ws, L.block_cnt), at<int32_t>(ws, L.block_base), off,
                               row_token, tok_slot_row, at<int32_t>(ws, L.row_pair), active,
                               status, st, true),
                "moe_layer_forward: permute");
-    if (has_shared)
+    if (sep_shared)
       CUDA_CHECK(launch_identity_perm(d.T, soff, srows, sact, st, true),
                  "moe_layer_forward: shared");
   }
@@ -472,8 +491,8 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
     CUDA_CHECK(launch_expert_gemm_tc(x, d.T, off, row_token, at<uint16_t>(ws, L.x_perm),
                                      at<int32_t>(ws, L.xexp), d.E, P, routed, d.H, d.I,
                                      at<int32_t>(ws, L.tile_off), at<int32_t>(ws, L.slot_done),
-                                     at<uint16_t>(ws, L.hid), y_perm, yexp, P, status, st, true,
-                                     /*tile_off_ready=*/small, gth),
+                                     at<uint16_t>(ws, L.hid), y_perm, yexp, y_rows, status, st,
+                                     true, /*tile_off_ready=*/small, gth),
                "moe_layer_forward: experts");
   } else {
     FusedCombine cmb;
@@ -484,16 +503,32 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
       cmb.T = d.T;
       cmb.k = d.k;
       cmb.out = out;
+      cmb.sgate = sgate;
     }
-    CUDA_CHECK(launch_expert_gemv(xn, xe, off, row_token, active, d.E < P ? d.E : P, routed,
-                                  d.H, d.I, cdiv(P, d.E), at<uint16_t>(ws, L.hid),
-                                  at<int8_t>(ws, L.hexp), y_perm, yexp, P, status, st, true,
-                                  cmb),
+    SharedExpert sx;
+    if (fused_shared) {
+      sx.gc = shared->gate.codes;
+      sx.gs = shared->gate.scales;
+      sx.uc = shared->up.codes;
+      sx.us = shared->up.scales;
+      sx.dc = shared->down.codes;
+      sx.ds = shared->down.scales;
+      sx.T = d.T;
+      sx.row0 = P;
+    }
+    CUDA_CHECK(launch_expert_gemv(xn, xe, off, row_token, active, max_active, routed, d.H, d.I,
+                                  cdiv(P, d.E), at<uint16_t>(ws, L.hid), at<int8_t>(ws, L.hexp),
+                                  y_perm, yexp, y_rows, status, st, true, cmb, sx),
                "moe_layer_forward: experts");
   }
   uint16_t* shared_y = nullptr;
   int16_t* shared_yexp = nullptr;
-  if (has_shared) {
+  int shared_stride = d.T;
+  if (fused_shared) {
+    shared_y = y_perm + (size_t)P * d.H;
+    shared_yexp = yexp + P;
+    shared_stride = y_rows;
+  } else if (has_shared) {
     shared_y = at<uint16_t>(ws, L.sh_y);
     shared_yexp = at<int16_t>(ws, L.sh_yexp);
     if (shared_gemm) {
@@ -513,10 +548,35 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bi
                  "moe_layer_forward: shared expert");
   }
   if (!fuse_combine)
-    CUDA_CHECK(launch_combine_layer(y_perm, yexp, P, tok_slot_row, w, shared_y, shared_yexp, d.T,
-                                    d.H, d.k, out, st),
+    CUDA_CHECK(launch_combine_layer(y_perm, yexp, y_rows, tok_slot_row, w, shared_y,
+                                    shared_yexp, shared_stride, sgate, d.T, d.H, d.k, out, st),
                "moe_layer_forward: combine");
   return MOE_OK;
+}
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
+moe_status moe_layer_forward(const uint16_t* x, const float* Wr, const float* bias,
+                             moe_fp8_ffn routed, const moe_fp8_ffn* shared, moe_dims d,
+                             uint16_t* out, int32_t* topk_idx_out, float* topk_w_out, void* ws,
+                             size_t ws_bytes, void* stream) {
+  return layer_forward(x, Wr, bias, routed, shared, nullptr, d, out, topk_idx_out, topk_w_out,
+                       ws, ws_bytes, stream);
+}
+
+moe_status moe_layer_forward_gated(const uint16_t* x, const float* Wr, const float* bias,
+                                   moe_fp8_ffn routed, const moe_fp8_ffn* shared,
+                                   const float* shared_gate, moe_dims d, uint16_t* out,
+                                   int32_t* topk_idx_out, float* topk_w_out, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  if (check_dims(d) != MOE_OK) return check_dims(d);
+  if (d.I_shared == 0 || !shared)
+    return fail(MOE_ERR_INVALID_ARG, "the gated layer needs a shared expert (I_shared > 0)");
+  if (!shared_gate) return fail(MOE_ERR_INVALID_ARG, "shared_gate is NULL");
+  return layer_forward(x, Wr, bias, routed, shared, shared_gate, d, out, topk_idx_out,
+                       topk_w_out, ws, ws_bytes, stream);
 }
 
 moe_status moe_read_device_status(const void* ws, int32_t* status, void* stream) {

@@ -61,7 +61,8 @@ int num_sms();
 // Workspace layout for one set of dims (byte offsets, each 256-aligned).
 struct WsLayout {
   size_t status, logits, rank, block_cnt, block_base, active, idx, w, off, row_token,
-      tok_slot_row, row_pair, xn, xe, hid, hexp, y_perm, yexp, sh_hid, sh_hexp, sh_y, sh_yexp, sh_off,
+      tok_slot_row, row_pair, xn, xe, hid, hexp, y_perm, yexp, sh_hid, sh_hexp, sh_y, sh_yexp,
+      sgate, sh_off,
       sh_rows, sh_active, tile_off, sh_tile_off, x_perm, xexp, sh_x, sh_xexp, wr_planes,
       slot_done, sh_slot_done, ticket, total;
 };
@@ -78,7 +79,8 @@ WsLayout ws_layout(const moe_dims& d);
 cudaError_t launch_route(const uint16_t* x, const float* Wr, const float* bias, int T, int H,
                          int E, int k, float* part, uint16_t* planes, int32_t* topk_idx,
                          float* topk_w, uint16_t* xn, int8_t* xe, int32_t* status,
-                         cudaStream_t s, bool pdl);
+                         cudaStream_t s, bool pdl, const float* shared_gate = nullptr,
+                         float* sgate = nullptr);
 
 // Router logits on the tensor cores (route_tc.cu): T >= 128, E % 128 == 0,
 // H % 64 == 0.  Writes KS slices of partial logits (KS from route_kslices).
@@ -89,6 +91,9 @@ cudaError_t launch_router_logits_tc(const uint16_t* x, const float* Wr, int T, i
 
 // Token rows per tile of the tensor-core GEMM (its MMA N, at most).
 constexpr int kGemmTokenTile = 128;
+
+// Both route launchers: with sgate set, the top-k warps also write
+// sgate[t] = sigmoid(x[t] . shared_gate) (the gated shared expert's factor).
 
 // Router logits, then top-k and the full permutation in one CTA, for
 // T*k <= 4096 (small_route_permute_ok).  sh_* may be NULL (no shared expert).
@@ -104,7 +109,9 @@ cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const
                                        int32_t* sh_rows, int32_t* sh_active, uint16_t* xn,
                                        int8_t* xe, int32_t* tile_off, int32_t* counters,
                                        int n_counters,
-                                       int32_t* status, cudaStream_t s, bool pdl);
+                                       int32_t* status, cudaStream_t s, bool pdl,
+                                       const float* shared_gate = nullptr,
+                                       float* sgate = nullptr);
 
 cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, int32_t* rank,
                            int32_t* block_cnt, int32_t* block_base, int32_t* expert_off,
@@ -137,15 +144,26 @@ struct FusedCombine {
   int32_t* ticket = nullptr;
   const int32_t* tok_slot_row = nullptr;
   const float* topk_w = nullptr;
+  const float* sgate = nullptr;  // the shared expert's per-token factor, or NULL
   int T = 0, k = 0;
   uint16_t* out = nullptr;
+};
+// The shared expert as one more, always-selected expert of the same GEMV
+// launches (the last CTA column of each grid): rows row0 .. row0 + T - 1 of
+// hid and y hold tokens 0 .. T - 1, and its weights are these (one expert
+// with the routed experts' I).  gc == NULL: no shared expert.
+struct SharedExpert {
+  const uint8_t *gc = nullptr, *uc = nullptr, *dc = nullptr;
+  const float *gs = nullptr, *us = nullptr, *ds = nullptr;
+  int T = 0, row0 = 0;
 };
 cudaError_t launch_expert_gemv(const uint16_t* xn, const int8_t* xe, const int32_t* expert_off,
                                const int32_t* row_token, const int32_t* active, int max_active,
                                const moe_fp8_ffn& w, int H, int I, int tokens_per_expert_hint,
                                uint16_t* hid, int8_t* hexp, void* y, int16_t* yexp, int y_rows,
                                int32_t* status, cudaStream_t s, bool pdl,
-                               const FusedCombine& cmb = FusedCombine{});
+                               const FusedCombine& cmb = FusedCombine{},
+                               const SharedExpert& sx = SharedExpert{});
 
 // Grouped GEMM on the tensor cores (tcgen05) for many tokens per expert:
 // gate/up + SwiGLU -> hid, then down -> y.  Needs H % 256 == 0 and
@@ -197,10 +215,13 @@ cudaError_t launch_combine(const float* y_perm, const int32_t* tok_slot_row, con
 // rows sy [T, H] with syexp [H/32][T] (both NULL without a shared expert).
 // The slot rows and weights, which the routing wrote before any expert
 // kernel ran, are loaded before the kernel waits for the expert outputs.
+// yexp's row stride is P, syexp's sstride; sgate (may be NULL) scales the
+// shared row per token.
 cudaError_t launch_combine_layer(const uint16_t* y, const int16_t* yexp, int P,
                                  const int32_t* tok_slot_row, const float* topk_w,
-                                 const uint16_t* sy, const int16_t* syexp, int T, int H, int k,
-                                 uint16_t* out, cudaStream_t s);
+                                 const uint16_t* sy, const int16_t* syexp, int sstride,
+                                 const float* sgate, int T, int H, int k, uint16_t* out,
+                                 cudaStream_t s);
 
 // Device address of the status word of moe_permute_static_scratch's fixed
 // array on the current device.

@@ -241,10 +241,45 @@ __device__ __forceinline__ void warp_topk(const float* __restrict__ part, int KS
   my_w = ex / s;
 }
 
+// Gated shared expert: sigmoid(x[t] . g) for token t by one warp (H % 8 ==
+// 0), fp32 products summed per lane in order, then over the lanes; lane 0's
+// value is the result (returned in every lane).
+__device__ __forceinline__ float warp_shared_gate(const uint16_t* __restrict__ x,
+                                                  const float* __restrict__ g, int H, int t,
+                                                  int lane) {
+  float s = 0.f;
+  for (int h = lane * 8; h < H; h += 256) {
+    const uint4 v = ldg16(x + (size_t)t * H + h);
+    const float4 g0 = __ldg(reinterpret_cast<const float4*>(g + h));
+    const float4 g1 = __ldg(reinterpret_cast<const float4*>(g + h + 4));
+    s = fmaf(bf16_lo(v.x), g0.x, s);
+    s = fmaf(bf16_hi(v.x), g0.y, s);
+    s = fmaf(bf16_lo(v.y), g0.z, s);
+    s = fmaf(bf16_hi(v.y), g0.w, s);
+    s = fmaf(bf16_lo(v.z), g1.x, s);
+    s = fmaf(bf16_hi(v.z), g1.y, s);
+    s = fmaf(bf16_lo(v.w), g1.z, s);
+    s = fmaf(bf16_hi(v.w), g1.w, s);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  s = __shfl_sync(0xffffffffu, s, 0);
+  return 1.f / (1.f + expf(-s));
+}
+
+// The gate inputs of the layer call's top-k kernels (sgate == NULL: none).
+struct SharedGate {
+  const uint16_t* x = nullptr;
+  const float* g = nullptr;
+  int H = 0;
+  float* sgate = nullptr;  // [T] out
+};
+
 template <int EPL>
 __global__ void __launch_bounds__(256)
 k_router_topk(const float* __restrict__ part, int KS, const float* __restrict__ bias, int T,
-              int E, int k, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+              int E, int k, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+              const SharedGate sg) {
   griddep_wait();
   griddep_trigger();
   const int lane = threadIdx.x & 31;
@@ -256,6 +291,10 @@ k_router_topk(const float* __restrict__ part, int KS, const float* __restrict__ 
   if (lane < k) {
     topk_idx[(size_t)t * k + lane] = idx;
     topk_w[(size_t)t * k + lane] = w;
+  }
+  if (sg.sgate) {
+    const float gt = warp_shared_gate(sg.x, sg.g, sg.H, t, lane);
+    if (lane == 0) sg.sgate[t] = gt;
   }
 }
 
@@ -290,7 +329,7 @@ k_topk_permute_small(const float* __restrict__ part, int KS, const float* __rest
                      int32_t* __restrict__ row_pair, int32_t* __restrict__ active,
                      int32_t* __restrict__ sh_off, int32_t* __restrict__ sh_rows,
                      int32_t* __restrict__ sh_active, int32_t* __restrict__ tile_off,
-                     int32_t* __restrict__ counters, int n_counters) {
+                     int32_t* __restrict__ counters, int n_counters, const SharedGate sg) {
   extern __shared__ int32_t sm[];
   int32_t* s_idx = sm;                   // [kSmallPairs] expert of pair q
   int32_t* s_cnt = s_idx + kSmallPairs;  // [1024] counts, then rows taken so far
@@ -317,6 +356,10 @@ k_topk_permute_small(const float* __restrict__ part, int KS, const float* __rest
         topk_idx[(size_t)t * k + lane] = idx;
         topk_w[(size_t)t * k + lane] = w;
         s_idx[t * k + lane] = idx;
+      }
+      if (sg.sgate) {
+        const float gt = warp_shared_gate(sg.x, sg.g, sg.H, t, lane);
+        if (lane == 0) sg.sgate[t] = gt;
       }
     }
   }
@@ -450,7 +493,7 @@ k_topk_permute_tiny(const float* __restrict__ part, int KS, const float* __restr
                     int32_t* __restrict__ row_pair, int32_t* __restrict__ active,
                     int32_t* __restrict__ sh_off, int32_t* __restrict__ sh_rows,
                     int32_t* __restrict__ sh_active, int32_t* __restrict__ tile_off,
-                    int32_t* __restrict__ counters, int n_counters) {
+                    int32_t* __restrict__ counters, int n_counters, const SharedGate sg) {
   __shared__ int32_t s_idx[kTinyPairs];
   __shared__ int32_t s_cnt[kMaxExperts];
   griddep_wait();
@@ -465,6 +508,10 @@ k_topk_permute_tiny(const float* __restrict__ part, int KS, const float* __restr
       topk_idx[(size_t)t * k + lane] = idx;
       topk_w[(size_t)t * k + lane] = w;
       s_idx[t * k + lane] = idx;
+    }
+    if (sg.sgate) {
+      const float gt = warp_shared_gate(sg.x, sg.g, sg.H, t, lane);
+      if (lane == 0) sg.sgate[t] = gt;
     }
   }
   for (int e = tid; e < E; e += blockDim.x) s_cnt[e] = 0;
@@ -585,15 +632,22 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* Wr, int T, int 
 cudaError_t launch_route(const uint16_t* x, const float* Wr, const float* bias, int T, int H,
                          int E, int k, float* part, uint16_t* planes, int32_t* topk_idx,
                          float* topk_w, uint16_t* xn, int8_t* xe, int32_t* status,
-                         cudaStream_t s, bool pdl) {
+                         cudaStream_t s, bool pdl, const float* shared_gate, float* sgate) {
   if (T == 0) return cudaSuccess;
+  SharedGate sg;
+  if (sgate) {
+    sg.x = x;
+    sg.g = shared_gate;
+    sg.H = H;
+    sg.sgate = sgate;
+  }
   cudaError_t err = launch_router_logits(x, Wr, T, H, E, part, planes, xn, xe, status, s, pdl);
   if (err != cudaSuccess) return err;
   const int KS = route_kslices(T, H, E);
   const int epl = cdiv(E, 32);
   const dim3 g2(cdiv(T, 8)), blk(256);
 #define MOE_TOPK(EPLV) \
-  launch_k(k_router_topk<EPLV>, g2, blk, 0, s, pdl, part, KS, bias, T, E, k, topk_idx, topk_w)
+  launch_k(k_router_topk<EPLV>, g2, blk, 0, s, pdl, part, KS, bias, T, E, k, topk_idx, topk_w, sg)
   if (epl <= 1) return MOE_TOPK(1);
   if (epl <= 2) return MOE_TOPK(2);
   if (epl <= 4) return MOE_TOPK(4);
@@ -615,8 +669,16 @@ cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const
                                        int32_t* row_pair, int32_t* active, int32_t* sh_off,
                                        int32_t* sh_rows, int32_t* sh_active, uint16_t* xn,
                                        int8_t* xe, int32_t* tile_off, int32_t* counters,
-                                       int n_counters, int32_t* status, cudaStream_t s, bool pdl) {
+                                       int n_counters, int32_t* status, cudaStream_t s, bool pdl,
+                                       const float* shared_gate, float* sgate) {
   cudaError_t err = launch_router_logits(x, Wr, T, H, E, part, planes, xn, xe, status, s, pdl);
+  SharedGate sg;
+  if (sgate) {
+    sg.x = x;
+    sg.g = shared_gate;
+    sg.H = H;
+    sg.sgate = sgate;
+  }
   if (err != cudaSuccess) return err;
   const int KS = route_kslices(T, H, E);
   const size_t smem = small_route_smem(E);
@@ -627,7 +689,7 @@ cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const
     // on a single SM
     const dim3 g2(cdiv(T, 8)), blk(256);
 #define MOE_TOPK(EPLV) \
-  launch_k(k_router_topk<EPLV>, g2, blk, 0, s, pdl, part, KS, bias, T, E, k, topk_idx, topk_w)
+  launch_k(k_router_topk<EPLV>, g2, blk, 0, s, pdl, part, KS, bias, T, E, k, topk_idx, topk_w, sg)
     err = epl <= 1 ? MOE_TOPK(1) : epl <= 2 ? MOE_TOPK(2) : epl <= 4 ? MOE_TOPK(4)
         : epl <= 8 ? MOE_TOPK(8) : epl <= 16 ? MOE_TOPK(16) : MOE_TOPK(32);
 #undef MOE_TOPK
@@ -636,14 +698,14 @@ cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const
     if (err != cudaSuccess) return err;
     return launch_k(k_topk_permute_small<0>, dim3(1), dim3(1024), smem, s, pdl, part, KS, bias,
                     T, E, k, topk_idx, topk_w, expert_off, row_token, tok_slot_row, row_pair,
-                    active, sh_off, sh_rows, sh_active, tile_off, counters, n_counters);
+                    active, sh_off, sh_rows, sh_active, tile_off, counters, n_counters, sg);
   }
   if ((long long)T * k <= kTinyPairs) {
     const dim3 blk(32 * T);  // T < kSplitTopkTokens: at most 480 threads
 #define MOE_TINY(EPLV)                                                                        \
   return launch_k(k_topk_permute_tiny<EPLV>, dim3(1), blk, 0, s, pdl, part, KS, bias, T, E, k, \
                   topk_idx, topk_w, expert_off, row_token, tok_slot_row, row_pair, active,     \
-                  sh_off, sh_rows, sh_active, tile_off, counters, n_counters)
+                  sh_off, sh_rows, sh_active, tile_off, counters, n_counters, sg)
     if (epl <= 1) MOE_TINY(1);
     if (epl <= 2) MOE_TINY(2);
     if (epl <= 4) MOE_TINY(4);
@@ -659,7 +721,7 @@ cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const
     return launch_k(k_topk_permute_small<EPLV>, dim3(1), dim3(1024), smem, s, pdl, part, KS, \
                     bias, T, E, k, topk_idx, topk_w, expert_off, row_token, tok_slot_row,    \
                     row_pair, active, sh_off, sh_rows, sh_active, tile_off, counters,        \
-                    n_counters);                                                             \
+                    n_counters, sg);                                                         \
   } while (0)
   if (epl <= 1) MOE_SMALL(1);
   if (epl <= 2) MOE_SMALL(2);

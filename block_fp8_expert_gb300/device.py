@@ -48,6 +48,8 @@ class DeviceLayer:
     bias: Optional[torch.Tensor]
     routed: DeviceFfn
     shared: Optional[DeviceFfn]
+    # gated shared expert: float32 [H] (None: ungated)
+    shared_gate_w: Optional[torch.Tensor] = None
 
     @classmethod
     def from_host(cls, layer, device="cuda") -> "DeviceLayer":
@@ -60,10 +62,12 @@ class DeviceLayer:
         shared = None
         if layer.I_shared:
             shared = ffn(layer.shared_gate, layer.shared_up, layer.shared_down)
+        gw = getattr(layer, "shared_gate_w", None)
         return cls(H=layer.H, I=layer.I, E=layer.E, k=layer.k, I_shared=layer.I_shared,
                    Wr=_dev(layer.Wr, device),
                    bias=None if layer.bias is None else _dev(layer.bias, device),
-                   routed=ffn(layer.gate, layer.up, layer.down), shared=shared)
+                   routed=ffn(layer.gate, layer.up, layer.down), shared=shared,
+                   shared_gate_w=None if gw is None else _dev(gw, device))
 
     def dims(self, T: int) -> _lib.Dims:
         return _lib.dims(T, self.H, self.I, self.E, self.k, self.I_shared)
@@ -81,9 +85,14 @@ class DeviceLayer:
             out = torch.empty((T, self.H), dtype=torch.bfloat16, device=x.device)
         if ws is None:
             ws = self.workspace(T)
-        _lib.moe_layer_forward(x, self.Wr, self.bias, self.routed.abi(),
-                               self.shared.abi() if self.shared is not None else None,
-                               self.dims(T), out, topk_idx, topk_w, ws, stream)
+        if self.shared_gate_w is not None:
+            _lib.moe_layer_forward_gated(x, self.Wr, self.bias, self.routed.abi(),
+                                         self.shared.abi(), self.shared_gate_w, self.dims(T), out,
+                                         topk_idx, topk_w, ws, stream)
+        else:
+            _lib.moe_layer_forward(x, self.Wr, self.bias, self.routed.abi(),
+                                   self.shared.abi() if self.shared is not None else None,
+                                   self.dims(T), out, topk_idx, topk_w, ws, stream)
         return out
 
 

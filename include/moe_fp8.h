@@ -230,6 +230,25 @@ moe_status moe_layer_forward(const uint16_t* x, const float* Wr,
                              void* stream);
 
 /*
+ * The layer with a gated shared expert: as moe_layer_forward, except that
+ * the shared expert's output for token t is scaled by
+ * sigmoid(sum_h x[t,h] shared_gate[h]) before it is added.  This variant is
+ * not on the colizig README (its 512-expert family lists "top-10 + 1 shared"
+ * without a gate); it is the sigmoid-gated form of that shared expert.
+ *   shared_gate float [H]; the layer must have a shared expert
+ *               (d.I_shared > 0, shared not NULL).
+ * The gate is computed by the routing kernels in fp32 and applied in the
+ * combine.
+ */
+moe_status moe_layer_forward_gated(const uint16_t* x, const float* Wr,
+                                   const float* bias, moe_fp8_ffn routed,
+                                   const moe_fp8_ffn* shared,
+                                   const float* shared_gate, moe_dims d,
+                                   uint16_t* out, int32_t* topk_idx_out,
+                                   float* topk_w_out, void* ws, size_t ws_bytes,
+                                   void* stream);
+
+/*
  * moe_permute without a workspace, for callers that cannot allocate device
  * memory: for example a plugin whose host framework passes it only the input
  * and output buffers of each call, or a serving loop whose device memory is

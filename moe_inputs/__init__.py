@@ -51,7 +51,7 @@ GAP_MIN = 1e-4
 # of them can be regenerated alone.
 _TAG = {"wr": 1, "bias": 2, "gate": 3, "up": 4, "down": 5, "gate_s": 6,
         "up_s": 7, "down_s": 8, "sh_gate": 9, "sh_up": 10, "sh_down": 11,
-        "sh_gate_s": 12, "sh_up_s": 13, "sh_down_s": 14, "x": 15}
+        "sh_gate_s": 12, "sh_up_s": 13, "sh_down_s": 14, "x": 15, "sh_gate_w": 16}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -105,6 +105,9 @@ class LayerWeights:
     shared_gate: Optional[Fp8Mat] = None
     shared_up: Optional[Fp8Mat] = None
     shared_down: Optional[Fp8Mat] = None
+    # gated shared expert only: float32 [H], the shared expert's output is
+    # scaled per token by sigmoid(x . shared_gate_w)
+    shared_gate_w: Optional[np.ndarray] = None
 
     @property
     def has_shared(self) -> bool:
@@ -205,13 +208,16 @@ def zipf_bias(E: int, s: float, seed: int) -> np.ndarray:
 
 def make_layer(workload: str | Workload, seed: int = 0,
                threads: Optional[int] = None, code_gain: float = 1.0,
-               scale_range=SCALE_RANGE, scale_dist: str = "uniform") -> LayerWeights:
+               scale_range=SCALE_RANGE, scale_dist: str = "uniform",
+               shared_gated: bool = False) -> LayerWeights:
     """Draw every weight of one layer of the named workload.
 
     The defaults are the workloads' distributions.  code_gain multiplies the
     N(0, 1) draw before it is encoded (100 gives codes spread over the whole
     E4M3 range, as an amax-scaled checkpoint has); scale_range and scale_dist
-    choose the block scales' distribution (see _draw_scales)."""
+    choose the block scales' distribution (see _draw_scales); shared_gated
+    adds a gate vector ~ N(0, 0.02^2) for the shared expert (layers with a
+    shared expert only)."""
     w = WORKLOADS[workload] if isinstance(workload, str) else workload
     H, I, E = w.H, w.I, w.E
     threads = threads or min(32, os.cpu_count() or 1)
@@ -229,9 +235,13 @@ def make_layer(workload: str | Workload, seed: int = 0,
             sg = _draw_fp8(seed, "sh_gate", "sh_gate_s", 1, Is, H, pool, **kw)
             su = _draw_fp8(seed, "sh_up", "sh_up_s", 1, Is, H, pool, **kw)
             sd = _draw_fp8(seed, "sh_down", "sh_down_s", 1, H, Is, pool, **kw)
+    gw = None
+    if shared_gated and w.I_shared:
+        gw = (_rng(seed, "sh_gate_w").standard_normal(H, dtype=np.float32)
+              * np.float32(0.02))
     return LayerWeights(H=H, I=I, E=E, k=w.k, I_shared=w.I_shared, Wr=Wr,
                         bias=bias, gate=gate, up=up, down=down,
-                        shared_gate=sg, shared_up=su, shared_down=sd)
+                        shared_gate=sg, shared_up=su, shared_down=sd, shared_gate_w=gw)
 
 
 def with_scales(layer: LayerWeights, seed: int, scale_range,

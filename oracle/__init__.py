@@ -29,6 +29,7 @@ from .moe_ref import (  # noqa: F401
     silu,
     expert_ffn,
     combine,
+    shared_gate_factor,
     moe_layer,
     moe_layer_sampled,
 )

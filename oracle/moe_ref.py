@@ -33,6 +33,9 @@ R5  The permutation is expert-major and, inside one expert's segment,
 R6  SwiGLU is silu(x Wg^T) * (x Wu^T) with silu(z) = z / (1 + exp(-z)).
 R7  The shared expert sees every token with weight 1 (no gate) and is added
     after the routed combine.
+R8  Gated variant (not on the pages, which say only "+ 1 shared"): when the
+    layer carries a gate vector g [H], the shared expert's output for token
+    t is scaled by sigmoid(x[t] . g) before it is added.
 """
 from __future__ import annotations
 
@@ -184,6 +187,18 @@ def combine(y_perm, tok_slot_row, topk_w, shared_y=None) -> np.ndarray:
 # the whole layer
 # ---------------------------------------------------------------------------
 
+def shared_gate_factor(x, layer) -> np.ndarray:
+    """Per-token factor of the shared expert's output (readings R7, R8): 1
+    without a gate vector, else sigmoid(x . g), float64 [T]."""
+    g = getattr(layer, "shared_gate_w", None)
+    x = np.asarray(x, dtype=np.float64)
+    if g is None:
+        return np.ones(x.shape[0])
+    z = x @ np.asarray(g, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-z))
+
+
 def _expert_mats(mat, e):
     return dequantize(mat.codes[e], mat.scales[e])
 
@@ -217,6 +232,7 @@ def moe_layer(x_bits, layer, keep_intermediates: bool = True) -> dict:
         shared_y = expert_ffn(x, _expert_mats(layer.shared_gate, 0),
                               _expert_mats(layer.shared_up, 0),
                               _expert_mats(layer.shared_down, 0))
+        shared_y = shared_y * shared_gate_factor(x, layer)[:, None]
     out = combine(y_perm, tok_slot_row, w, shared_y)
     res = dict(topk_idx=idx, topk_w=w, expert_off=off, row_token=row_token,
                tok_slot_row=tok_slot_row, out=out)
@@ -253,8 +269,9 @@ def moe_layer_sampled(x_bits, layer, tokens) -> dict:
         for (n, t, j), yr in zip(lst, y):
             out[n] += w[t, j] * yr
     if layer.I_shared:
-        out += expert_ffn(x[tokens], _expert_mats(layer.shared_gate, 0),
-                          _expert_mats(layer.shared_up, 0),
-                          _expert_mats(layer.shared_down, 0))
+        out += (expert_ffn(x[tokens], _expert_mats(layer.shared_gate, 0),
+                           _expert_mats(layer.shared_up, 0),
+                           _expert_mats(layer.shared_down, 0))
+                * shared_gate_factor(x[tokens], layer)[:, None])
     return dict(topk_idx=idx, topk_w=w, expert_off=off, row_token=row_token,
                 tok_slot_row=tok_slot_row, out_sampled=out)

@@ -235,3 +235,23 @@ def test_nonfinite_inputs_flagged(torch, monkeypatch, path):
     assert bits & m._lib.MOE_DEV_NONFINITE, f"status 0x{bits:x}"
     _, bits = _ffn(torch, D, xb, ref)
     assert bits == 0, f"status 0x{bits:x}"
+
+
+@pytest.mark.parametrize("path,T", [("auto", 8), ("gemv", 64), ("gemm", 64), ("auto", 300)])
+def test_gated_shared_expert(torch, monkeypatch, path, T):
+    """moe_layer_forward_gated: the shared expert's output scaled by
+    sigmoid(x . g) per token.  T = 8 runs the shared expert as one more
+    expert of the streamed GEMV launches with the combine folded into the
+    down kernel; T = 64 on each forced regime; T = 300 the default regime
+    (tensor-core GEMM, token-major gather writing the shared rows)."""
+    if path != "auto":
+        monkeypatch.setenv("MOE_FP8_EXPERT_PATH", path)
+    w = mi.Workload("shared_mid", H=512, I=256, E=32, k=4, I_shared=256)
+    L = mi.make_layer(w, seed=15, shared_gated=True)
+    D = _device(L)
+    assert D.shared_gate_w is not None
+    xb, _ = mi.make_tokens(L, T, seed=15)
+    ref = oracle.moe_layer(xb, L, keep_intermediates=False)
+    fac = oracle.shared_gate_factor(oracle.bf16_to_f64(xb), L)
+    assert fac.max() - fac.min() > 0.05  # the gate really varies over the tokens
+    _check_layer(torch, D, L, xb, f"gated shared expert {path} T={T}", ref)

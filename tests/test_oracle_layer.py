@@ -158,6 +158,55 @@ def test_zero_shared_expert_reduces_to_routed_layer():
     assert not np.allclose(with_sh, routed)
 
 
+def _gated(L, g):
+    import dataclasses
+    return dataclasses.replace(L, shared_gate_w=np.asarray(g, dtype=np.float32))
+
+
+def test_gated_shared_expert_limits():
+    """Gate vector zero: the shared output is halved (sigmoid(0) = 1/2); a
+    gate driven to +inf keeps it whole, to -inf removes it.  The difference
+    to the ungated layer is exactly the shared expert's output times
+    (1 - factor), which pins where and with which sign the gate enters."""
+    L = _small_shared_layer(2)
+    xb, _ = mi.make_tokens(L, 7, seed=2)
+    x = oracle.bf16_to_f64(xb)
+    plain = oracle.moe_layer(xb, L)
+    sh = plain["shared_y"]
+    assert np.abs(sh).max() > 0
+    half = oracle.moe_layer(xb, _gated(L, np.zeros(L.H)))["out"]
+    assert np.allclose(half, plain["out"] - 0.5 * sh, rtol=1e-13, atol=1e-13 * np.abs(sh).max())
+    # a gate along the sum of the token vectors: x_t . g is dominated by
+    # |x_t|^2 > 0 for every token (checked), so +g keeps the shared output
+    # whole and -g removes it
+    g = 1e4 * x.sum(axis=0)
+    assert np.all(x @ g > 50)
+    whole = oracle.moe_layer(xb, _gated(L, g))["out"]
+    assert np.allclose(whole, plain["out"], rtol=1e-13, atol=1e-13 * np.abs(sh).max())
+    none = oracle.moe_layer(xb, _gated(L, -g))["out"]
+    assert np.allclose(none, plain["out"] - sh, rtol=1e-12, atol=1e-12 * np.abs(sh).max())
+
+
+def test_gate_factor_against_scalar_loop():
+    """sigmoid(x . g) per token, against a math.fsum dot and math.exp."""
+    w = mi.Workload("small_shared", H=256, I=128, E=8, k=2, I_shared=128)
+    L = mi.make_layer(w, seed=3, shared_gated=True)
+    assert L.shared_gate_w is not None and L.shared_gate_w.shape == (L.H,)
+    xb, _ = mi.make_tokens(L, 5, seed=3)
+    x = oracle.bf16_to_f64(xb)
+    got = oracle.shared_gate_factor(x, L)
+    for t in range(5):
+        z = math.fsum(float(x[t, h]) * float(L.shared_gate_w[h]) for h in range(L.H))
+        assert abs(got[t] - 1.0 / (1.0 + math.exp(-z))) <= 1e-14
+    # and the gated layer scales the shared output by it, token by token
+    ungated = oracle.moe_layer(xb, _gated(L, np.zeros(L.H)))  # factor 1/2
+    gated = oracle.moe_layer(xb, L)
+    sh_half = ungated["shared_y"]  # already scaled by 1/2
+    assert np.allclose(gated["out"] - (ungated["out"] - sh_half),
+                       2.0 * sh_half * got[:, None], rtol=1e-12,
+                       atol=1e-12 * np.abs(sh_half).max())
+
+
 def test_sampled_path_equals_full_layer():
     L = mi.make_layer("tiny", seed=3)
     xb, _ = mi.make_tokens(L, 8, seed=3)
