@@ -536,6 +536,12 @@ def run_gpu(args):
     roof.update({"avg_duration_us": t_exp * 1e6, "traffic": kernel_traffic(tkey, src),
                  "traffic_unit": "DRAM bytes per launch (ncu)"})
 
+    # runtime cross-check of the headline layer call on 16 sampled tokens
+    # (independent GPU recomputation; outside every timed region)
+    run.step()
+    torch.cuda.synchronize()
+    verify = D.verify(run.x, run.out, run.idx, run.w, list(range(0, T, max(1, T // 16)))[:16])
+
     # e2e: host buffers, copies inside the timed region
     x_host = torch.from_numpy(x_bits.view(np.int16)).pin_memory()
     out_host = torch.empty((T, w.H), dtype=torch.int16).pin_memory()
@@ -603,6 +609,7 @@ def run_gpu(args):
                     "h2d_bytes_per_step": T * w.H * 2, "d2h_bytes_per_step": T * w.H * 2},
             "gpu_launches": launches_per_step * args.steps,
             "device_status": headline_status,
+            "verify": verify,
             "ms_step_max": max(times) * 1e3,
             "clocks": ck,
             "sweep": sweep,

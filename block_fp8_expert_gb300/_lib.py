@@ -70,6 +70,9 @@ _SIGNATURES = {
                                 _vp, _vp, _sz, _vp]),
     "moe_layer_forward_gated": (_st, [_vp, _vp, _vp, Fp8Ffn, ctypes.POINTER(Fp8Ffn), _vp, Dims,
                                       _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_verify_workspace_bytes": (_st, [Dims, ctypes.c_int, ctypes.POINTER(_sz)]),
+    "moe_verify_layer": (_st, [_vp, Fp8Ffn, ctypes.POINTER(Fp8Ffn), _vp, Dims, _vp, _vp, _vp,
+                               _vp, ctypes.c_int, _vp, _vp, _sz, _vp]),
     "moe_read_device_status": (_st, [_vp, ctypes.POINTER(ctypes.c_int32), _vp]),
     "moe_permute_static_scratch": (_st, [_vp, Dims, _vp, _vp, _vp, _vp]),
 }
@@ -204,6 +207,22 @@ def moe_layer_forward_gated(x, Wr, bias, routed: Fp8Ffn, shared: Fp8Ffn, shared_
                                          ctypes.byref(shared), _ptr(shared_gate), d, _ptr(out),
                                          _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(ws),
                                          _nbytes(ws), _stream(stream)), "moe_layer_forward_gated")
+
+
+def verify_workspace_bytes(d: Dims, n_tokens: int) -> int:
+    n = _sz(0)
+    _check(lib().moe_verify_workspace_bytes(d, n_tokens, ctypes.byref(n)),
+           "moe_verify_workspace_bytes")
+    return n.value
+
+
+def moe_verify_layer(x, routed: Fp8Ffn, shared: Optional[Fp8Ffn], shared_gate, d: Dims, out,
+                     topk_idx, topk_w, tokens, result, ws, stream=None) -> None:
+    sh = ctypes.byref(shared) if shared is not None else None
+    _check(lib().moe_verify_layer(_ptr(x), routed, sh, _ptr(shared_gate), d, _ptr(out),
+                                  _ptr(topk_idx), _ptr(topk_w), _ptr(tokens),
+                                  int(tokens.numel()), _ptr(result), _ptr(ws), _nbytes(ws),
+                                  _stream(stream)), "moe_verify_layer")
 
 
 def moe_read_device_status(ws, stream=None) -> int:

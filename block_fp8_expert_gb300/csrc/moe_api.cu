@@ -579,6 +579,52 @@ moe_status moe_layer_forward_gated(const uint16_t* x, const float* Wr, const flo
                        topk_w_out, ws, ws_bytes, stream);
 }
 
+moe_status moe_verify_workspace_bytes(moe_dims d, int n_tokens, size_t* bytes) {
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  if (!bytes) return fail(MOE_ERR_INVALID_ARG, "bytes is NULL");
+  if (n_tokens < 1 || n_tokens > verify_max_tokens())
+    return fail(MOE_ERR_UNSUPPORTED, "n_tokens = %d outside [1, %d]", n_tokens,
+                verify_max_tokens());
+  *bytes = verify_workspace(d, n_tokens);
+  return MOE_OK;
+}
+
+moe_status moe_verify_layer(const uint16_t* x, moe_fp8_ffn routed, const moe_fp8_ffn* shared,
+                            const float* shared_gate, moe_dims d, const uint16_t* out,
+                            const int32_t* topk_idx, const float* topk_w, const int32_t* tokens,
+                            int n_tokens, float* result, void* ws, size_t ws_bytes,
+                            void* stream) {
+  moe_status s;
+  if ((s = check_dims(d)) != MOE_OK) return s;
+  if (d.T < 1) return fail(MOE_ERR_INVALID_ARG, "no token to verify (T = 0)");
+  if (n_tokens < 1 || n_tokens > verify_max_tokens())
+    return fail(MOE_ERR_UNSUPPORTED, "n_tokens = %d outside [1, %d]", n_tokens,
+                verify_max_tokens());
+  REQUIRE_PTR(x);
+  REQUIRE_PTR(out);
+  REQUIRE_PTR(topk_idx);
+  REQUIRE_PTR(topk_w);
+  REQUIRE_PTR(tokens);
+  REQUIRE_PTR(result);
+  REQUIRE_OPT_PTR(shared_gate);
+  if ((s = check_ffn(routed, "routed")) != MOE_OK) return s;
+  if (d.I_shared > 0) {
+    if (!shared) return fail(MOE_ERR_INVALID_ARG, "I_shared > 0 but shared is NULL");
+    if ((s = check_ffn(*shared, "shared")) != MOE_OK) return s;
+  } else if (shared || shared_gate) {
+    return fail(MOE_ERR_INVALID_ARG, "shared expert given but I_shared == 0");
+  }
+  REQUIRE_PTR(ws);
+  if (ws_bytes < verify_workspace(d, n_tokens))
+    return fail(MOE_ERR_WORKSPACE, "verify workspace of %zu bytes, need %zu", ws_bytes,
+                verify_workspace(d, n_tokens));
+  CUDA_CHECK(launch_verify(x, routed, shared, shared_gate, d, out, topk_idx, topk_w, tokens,
+                           n_tokens, result, ws, (cudaStream_t)stream),
+             "moe_verify_layer");
+  return MOE_OK;
+}
+
 moe_status moe_read_device_status(const void* ws, int32_t* status, void* stream) {
   REQUIRE_OPT_PTR(ws);
   if (!status) return fail(MOE_ERR_INVALID_ARG, "status is NULL");

@@ -227,6 +227,15 @@ cudaError_t launch_combine_layer(const uint16_t* y, const int16_t* yexp, int P,
 // array on the current device.
 cudaError_t static_scratch_status(int32_t** out);
 
+// Runtime cross-check (verify.cu): scratch bytes for n sampled tokens, the
+// largest n, and the launch (result: device float[3]).
+size_t verify_workspace(const moe_dims& d, int n);
+int verify_max_tokens();
+cudaError_t launch_verify(const uint16_t* x, const moe_fp8_ffn& routed, const moe_fp8_ffn* shared,
+                          const float* shared_gate, const moe_dims& d, const uint16_t* out,
+                          const int32_t* topk_idx, const float* topk_w, const int32_t* tokens,
+                          int n, float* result, void* ws, cudaStream_t s);
+
 // Identity permutation of T tokens onto one expert (the shared expert):
 // off = {0, T}, rows = 0..T-1, active = {1, 0}.
 cudaError_t launch_identity_perm(int T, int32_t* off, int32_t* rows, int32_t* active,

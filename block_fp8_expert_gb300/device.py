@@ -96,6 +96,25 @@ class DeviceLayer:
         return out
 
 
+    def verify(self, x: torch.Tensor, out: torch.Tensor, topk_idx: torch.Tensor,
+               topk_w: torch.Tensor, tokens, stream=None) -> dict:
+        """Runtime cross-check of a forward call on the listed tokens (at most
+        64): the worst error in units of the layer tolerance, the worst
+        absolute error and rms of the recomputed outputs (see
+        moe_verify_layer)."""
+        T = x.shape[0]
+        tok = torch.as_tensor(tokens, dtype=torch.int32).to(x.device)
+        d = self.dims(T)
+        ws = torch.empty(_lib.verify_workspace_bytes(d, int(tok.numel())), dtype=torch.uint8,
+                         device=x.device)
+        res = torch.empty(3, dtype=torch.float32, device=x.device)
+        _lib.moe_verify_layer(x, self.routed.abi(),
+                              self.shared.abi() if self.shared is not None else None,
+                              self.shared_gate_w, d, out, topk_idx, topk_w, tok, res, ws, stream)
+        r = res.cpu().tolist()
+        return {"max_err_over_tol": r[0], "max_abs_err": r[1], "rms_ref": r[2]}
+
+
 def x_to_device(x_bits: np.ndarray, device="cuda") -> torch.Tensor:
     """bf16 bit patterns (uint16 [T, H]) -> a bf16 device tensor."""
     return torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16)).to(device).view(

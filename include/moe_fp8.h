@@ -276,6 +276,36 @@ moe_status moe_permute_static_scratch(const int32_t* topk_idx, moe_dims d,
                                       int32_t* tok_slot_row, void* stream);
 
 /*
+ * Runtime cross-check of a layer call on sampled tokens, the GPU counterpart
+ * of the colizig README's --cuda-verify (CLI reference), which checks the
+ * CUDA path against the CPU path.  It recomputes the layer output of each
+ * listed token on an arithmetic path independent of the layer kernels
+ * (plain fp32 dot products, the E4M3 codes decoded from their bit fields
+ * times their block scale, no tensor cores, no power-of-two normalisation),
+ * from the routing the layer call produced, and compares it with `out`.
+ *   x, routed, shared, shared_gate, d   as given to the layer call
+ *                  (shared_gate NULL for moe_layer_forward)
+ *   out            bf16 [T, H], the layer call's output
+ *   topk_idx, topk_w  the layer call's routing ([T, k]; pass topk_idx_out /
+ *                  topk_w_out of the layer call)
+ *   tokens         int32 [n_tokens], token indices in [0, T); 1 <= n_tokens
+ *                  <= 64
+ *   result         float [3] out (device): worst |out - ref| / (1e-2 (|ref| +
+ *                  rms(ref))) over the sampled outputs (<= 1: within the
+ *                  layer tolerance; infinite for a NaN or an expert index
+ *                  outside [0, E)), worst |out - ref|, rms(ref)
+ *   ws, ws_bytes   scratch of at least moe_verify_workspace_bytes(d, n_tokens)
+ * Enqueued on `stream` like every call; read `result` after synchronising.
+ */
+moe_status moe_verify_workspace_bytes(moe_dims d, int n_tokens, size_t* bytes);
+moe_status moe_verify_layer(const uint16_t* x, moe_fp8_ffn routed,
+                            const moe_fp8_ffn* shared, const float* shared_gate,
+                            moe_dims d, const uint16_t* out,
+                            const int32_t* topk_idx, const float* topk_w,
+                            const int32_t* tokens, int n_tokens, float* result,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Copy the workspace's device status word to *status (MOE_DEV_* bits) after
  * synchronising `stream`.  Returns MOE_ERR_DEVICE_STATUS when any bit is set.
  * The word is cleared at the start of moe_route, moe_permute,
