@@ -33,7 +33,7 @@ R5  The permutation is expert-major and, inside one expert's segment,
 R6  SwiGLU is silu(x Wg^T) * (x Wu^T) with silu(z) = z / (1 + exp(-z)).
 R7  The shared expert sees every token with weight 1 (no gate) and is added
     after the routed combine.
-R8  Gated variant (not on the pages, which say only "+ 1 shared"): when the
+R10 Gated variant (not on the pages, which say only "+ 1 shared"): when the
     layer carries a gate vector g [H], the shared expert's output for token
     t is scaled by sigmoid(x[t] . g) before it is added.
 """
@@ -188,7 +188,7 @@ def combine(y_perm, tok_slot_row, topk_w, shared_y=None) -> np.ndarray:
 # ---------------------------------------------------------------------------
 
 def shared_gate_factor(x, layer) -> np.ndarray:
-    """Per-token factor of the shared expert's output (readings R7, R8): 1
+    """Per-token factor of the shared expert's output (readings R7, R10): 1
     without a gate vector, else sigmoid(x . g), float64 [T]."""
     g = getattr(layer, "shared_gate_w", None)
     x = np.asarray(x, dtype=np.float64)
