@@ -364,6 +364,69 @@ def time_steps(torch, fn, steps, warmup, flush):
     return times
 
 
+def _nvtx_range(torch, name, fn):
+    """fn() inside an NVTX push/pop range (host-side marker only; lets a
+    profiler select the expert-FFN call's kernels: `--nvtx --nvtx-include
+    moe_expert_ffn_fp8/`)."""
+    torch.cuda.nvtx.range_push(name)
+    try:
+        return fn()
+    finally:
+        torch.cuda.nvtx.range_pop()
+
+
+def record_traffic(csv_path, workload):
+    """Store the DRAM bytes per expert-FFN call from an ncu CSV (metrics
+    dram__bytes_read.sum and dram__bytes_write.sum of the kernels inside the
+    `moe_expert_ffn_fp8` NVTX range) in profiles/dram_traffic.json under the
+    workload's key, with the hash of the sources it was measured on."""
+    import csv
+    import collections
+    rows = list(csv.reader(open(csv_path)))
+    hi = next(i for i, r in enumerate(rows) if "Kernel Name" in r)
+    hdr = rows[hi]
+    ki, mi_, vi, ii = (hdr.index("Kernel Name"), hdr.index("Metric Name"),
+                       hdr.index("Metric Value"), hdr.index("ID"))
+    per = collections.defaultdict(lambda: collections.defaultdict(float))
+    for r in rows[hi + 1:]:
+        if len(r) <= vi or r[mi_] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        unit = r[hdr.index("Metric Unit")] if "Metric Unit" in hdr else "byte"
+        scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}.get(unit, 1)
+        name = r[ki].split("(")[0].replace("void ", "").replace("moe::", "")
+        if name.startswith("k_"):  # this library's kernels only (not torch's fills)
+            per[name][r[ii]] += float(r[vi].replace(",", "")) * scale
+    kern = {k: sum(v.values()) / len(v) for k, v in per.items()}
+    gemm = any("k_expert_gemm_ws" in k for k in kern)
+    nm, T = workload.split(":")
+    csrc = os.path.join("block_fp8_expert_gb300", "csrc")
+    files = ["expert_gemm_tc.cu", "tcgen05.cuh", "moe_common.cuh"] if gemm else \
+        ["expert_gemv.cu", "moe_common.cuh"]
+    src = [os.path.join(csrc, f) for f in files]
+    key = f"expert_ffn_{'gemm' if gemm else 'gemv'}_{nm}_T{T}"
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    table = json.load(open(path)) if os.path.exists(path) else {}
+    table[key] = {
+        "what": f"DRAM bytes (read + write) of one moe_expert_ffn_fp8 call at {nm} T={T}",
+        "bytes_per_launch": int(round(sum(kern.values()))),
+        "per_kernel": {k: int(round(v)) for k, v in kern.items()},
+        "src_hash": file_hash([os.path.join(ROOT, f) for f in src]),
+        "src": src,
+        "command": f"ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,"
+                   f"dram__bytes_write.sum --clock-control none --nvtx --nvtx-include "
+                   f"moe_expert_ffn_fp8/ -c 10 --csv --log-file traffic.csv python bench.py "
+                   f"--workload {workload} --steps 3 --warmup 3 --no-sweep --no-cpu-baseline "
+                   f"--max-passes 2; python bench.py --record-traffic traffic.csv "
+                   f"--workload {workload}",
+        "note": "per kernel: the mean over its captured launches; the call's total is "
+                "their sum"}
+    with open(path, "w") as f:
+        json.dump(table, f, indent=1)
+        f.write("\n")
+    print(json.dumps({key: table[key]}, indent=1))
+    return 0
+
+
 def phase_times(torch, D, run, steps, flush):
     """Per ABI call timing of one forward, split into route / permute /
     experts / combine (each call timed with events on the same stream)."""
@@ -384,7 +447,8 @@ def phase_times(torch, D, run, steps, flush):
     calls = {
         "route": lambda: m.moe_route(run.x, D.Wr, D.bias, d, idx, w, ws),
         "permute": lambda: m.moe_permute(idx, d, off, rt, tsr, ws),
-        "experts": lambda: m.moe_expert_ffn_fp8(run.x, off, rt, D.routed.abi(), d, y, ws),
+        "experts": lambda: _nvtx_range(torch, "moe_expert_ffn_fp8", lambda: m.moe_expert_ffn_fp8(
+            run.x, off, rt, D.routed.abi(), d, y, ws)),
         "combine": lambda: m.moe_combine(y, tsr, w, sy, d, out),
     }
     res = {k: [] for k in calls}
@@ -477,7 +541,8 @@ def run_gpu(args):
     B, F, expert_B = algorithmic(w, T, Dn)
     # M passes per step over R rotating copies: the K steps last ~1.5 s
     R = copies_for_l2(torch, B)
-    M = passes_per_step(single_pass_time(torch, run, flush), args.steps, R, 1.5)
+    M = passes_per_step(single_pass_time(torch, run, flush), args.steps, R, 1.5,
+                        max_passes=args.max_passes)
     if dist:  # every rank runs the same number of passes
         import torch.distributed as _d
         mt = torch.tensor([M], dtype=torch.int64, device="cuda")
@@ -658,11 +723,18 @@ def main(argv=None):
     ap.add_argument("--sweep-steps", type=int, default=10)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--max-passes", type=int, default=4096,
+                    help="at most this many layer passes per timed step (profiling runs)")
+    ap.add_argument("--record-traffic", metavar="CSV",
+                    help="store an ncu CSV's DRAM bytes per expert-FFN call for --workload "
+                         "in profiles/dram_traffic.json and exit (no GPU)")
     ap.add_argument("--oracle-sweep", action="store_true",
                     help="time the fp64 oracle on every workload (host only) and exit")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.record_traffic:
+        return record_traffic(args.record_traffic, args.workload)
     if args.oracle_sweep:
         return run_oracle_sweep(args)
     if args.impl == "reference":

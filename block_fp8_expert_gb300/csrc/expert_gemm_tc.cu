@@ -139,6 +139,8 @@ struct WsShared {
   // so that finding a tile's expert costs shared-memory reads only
   int tile_off[kMaxExperts + 1];
   int expert_off[kMaxExperts + 1];
+  // down epilogue: each warp's row exponents a of the current tile
+  int8_t ax[kEpiWarps][BT];
 };
 
 // Warp-uniform bounded wait: every lane polls the barrier together (the
@@ -557,6 +559,9 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     uint8_t* stg = smem + OFF_STG + (warp - W_EPI0) * STG_WARP_BYTES;
     const int nKb = cdiv(a.K, kScaleBlock), nRb = cdiv(a.rows_per_expert, kScaleBlock);
     const float inv_c = pow2f(-a.hid_shift);
+    // gate/up reads the row exponents ahead of its accumulators: after the
+    // kernel that wrote them has completed
+    if (GATEUP && !a.all_wait) griddep_wait();
     bool bad = false;
     int tl = 0;
     for (int t = blockIdx.x; t < n_tiles; t += tstride, ++tl) {
@@ -573,12 +578,40 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
              warp_max_exp_of(a.us + (size_t)ti.e * a.n_gu_scales, a.n_gu_scales, lane, bad) +
              a.hid_shift;
       }
+      // a of the tile's tokens, lane i holding token 32 c + i's for each
+      // chunk c this warp takes (gate/up: c = eh, eh + 2; down: c = 0 .. 3),
+      // all requested at once.  gate/up reads them before the accumulators
+      // are ready (its epilogue warps waited for the kernel that wrote them);
+      // down after its accumulator wait, which follows the token warp's
+      // acquire of the tile's hid rows (the rows' writer had waited for them).
+      // (|a| <= 126: one byte each; gate/up packs its two into a register,
+      // down parks its four in the warp's shared bytes, chunk u at 32 u + lane)
+      uint32_t axp = 0;
+      int8_t* axs = sh.ax[warp - W_EPI0];
+      auto load_ax = [&](int c0, int dc, int n) {
+        int v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = c0 + dc * u;
+          v[u] = (u < n && lane < ti.rows - 32 * c) ? __ldg(a.xexp + ti.r0 + ti.m0 + 32 * c + lane) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (GATEUP) axp |= ((uint32_t)v[u] & 0xffu) << (8 * u);
+          else axs[32 * u + lane] = (int8_t)v[u];
+        }
+      };
+      auto ax_of = [&](int u) {
+        return GATEUP ? (int)(int8_t)(axp >> (8 * u)) : (int)axs[32 * u + lane];
+      };
+      if (GATEUP) load_ax(eh, 2, 2);
       // this warp's copies of the previous tile have read its staging
       tc::bulk_wait_read_all();
       __syncwarp();
       if (!warp_wait(sh, &sh.acc_full, (uint32_t)(tl & 1), a.status, 8, tl)) break;
       tc::fence_after_sync();
       const int nchunks = (ti.n + 31) >> 5;
+      if (!GATEUP) load_ax(0, 1, 4);
       if (GATEUP) {
         bool overflow = false, underflow = false;
 #pragma unroll 1
@@ -586,9 +619,8 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
           uint32_t gr[32], ur[32];
           tc::ld_32x32b_x32(t_lane + 32 * c, gr);
           tc::ld_32x32b_x32(t_lane + COL_D1 + 32 * c, ur);
-          // a of this chunk's tokens: lane i holds token 32 c + i's
           const int nv = ti.rows - 32 * c;  // columns of real tokens in this chunk
-          const int ax = lane < nv ? __ldg(a.xexp + ti.r0 + ti.m0 + 32 * c + lane) : 0;
+          const int ax = ax_of((c - eh) >> 1);
           tc::wait_ld();
           uint8_t* rows = stg + (c >> 1) * (32 * 64);
           uint32_t small = 0, nonzero = 0;
@@ -653,7 +685,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
           tc::ld_32x32b_x32(t_lane + eh * COL_D1 + 32 * c, v);
           const int nv = ti.rows - 32 * c;
           const size_t row = (size_t)(ti.r0 + ti.m0 + 32 * c + lane);  // this lane's token row
-          const int ax = lane < nv ? __ldg(a.xexp + row) : 0;
+          const int ax = ax_of(c);
           tc::wait_ld();
           if (c == nchunks - 1) {
             // this warp's reads of the accumulators are done
