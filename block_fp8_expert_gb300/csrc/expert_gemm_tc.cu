@@ -124,13 +124,9 @@ struct GemmArgs {
 
 struct WsShared {
   uint64_t c_full[NCD], c_empty[NCD];
-  uint64_t t_full[2 * NT], t_empty[2 * NT];  // 2 NT half-size stages for a pair
+  uint64_t t_full[NT], t_empty[NT];
   uint64_t a_full[NA], a_empty[NA];
   uint64_t acc_full, acc_empty;
-  // CTA pair, even CTA only: the odd CTA's token stages (forwarded by its
-  // MMA warp: one arrival), decoded weight stages (its decoder warps arrive)
-  // and accumulator releases (its epilogue warps arrive)
-  uint64_t t_peer[2 * NT], a_peer[NA], acc_peer;
   uint32_t tmem_base;
   int abort_flag;
   uint64_t wait_ns;  // the role waits' budget (GemmArgs::wait_ns)
@@ -155,14 +151,10 @@ struct WsShared {
 // runs out records where: status[1] = warp + 1, status[2] = barrier id,
 // status[3] = step, status[4] = parity, status[5] = CTA, status[6..13] = how
 // far each role of that CTA had got.
-// CL: the barrier receives arrivals from the other CTA of a pair (acquire at
-// cluster scope).
-template <bool CL = false>
 __device__ __forceinline__ bool warp_wait(WsShared& sh, uint64_t* bar, uint32_t parity,
                                           int32_t* status, int bar_id = 0, int step = 0) {
   constexpr unsigned kAll = 0xffffffffu;
-  auto probe = [&]() { return CL ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
-  bool done = probe();
+  bool done = mbar_try_wait(bar, parity);
   if (__all_sync(kAll, done)) return true;
   const WaitBudget b = wait_budget(sh.wait_ns);
   for (uint32_t n = 1;; ++n) {
@@ -170,7 +162,7 @@ __device__ __forceinline__ bool warp_wait(WsShared& sh, uint64_t* bar, uint32_t 
       // the phase is complete: lanes that polled just before it completed
       // observe it now (bounded, although the phase cannot move on while
       // this warp has not consumed it)
-      for (int r = 0; !done && r < (1 << 16); ++r) done = probe();
+      for (int r = 0; !done && r < (1 << 16); ++r) done = mbar_try_wait(bar, parity);
       if (__all_sync(kAll, done)) return true;
       break;
     }
@@ -178,7 +170,7 @@ __device__ __forceinline__ bool warp_wait(WsShared& sh, uint64_t* bar, uint32_t 
       const bool give_up = *reinterpret_cast<volatile int*>(&sh.abort_flag) != 0 || budget_spent(b);
       if (__any_sync(kAll, give_up)) break;
     }
-    done = probe();
+    done = mbar_try_wait(bar, parity);
   }
   if ((threadIdx.x & 31) == 0 && !sh.abort_flag) {
     sh.abort_flag = 1;
@@ -228,18 +220,19 @@ __device__ __forceinline__ bool warp_wait_all(WsShared& sh, uint64_t* const (&ba
 }
 
 struct TileInfo {
-  int e, r0, m0, rows, n, n0;  // n = rows rounded up to 16 (32 for a pair): the MMA's N
+  int e, r0, m0, rows, n, n0;  // n = rows rounded up to 16 (the MMA's N)
   int slot;                    // token tile index (tile_off[e] + m0 / 128)
 };
 
-// CTAs (pairs) that take tiles, each taking every stride-th one; G of them.  All of them, except
+// CTAs that take tiles, each taking every stride-th one.  All of them, except
 // in this case: the down GEMM's CTAs can only start on SMs that gate/up CTAs
 // have left, and when gate/up's tiles do not divide evenly over its grid, r of
 // its CTAs run one tile longer, so the last r down CTAs (dispatched in order)
 // start one gate/up tile late.  If leaving those r CTAs without tiles ends
 // the launch sooner, in units of down tiles (a gate/up tile is H / I of one:
 // the same 256 x K x N shape with K = H rather than I), the stride is G - r.
-__device__ __forceinline__ int tile_stride(const GemmArgs& a, int n_tiles, int G) {
+__device__ __forceinline__ int tile_stride(const GemmArgs& a, int n_tiles) {
+  const int G = (int)gridDim.x;
   if (a.gu_grid != G || a.gu_grid <= 0) return G;
   const long long gu_tiles = (long long)a.tile_off[a.E] * a.gu_wblocks;
   if (gu_tiles <= a.gu_grid) return G;
@@ -254,13 +247,8 @@ __device__ __forceinline__ int tile_stride(const GemmArgs& a, int n_tiles, int G
 }
 
 // Tile t -> expert, token rows and weight rows, from the shared-memory copies.
-// A CTA pair's tile has twice the weight rows of a single CTA's (gate/up: 256
-// features, down: 512 output rows); CTA `rank` of the pair takes features
-// n0 .. n0 + 127 (gate/up; both matrices) or the two 128-row blocks n0 and
-// n0 + 256 (down), and the pair's token rows are split in halves of n / 2.
-template <bool PAIR>
 __device__ __forceinline__ TileInfo tile_info(const WsShared& sh, const GemmArgs& a, int t,
-                                              bool gateup, int rank) {
+                                              bool gateup) {
   TileInfo ti;
   const int slot = t / a.n_wblocks, wb = t % a.n_wblocks;
   int lo = 0, hi = a.E;  // largest e with tile_off[e] <= slot
@@ -273,21 +261,14 @@ __device__ __forceinline__ TileInfo tile_info(const WsShared& sh, const GemmArgs
   ti.r0 = sh.expert_off[lo];
   ti.m0 = (slot - sh.tile_off[lo]) * BT;
   ti.rows = min(BT, sh.expert_off[lo + 1] - ti.r0 - ti.m0);
-  ti.n = PAIR ? (ti.rows + 31) & ~31 : (ti.rows + 15) & ~15;
-  ti.n0 = PAIR ? wb * (gateup ? 2 * BW : 4 * BW) + BW * rank : wb * (gateup ? BW : 2 * BW);
+  ti.n = (ti.rows + 15) & ~15;
+  ti.n0 = wb * (gateup ? BW : 2 * BW);
   return ti;
 }
 
 }  // namespace
 
-// PAIR: launched in clusters of two CTAs (an SM pair).  The even CTA issues
-// the MMAs for both (cta_group::2, M = 256: its weight rows, then the odd
-// CTA's), each CTA holding half of the token tile in its shared memory and
-// its own accumulators; the MMA commits arrive on both CTAs' barriers.  The
-// odd CTA's MMA warp forwards its token stages, decoded weight stages and
-// accumulator releases to the even CTA (remote mbarrier arrivals).  Per SM
-// this halves the token copies and the MMA's shared-memory operand reads.
-template <bool GATEUP, bool PAIR>
+template <bool GATEUP>
 __global__ void __launch_bounds__(kThreadsWS, 1)
 k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant__ CUtensorMap cm1,
                  const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_y,
@@ -303,20 +284,10 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
   griddep_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const GemmArgs& a = args;
-  // tile takers: CTAs, or CTA pairs (unit = the pair's index, rank = the
-  // CTA's place in it)
-  const int rank = PAIR ? (int)tc::cluster_rank() : 0;
-  const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int G = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   const int n_tiles = a.tile_off[a.E] * a.n_wblocks;
-  const int tstride = GATEUP ? G : tile_stride(a, n_tiles, G);
-  // uniform per CTA (and per pair), before any barrier
-  if (unit >= n_tiles || unit >= tstride) return;
-  constexpr int kBlkRows = PAIR ? 2 * BW : BW;  // down: block 1's rows after block 0's
-  // a pair's CTA holds half of each token tile: twice the stages of half the
-  // size in the same shared memory
-  constexpr int kNT = PAIR ? 2 * NT : NT;
-  constexpr int kTB = PAIR ? T_BYTES / 2 : T_BYTES;  // token bytes per stage and CTA
+  const int tstride = GATEUP ? (int)gridDim.x : tile_stride(a, n_tiles);
+  // uniform per CTA, before any barrier
+  if ((int)blockIdx.x >= n_tiles || (int)blockIdx.x >= tstride) return;
   const int nK = a.K / BK;
   const int nKb = cdiv(a.K, kScaleBlock);
   const int nRb = cdiv(a.rows_per_expert, kScaleBlock);
@@ -330,7 +301,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
       mbar_init(&sh.c_full[s], 1);
       mbar_init(&sh.c_empty[s], kDecWarps);
     }
-    for (int s = 0; s < kNT; ++s) {
+    for (int s = 0; s < NT; ++s) {
       mbar_init(&sh.t_full[s], 1);
       mbar_init(&sh.t_empty[s], 1);
     }
@@ -340,11 +311,6 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     }
     mbar_init(&sh.acc_full, 1);
     mbar_init(&sh.acc_empty, kEpiWarps);
-    if (PAIR) {
-      for (int s = 0; s < kNT; ++s) mbar_init(&sh.t_peer[s], 1);
-      for (int s = 0; s < NA; ++s) mbar_init(&sh.a_peer[s], kDecWarps);
-      mbar_init(&sh.acc_peer, kEpiWarps);
-    }
     sh.abort_flag = 0;
     sh.wait_ns = a.wait_ns;
     for (int i = 0; i < kWarps + 3; ++i) sh.prog[i] = 0;
@@ -355,19 +321,11 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     sh.expert_off[i] = a.expert_off[i];
   }
   if (warp == 0) {
-    if (PAIR) {
-      tc::tmem_alloc_pair(&sh.tmem_base, TMEM_COLS);
-      tc::tmem_relinquish_pair();
-    } else {
-      tc::tmem_alloc(&sh.tmem_base, TMEM_COLS);
-      tc::tmem_relinquish();
-    }
+    tc::tmem_alloc(&sh.tmem_base, TMEM_COLS);
+    tc::tmem_relinquish();
   }
   tc::fence_before_sync();
   __syncthreads();
-  // a pair: both CTAs' barriers are initialised before either arrives on
-  // the other's
-  if (PAIR) tc::cluster_sync();
   tc::fence_after_sync();
   const uint32_t tmem = sh.tmem_base;
 
@@ -375,8 +333,8 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     // ------------------------------------------------ E4M3 code blocks (TMA)
     int j = 0;
     bool ok = true;
-    for (int t = unit; t < n_tiles && ok; t += tstride) {
-      const TileInfo ti = tile_info<PAIR>(sh, a, t, GATEUP, rank);
+    for (int t = blockIdx.x; t < n_tiles && ok; t += tstride) {
+      const TileInfo ti = tile_info(sh, a, t, GATEUP);
       const int row = ti.e * a.rows_per_expert + ti.n0;
       for (int ks = 0; ks < nK; ++ks, ++j) {
         const int sc = j % NCD;
@@ -395,7 +353,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
             tc::tma_load_2d(dst + BW * BK, &cm1, ks * BK, row, &sh.c_full[sc]);
           } else {
             tc::tma_load_2d(dst, &cm0, ks * BK, row, &sh.c_full[sc]);
-            tc::tma_load_2d(dst + BW * BK, &cm0, ks * BK, row + kBlkRows, &sh.c_full[sc]);
+            tc::tma_load_2d(dst + BW * BK, &cm0, ks * BK, row + BW, &sh.c_full[sc]);
           }
           reinterpret_cast<volatile int*>(sh.prog)[W_CODES] = j + 1;
         }
@@ -413,8 +371,8 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     // are never stored; rows past the matrix read 0).
     int j = 0;
     bool ok = true;
-    for (int t = unit; t < n_tiles && ok; t += tstride) {
-      const TileInfo ti = tile_info<PAIR>(sh, a, t, GATEUP, rank);
+    for (int t = blockIdx.x; t < n_tiles && ok; t += tstride) {
+      const TileInfo ti = tile_info(sh, a, t, GATEUP);
       if (!GATEUP && a.slot_done) {
         // this token tile's hid rows: every gate/up weight-block tile of the
         // slot has stored them (bounded warp-uniform poll, then the acquired
@@ -449,25 +407,22 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
         tc::fence_proxy_async_global();
       }
       for (int ks = 0; ks < nK; ++ks, ++j) {
-        const int st = j % kNT;
-        if (j >= kNT && !warp_wait(sh, &sh.t_empty[st], (uint32_t)(((j / kNT) - 1) & 1), a.status, 2, j)) {
+        const int st = j % NT;
+        if (j >= NT && !warp_wait(sh, &sh.t_empty[st], (uint32_t)(((j / NT) - 1) & 1), a.status, 2, j)) {
           ok = false;
           break;
         }
         if (tc::elect_one()) {
-          // a pair's CTA holds token rows rank n / 2 .. of the tile (a box of
-          // BT / 2 rows; rows past n / 2 are not read by the MMA)
-          mbar_arrive_expect_tx(&sh.t_full[st], kTB);
-          tc::tma_load_2d(smem + OFF_T + st * kTB, &tmap, ks * BK,
-                          ti.r0 + ti.m0 + (PAIR ? rank * (ti.n >> 1) : 0), &sh.t_full[st]);
+          mbar_arrive_expect_tx(&sh.t_full[st], T_BYTES);
+          tc::tma_load_2d(smem + OFF_T + st * T_BYTES, &tmap, ks * BK, ti.r0 + ti.m0, &sh.t_full[st]);
           reinterpret_cast<volatile int*>(sh.prog)[warp] = j + 1;
         }
         __syncwarp();
       }
     }
-    // drain: the copies of the last kNT steps issued must have landed
+    // drain: the copies of the last NT steps issued must have landed
     if (lane == 0)
-      for (int i = max(0, j - kNT); i < j; ++i) mbar_wait(&sh.t_full[i % kNT], (uint32_t)((i / kNT) & 1));
+      for (int i = max(0, j - NT); i < j; ++i) mbar_wait(&sh.t_full[i % NT], (uint32_t)((i / NT) & 1));
     __syncwarp();
   } else if (warp >= W_DEC0 && warp < W_DEC0 + kDecWarps) {
     // ------------------------------------------------ decode E4M3 -> fp16 -> TMEM
@@ -490,17 +445,17 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     const float* sp = (GATEUP && blk) ? a.s1 : a.s0;
     bool bad = false;
     auto scale_of = [&](int t) -> float {
-      const TileInfo ti = tile_info<PAIR>(sh, a, t, GATEUP, rank);
-      const size_t srow = (size_t)ti.e * nRb + (ti.n0 + (GATEUP ? 0 : blk * kBlkRows)) / kScaleBlock;
+      const TileInfo ti = tile_info(sh, a, t, GATEUP);
+      const size_t srow = (size_t)ti.e * nRb + ti.n0 / kScaleBlock + (GATEUP ? 0 : blk);
       const float sc = lane < nKb ? sp[srow * nKb + lane] : 0.f;
       const int p = GATEUP ? warp_max_exp_of(sp + (size_t)ti.e * nRb * nKb, nRb * nKb, lane, bad)
                            : warp_max_exp(__float_as_uint(sc) & 0x7fffffffu, bad);
       return sc * pow2f(-p);
     };
-    float scale_next = scale_of(unit);
+    float scale_next = scale_of(blockIdx.x);
     int j = 0;
     bool ok = true;
-    for (int t = unit; t < n_tiles && ok; t += tstride) {
+    for (int t = blockIdx.x; t < n_tiles && ok; t += tstride) {
       const float scale_tile = scale_next;
       if (t + tstride < n_tiles) scale_next = scale_of(t + tstride);
       for (int ks = 0; ks < nK; ++ks, ++j) {
@@ -534,50 +489,21 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) {
-          // a pair's odd CTA: straight to the even CTA, whose MMA reads it
-          if (PAIR && rank == 1) tc::mbar_arrive_remote(tc::map_to_rank(&sh.a_peer[sa], 0));
-          else mbar_arrive(&sh.a_full[sa]);
+          mbar_arrive(&sh.a_full[sa]);
           mbar_arrive(&sh.c_empty[sc]);
           reinterpret_cast<volatile int*>(sh.prog)[warp] = j + 1;
         }
       }
     }
     if (bad && lane == 0) raise_status(a.status, MOE_DEV_NONFINITE);
-  } else if (warp == W_MMA && PAIR && rank == 1) {
-    // ------------------------------------------------ pair, odd CTA: forward
-    // this CTA's landed token stages to the even CTA, whose MMAs read them
-    // (its decoder and epilogue warps arrive on the even CTA's barriers
-    // themselves)
-    int j = 0;
-    bool ok = true;
-    for (int t = unit; t < n_tiles && ok; t += tstride) {
-      for (int ks = 0; ks < nK; ++ks, ++j) {
-        const int st = j % kNT;
-        if (!warp_wait(sh, &sh.t_full[st], (uint32_t)((j / kNT) & 1), a.status, 11, j)) {
-          ok = false;
-          break;
-        }
-        if (tc::elect_one()) {
-          tc::mbar_arrive_remote(tc::map_to_rank(&sh.t_peer[st], 0));
-          reinterpret_cast<volatile int*>(sh.prog)[kWarps] = j + 1;
-        }
-        __syncwarp();
-      }
-    }
   } else if (warp == W_MMA) {
     // ------------------------------------------------ tcgen05.mma issue
     int j = 0, tl = 0;
     bool ok = true;
-    for (int t = unit; t < n_tiles && ok; t += tstride, ++tl) {
-      const TileInfo ti = tile_info<PAIR>(sh, a, t, GATEUP, rank);
-      const uint32_t idesc = tc::idesc_f16_f32(PAIR ? 2 * BW : BW, ti.n);
+    for (int t = blockIdx.x; t < n_tiles && ok; t += tstride, ++tl) {
+      const TileInfo ti = tile_info(sh, a, t, GATEUP);
+      const uint32_t idesc = tc::idesc_f16_f32(BW, ti.n);
       if (tl >= 1 && !warp_wait(sh, &sh.acc_empty, (uint32_t)((tl - 1) & 1), a.status, 5, tl)) {
-        ok = false;
-        break;
-      }
-      // a pair: the odd CTA's epilogue has released its accumulators too
-      if (PAIR && tl >= 1 &&
-          !warp_wait<true>(sh, &sh.acc_peer, (uint32_t)((tl - 1) & 1), a.status, 13, tl)) {
         ok = false;
         break;
       }
@@ -586,21 +512,13 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
       // both steps' operands, then their 16 MMAs back to back, so that the
       // tensor pipe's queue stays ahead of the barrier round trips.
       for (int ks = 0; ks < nK; ks += 2, j += 2) {
-        const int st0 = j % kNT, sa0 = j % NA, st1 = (j + 1) % kNT, sa1 = (j + 1) % NA;
+        const int st0 = j % NT, sa0 = j % NA, st1 = (j + 1) % NT, sa1 = (j + 1) % NA;
         uint64_t* const bars[4] = {&sh.t_full[st0], &sh.a_full[sa0], &sh.t_full[st1],
                                    &sh.a_full[sa1]};
-        const uint32_t par[4] = {(uint32_t)((j / kNT) & 1), (uint32_t)((j / NA) & 1),
-                                 (uint32_t)(((j + 1) / kNT) & 1), (uint32_t)(((j + 1) / NA) & 1)};
+        const uint32_t par[4] = {(uint32_t)((j / NT) & 1), (uint32_t)((j / NA) & 1),
+                                 (uint32_t)(((j + 1) / NT) & 1), (uint32_t)(((j + 1) / NA) & 1)};
         const int ids[4] = {6, 7, 6, 7};
         if (!warp_wait_all(sh, bars, par, a.status, ids, j)) {
-          ok = false;
-          break;
-        }
-        // a pair: the odd CTA's halves of both steps are in place too
-        if (PAIR && (!warp_wait<true>(sh, &sh.t_peer[st0], par[0], a.status, 14, j) ||
-                     !warp_wait<true>(sh, &sh.a_peer[sa0], par[1], a.status, 15, j) ||
-                     !warp_wait<true>(sh, &sh.t_peer[st1], par[2], a.status, 14, j + 1) ||
-                     !warp_wait<true>(sh, &sh.a_peer[sa1], par[3], a.status, 15, j + 1))) {
           ok = false;
           break;
         }
@@ -609,32 +527,19 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int st = h ? st1 : st0, sa = h ? sa1 : sa0;
-            const uint32_t b_addr = smem_base + OFF_T + st * kTB;
+            const uint32_t b_addr = smem_base + OFF_T + st * T_BYTES;
             const uint32_t a_col = tmem + COL_A + (uint32_t)sa * A_STAGE_COLS;
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
               const uint64_t bdesc = tc::sw128_desc(b_addr + kk * 32);
               const uint32_t acc = (ks + h > 0 || kk > 0) ? 1u : 0u;
-              if (PAIR) {
-                tc::mma_f16_ts_pair(tmem, a_col + kk * 8, bdesc, idesc, acc);
-                tc::mma_f16_ts_pair(tmem + COL_D1, a_col + 32 + kk * 8, bdesc, idesc, acc);
-              } else {
-                tc::mma_f16_ts(tmem, a_col + kk * 8, bdesc, idesc, acc);
-                tc::mma_f16_ts(tmem + COL_D1, a_col + 32 + kk * 8, bdesc, idesc, acc);
-              }
+              tc::mma_f16_ts(tmem, a_col + kk * 8, bdesc, idesc, acc);
+              tc::mma_f16_ts(tmem + COL_D1, a_col + 32 + kk * 8, bdesc, idesc, acc);
             }
-            if (PAIR) {  // both CTAs' stages are free once these MMAs complete
-              tc::commit_pair(&sh.t_empty[st], 3);
-              tc::commit_pair(&sh.a_empty[sa], 3);
-            } else {
-              tc::commit(&sh.t_empty[st]);
-              tc::commit(&sh.a_empty[sa]);
-            }
+            tc::commit(&sh.t_empty[st]);
+            tc::commit(&sh.a_empty[sa]);
           }
-          if (ks + 2 == nK) {
-            if (PAIR) tc::commit_pair(&sh.acc_full, 3);
-            else tc::commit(&sh.acc_full);
-          }
+          if (ks + 2 == nK) tc::commit(&sh.acc_full);
           reinterpret_cast<volatile int*>(sh.prog)[kWarps] = j + 2;
           reinterpret_cast<volatile int*>(sh.prog)[kWarps + 1] = tl + 1;
         }
@@ -659,14 +564,14 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     if (GATEUP && !a.all_wait) griddep_wait();
     bool bad = false;
     int tl = 0;
-    for (int t = unit; t < n_tiles; t += tstride, ++tl) {
-      const TileInfo ti = tile_info<PAIR>(sh, a, t, GATEUP, rank);
+    for (int t = blockIdx.x; t < n_tiles; t += tstride, ++tl) {
+      const TileInfo ti = tile_info(sh, a, t, GATEUP);
       // the tile's powers of two (scales only: computed before the wait)
       int p0 = 0;  // gate/up: pg; down: pd + pg + pu + c
       if (GATEUP) {
         p0 = warp_max_exp_of(a.s0 + (size_t)ti.e * nRb * nKb, nRb * nKb, lane, bad);
       } else {
-        const size_t srow = (size_t)ti.e * nRb + (ti.n0 + eh * kBlkRows) / kScaleBlock;
+        const size_t srow = (size_t)ti.e * nRb + ti.n0 / kScaleBlock + eh;
         const float sc = lane < nKb ? a.s0[srow * nKb + lane] : 0.f;
         p0 = warp_max_exp(__float_as_uint(sc) & 0x7fffffffu, bad) +
              warp_max_exp_of(a.gs + (size_t)ti.e * a.n_gu_scales, a.n_gu_scales, lane, bad) +
@@ -742,10 +647,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
         if (overflow || underflow) raise_status(a.status, MOE_DEV_FP16_RANGE);
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) {  // a pair's odd CTA: to the even CTA, which issues the MMAs
-          if (PAIR && rank == 1) tc::mbar_arrive_remote(tc::map_to_rank(&sh.acc_peer, 0));
-          else mbar_arrive(&sh.acc_empty);
-        }
+        if (lane == 0) mbar_arrive(&sh.acc_empty);
         // staged rows -> bulk copies (async proxy): features 32 q .. + 31 of
         // each of this half's token rows, 64 bytes
         tc::fence_proxy_async();
@@ -776,7 +678,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
         // and the group exponent of its 32 values are lane-local.  A chunk of
         // 32 real tokens leaves by one TMA store from the staging tile; a
         // ragged chunk's real rows by plain stores.
-        const int col0 = ti.n0 + eh * kBlkRows + 32 * q;  // first of this warp's 32 columns
+        const int col0 = ti.n0 + eh * BW + 32 * q;  // first of this warp's 32 columns
 #pragma unroll 1
         for (int c = 0; c < nchunks; ++c) {
           uint32_t v[32];
@@ -789,10 +691,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
             // this warp's reads of the accumulators are done
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) {  // a pair's odd CTA: to the even CTA
-              if (PAIR && rank == 1) tc::mbar_arrive_remote(tc::map_to_rank(&sh.acc_peer, 0));
-              else mbar_arrive(&sh.acc_empty);
-            }
+            if (lane == 0) mbar_arrive(&sh.acc_empty);
           }
           // the previous store from the staging tile has read it
           tc::bulk_wait_read_all();
@@ -881,15 +780,12 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     __syncwarp();
   }
 
-  // ---- all roles done: free TMEM (a pair: after the even CTA's MMAs into
-  // both CTAs' tensor memory have completed)
+  // ---- all roles done: free TMEM
   tc::fence_before_sync();
   __syncthreads();
-  if (PAIR) tc::cluster_sync();
   if (warp == 0) {
     tc::fence_after_sync();
-    if (PAIR) tc::tmem_dealloc_pair(tmem, TMEM_COLS);
-    else tc::tmem_dealloc(tmem, TMEM_COLS);
+    tc::tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
@@ -1120,19 +1016,6 @@ bool expert_gemm_tc_ok(int H, int I) {
          I <= 32 * kScaleBlock;
 }
 
-// CTA pairs (two-SM tiles): only when MOE_FP8_GEMM_PAIR=1 (read on every
-// call).  The pair halves each SM's token copies and the MMA's shared-memory
-// operand reads, but each SM still decodes both of its weight blocks per K
-// step, and that decode is what bounds the K step: measured at prefill
-// T = 4096, 468 us per layer pass against 438 us with single CTAs.
-bool use_gemm_pair(int P, int E, int H, int I) {
-  (void)P;
-  (void)E;
-  if (H % (4 * BW) != 0 || I % (2 * BW) != 0 || num_sms() < 2) return false;
-  const char* v = getenv("MOE_FP8_GEMM_PAIR");
-  return v && v[0] == '1';
-}
-
 cudaError_t launch_expert_gemm_tc(const uint16_t* x, int T, const int32_t* expert_off,
                                   const int32_t* row_token, uint16_t* x_perm, int32_t* xexp,
                                   int E, int P, const moe_fp8_ffn& w, int H, int I,
@@ -1142,31 +1025,20 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x, int T, const int32_t* exper
   static_assert(BT == kGemmTokenTile, "token tile of the permutation's tile prefix");
   if (!x_perm || !xexp || H > kGatherMaxPieces * 256) return cudaErrorInvalidValue;
   cudaError_t err;
-  const bool pair = use_gemm_pair(P, E, H, I);
-  if (pair) {
-    if ((err = ensure_smem((const void*)k_expert_gemm_ws<true, true>, SMEM_WS)) != cudaSuccess)
-      return err;
-    if ((err = ensure_smem((const void*)k_expert_gemm_ws<false, true>, SMEM_WS)) != cudaSuccess)
-      return err;
-  } else {
-    if ((err = ensure_smem((const void*)k_expert_gemm_ws<true, false>, SMEM_WS)) != cudaSuccess)
-      return err;
-    if ((err = ensure_smem((const void*)k_expert_gemm_ws<false, false>, SMEM_WS)) != cudaSuccess)
-      return err;
-  }
+  if ((err = ensure_smem((const void*)k_expert_gemm_ws<true>, SMEM_WS)) != cudaSuccess) return err;
+  if ((err = ensure_smem((const void*)k_expert_gemm_ws<false>, SMEM_WS)) != cudaSuccess) return err;
   CUtensorMap gmap, umap, dmap, xmap, hmap, ymap;
   if ((err = code_map(&gmap, w.gate.codes, (long long)E * I, H)) != cudaSuccess) return err;
   if ((err = code_map(&umap, w.up.codes, (long long)E * I, H)) != cudaSuccess) return err;
   if ((err = code_map(&dmap, w.down.codes, (long long)E * H, I)) != cudaSuccess) return err;
   // Normalised activations in expert order [P, H] fp16 and hid [P, I] fp16:
-  // 64 columns x 128 rows per box (a pair's CTA: 64 rows, half of the
-  // tile), 128-byte swizzled (the K-major operand layout of the MMA)
-  const int tbox = pair ? BT / 2 : BT;
-  if ((err = make_tensor_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x_perm, P, H, BK, tbox,
+  // 64 columns x 128 rows per box, 128-byte swizzled (the K-major operand
+  // layout of the MMA)
+  if ((err = make_tensor_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x_perm, P, H, BK, BT,
                                 128)) != cudaSuccess)
     return err;
-  if ((err = make_tensor_map_2d(&hmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, hid, P, I, BK, tbox,
-                                128)) != cudaSuccess)
+  if ((err = make_tensor_map_2d(&hmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, hid, P, I, BK, BT, 128)) !=
+      cudaSuccess)
     return err;
   // y [P, H], written by the down epilogue: 32 columns x 32 rows; fp32 rows of
   // 128 bytes (128-byte swizzle) or fp16 rows of 64 bytes (64-byte swizzle)
@@ -1209,9 +1081,7 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x, int T, const int32_t* exper
   }
   const char* stall = getenv("MOE_FP8_TEST_STALL");
   const bool stall_down = stall && strcmp(stall, "down") == 0 && slot_done;
-  // tile takers: one CTA per SM, or one pair per two SMs
-  const int units = pair ? num_sms() / 2 : num_sms();
-  const int per_unit = pair ? 2 : 1;  // CTAs per taker
+  const int nsm = num_sms();
   const dim3 blk(kThreadsWS);
   GemmArgs g{};
   g.expert_off = expert_off;
@@ -1223,7 +1093,7 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x, int T, const int32_t* exper
   g.s1 = w.up.scales;
   g.out = hid;
   g.out_ld = I;
-  g.n_wblocks = I / (BW * per_unit);
+  g.n_wblocks = I / BW;
   // every warp waits when the previous kernel wrote the tile offsets
   g.all_wait = prev_wrote_offsets ? 1 : 0;
   g.slot_done = slot_done;
@@ -1232,11 +1102,8 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x, int T, const int32_t* exper
   g.xexp = xexp;
   g.hid_shift = log2H + 4;
   g.wait_ns = wait_ns;
-  const int gu_units = min(units, max_ttiles * g.n_wblocks);
-  err = pair ? launch_k_pair(k_expert_gemm_ws<true, true>, dim3(2 * gu_units), blk,
-                             (size_t)SMEM_WS, s, pdl, gmap, umap, xmap, ymap, g)
-             : launch_k(k_expert_gemm_ws<true, false>, dim3(gu_units), blk, (size_t)SMEM_WS, s,
-                        pdl, gmap, umap, xmap, ymap, g);
+  err = launch_k(k_expert_gemm_ws<true>, dim3(min(nsm, max_ttiles * g.n_wblocks)), blk,
+                 (size_t)SMEM_WS, s, pdl, gmap, umap, xmap, ymap, g);
   if (err != cudaSuccess) return err;
   GemmArgs d{};
   d.expert_off = expert_off;
@@ -1248,7 +1115,7 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x, int T, const int32_t* exper
   d.s1 = nullptr;
   d.out = y;
   d.out_ld = H;
-  d.n_wblocks = H / (2 * BW * per_unit);
+  d.n_wblocks = H / (2 * BW);
   d.all_wait = 0;
   d.slot_done = slot_done;
   d.slot_need = (I / BW) * kEpiWarps;
@@ -1262,15 +1129,13 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x, int T, const int32_t* exper
   d.yexp_rows = yexp_rows;
   d.wait_ns = wait_ns;
   if (stall_down) d.slot_need += 1;
-  const int dn_units = min(units, max_ttiles * d.n_wblocks);
-  if (gu_units == units && dn_units == units) {
-    d.gu_grid = gu_units;
+  const int gu_grid = min(nsm, max_ttiles * g.n_wblocks);
+  if (gu_grid == nsm && min(nsm, max_ttiles * d.n_wblocks) == nsm) {
+    d.gu_grid = gu_grid;
     d.gu_wblocks = g.n_wblocks;
   }
-  return pair ? launch_k_pair(k_expert_gemm_ws<false, true>, dim3(2 * dn_units), blk,
-                              (size_t)SMEM_WS, s, pdl, dmap, dmap, hmap, ymap, d)
-              : launch_k(k_expert_gemm_ws<false, false>, dim3(dn_units), blk, (size_t)SMEM_WS, s,
-                         pdl, dmap, dmap, hmap, ymap, d);
+  return launch_k(k_expert_gemm_ws<false>, dim3(min(nsm, max_ttiles * d.n_wblocks)), blk,
+                  (size_t)SMEM_WS, s, pdl, dmap, dmap, hmap, ymap, d);
 }
 
 }  // namespace moe

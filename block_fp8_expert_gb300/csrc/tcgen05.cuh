@@ -40,22 +40,6 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols)
                : "memory");
 }
-// The same for a CTA pair (cta_group::2): one warp of each of the two CTAs
-// executes these together; the pair's tensor memory is allocated alike in
-// both CTAs.  A kernel uses one cta_group for all of its tcgen05 operations.
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
-                   smem_u32(dst)),
-               "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish_pair() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;\n" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
 __device__ __forceinline__ void fence_before_sync() {
   asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
 }
@@ -110,29 +94,6 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, uin
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
       "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// CTA pair: D (M = 256 rows: lanes 0..127 of this CTA's and of the peer's
-// tensor memory) (+)= A (rows 0..127 at `tmem_a` in this CTA, 128..255 at the
-// same address in the peer) * B^T, B's N columns split in halves between the
-// two CTAs' shared memory at the same address.  Issued by one thread of the
-// even CTA of the pair.
-__device__ __forceinline__ void mma_f16_ts_pair(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc,
-                                                uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
-      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Arrive once on the mbarrier at `bar`'s offset in every CTA of `cta_mask`
-// (bit = rank in the cluster) when the pair's tcgen05 operations this thread
-// issued so far have completed.
-__device__ __forceinline__ void commit_pair(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;\n" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
       : "memory");
 }
 // Arrive once on `bar` when all tcgen05 operations this thread issued so far
@@ -193,29 +154,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// --- thread-block clusters --------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
-  return r;
-}
-// Shared::cluster address of this CTA's shared variable `p` in CTA `rank`.
-__device__ __forceinline__ uint32_t map_to_rank(const void* p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-  return r;
-}
-// Arrive on an mbarrier of another CTA of the cluster, given by its
-// shared::cluster address (default semantics: release; what the arriving
-// thread wrote before is ordered before the arrival).
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];\n" ::"r"(cluster_addr) : "memory");
-}
-// All threads of every CTA of the cluster (release / acquire).
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" :::
-                   "memory");
-}
 // Global-memory accesses of the generic proxy <-> the async proxy (bulk and
 // tensor copies) of this thread.
 __device__ __forceinline__ void fence_proxy_async_global() {
