@@ -464,10 +464,14 @@ moe_status layer_forward(const uint16_t* x, const float* Wr, const float* bias,
                             at<uint16_t>(ws, L.wr_planes), idx, w, xn, xe, status, st, true,
                             shared_gate, sgate),
                "moe_layer_forward: route");
+    // (with the tensor-core GEMM: also its token-tile prefix and zeroed
+    // completion counters, so that no tile-offset launch follows)
     CUDA_CHECK(launch_permute(idx, d.T, d.E, d.k, at<int32_t>(ws, L.rank),
                               at<int32_t>(ws, L.block_cnt), at<int32_t>(ws, L.block_base), off,
                               row_token, tok_slot_row, at<int32_t>(ws, L.row_pair), active,
-                              status, st, true),
+                              status, st, true, gemm ? at<int32_t>(ws, L.tile_off) : nullptr,
+                              gemm ? at<int32_t>(ws, L.slot_done) : nullptr,
+                              gemm ? expert_gemm_slots(P, d.E) : 0),
                "moe_layer_forward: permute");
     if (sep_shared)
       CUDA_CHECK(launch_identity_perm(d.T, soff, srows, sact, st, true),
@@ -492,7 +496,7 @@ moe_status layer_forward(const uint16_t* x, const float* Wr, const float* bias,
                                      at<int32_t>(ws, L.xexp), d.E, P, routed, d.H, d.I,
                                      at<int32_t>(ws, L.tile_off), at<int32_t>(ws, L.slot_done),
                                      at<uint16_t>(ws, L.hid), y_perm, yexp, y_rows, status, st,
-                                     true, /*tile_off_ready=*/small, gth),
+                                     true, /*tile_off_ready=*/true, gth),
                "moe_layer_forward: experts");
   } else {
     FusedCombine cmb;

@@ -113,10 +113,15 @@ cudaError_t launch_route_permute_small(const uint16_t* x, const float* Wr, const
                                        const float* shared_gate = nullptr,
                                        float* sgate = nullptr);
 
+// The multi-kernel permutation (T*k > 4096).  tile_off (E + 1 ints, may be
+// NULL): also the tensor-core GEMM's token-tile prefix; counters[0,
+// n_counters) (may be NULL) are zeroed (the GEMM's completion counters).
 cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, int32_t* rank,
                            int32_t* block_cnt, int32_t* block_base, int32_t* expert_off,
                            int32_t* row_token, int32_t* tok_slot_row, int32_t* row_pair,
-                           int32_t* active, int32_t* status, cudaStream_t s, bool pdl);
+                           int32_t* active, int32_t* status, cudaStream_t s, bool pdl,
+                           int32_t* tile_off = nullptr, int32_t* counters = nullptr,
+                           int n_counters = 0);
 
 cudaError_t launch_active_from_offsets(const int32_t* expert_off, int E, int32_t* active,
                                        int32_t* status, cudaStream_t s, bool pdl);

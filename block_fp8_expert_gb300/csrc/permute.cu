@@ -55,77 +55,103 @@ k_perm_count(const int32_t* __restrict__ topk_idx, int P, int E,
   if (q < P) rank[q] = e >= 0 ? cnt_w[warp * E + e] + rank_w : -1;
 }
 
-// One CTA of 1024 threads; E <= 1024.
+// One CTA of 1024 threads; E <= 1024.  Each expert's column of block counts
+// is split among G = 1024 / E threads (contiguous runs of blocks): each sums
+// its run (independent loads), the runs' sums are prefixed in shared memory,
+// and each thread writes its run's block bases.  Then the scan over experts
+// gives the offsets, the active list and, when tile_off is set, the
+// tensor-core GEMM's token-tile prefix (tile_off[e] = sum over e' < e of
+// ceil(count / kGemmTokenTile)); counters[0, n_counters) are zeroed.
 __global__ void __launch_bounds__(1024)
 k_perm_scan(const int32_t* __restrict__ block_cnt, int nblocks, int E,
             int32_t* __restrict__ block_base, int32_t* __restrict__ expert_off,
-            int32_t* __restrict__ active) {
+            int32_t* __restrict__ active, int32_t* __restrict__ tile_off,
+            int32_t* __restrict__ counters, int n_counters) {
+  __shared__ int32_t part[1024];
   __shared__ int32_t warp_sum[32];
   __shared__ int32_t warp_act[32];
+  __shared__ int32_t warp_til[32];
   griddep_wait();
   griddep_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int total = 0;
-  if (tid < E) {
-    // exclusive prefix over blocks for expert tid
-    int b = 0;
-    for (; b + 4 <= nblocks; b += 4) {
-      const int c0 = block_cnt[(size_t)(b + 0) * E + tid];
-      const int c1 = block_cnt[(size_t)(b + 1) * E + tid];
-      const int c2 = block_cnt[(size_t)(b + 2) * E + tid];
-      const int c3 = block_cnt[(size_t)(b + 3) * E + tid];
-      block_base[(size_t)(b + 0) * E + tid] = total;
-      block_base[(size_t)(b + 1) * E + tid] = total + c0;
-      block_base[(size_t)(b + 2) * E + tid] = total + c0 + c1;
-      block_base[(size_t)(b + 3) * E + tid] = total + c0 + c1 + c2;
-      total += c0 + c1 + c2 + c3;
+  const int G = min(32, 1024 / E);  // threads per expert
+  const int e = tid % E, g = tid / E;
+  const bool mine = g < G;
+  const int b0 = mine ? (int)((long long)g * nblocks / G) : 0;
+  const int b1 = mine ? (int)((long long)(g + 1) * nblocks / G) : 0;
+  int run = 0;
+#pragma unroll 8
+  for (int b = b0; b < b1; ++b) run += block_cnt[(size_t)b * E + e];
+  part[tid] = run;
+  __syncthreads();
+  int before = 0, total = 0;
+  if (mine)
+    for (int h = 0; h < G; ++h) {
+      const int v = part[h * E + e];
+      if (h < g) before += v;
+      total += v;
     }
-    for (; b < nblocks; ++b) {
-      const int c = block_cnt[(size_t)b * E + tid];
-      block_base[(size_t)b * E + tid] = total;
-      total += c;
-    }
+  run = before;
+#pragma unroll 8
+  for (int b = b0; b < b1; ++b) {
+    const int c = block_cnt[(size_t)b * E + e];
+    block_base[(size_t)b * E + e] = run;
+    run += c;
   }
-  // exclusive scan of totals (and of the non-empty flags) over experts
-  int incl = total, act = total > 0 ? 1 : 0;
+  if (counters)
+    for (int i = tid; i < n_counters; i += 1024) counters[i] = 0;
+  // exclusive scans over experts (threads tid < E: expert tid) of the totals,
+  // of the non-empty flags and of the token-tile counts
+  if (tid >= E) total = 0;
+  const int ntile = (total + kGemmTokenTile - 1) / kGemmTokenTile;
+  int incl = total, act = total > 0 ? 1 : 0, til = ntile;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    const int a = __shfl_up_sync(0xffffffffu, act, o);
+    const int w = __shfl_up_sync(0xffffffffu, act, o);
+    const int u = __shfl_up_sync(0xffffffffu, til, o);
     if (lane >= o) {
       incl += v;
-      act += a;
+      act += w;
+      til += u;
     }
   }
   if (lane == 31) {
     warp_sum[warp] = incl;
     warp_act[warp] = act;
+    warp_til[warp] = til;
   }
   __syncthreads();
   if (warp == 0) {
-    int s = warp_sum[lane], a = warp_act[lane];
+    int sv = warp_sum[lane], av = warp_act[lane], tv = warp_til[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, s, o);
-      const int w = __shfl_up_sync(0xffffffffu, a, o);
+      const int v = __shfl_up_sync(0xffffffffu, sv, o);
+      const int w = __shfl_up_sync(0xffffffffu, av, o);
+      const int u = __shfl_up_sync(0xffffffffu, tv, o);
       if (lane >= o) {
-        s += v;
-        a += w;
+        sv += v;
+        av += w;
+        tv += u;
       }
     }
-    warp_sum[lane] = s;  // inclusive over warps
-    warp_act[lane] = a;
+    warp_sum[lane] = sv;  // inclusive over warps
+    warp_act[lane] = av;
+    warp_til[lane] = tv;
   }
   __syncthreads();
-  const int before = warp ? warp_sum[warp - 1] : 0;
-  const int before_a = warp ? warp_act[warp - 1] : 0;
+  const int wbefore = warp ? warp_sum[warp - 1] : 0;
+  const int abefore = warp ? warp_act[warp - 1] : 0;
+  const int tbefore = warp ? warp_til[warp - 1] : 0;
   if (tid < E) {
-    expert_off[tid] = before + incl - total;
-    if (total > 0) active[1 + before_a + act - 1] = tid;
+    expert_off[tid] = wbefore + incl - total;
+    if (total > 0) active[1 + abefore + act - 1] = tid;
+    if (tile_off) tile_off[tid] = tbefore + til - ntile;
   }
   if (tid == E - 1) {
-    expert_off[E] = before + incl;
-    active[0] = before_a + act;
+    expert_off[E] = wbefore + incl;
+    active[0] = abefore + act;
+    if (tile_off) tile_off[E] = tbefore + til;
   }
 }
 
@@ -187,7 +213,8 @@ k_active_from_offsets(const int32_t* __restrict__ expert_off, int E,
 cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, int32_t* rank,
                            int32_t* block_cnt, int32_t* block_base, int32_t* expert_off,
                            int32_t* row_token, int32_t* tok_slot_row, int32_t* row_pair,
-                           int32_t* active, int32_t* status, cudaStream_t s, bool pdl) {
+                           int32_t* active, int32_t* status, cudaStream_t s, bool pdl,
+                           int32_t* tile_off, int32_t* counters, int n_counters) {
   const int P = T * k;
   const int nb = cdiv(P, kPermBlock);
   cudaError_t e;
@@ -198,7 +225,7 @@ cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, int32_t
     if (e != cudaSuccess) return e;
   }
   e = launch_k(k_perm_scan, dim3(1), dim3(1024), 0, s, pdl, (const int32_t*)block_cnt, nb, E,
-               block_base, expert_off, active);
+               block_base, expert_off, active, tile_off, counters, n_counters);
   if (e != cudaSuccess || nb == 0) return e;
   return launch_k(k_perm_scatter, dim3(nb), dim3(kPermBlock), 0, s, pdl, topk_idx,
                   (const int32_t*)rank, (const int32_t*)block_base, (const int32_t*)expert_off, P,
