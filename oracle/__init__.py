@@ -28,6 +28,11 @@ from .moe_ref import (  # noqa: F401
     permute,
     silu,
     expert_ffn,
+    e4m3_encode_rne,
+    act8_quantize,
+    act8_dequantize,
+    act8_round,
+    expert_ffn_act8,
     combine,
     shared_gate_factor,
     moe_layer,

@@ -36,6 +36,16 @@ R7  The shared expert sees every token with weight 1 (no gate) and is added
 R10 Gated variant (not on the pages, which say only "+ 1 shared"): when the
     layer carries a gate vector g [H], the shared expert's output for token
     t is scaled by sigmoid(x[t] . g) before it is added.
+R11 FP8-activation variant (not on the pages, whose block-FP8 format covers
+    weights only): the expert projections' inputs (x, then hid) are
+    quantised to E4M3 per row and group of 128 consecutive input features,
+    the grouping of the weights' 128-wide scale blocks.  For a group with
+    largest magnitude a (float32): a == 0 gives codes 0 and scale 0;
+    otherwise inv = fp32(448 / a), each value v becomes the E4M3 code
+    nearest to fp32(v * inv) (ties to the even code, magnitudes at or above
+    448 saturate to 448), and the scale is s = fp32(a / 448); the
+    dequantised value is dec(code) * s.  hid is quantised from its float32
+    value.  Everything else is as in the bf16-activation layer.
 """
 from __future__ import annotations
 
@@ -92,6 +102,53 @@ def dequantize(codes, scales, block: int = BLOCK) -> np.ndarray:
     assert S.shape == (-(-R // block), -(-C // block)), S.shape
     full = np.repeat(np.repeat(S, block, axis=0), block, axis=1)[:R, :C]
     return _TABLE[codes] * full
+
+
+def e4m3_encode_rne(v) -> np.ndarray:
+    """float32 values -> E4M3 codes (uint8), rounded to the nearest finite
+    E4M3 value, ties to the code with the even mantissa, magnitudes at or
+    above 448 saturated to 448 (reading R11).  NaN is not accepted."""
+    v = np.asarray(v, dtype=np.float32).astype(np.float64)
+    assert not np.isnan(v).any()
+    pos = _TABLE[:127]                      # codes 0x00 .. 0x7E, increasing
+    a = np.minimum(np.abs(v), 448.0)
+    hi = np.searchsorted(pos, a, side="left")  # first value >= a
+    hi = np.minimum(hi, 126)
+    lo = np.maximum(hi - 1, 0)
+    d_lo = a - pos[lo]
+    d_hi = pos[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo)
+    return (code | np.where(np.signbit(v), 0x80, 0)).astype(np.uint8)
+
+
+def act8_quantize(rows, group: int = BLOCK):
+    """Per-row, per-128-group E4M3 quantisation of float32 activations
+    (reading R11).  rows [n, K] (float32-representable), K % group == 0.
+    Returns codes uint8 [n, K] and scales float32 [n, K / group]."""
+    r = np.asarray(rows, dtype=np.float32)
+    n, K = r.shape
+    assert K % group == 0
+    g = r.reshape(n, K // group, group)
+    amax = np.abs(g).max(axis=2).astype(np.float32)
+    safe = np.where(amax > 0, amax, np.float32(1))
+    inv = (np.float32(448.0) / safe).astype(np.float32)
+    v = (g * inv[:, :, None]).astype(np.float32)
+    codes = e4m3_encode_rne(v).reshape(n, K)
+    codes = np.where(np.repeat(amax, group, axis=1) > 0, codes, 0).astype(np.uint8)
+    scales = np.where(amax > 0, (amax / np.float32(448.0)).astype(np.float32),
+                      np.float32(0)).astype(np.float32)
+    return codes, scales
+
+
+def act8_dequantize(codes, scales, group: int = BLOCK) -> np.ndarray:
+    """dec(code) * s per group, float64 [n, K]."""
+    return _TABLE[np.asarray(codes)] * np.repeat(np.asarray(scales, np.float64), group, axis=1)
+
+
+def act8_round(rows, group: int = BLOCK) -> np.ndarray:
+    """Quantise then dequantise (reading R11), float64."""
+    return act8_dequantize(*act8_quantize(rows, group), group)
 
 
 # ---------------------------------------------------------------------------
@@ -171,6 +228,16 @@ def expert_ffn(xp, Wg, Wu, Wd) -> np.ndarray:
     return (silu(g) * u) @ Wd.T
 
 
+def expert_ffn_act8(xp, Wg, Wu, Wd, quant=None) -> np.ndarray:
+    """The FP8-activation expert (reading R11): the rows xp [n, H] and the
+    float32 hid are each quantised per 128-group before their projection.
+    ``quant`` replaces the quantise-dequantise step (tests only)."""
+    q = act8_round if quant is None else quant
+    xh = q(np.asarray(xp, dtype=np.float32))
+    hid = silu(xh @ Wg.T) * (xh @ Wu.T)
+    return q(hid.astype(np.float32)) @ Wd.T
+
+
 def combine(y_perm, tok_slot_row, topk_w, shared_y=None) -> np.ndarray:
     """out[t] = sum_j w[t, j] y_perm[tok_slot_row[t*k + j]] (+ shared_y[t])
     (reading R7 for the shared term)."""
@@ -203,8 +270,11 @@ def _expert_mats(mat, e):
     return dequantize(mat.codes[e], mat.scales[e])
 
 
-def moe_layer(x_bits, layer, keep_intermediates: bool = True) -> dict:
-    """The full layer on every token, float64.
+def moe_layer(x_bits, layer, keep_intermediates: bool = True, act8: bool = False,
+              quant=None) -> dict:
+    """The full layer on every token, float64.  act8: the FP8-activation
+    variant (reading R11) of every expert, routed and shared; the routing
+    is the same.
 
     ``layer`` carries Wr, bias, gate/up/down (codes [E, ...], scales) and the
     optional shared expert (see ``moe_inputs.LayerWeights``).  Returns a dict
@@ -218,20 +288,21 @@ def moe_layer(x_bits, layer, keep_intermediates: bool = True) -> dict:
     p = softmax(logits)
     idx, w = topk_renorm(p, k)
     off, row_token, tok_slot_row = permute(idx, E)
+    ffn = (lambda *m: expert_ffn_act8(*m, quant=quant)) if act8 else expert_ffn
     y_perm = np.zeros((T * k, layer.H), dtype=np.float64)
     for e in range(E):
         a, b = int(off[e]), int(off[e + 1])
         if a == b:
             continue
-        y_perm[a:b] = expert_ffn(x[row_token[a:b]],
-                                 _expert_mats(layer.gate, e),
-                                 _expert_mats(layer.up, e),
-                                 _expert_mats(layer.down, e))
+        y_perm[a:b] = ffn(x[row_token[a:b]],
+                          _expert_mats(layer.gate, e),
+                          _expert_mats(layer.up, e),
+                          _expert_mats(layer.down, e))
     shared_y = None
     if layer.I_shared:
-        shared_y = expert_ffn(x, _expert_mats(layer.shared_gate, 0),
-                              _expert_mats(layer.shared_up, 0),
-                              _expert_mats(layer.shared_down, 0))
+        shared_y = ffn(x, _expert_mats(layer.shared_gate, 0),
+                       _expert_mats(layer.shared_up, 0),
+                       _expert_mats(layer.shared_down, 0))
         shared_y = shared_y * shared_gate_factor(x, layer)[:, None]
     out = combine(y_perm, tok_slot_row, w, shared_y)
     res = dict(topk_idx=idx, topk_w=w, expert_off=off, row_token=row_token,
