@@ -9,6 +9,6 @@ the layer itself and has no CPU fallback.
 from ._lib import (  # noqa: F401
     Dims, Fp8Ffn, Fp8Mat, MoeError, dims, ffn, lib, version, workspace_bytes,
     moe_route, moe_permute, moe_expert_ffn_fp8, moe_combine, moe_layer_forward,
-    moe_layer_forward_gated,
+    moe_layer_forward_gated, moe_layer_forward_act8,
     moe_read_device_status, kernel_launches, expert_uses_gemm,
 )

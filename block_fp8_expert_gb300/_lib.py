@@ -70,6 +70,8 @@ _SIGNATURES = {
                                 _vp, _vp, _sz, _vp]),
     "moe_layer_forward_gated": (_st, [_vp, _vp, _vp, Fp8Ffn, ctypes.POINTER(Fp8Ffn), _vp, Dims,
                                       _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_layer_forward_act8": (_st, [_vp, _vp, _vp, Fp8Ffn, Dims, _vp, _vp, _vp, _vp, _sz,
+                                     _vp]),
     "moe_verify_workspace_bytes": (_st, [Dims, ctypes.c_int, ctypes.POINTER(_sz)]),
     "moe_verify_layer": (_st, [_vp, Fp8Ffn, ctypes.POINTER(Fp8Ffn), _vp, Dims, _vp, _vp, _vp,
                                _vp, ctypes.c_int, _vp, _vp, _sz, _vp]),
@@ -207,6 +209,13 @@ def moe_layer_forward_gated(x, Wr, bias, routed: Fp8Ffn, shared: Fp8Ffn, shared_
                                          ctypes.byref(shared), _ptr(shared_gate), d, _ptr(out),
                                          _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(ws),
                                          _nbytes(ws), _stream(stream)), "moe_layer_forward_gated")
+
+
+def moe_layer_forward_act8(x, Wr, bias, routed: Fp8Ffn, d: Dims, out, topk_idx_out, topk_w_out,
+                           ws, stream=None) -> None:
+    _check(lib().moe_layer_forward_act8(_ptr(x), _ptr(Wr), _ptr(bias), routed, d, _ptr(out),
+                                        _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(ws),
+                                        _nbytes(ws), _stream(stream)), "moe_layer_forward_act8")
 
 
 def verify_workspace_bytes(d: Dims, n_tokens: int) -> int:

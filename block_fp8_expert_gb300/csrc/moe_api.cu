@@ -384,14 +384,22 @@ moe_status moe_combine(const float* y_perm, const int32_t* tok_slot_row, const f
 
 namespace moe {
 namespace {
-// The layer call, with an optional gate vector for the shared expert.
+// The layer call, with an optional gate vector for the shared expert; act8:
+// the routed experts on E4M3 activations (routed experts only).
 moe_status layer_forward(const uint16_t* x, const float* Wr, const float* bias,
                          moe_fp8_ffn routed, const moe_fp8_ffn* shared,
                          const float* shared_gate, moe_dims d, uint16_t* out,
                          int32_t* topk_idx_out, float* topk_w_out, void* ws, size_t ws_bytes,
-                         void* stream) {
+                         void* stream, bool act8 = false) {
   moe_status s;
   if ((s = check_dims(d)) != MOE_OK) return s;
+  if (act8) {
+    if (d.I_shared > 0 || shared)
+      return fail(MOE_ERR_UNSUPPORTED, "E4M3 activations: layers with a shared expert are not supported");
+    if (!expert_gemm_tc_ok(d.H, d.I))
+      return fail(MOE_ERR_UNSUPPORTED, "E4M3 activations need the tensor-core GEMM's shapes "
+                                       "(H % 256 == 0, I % 128 == 0, H, I <= 4096)");
+  }
   if (d.T == 0) return MOE_OK;  // no token: nothing is read or written
   REQUIRE_PTR(x);
   REQUIRE_PTR(Wr);
@@ -426,7 +434,7 @@ moe_status layer_forward(const uint16_t* x, const float* Wr, const float* bias,
   int32_t* srows = at<int32_t>(ws, L.sh_rows);
   int32_t* sact = at<int32_t>(ws, L.sh_active);
   const bool has_shared = d.I_shared > 0;
-  const bool gemm = use_expert_gemm(P, d.E, d.H, d.I);
+  const bool gemm = act8 || use_expert_gemm(P, d.E, d.H, d.I);
   const bool small = small_route_permute_ok(d.T, d.E, d.k);
   // streamed GEMV, one-CTA permutation, no shared expert: the down kernel
   // also combines (its tickets cleared by the permutation)
@@ -482,7 +490,18 @@ moe_status layer_forward(const uint16_t* x, const float* Wr, const float* bias,
   // also runs on the GEMM); below, one warp per routed row keeps more CTAs
   // in flight (8 tokens per CTA would leave most SMs idle).
   const bool token_gather = gemm && d.T >= kTokenGatherMin;
-  if (gemm) {
+  if (act8) {
+    // E4M3 activations: x and hid codes with their group scales in the
+    // activation-row and hid scratch (codes first, then the scales)
+    uint8_t* x8 = at<uint8_t>(ws, L.x_perm);
+    float* xs = reinterpret_cast<float*>(x8 + (size_t)P * d.H);
+    uint8_t* hid8 = at<uint8_t>(ws, L.hid);
+    float* hs = reinterpret_cast<float*>(hid8 + (size_t)P * d.I);
+    CUDA_CHECK(launch_expert_gemm_f8(x, d.T, off, tok_slot_row, d.k, d.E, P, routed, d.H, d.I,
+                                     at<int32_t>(ws, L.tile_off), at<int32_t>(ws, L.slot_done),
+                                     x8, xs, hid8, hs, y_perm, yexp, y_rows, status, st, true),
+               "moe_layer_forward_act8: experts");
+  } else if (gemm) {
     GemmGather gth;
     if (token_gather) {
       gth.tok_slot_row = tok_slot_row;
@@ -581,6 +600,14 @@ moe_status moe_layer_forward_gated(const uint16_t* x, const float* Wr, const flo
   if (!shared_gate) return fail(MOE_ERR_INVALID_ARG, "shared_gate is NULL");
   return layer_forward(x, Wr, bias, routed, shared, shared_gate, d, out, topk_idx_out,
                        topk_w_out, ws, ws_bytes, stream);
+}
+
+moe_status moe_layer_forward_act8(const uint16_t* x, const float* Wr, const float* bias,
+                                  moe_fp8_ffn routed, moe_dims d, uint16_t* out,
+                                  int32_t* topk_idx_out, float* topk_w_out, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  return layer_forward(x, Wr, bias, routed, nullptr, nullptr, d, out, topk_idx_out, topk_w_out, ws,
+                       ws_bytes, stream, true);
 }
 
 moe_status moe_verify_workspace_bytes(moe_dims d, int n_tokens, size_t* bytes) {

@@ -203,6 +203,20 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x, int T, const int32_t* exper
                                   int16_t* yexp, int yexp_rows, int32_t* status, cudaStream_t s,
                                   bool pdl, bool tile_off_ready = false,
                                   const GemmGather& gather = GemmGather{});
+// The same GEMMs on E4M3 activations (tcgen05.mma kind::f8f6f4): x is
+// quantised per row and 128-column group while it is gathered (the layer
+// call's token -> row map), hid per row and 128 features by the gate/up
+// epilogue.  tile_off and zeroed slot_done come from the permutation.
+// x8 [P][H] / hid8 [P][I] codes, xs [P][act8_scale_ld(H)] / hs
+// [P][act8_scale_ld(I)] float scales (scratch); y [P][H] fp16 with yexp
+// [H/32][yexp_rows].  Needs expert_gemm_tc_ok(H, I).
+int act8_scale_ld(int K);
+cudaError_t launch_expert_gemm_f8(const uint16_t* x, int T, const int32_t* expert_off,
+                                  const int32_t* tok_slot_row, int k, int E, int P,
+                                  const moe_fp8_ffn& w, int H, int I, const int32_t* tile_off,
+                                  int32_t* slot_done, uint8_t* x8, float* xs, uint8_t* hid8,
+                                  float* hs, uint16_t* y, int16_t* yexp, int yexp_rows,
+                                  int32_t* status, cudaStream_t s, bool pdl);
 // slot_done entries the GEMM uses for P routed rows over E experts.
 inline int expert_gemm_slots(int P, int E) { return (P + 127) / 128 + (E < P ? E : P); }
 

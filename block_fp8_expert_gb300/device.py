@@ -78,14 +78,19 @@ class DeviceLayer:
 
     def forward(self, x: torch.Tensor, out: Optional[torch.Tensor] = None,
                 ws: Optional[torch.Tensor] = None, topk_idx: Optional[torch.Tensor] = None,
-                topk_w: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-        """out[T, H] (bf16) = the layer applied to x[T, H] (bf16)."""
+                topk_w: Optional[torch.Tensor] = None, stream=None,
+                act8: bool = False) -> torch.Tensor:
+        """out[T, H] (bf16) = the layer applied to x[T, H] (bf16).  act8: the
+        routed experts on E4M3 activations (moe_layer_forward_act8)."""
         T = x.shape[0]
         if out is None:
             out = torch.empty((T, self.H), dtype=torch.bfloat16, device=x.device)
         if ws is None:
             ws = self.workspace(T)
-        if self.shared_gate_w is not None:
+        if act8:
+            _lib.moe_layer_forward_act8(x, self.Wr, self.bias, self.routed.abi(), self.dims(T),
+                                        out, topk_idx, topk_w, ws, stream)
+        elif self.shared_gate_w is not None:
             _lib.moe_layer_forward_gated(x, self.Wr, self.bias, self.routed.abi(),
                                          self.shared.abi(), self.shared_gate_w, self.dims(T), out,
                                          topk_idx, topk_w, ws, stream)

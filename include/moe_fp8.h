@@ -249,6 +249,32 @@ moe_status moe_layer_forward_gated(const uint16_t* x, const float* Wr,
                                    void* stream);
 
 /*
+ * The layer with E4M3 activations in the routed experts.  The pages' block-FP8
+ * format covers the weights only; this variant also feeds the experts' inputs
+ * to the tensor cores as E4M3 (tcgen05.mma kind::f8f6f4), so the weight
+ * codes are multiplied without a decode.  Routing and combine are those of
+ * moe_layer_forward.  The inputs of each projection (x, then the SwiGLU
+ * output hid in fp32) are quantised per row and group of 128 input features
+ * (the weights' scale-block width): with a the group's largest magnitude,
+ * code = E4M3(v * fp32(448 / a)) rounded to nearest even and saturated to
+ * +-448, scale = fp32(a / 448); a = 0 gives zero codes and scale.  Each
+ * 128-wide K block's E4M3 product sums are scaled by the weight and
+ * activation scales in fp32 and accumulated in fp32.
+ * Accuracy: the quantisation of x and hid costs about 4.5% of the output's
+ * rms against the bf16-activation layer (measured on the synthetic
+ * workloads; largest elements up to about 20%), so the layer is checked
+ * against its own definition, not against moe_layer_forward's tolerance.
+ * Shapes: the tensor-core GEMM's (H % 256 == 0, I % 128 == 0, H, I <= 4096),
+ * any T; layers with a shared expert (d.I_shared > 0) return
+ * MOE_ERR_UNSUPPORTED.  Arguments as moe_layer_forward without `shared`.
+ */
+moe_status moe_layer_forward_act8(const uint16_t* x, const float* Wr,
+                                  const float* bias, moe_fp8_ffn routed,
+                                  moe_dims d, uint16_t* out,
+                                  int32_t* topk_idx_out, float* topk_w_out,
+                                  void* ws, size_t ws_bytes, void* stream);
+
+/*
  * moe_permute without a workspace, for callers that cannot allocate device
  * memory: for example a plugin whose host framework passes it only the input
  * and output buffers of each call, or a serving loop whose device memory is

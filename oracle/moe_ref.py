@@ -312,9 +312,11 @@ def moe_layer(x_bits, layer, keep_intermediates: bool = True, act8: bool = False
     return res
 
 
-def moe_layer_sampled(x_bits, layer, tokens) -> dict:
+def moe_layer_sampled(x_bits, layer, tokens, act8: bool = False) -> dict:
     """Routing and permutation for every token; the layer output only for the
-    listed tokens (each computed from its own k experts, one by one).
+    listed tokens (each computed from its own k experts, one by one).  act8:
+    the FP8-activation variant (reading R11; quantisation is per row, so a
+    token's rows do not depend on the other tokens).
 
     Returns the routing/permutation arrays of ``moe_layer`` plus
     out_sampled float64 [len(tokens), H] in the order of ``tokens``.
@@ -333,10 +335,11 @@ def moe_layer_sampled(x_bits, layer, tokens) -> dict:
     for n, t in enumerate(tokens):
         for j in range(k):
             pairs.setdefault(int(idx[t, j]), []).append((n, int(t), j))
+    ffn = expert_ffn_act8 if act8 else expert_ffn
     for e, lst in pairs.items():
         rows = np.array([t for _, t, _ in lst])
-        y = expert_ffn(x[rows], _expert_mats(layer.gate, e),
-                       _expert_mats(layer.up, e), _expert_mats(layer.down, e))
+        y = ffn(x[rows], _expert_mats(layer.gate, e),
+                _expert_mats(layer.up, e), _expert_mats(layer.down, e))
         for (n, t, j), yr in zip(lst, y):
             out[n] += w[t, j] * yr
     if layer.I_shared:
