@@ -17,10 +17,14 @@
 // add it to the running sum R, also in tensor memory:
 //   TMEM columns   0..255  P (two weight blocks x 128 token columns)
 //                256..511  R (the same two blocks)
+// Each weight block has its own partial sums and barriers, so the tensor
+// core computes one block's while the other's are promoted.
 // Warp roles (one CTA per SM, tiles as in the fp16-operand GEMM):
 //   warp 0      TMA: the step's two E4M3 code blocks (64-byte swizzled);
 //   warp 1      TMA: the step's E4M3 token rows (64-byte swizzled), and per
-//               tile the tokens' activation scales into shared memory;
+//               tile the promotion factors Sw Sx into shared memory (a
+//               weight block's scale is one number per K block, so the
+//               factor depends on the token column only);
 //   warp 2      one elected thread issues tcgen05.mma kind::f8f6f4
 //               (M = 128, N, K = 32), both operands from shared memory;
 //   warps 3-10  promote each K block's partial sums: R += Sw Sx P;
@@ -45,8 +49,9 @@ constexpr int BK = 64;   // K per step: 64 E4M3 (two MMAs of K = 32)
 constexpr int NT = 6, NCD = 5;
 constexpr int T_BYTES = BT * BK;      // 8 KB
 constexpr int C_BYTES = 2 * BW * BK;  // 16 KB: two code blocks of 8 KB
-constexpr int kMaxKb = 32;            // K <= 4096: 128-wide K blocks per row
-constexpr int SX_BYTES = kMaxKb * BT * 4;  // a tile's activation scales [kb][token]
+constexpr int kMaxKb = 16;  // K <= 2048: 128-wide K blocks per row
+// a tile's promotion factors Sw[blk, kb] Sx[token, kb], [blk][kb][token]
+constexpr int SX_BYTES = 2 * kMaxKb * BT * 4;
 constexpr int STG_WARP_BYTES = 4096;
 constexpr int OFF_T = 0;
 constexpr int OFF_C = OFF_T + NT * T_BYTES;
@@ -91,7 +96,7 @@ struct F8Shared {
   uint64_t c_full[NCD], c_empty[NCD];
   uint64_t t_full[NT], t_empty[NT];
   uint64_t sx_full[2], sx_empty[2];
-  uint64_t p_full, p_empty;
+  uint64_t p_full[2], p_empty[2];  // per weight block
   uint64_t acc_full, acc_empty;
   // gate/up epilogue's exchange of per-token maxima among the four warps of a
   // half, per chunk pair: written (amx_full) and read (amx_free)
@@ -217,7 +222,7 @@ k_expert_gemm_f8(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t smem_base = smem_u32(smem);
-  float* sx_buf = reinterpret_cast<float*>(smem + OFF_SX);  // [2][kMaxKb][BT]
+  float* sx_buf = reinterpret_cast<float*>(smem + OFF_SX);  // [2][2][kMaxKb][BT]
 
   if (tid == 0) {
     for (int s = 0; s < NCD; ++s) {
@@ -232,8 +237,10 @@ k_expert_gemm_f8(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
       mbar_init(&sh.sx_full[s], 1);
       mbar_init(&sh.sx_empty[s], kProWarps);
     }
-    mbar_init(&sh.p_full, 1);
-    mbar_init(&sh.p_empty, kProWarps);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sh.p_full[b], 1);
+      mbar_init(&sh.p_empty[b], kProWarps / 2);
+    }
     mbar_init(&sh.acc_full, kProWarps);
     mbar_init(&sh.acc_empty, kEpiWarps);
     for (int h = 0; h < 2; ++h)
@@ -324,22 +331,36 @@ k_expert_gemm_f8(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
         }
         tc::fence_proxy_async_global();
       }
-      // the tile's activation scales, transposed to [kb][token] (0 past the
-      // tile's rows), once the promoters have released the buffer
+      // the tile's promotion factors Sw[blk, kb] Sx[token, kb], laid out
+      // [blk][kb][token] (0 past the tile's rows), once the promoters have
+      // released the buffer; lane kb holds the two weight blocks' scales
       const int sb = tl & 1;
       if (tl >= 2 && !f8_wait(sh, &sh.sx_empty[sb], (uint32_t)(((tl >> 1) - 1) & 1), a.status, 12, tl))
         break;
-      float* sx = sx_buf + sb * (kMaxKb * BT);
+      float* fs = sx_buf + sb * (2 * kMaxKb * BT);
+      float sw[2];
+#pragma unroll
+      for (int blk = 0; blk < 2; ++blk) {
+        const float* sp = (GATEUP && blk) ? a.s1 : a.s0;
+        const size_t srow = (size_t)ti.e * nRb + ti.n0 / kScaleBlock + (GATEUP ? 0 : blk);
+        sw[blk] = lane < nKb ? __ldg(sp + srow * nKb + lane) : 0.f;
+      }
       for (int r = lane; r < BT; r += 32) {
         const bool real = r < ti.rows;
         const float* src = a.xs + (size_t)(ti.r0 + ti.m0 + r) * a.xs_ld;
         for (int b = 0; b < nKb; b += 4) {
           float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
           if (real) v = __ldcg(reinterpret_cast<const float4*>(src + b));
-          sx[(b + 0) * BT + r] = v.x;
-          if (b + 1 < nKb) sx[(b + 1) * BT + r] = v.y;
-          if (b + 2 < nKb) sx[(b + 2) * BT + r] = v.z;
-          if (b + 3 < nKb) sx[(b + 3) * BT + r] = v.w;
+          const float x4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float w0 = __shfl_sync(0xffffffffu, sw[0], b + i);
+            const float w1 = __shfl_sync(0xffffffffu, sw[1], b + i);
+            if (b + i < nKb) {
+              fs[(0 * kMaxKb + b + i) * BT + r] = w0 * x4[i];
+              fs[(1 * kMaxKb + b + i) * BT + r] = w1 * x4[i];
+            }
+          }
         }
       }
       __syncwarp();
@@ -362,9 +383,10 @@ k_expert_gemm_f8(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     __syncwarp();
   } else if (warp == W_MMA) {
     // ------------------------------------------------ tcgen05.mma kind::f8f6f4
-    // Per K block (two steps): wait until the promoters have read the
-    // previous block's partial sums, then 8 MMAs (2 steps x 2 halves of K x 2
-    // weight blocks) into P, the first of each block overwriting it.  The
+    // Per K block (two steps), per weight block b: once the promoters of b
+    // have read its previous partial sums, 4 MMAs (2 steps x 2 halves of K)
+    // into P_b, the first overwriting it, then a commit to p_full[b]; so the
+    // tensor core works on one block while the other is promoted.  The
     // instruction descriptor has the same fields as for kind::f16: fp32 D,
     // A and B format code 0 (E4M3 here), both K-major.
     int j = 0, kbg = 0;
@@ -372,38 +394,49 @@ k_expert_gemm_f8(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     for (int t = blockIdx.x; t < n_tiles && ok; t += tstride) {
       const F8Tile ti = f8_tile(sh, a, t, GATEUP);
       const uint32_t idesc = tc::idesc_f16_f32(BW, ti.n);
-      for (int kb = 0; kb < nKb && ok; ++kb, ++kbg) {
-        if (kbg > 0 && !f8_wait(sh, &sh.p_empty, (uint32_t)((kbg - 1) & 1), a.status, 5, kbg)) {
+      for (int kb = 0; kb < nKb && ok; ++kb, ++kbg, j += 2) {
+        const int st0 = j % NT, sc0 = j % NCD, st1 = (j + 1) % NT, sc1 = (j + 1) % NCD;
+        if (!f8_wait(sh, &sh.t_full[st0], (uint32_t)((j / NT) & 1), a.status, 6, j) ||
+            !f8_wait(sh, &sh.c_full[sc0], (uint32_t)((j / NCD) & 1), a.status, 7, j) ||
+            !f8_wait(sh, &sh.t_full[st1], (uint32_t)(((j + 1) / NT) & 1), a.status, 6, j + 1) ||
+            !f8_wait(sh, &sh.c_full[sc1], (uint32_t)(((j + 1) / NCD) & 1), a.status, 7, j + 1)) {
           ok = false;
           break;
         }
-        for (int h = 0; h < 2; ++h, ++j) {
-          const int st = j % NT, sc = j % NCD;
-          if (!f8_wait(sh, &sh.t_full[st], (uint32_t)((j / NT) & 1), a.status, 6, j) ||
-              !f8_wait(sh, &sh.c_full[sc], (uint32_t)((j / NCD) & 1), a.status, 7, j)) {
+        for (int blk = 0; blk < 2 && ok; ++blk) {
+          if (kbg > 0 &&
+              !f8_wait(sh, &sh.p_empty[blk], (uint32_t)((kbg - 1) & 1), a.status, 5, kbg)) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
           if (tc::elect_one()) {
-            const uint32_t b_addr = smem_base + OFF_T + st * T_BYTES;
-            const uint32_t a_addr = smem_base + OFF_C + sc * C_BYTES;
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk)
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t b_addr = smem_base + OFF_T + (h ? st1 : st0) * T_BYTES;
+              const uint32_t a_addr = smem_base + OFF_C + (h ? sc1 : sc0) * C_BYTES + blk * (BW * BK);
 #pragma unroll
-              for (int blk = 0; blk < 2; ++blk)
-                mma_f8_ss(tmem + COL_P + blk * BT, sw64_desc(a_addr + blk * (BW * BK) + kk * 32),
+              for (int kk = 0; kk < 2; ++kk)
+                mma_f8_ss(tmem + COL_P + blk * BT, sw64_desc(a_addr + kk * 32),
                           sw64_desc(b_addr + kk * 32), idesc, (h | kk) ? 1u : 0u);
-            tc::commit(&sh.t_empty[st]);
-            tc::commit(&sh.c_empty[sc]);
-            if (h == 1) tc::commit(&sh.p_full);
+            }
+            tc::commit(&sh.p_full[blk]);
           }
           __syncwarp();
         }
+        if (!ok) break;
+        if (tc::elect_one()) {
+          // both blocks' MMAs have read the two steps' operands
+          tc::commit(&sh.t_empty[st0]);
+          tc::commit(&sh.c_empty[sc0]);
+          tc::commit(&sh.t_empty[st1]);
+          tc::commit(&sh.c_empty[sc1]);
+        }
+        __syncwarp();
       }
     }
     // drain: the newest commit completes once every MMA issued has
-    if (lane == 0 && kbg > 0) mbar_wait(&sh.p_full, (uint32_t)((kbg - 1) & 1));
+    if (lane == 0 && kbg > 0) mbar_wait(&sh.p_full[1], (uint32_t)((kbg - 1) & 1));
     __syncwarp();
   } else if (warp >= W_PRO0 && warp < W_PRO0 + kProWarps) {
     // ------------------------------------------------ promotion: R += Sw Sx P
@@ -413,32 +446,22 @@ k_expert_gemm_f8(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     const int blk = (warp - W_PRO0) >> 2, q = warp & 3;
     const uint32_t t_p = tmem + ((uint32_t)(32 * q) << 16) + COL_P + (uint32_t)blk * BT;
     const uint32_t t_r = tmem + ((uint32_t)(32 * q) << 16) + COL_R + (uint32_t)blk * BT;
-    const float* sp = (GATEUP && blk) ? a.s1 : a.s0;
-    auto wscale = [&](int t) -> float {
-      const F8Tile ti = f8_tile(sh, a, t, GATEUP);
-      const size_t srow = (size_t)ti.e * nRb + ti.n0 / kScaleBlock + (GATEUP ? 0 : blk);
-      return lane < nKb ? __ldg(sp + srow * nKb + lane) : 0.f;
-    };
-    float sw_next = wscale(blockIdx.x);
     int kbg = 0, tl = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < n_tiles && ok; t += tstride, ++tl) {
       const F8Tile ti = f8_tile(sh, a, t, GATEUP);
-      const float sw = sw_next;
-      if (t + tstride < n_tiles) sw_next = wscale(t + tstride);
       const int nchunks = (ti.n + 31) >> 5;
       const int sb = tl & 1;
-      const float* sx = sx_buf + sb * (kMaxKb * BT);
+      const float* fs = sx_buf + (sb * 2 + blk) * (kMaxKb * BT);
       if (!f8_wait(sh, &sh.sx_full[sb], (uint32_t)((tl >> 1) & 1), a.status, 13, tl)) break;
       for (int kb = 0; kb < nKb; ++kb, ++kbg) {
-        if (!f8_wait(sh, &sh.p_full, (uint32_t)(kbg & 1), a.status, 3, kbg) ||
+        if (!f8_wait(sh, &sh.p_full[blk], (uint32_t)(kbg & 1), a.status, 3, kbg) ||
             (kb == 0 && tl > 0 &&
              !f8_wait(sh, &sh.acc_empty, (uint32_t)((tl - 1) & 1), a.status, 4, tl))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-        const float swk = __shfl_sync(0xffffffffu, sw, kb);
 #pragma unroll 1
         for (int c = 0; c < nchunks; ++c) {
           uint32_t p[32], r[32];
@@ -450,14 +473,20 @@ k_expert_gemm_f8(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
             // MMAs may overwrite them
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.p_empty);
+            if (lane == 0) mbar_arrive(&sh.p_empty[blk]);
           }
-          const float* sxc = sx + kb * BT + 32 * c;  // token 32 c + v's scale of block kb
+          // token 32 c + v's factor of block kb (16-byte broadcast reads)
+          const float4* fc = reinterpret_cast<const float4*>(fs + kb * BT + 32 * c);
 #pragma unroll
-          for (int v = 0; v < 32; ++v) {
-            const float f = swk * sxc[v];
-            const float pv = __uint_as_float(p[v]);
-            r[v] = __float_as_uint(kb > 0 ? fmaf(pv, f, __uint_as_float(r[v])) : pv * f);
+          for (int v4 = 0; v4 < 8; ++v4) {
+            const float4 s4 = fc[v4];
+            const float f[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int v = 4 * v4 + i;
+              const float pv = __uint_as_float(p[v]);
+              r[v] = __float_as_uint(kb > 0 ? fmaf(pv, f[i], __uint_as_float(r[v])) : pv * f[i]);
+            }
           }
           tc::st_32x32b_x32(t_r + 32 * c, r);
         }

@@ -396,9 +396,9 @@ moe_status layer_forward(const uint16_t* x, const float* Wr, const float* bias,
   if (act8) {
     if (d.I_shared > 0 || shared)
       return fail(MOE_ERR_UNSUPPORTED, "E4M3 activations: layers with a shared expert are not supported");
-    if (!expert_gemm_tc_ok(d.H, d.I))
-      return fail(MOE_ERR_UNSUPPORTED, "E4M3 activations need the tensor-core GEMM's shapes "
-                                       "(H % 256 == 0, I % 128 == 0, H, I <= 4096)");
+    if (!expert_gemm_tc_ok(d.H, d.I) || d.H > 2048 || d.I > 2048)
+      return fail(MOE_ERR_UNSUPPORTED, "E4M3 activations need H % 256 == 0, I % 128 == 0 "
+                                       "and H, I <= 2048");
   }
   if (d.T == 0) return MOE_OK;  // no token: nothing is read or written
   REQUIRE_PTR(x);

@@ -264,8 +264,8 @@ moe_status moe_layer_forward_gated(const uint16_t* x, const float* Wr,
  * rms against the bf16-activation layer (measured on the synthetic
  * workloads; largest elements up to about 20%), so the layer is checked
  * against its own definition, not against moe_layer_forward's tolerance.
- * Shapes: the tensor-core GEMM's (H % 256 == 0, I % 128 == 0, H, I <= 4096),
- * any T; layers with a shared expert (d.I_shared > 0) return
+ * Shapes: H % 256 == 0, I % 128 == 0, H, I <= 2048, any T; other shapes
+ * and layers with a shared expert (d.I_shared > 0) return
  * MOE_ERR_UNSUPPORTED.  Arguments as moe_layer_forward without `shared`.
  */
 moe_status moe_layer_forward_act8(const uint16_t* x, const float* Wr,
