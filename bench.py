@@ -227,10 +227,11 @@ def run_reference(args):
 class LayerRun:
     """A captured layer forward for one (layer, T) with static buffers."""
 
-    def __init__(self, torch, D, x_bits, graph=True):
+    def __init__(self, torch, D, x_bits, graph=True, act8=False):
         from block_fp8_expert_gb300.device import x_to_device
         self.torch = torch
         self.D = D
+        self.act8 = act8  # E4M3 activations (moe_layer_forward_act8)
         self.T = x_bits.shape[0]
         self.x = x_to_device(x_bits)
         self.out = torch.empty((self.T, D.H), dtype=torch.bfloat16, device="cuda")
@@ -258,7 +259,8 @@ class LayerRun:
             self.launches = _lib.kernel_launches() - n0
 
     def fwd(self):
-        self.D.forward(self.x, out=self.out, ws=self.ws, topk_idx=self.idx, topk_w=self.w)
+        self.D.forward(self.x, out=self.out, ws=self.ws, topk_idx=self.idx, topk_w=self.w,
+                       act8=self.act8)
 
     def step(self):
         if self.graph is not None:
@@ -281,14 +283,15 @@ class PassGraph:
     weights at different addresses, so a pass reads its weights from HBM
     whenever R copies exceed the L2."""
 
-    def __init__(self, torch, D, host, x_bits, R, M):
+    def __init__(self, torch, D, host, x_bits, R, M, act8=False):
         from block_fp8_expert_gb300 import _lib
         from block_fp8_expert_gb300.device import DeviceLayer
         self.torch = torch
         self.R, self.M = R, M
-        self.runs = [LayerRun(torch, D, x_bits, graph=False)]
+        self.runs = [LayerRun(torch, D, x_bits, graph=False, act8=act8)]
         for _ in range(R - 1):
-            self.runs.append(LayerRun(torch, DeviceLayer.from_host(host), x_bits, graph=False))
+            self.runs.append(LayerRun(torch, DeviceLayer.from_host(host), x_bits, graph=False,
+                                      act8=act8))
         torch.cuda.synchronize()
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
@@ -467,9 +470,11 @@ def phase_times(torch, D, run, steps, flush):
 
 
 def measure_workload(torch, name, T, steps, warmup, flush, pk, dev_cache, seed=0,
-                     target_s=0.4):
+                     target_s=0.4, act8=False):
     """One sweep entry: `steps` steps of M passes over rotating copies (about
-    target_s of timed work), with its own clock record."""
+    target_s of timed work), with its own clock record.  act8: the layer on
+    E4M3 activations, whose contraction runs on the fp8 tensor rate (the
+    measured bf16 peak times the nominal 4.5 / 2.25 ratio)."""
     from block_fp8_expert_gb300.device import DeviceLayer
     w = mi.WORKLOADS[name]
     key = (w.H, w.I, w.E, w.k, w.I_shared, w.zipf_s)
@@ -480,12 +485,12 @@ def measure_workload(torch, name, T, steps, warmup, flush, pk, dev_cache, seed=0
         dev_cache[key] = (host, DeviceLayer.from_host(host))
     host, D = dev_cache[key]
     x_bits, _ = mi.make_tokens(host, T, seed=seed)
-    run = LayerRun(torch, D, x_bits)
+    run = LayerRun(torch, D, x_bits, act8=act8)
     Dn = run.distinct_experts()
     B, F, _ = algorithmic(w, T, Dn)
     R = copies_for_l2(torch, B)
     M = passes_per_step(single_pass_time(torch, run, flush), steps, R, target_s)
-    pg = PassGraph(torch, D, host, x_bits, R, M)
+    pg = PassGraph(torch, D, host, x_bits, R, M, act8=act8)
     for _ in range(warmup):
         pg.step()
     torch.cuda.synchronize()
@@ -493,10 +498,12 @@ def measure_workload(torch, name, T, steps, warmup, flush, pk, dev_cache, seed=0
         times = time_steps(torch, pg.step, steps, 0, flush)
     t = sum(times) / (len(times) * M)  # per pass
     t_hbm = B / (pk["hbm_gbs"] * 1e9)
-    t_tc = F / (pk["bf16_tflops"] * 1e12)
+    tc_peak = pk["bf16_tflops"] * (2.0 if act8 else 1.0)
+    t_tc = F / (tc_peak * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
     ck = clk.summary()
-    res = {"workload": f"{name}_T{T}", "T": T, "ms": t * 1e3, "tokens_per_s": T / t,
+    res = {"workload": f"{name}_T{T}" + ("_act8" if act8 else ""), "T": T, "ms": t * 1e3,
+           "tokens_per_s": T / t, "tensor_peak_tflops": tc_peak,
            "passes": len(times) * M, "layer_copies": R,
            "device_status": pg.device_status(), "distinct_experts": Dn, "bytes": B,
            "flops": F, "hbm_gbs": B / t / 1e9, "tflops": F / t / 1e12, "bound": bound,
@@ -628,11 +635,11 @@ def run_gpu(args):
         plan = [("qwen3moe_decode", 1), ("qwen3moe_decode", 8), ("qwen3moe_decode", 64),
                 ("qwen3moe_prefill", 4096), ("skewed", 1), ("skewed", 16), ("skewed", 256),
                 ("skewed", 2048), ("skewed", 16384), ("large_sparse", 1), ("large_sparse", 256),
-                ("tiny", 8)]
-        for nm, tt_ in plan:
+                ("tiny", 8), ("qwen3moe_prefill", 4096, True), ("skewed", 2048, True)]
+        for nm, tt_, *a8 in plan:
             try:
                 r, *_ = measure_workload(torch, nm, tt_, args.sweep_steps, 3, flush, pk,
-                                         dev_cache)
+                                         dev_cache, act8=bool(a8 and a8[0]))
                 sweep.append(r)
             except Exception as ex:  # report, do not hide
                 sweep.append({"workload": f"{nm}_T{tt_}", "error": repr(ex)[:200]})
