@@ -400,7 +400,7 @@ def record_traffic(csv_path, workload):
         if name.startswith("k_"):  # this library's kernels only (not torch's fills)
             per[name][r[ii]] += float(r[vi].replace(",", "")) * scale
     kern = {k: sum(v.values()) / len(v) for k, v in per.items()}
-    gemm = any("k_expert_gemm_ws" in k for k in kern)
+    gemm = any("k_expert_ffn_ws" in k for k in kern)
     nm, T = workload.split(":")
     csrc = os.path.join("block_fp8_expert_gb300", "csrc")
     files = ["expert_gemm_tc.cu", "tcgen05.cuh", "moe_common.cuh"] if gemm else \

@@ -26,10 +26,17 @@
 // use TMEM columns 0..255; columns 256..511 hold four stages of decoded
 // weights (two 128 x 64 fp16 blocks per 64-wide K step).  N is the tile's row
 // count rounded up to 16, so a ragged last tile of an expert costs only its
-// rows.  Persistent CTAs (one per SM) walk the tiles with warp-specialised
-// roles that hand work to each other through mbarriers:
-//   warp 0      TMA: the step's two E4M3 code blocks (64-byte swizzled) into a
-//               ring in shared memory;
+// rows.  A tile list holds the gate/up tiles, then the down tiles; a down
+// tile's token rows wait only for its own token tile's gate/up tiles (a
+// per-token-tile counter).  With few tiles per SM (decode batches) one
+// launch runs the whole list (kBoth), so an SM streams down codes as soon as
+// its last gate/up tile's codes are in, instead of leaving the SM to a second
+// launch; otherwise the gate/up tiles (kGateUp) and the down tiles (kDown)
+// are two launches, the second's CTAs starting on SMs the first has left.
+// Persistent CTAs (one per SM) walk a static sequence of the list (TileSeq).
+// Warp-specialised roles hand work to each other through mbarriers:
+//   warp 0      TMA: the step's two E4M3 code blocks (64-byte swizzled) into
+//               a ring in shared memory;
 //   warp 1      TMA: the step's token rows into a ring in shared memory, one
 //               128-byte-swizzled box of 128 consecutive rows of the
 //               permuted activations (gate/up: x gathered into expert order
@@ -85,42 +92,41 @@ constexpr uint32_t A_STAGE_COLS = 64;  // two blocks x 32 columns (64 fp16 of K)
 static_assert(COL_A + NA * A_STAGE_COLS <= TMEM_COLS, "TMEM budget");
 static_assert(kDecWarps == 8 && kEpiWarps == 8, "two blocks (or halves) x four lane quarters");
 
-struct GemmArgs {
+// The expert FFN's two GEMMs as one tile list: every gate/up tile (a token
+// tile x 128 gate rows and the same up rows, K = H), then every down tile (a
+// token tile x 256 output rows, K = I), each part in token-tile ("slot")
+// order.  A launch runs all of it or one part (FfnMode).
+enum FfnMode { kBoth = 0, kGateUp = 1, kDown = 2 };
+
+struct FfnArgs {
   const int32_t* expert_off;
   const int32_t* tile_off;  // token-tile prefix per expert, [E + 1]
   int E;
-  int K;                // H for gate/up, I for down
-  int rows_per_expert;  // I for gate/up, H for down
-  const float* s0;      // gate (or down) scales
-  const float* s1;      // up scales (gate/up only)
-  void* out;            // hid fp16 [P, I] or y [P, H] (fp32, or fp16 when yexp is set)
-  int out_ld;
-  int n_wblocks;  // weight-block pairs per expert (tiles per token tile)
-  int all_wait;   // 1: the previous kernel wrote the tile offsets (every warp waits)
-  // Per token tile ("slot") of the gate/up GEMM: completed epilogue-warp
-  // tiles.  gate/up adds kEpiWarps per weight-block tile once its hid rows are
-  // stored; down's token warp waits for slot_need before loading hid rows,
-  // instead of waiting for the whole gate/up grid.  NULL: whole-grid wait.
+  int H, I;
+  const float* gs;  // gate, up and down block scales
+  const float* us;
+  const float* ds;
+  uint16_t* hid;    // [P, I] fp16: the gate/up output, the down input
+  void* y;          // [P, H]: fp32, or fp16 when yexp is set
+  int all_wait;     // 1: the previous kernel wrote the tile offsets (every warp waits)
+  // Per token tile: completed gate/up epilogue-warp tiles.  Each gate/up
+  // weight-block tile adds kEpiWarps once its hid rows are stored; a down
+  // tile's token warp waits for slot_need before it loads the slot's rows.
   int32_t* slot_done;
   int slot_need;
   int32_t* status;
-  // down only: the gate/up launch's grid and weight blocks per token tile
-  // when both GEMMs run one CTA per SM (0: no stride adjustment)
-  int gu_grid, gu_wblocks;
   // Range normalisation (see the top of this file)
   const int32_t* xexp;  // a of each permuted row: its activations are x' 2^a
-  const float* gs;      // down only: the gate and up scales, for pg and pu
-  const float* us;
-  int n_gu_scales;      // scales per expert of one gate/up matrix
   int hid_shift;        // c
-  // down, fp16 y only: exponent s per 32 columns and row (y = y'' 2^s),
-  // [rows_per_expert / 32][yexp_rows]; NULL: y is fp32
+  // fp16 y only: exponent s per 32 columns and row (y = y'' 2^s),
+  // [H / 32][yexp_rows]; NULL: y is fp32
   int16_t* yexp;
   int yexp_rows;
   // bounded waits give up after this many nanoseconds (0: the default);
   // a diagnostic setting (MOE_FP8_WAIT_LIMIT_US)
   uint64_t wait_ns;
 };
+
 
 struct WsShared {
   uint64_t c_full[NCD], c_empty[NCD];
@@ -129,7 +135,7 @@ struct WsShared {
   uint64_t acc_full, acc_empty;
   uint32_t tmem_base;
   int abort_flag;
-  uint64_t wait_ns;  // the role waits' budget (GemmArgs::wait_ns)
+  uint64_t wait_ns;  // the role waits' budget (FfnArgs::wait_ns)
   // Steps each role has completed, for the timeout record: [warp] for the
   // TMA warps (steps issued) and the decoder warps (steps decoded),
   // [kWarps] steps issued to the tensor core, [kWarps + 1] tiles started by
@@ -222,35 +228,20 @@ __device__ __forceinline__ bool warp_wait_all(WsShared& sh, uint64_t* const (&ba
 struct TileInfo {
   int e, r0, m0, rows, n, n0;  // n = rows rounded up to 16 (the MMA's N)
   int slot;                    // token tile index (tile_off[e] + m0 / 128)
+  bool gu;                     // a gate/up tile (else down)
+  int K, nK;                   // the contraction length and its 64-wide steps
 };
 
-// CTAs that take tiles, each taking every stride-th one.  All of them, except
-// in this case: the down GEMM's CTAs can only start on SMs that gate/up CTAs
-// have left, and when gate/up's tiles do not divide evenly over its grid, r of
-// its CTAs run one tile longer, so the last r down CTAs (dispatched in order)
-// start one gate/up tile late.  If leaving those r CTAs without tiles ends
-// the launch sooner, in units of down tiles (a gate/up tile is H / I of one:
-// the same 256 x K x N shape with K = H rather than I), the stride is G - r.
-__device__ __forceinline__ int tile_stride(const GemmArgs& a, int n_tiles) {
-  const int G = (int)gridDim.x;
-  if (a.gu_grid != G || a.gu_grid <= 0) return G;
-  const long long gu_tiles = (long long)a.tile_off[a.E] * a.gu_wblocks;
-  if (gu_tiles <= a.gu_grid) return G;
-  const int r = (int)(gu_tiles % a.gu_grid);
-  if (r == 0 || n_tiles <= G) return G;
-  const float rho = (float)a.rows_per_expert / (float)a.K;
-  const int c_first = cdiv(n_tiles, G);                // tiles of CTA 0
-  const int c_late = cdiv(n_tiles - (G - r), G);       // tiles of the first late CTA
-  const float end_all = fmaxf((float)c_first, rho + (float)c_late);
-  const float end_early = (float)cdiv(n_tiles, G - r);
-  return end_early < end_all ? G - r : G;
-}
-
-// Tile t -> expert, token rows and weight rows, from the shared-memory copies.
-__device__ __forceinline__ TileInfo tile_info(const WsShared& sh, const GemmArgs& a, int t,
-                                              bool gateup) {
+// List entry t -> phase, expert, token rows and weight rows, from the
+// shared-memory copies of the offsets (n_gu: gate/up tiles in the list).
+template <int MODE>
+__device__ __forceinline__ TileInfo tile_info(const WsShared& sh, const FfnArgs& a, int t,
+                                              int n_gu) {
   TileInfo ti;
-  const int slot = t / a.n_wblocks, wb = t % a.n_wblocks;
+  ti.gu = MODE == kBoth ? t < n_gu : MODE == kGateUp;
+  const int u = ti.gu ? t : t - n_gu;
+  const int nwb = ti.gu ? a.I / BW : a.H / (2 * BW);  // weight tiles per token tile
+  const int slot = u / nwb, wb = u - slot * nwb;
   int lo = 0, hi = a.E;  // largest e with tile_off[e] <= slot
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -262,35 +253,67 @@ __device__ __forceinline__ TileInfo tile_info(const WsShared& sh, const GemmArgs
   ti.m0 = (slot - sh.tile_off[lo]) * BT;
   ti.rows = min(BT, sh.expert_off[lo + 1] - ti.r0 - ti.m0);
   ti.n = (ti.rows + 15) & ~15;
-  ti.n0 = wb * (gateup ? BW : 2 * BW);
+  ti.n0 = wb * (ti.gu ? BW : 2 * BW);
+  ti.K = ti.gu ? a.H : a.I;
+  ti.nK = ti.K / BK;
   return ti;
 }
 
+// This CTA's tiles, in order: gate/up tiles i, i + G, ... (the first r of
+// the G CTAs hold one more when G does not divide them), then down tiles.
+// A gate/up tile costs about m = round(H / I) down tiles (the same 256 x N
+// shape with K = H rather than I), so the r CTAs with the extra gate/up tile
+// sit out the first m rounds of down tiles; every other round goes to all G.
+// Every role of the CTA walks the same sequence.
+struct TileSeq {
+  int i, G, n_gu, n_dn, r, m, k = 0, jj = 0;
+  bool in_gu = true;
+  __device__ TileSeq(int i_, int G_, int n_gu_, int n_dn_, int m_)
+      : i(i_), G(G_), n_gu(n_gu_), n_dn(n_dn_), r(n_gu_ % G_), m(m_) {}
+  __device__ int next() {  // a list index, or -1 after the last
+    if (in_gu) {
+      const int t = i + k * G;
+      if (t < n_gu) {
+        ++k;
+        return t;
+      }
+      in_gu = false;
+    }
+    const int d = i >= r ? (jj < m ? jj * (G - r) + (i - r) : m * (G - r) + (jj - m) * G + i)
+                         : m * (G - r) + jj * G + i;
+    if (d >= n_dn) return -1;
+    ++jj;
+    return n_gu + d;
+  }
+};
+
 }  // namespace
 
-template <bool GATEUP>
+template <int MODE>
 __global__ void __launch_bounds__(kThreadsWS, 1)
-k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant__ CUtensorMap cm1,
-                 const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_y,
-                 const GemmArgs args) {
+k_expert_ffn_ws(const __grid_constant__ CUtensorMap cm_g, const __grid_constant__ CUtensorMap cm_u,
+                const __grid_constant__ CUtensorMap cm_d, const __grid_constant__ CUtensorMap tm_x,
+                const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_y,
+                const FfnArgs args) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ WsShared sh;
-  // Only the token warp waits for the previous kernel (it reads that
-  // kernel's output: the expert-order activation rows or hid).  Everything
-  // else reads data written two or more launches back (tile and row offsets,
-  // weights), so on SMs the previous kernel has already left the codes are
-  // fetched and decoded while its last tiles finish.
+  // Only the token warp and the epilogue wait for the previous kernel (they
+  // read its output: the expert-order activation rows and their exponents).
+  // Everything else reads data written two or more launches back (tile and
+  // row offsets, weights), so on SMs the previous kernel
+  // has already left the codes are fetched and decoded while it finishes.
   if (args.all_wait) griddep_wait();
   griddep_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const GemmArgs& a = args;
-  const int n_tiles = a.tile_off[a.E] * a.n_wblocks;
-  const int tstride = GATEUP ? (int)gridDim.x : tile_stride(a, n_tiles);
+  const FfnArgs& a = args;
+  const int n_slots = a.tile_off[a.E];
+  const int n_gu = MODE == kDown ? 0 : n_slots * (a.I / BW);
+  const int n_all = n_gu + (MODE == kGateUp ? 0 : n_slots * (a.H / (2 * BW)));
   // uniform per CTA, before any barrier
-  if ((int)blockIdx.x >= n_tiles || (int)blockIdx.x >= tstride) return;
-  const int nK = a.K / BK;
-  const int nKb = cdiv(a.K, kScaleBlock);
-  const int nRb = cdiv(a.rows_per_expert, kScaleBlock);
+  if ((int)blockIdx.x >= n_all) return;
+  const int G = (int)gridDim.x;
+  const int m_skip = (a.H + a.I / 2) / a.I;
+  auto seq = [&]() { return TileSeq((int)blockIdx.x, G, n_gu, n_all - n_gu, m_skip); };
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -333,55 +356,59 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     // ------------------------------------------------ E4M3 code blocks (TMA)
     int j = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < n_tiles && ok; t += tstride) {
-      const TileInfo ti = tile_info(sh, a, t, GATEUP);
-      const int row = ti.e * a.rows_per_expert + ti.n0;
-      for (int ks = 0; ks < nK; ++ks, ++j) {
+    TileSeq sq = seq();
+    for (int t = sq.next(); t >= 0 && ok; t = sq.next()) {
+      const TileInfo ti = tile_info<MODE>(sh, a, t, n_gu);
+      const int row = ti.e * (ti.gu ? a.I : a.H) + ti.n0;
+      for (int ks = 0; ks < ti.nK; ++ks, ++j) {
         const int sc = j % NCD;
         if (j >= NCD && !warp_wait(sh, &sh.c_empty[sc], (uint32_t)(((j / NCD) - 1) & 1), a.status, 1, j)) {
           ok = false;
           break;
         }
-        // the decoders' reads of this slot (generic proxy) are ordered before
-        // the copies that overwrite it (async proxy)
         tc::fence_proxy_async();
         if (tc::elect_one()) {
           uint8_t* dst = smem + OFF_C + sc * C_BYTES;
           mbar_arrive_expect_tx(&sh.c_full[sc], C_BYTES);
-          if (GATEUP) {
-            tc::tma_load_2d(dst, &cm0, ks * BK, row, &sh.c_full[sc]);
-            tc::tma_load_2d(dst + BW * BK, &cm1, ks * BK, row, &sh.c_full[sc]);
+          if (ti.gu) {
+            tc::tma_load_2d(dst, &cm_g, ks * BK, row, &sh.c_full[sc]);
+            tc::tma_load_2d(dst + BW * BK, &cm_u, ks * BK, row, &sh.c_full[sc]);
           } else {
-            tc::tma_load_2d(dst, &cm0, ks * BK, row, &sh.c_full[sc]);
-            tc::tma_load_2d(dst + BW * BK, &cm0, ks * BK, row + BW, &sh.c_full[sc]);
+            tc::tma_load_2d(dst, &cm_d, ks * BK, row, &sh.c_full[sc]);
+            tc::tma_load_2d(dst + BW * BK, &cm_d, ks * BK, row + BW, &sh.c_full[sc]);
           }
           reinterpret_cast<volatile int*>(sh.prog)[W_CODES] = j + 1;
         }
         __syncwarp();
       }
     }
-    // drain: the copies of the last NCD steps issued must have landed
     if (lane == 0)
       for (int i = max(0, j - NCD); i < j; ++i) mbar_wait(&sh.c_full[i % NCD], (uint32_t)((i / NCD) & 1));
     __syncwarp();
   } else if (warp == W_TOK) {
     // ------------------------------------------------ token rows (TMA)
-    if (!a.slot_done || GATEUP) griddep_wait();
     // One box of 128 consecutive permuted rows per step (rows past the tile
-    // are never stored; rows past the matrix read 0).
+    // are never stored; rows past the matrix read 0): x' for gate/up (after
+    // the previous kernel, which wrote it, has completed), hid for down
+    // (after the slot's gate/up tiles have stored it).
+    bool waited = a.all_wait != 0;
     int j = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < n_tiles && ok; t += tstride) {
-      const TileInfo ti = tile_info(sh, a, t, GATEUP);
-      if (!GATEUP && a.slot_done) {
-        // this token tile's hid rows: every gate/up weight-block tile of the
-        // slot has stored them (bounded warp-uniform poll, then the acquired
-        // data is ordered before the async-proxy loads below)
+    TileSeq sq = seq();
+    for (int t = sq.next(); t >= 0 && ok; t = sq.next()) {
+      const TileInfo ti = tile_info<MODE>(sh, a, t, n_gu);
+      if (ti.gu) {
+        if (!waited) griddep_wait();
+        waited = true;
+      } else {
+        // every gate/up weight-block tile of the slot has stored its hid
+        // rows (bounded warp-uniform poll, then the acquired data is ordered
+        // before the async-proxy loads below)
         const WaitBudget b = wait_budget(sh.wait_ns);
         bool done = false;
-        for (uint32_t n = 0; !done; ++n) {
+        for (uint32_t i = 0; !done; ++i) {
           done = __all_sync(0xffffffffu, tc::ld_acquire_gpu(a.slot_done + ti.slot) >= a.slot_need);
-          if (!done && (n & 31) == 31) {
+          if (!done && (i & 31) == 31) {
             const bool give_up =
                 *reinterpret_cast<volatile int*>(&sh.abort_flag) != 0 || budget_spent(b);
             if (__any_sync(0xffffffffu, give_up)) break;
@@ -406,7 +433,8 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
         }
         tc::fence_proxy_async_global();
       }
-      for (int ks = 0; ks < nK; ++ks, ++j) {
+      const CUtensorMap* tm = ti.gu ? &tm_x : &tm_h;
+      for (int ks = 0; ks < ti.nK; ++ks, ++j) {
         const int st = j % NT;
         if (j >= NT && !warp_wait(sh, &sh.t_empty[st], (uint32_t)(((j / NT) - 1) & 1), a.status, 2, j)) {
           ok = false;
@@ -414,7 +442,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
         }
         if (tc::elect_one()) {
           mbar_arrive_expect_tx(&sh.t_full[st], T_BYTES);
-          tc::tma_load_2d(smem + OFF_T + st * T_BYTES, &tmap, ks * BK, ti.r0 + ti.m0, &sh.t_full[st]);
+          tc::tma_load_2d(smem + OFF_T + st * T_BYTES, tm, ks * BK, ti.r0 + ti.m0, &sh.t_full[st]);
           reinterpret_cast<volatile int*>(sh.prog)[warp] = j + 1;
         }
         __syncwarp();
@@ -435,29 +463,31 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     // 64-byte swizzle of the code block: 16-byte chunk u of row r sits at
     // chunk u ^ ((r >> 1) & 3)
     const int swz = (r >> 1) & 3;
-    // Block scales: lane i holds the scale of K block i of the tile's weight
-    // row block (nKb <= 32), loaded one tile ahead so that no step waits for
-    // global memory.
-    // The scale is divided by the power of two 2^p of the expert matrix's
-    // (gate/up) or the row block's (down) largest scale, so the fp16 operand
-    // fp16(dec * fp16(S / 2^p)) stays in range for any scale magnitude; the
-    // epilogue multiplies 2^p back in fp32.
-    const float* sp = (GATEUP && blk) ? a.s1 : a.s0;
+    // Block scales: lane i holds the decoder scale of K block i of the
+    // tile's weight block (nKb <= 32), published with the tile's list entry
+    // by the code warp, so that no step waits for global memory.
     bool bad = false;
     auto scale_of = [&](int t) -> float {
-      const TileInfo ti = tile_info(sh, a, t, GATEUP);
-      const size_t srow = (size_t)ti.e * nRb + ti.n0 / kScaleBlock + (GATEUP ? 0 : blk);
+      const TileInfo ti = tile_info<MODE>(sh, a, t, n_gu);
+      const float* sp = ti.gu ? (blk ? a.us : a.gs) : a.ds;
+      const int nKb = cdiv(ti.K, kScaleBlock);
+      const int nRb = cdiv(ti.gu ? a.I : a.H, kScaleBlock);
+      const size_t srow = (size_t)ti.e * nRb + ti.n0 / kScaleBlock + (ti.gu ? 0 : blk);
       const float sc = lane < nKb ? sp[srow * nKb + lane] : 0.f;
-      const int p = GATEUP ? warp_max_exp_of(sp + (size_t)ti.e * nRb * nKb, nRb * nKb, lane, bad)
-                           : warp_max_exp(__float_as_uint(sc) & 0x7fffffffu, bad);
+      const int p = ti.gu ? warp_max_exp_of(sp + (size_t)ti.e * nRb * nKb, nRb * nKb, lane, bad)
+                          : warp_max_exp(__float_as_uint(sc) & 0x7fffffffu, bad);
       return sc * pow2f(-p);
     };
-    float scale_next = scale_of(blockIdx.x);
+    TileSeq sq = seq();
+    int t = sq.next();
+    float scale_next = t >= 0 ? scale_of(t) : 0.f;
     int j = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < n_tiles && ok; t += tstride) {
+    for (int t_next; t >= 0 && ok; t = t_next) {
       const float scale_tile = scale_next;
-      if (t + tstride < n_tiles) scale_next = scale_of(t + tstride);
+      t_next = sq.next();
+      if (t_next >= 0) scale_next = scale_of(t_next);
+      const int nK = tile_info<MODE>(sh, a, t, n_gu).nK;
       for (int ks = 0; ks < nK; ++ks, ++j) {
         const int sc = j % NCD, sa = j % NA;
         const float scale = __shfl_sync(0xffffffffu, scale_tile, ks * BK / kScaleBlock);
@@ -500,8 +530,10 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     // ------------------------------------------------ tcgen05.mma issue
     int j = 0, tl = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < n_tiles && ok; t += tstride, ++tl) {
-      const TileInfo ti = tile_info(sh, a, t, GATEUP);
+    TileSeq sq = seq();
+    for (int t = sq.next(); t >= 0 && ok; t = sq.next(), ++tl) {
+      const TileInfo ti = tile_info<MODE>(sh, a, t, n_gu);
+      const int nK = ti.nK;
       const uint32_t idesc = tc::idesc_f16_f32(BW, ti.n);
       if (tl >= 1 && !warp_wait(sh, &sh.acc_empty, (uint32_t)((tl - 1) & 1), a.status, 5, tl)) {
         ok = false;
@@ -557,25 +589,30 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
     const int q = warp & 3, eh = (warp - W_EPI0) >> 2;
     const uint32_t t_lane = tmem + ((uint32_t)(32 * q) << 16);
     uint8_t* stg = smem + OFF_STG + (warp - W_EPI0) * STG_WARP_BYTES;
-    const int nKb = cdiv(a.K, kScaleBlock), nRb = cdiv(a.rows_per_expert, kScaleBlock);
+    // block scales per expert of one gate/up matrix, and of the down matrix:
+    // [rows / 128][K / 128]
+    const int nKb_g = cdiv(a.H, kScaleBlock), nRb_g = cdiv(a.I, kScaleBlock);
+    const int n_gu_scales = nRb_g * nKb_g;
+    const int nKb_d = cdiv(a.I, kScaleBlock), nRb_d = cdiv(a.H, kScaleBlock);
     const float inv_c = pow2f(-a.hid_shift);
-    // gate/up reads the row exponents ahead of its accumulators: after the
-    // kernel that wrote them has completed
-    if (GATEUP && !a.all_wait) griddep_wait();
+    // the row exponents are read ahead of the accumulators: after the kernel
+    // that wrote them has completed
+    if (MODE != kDown && !a.all_wait) griddep_wait();
     bool bad = false;
     int tl = 0;
-    for (int t = blockIdx.x; t < n_tiles; t += tstride, ++tl) {
-      const TileInfo ti = tile_info(sh, a, t, GATEUP);
+    TileSeq sq = seq();
+    for (int t = sq.next(); t >= 0; t = sq.next(), ++tl) {
+      const TileInfo ti = tile_info<MODE>(sh, a, t, n_gu);
       // the tile's powers of two (scales only: computed before the wait)
       int p0 = 0;  // gate/up: pg; down: pd + pg + pu + c
-      if (GATEUP) {
-        p0 = warp_max_exp_of(a.s0 + (size_t)ti.e * nRb * nKb, nRb * nKb, lane, bad);
+      if (ti.gu) {
+        p0 = warp_max_exp_of(a.gs + (size_t)ti.e * n_gu_scales, n_gu_scales, lane, bad);
       } else {
-        const size_t srow = (size_t)ti.e * nRb + ti.n0 / kScaleBlock + eh;
-        const float sc = lane < nKb ? a.s0[srow * nKb + lane] : 0.f;
+        const size_t srow = (size_t)ti.e * nRb_d + ti.n0 / kScaleBlock + eh;
+        const float sc = lane < nKb_d ? a.ds[srow * nKb_d + lane] : 0.f;
         p0 = warp_max_exp(__float_as_uint(sc) & 0x7fffffffu, bad) +
-             warp_max_exp_of(a.gs + (size_t)ti.e * a.n_gu_scales, a.n_gu_scales, lane, bad) +
-             warp_max_exp_of(a.us + (size_t)ti.e * a.n_gu_scales, a.n_gu_scales, lane, bad) +
+             warp_max_exp_of(a.gs + (size_t)ti.e * n_gu_scales, n_gu_scales, lane, bad) +
+             warp_max_exp_of(a.us + (size_t)ti.e * n_gu_scales, n_gu_scales, lane, bad) +
              a.hid_shift;
       }
       // a of the tile's tokens, lane i holding token 32 c + i's for each
@@ -588,31 +625,31 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
       // down parks its four in the warp's shared bytes, chunk u at 32 u + lane)
       uint32_t axp = 0;
       int8_t* axs = sh.ax[warp - W_EPI0];
-      auto load_ax = [&](int c0, int dc, int n) {
+      auto load_ax = [&](int c0, int dc, int cnt) {
         int v[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int c = c0 + dc * u;
-          v[u] = (u < n && lane < ti.rows - 32 * c) ? __ldg(a.xexp + ti.r0 + ti.m0 + 32 * c + lane) : 0;
+          v[u] = (u < cnt && lane < ti.rows - 32 * c) ? __ldg(a.xexp + ti.r0 + ti.m0 + 32 * c + lane) : 0;
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          if (GATEUP) axp |= ((uint32_t)v[u] & 0xffu) << (8 * u);
+          if (ti.gu) axp |= ((uint32_t)v[u] & 0xffu) << (8 * u);
           else axs[32 * u + lane] = (int8_t)v[u];
         }
       };
       auto ax_of = [&](int u) {
-        return GATEUP ? (int)(int8_t)(axp >> (8 * u)) : (int)axs[32 * u + lane];
+        return ti.gu ? (int)(int8_t)(axp >> (8 * u)) : (int)axs[32 * u + lane];
       };
-      if (GATEUP) load_ax(eh, 2, 2);
+      if (ti.gu) load_ax(eh, 2, 2);
       // this warp's copies of the previous tile have read its staging
       tc::bulk_wait_read_all();
       __syncwarp();
       if (!warp_wait(sh, &sh.acc_full, (uint32_t)(tl & 1), a.status, 8, tl)) break;
       tc::fence_after_sync();
       const int nchunks = (ti.n + 31) >> 5;
-      if (!GATEUP) load_ax(0, 1, 4);
-      if (GATEUP) {
+      if (!ti.gu) load_ax(0, 1, 4);
+      if (ti.gu) {
         bool overflow = false, underflow = false;
 #pragma unroll 1
         for (int c = eh; c < nchunks; c += 2) {
@@ -652,11 +689,10 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
         // each of this half's token rows, 64 bytes
         tc::fence_proxy_async();
         __syncwarp();
-        uint16_t* hid = reinterpret_cast<uint16_t*>(a.out) + (size_t)(ti.r0 + ti.m0) * a.out_ld +
-                        ti.n0 + 32 * q;
+        uint16_t* hid = a.hid + (size_t)(ti.r0 + ti.m0) * a.I + ti.n0 + 32 * q;
         for (int i = lane; i < 64; i += 32) {
           const int c = 2 * (i >> 5) + eh, m = 32 * c + (i & 31);  // token row of staged row i
-          if (m < ti.rows) tc::bulk_store(hid + (size_t)m * a.out_ld, stg + i * 64, 64);
+          if (m < ti.rows) tc::bulk_store(hid + (size_t)m * a.I, stg + i * 64, 64);
         }
         tc::bulk_commit();
         if (a.slot_done) {
@@ -724,8 +760,8 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
             // row r of 32 fp16 (64 bytes): into the staging tile at r * 64,
             // 16-byte groups swizzled by (r >> 1) & 3 (the 64-byte TMA
             // swizzle), or straight to its row when the chunk is ragged
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) +
-                                                  row * a.out_ld + col0);
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.y) +
+                                                  row * a.H + col0);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const uint4 w4 = make_uint4(pack_f16x2(f[8 * j] * sc, f[8 * j + 1] * sc),
@@ -741,7 +777,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
               tc::fence_proxy_async();
               __syncwarp();
               if (lane == 0) {  // bulk groups are per thread: always the same lane
-                tc::tma_store_2d(&tmap_y, col0, ti.r0 + ti.m0 + 32 * c, stg);
+                tc::tma_store_2d(&tm_y, col0, ti.r0 + ti.m0 + 32 * c, stg);
                 tc::bulk_commit();
               }
               __syncwarp();
@@ -750,8 +786,8 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
             // fp32 y = D 2^(pd + pg + pu + c + 2a), in two exact steps
             const int n = min(max(p0 + 2 * ax, -252), 252), h1 = n / 2;
             const float s1 = pow2f(h1), s2 = pow2f(n - h1);
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) +
-                                                    row * a.out_ld + col0);
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.y) +
+                                                    row * a.H + col0);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const float4 w4 = make_float4(f[4 * j] * s1 * s2, f[4 * j + 1] * s1 * s2,
@@ -765,7 +801,7 @@ k_expert_gemm_ws(const __grid_constant__ CUtensorMap cm0, const __grid_constant_
               tc::fence_proxy_async();
               __syncwarp();
               if (lane == 0) {
-                tc::tma_store_2d(&tmap_y, col0, ti.r0 + ti.m0 + 32 * c, stg);
+                tc::tma_store_2d(&tm_y, col0, ti.r0 + ti.m0 + 32 * c, stg);
                 tc::bulk_commit();
               }
               __syncwarp();
@@ -1025,8 +1061,11 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x, int T, const int32_t* exper
   static_assert(BT == kGemmTokenTile, "token tile of the permutation's tile prefix");
   if (!x_perm || !xexp || H > kGatherMaxPieces * 256) return cudaErrorInvalidValue;
   cudaError_t err;
-  if ((err = ensure_smem((const void*)k_expert_gemm_ws<true>, SMEM_WS)) != cudaSuccess) return err;
-  if ((err = ensure_smem((const void*)k_expert_gemm_ws<false>, SMEM_WS)) != cudaSuccess) return err;
+  if (!slot_done) return cudaErrorInvalidValue;
+  if ((err = ensure_smem((const void*)k_expert_ffn_ws<kBoth>, SMEM_WS)) != cudaSuccess ||
+      (err = ensure_smem((const void*)k_expert_ffn_ws<kGateUp>, SMEM_WS)) != cudaSuccess ||
+      (err = ensure_smem((const void*)k_expert_ffn_ws<kDown>, SMEM_WS)) != cudaSuccess)
+    return err;
   CUtensorMap gmap, umap, dmap, xmap, hmap, ymap;
   if ((err = code_map(&gmap, w.gate.codes, (long long)E * I, H)) != cudaSuccess) return err;
   if ((err = code_map(&umap, w.up.codes, (long long)E * I, H)) != cudaSuccess) return err;
@@ -1071,7 +1110,7 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x, int T, const int32_t* exper
   int log2H = 0;
   while ((2 << log2H) <= H) ++log2H;
   // Diagnostics (read on every call): a shorter limit for the bounded waits
-  // (MOE_FP8_WAIT_LIMIT_US), and a down GEMM that waits for one more
+  // (MOE_FP8_WAIT_LIMIT_US), and down tiles that wait for one more
   // completed gate/up tile per token tile than exist, so that its wait runs
   // out (MOE_FP8_TEST_STALL=down; the failure-path test).
   uint64_t wait_ns = 0;
@@ -1080,62 +1119,52 @@ cudaError_t launch_expert_gemm_tc(const uint16_t* x, int T, const int32_t* exper
     if (us > 0) wait_ns = (uint64_t)us * 1000ull;
   }
   const char* stall = getenv("MOE_FP8_TEST_STALL");
-  const bool stall_down = stall && strcmp(stall, "down") == 0 && slot_done;
-  const int nsm = num_sms();
-  const dim3 blk(kThreadsWS);
-  GemmArgs g{};
-  g.expert_off = expert_off;
-  g.tile_off = tile_off;
-  g.E = E;
-  g.K = H;
-  g.rows_per_expert = I;
-  g.s0 = w.gate.scales;
-  g.s1 = w.up.scales;
-  g.out = hid;
-  g.out_ld = I;
-  g.n_wblocks = I / BW;
+  const bool stall_down = stall && strcmp(stall, "down") == 0;
+  FfnArgs f{};
+  f.expert_off = expert_off;
+  f.tile_off = tile_off;
+  f.E = E;
+  f.H = H;
+  f.I = I;
+  f.gs = w.gate.scales;
+  f.us = w.up.scales;
+  f.ds = w.down.scales;
+  f.hid = hid;
+  f.y = y;
   // every warp waits when the previous kernel wrote the tile offsets
-  g.all_wait = prev_wrote_offsets ? 1 : 0;
-  g.slot_done = slot_done;
-  g.slot_need = 0;
-  g.status = status;
-  g.xexp = xexp;
-  g.hid_shift = log2H + 4;
-  g.wait_ns = wait_ns;
-  err = launch_k(k_expert_gemm_ws<true>, dim3(min(nsm, max_ttiles * g.n_wblocks)), blk,
-                 (size_t)SMEM_WS, s, pdl, gmap, umap, xmap, ymap, g);
-  if (err != cudaSuccess) return err;
-  GemmArgs d{};
-  d.expert_off = expert_off;
-  d.tile_off = tile_off;
-  d.E = E;
-  d.K = I;
-  d.rows_per_expert = H;
-  d.s0 = w.down.scales;
-  d.s1 = nullptr;
-  d.out = y;
-  d.out_ld = H;
-  d.n_wblocks = H / (2 * BW);
-  d.all_wait = 0;
-  d.slot_done = slot_done;
-  d.slot_need = (I / BW) * kEpiWarps;
-  d.status = status;
-  d.xexp = xexp;
-  d.gs = w.gate.scales;
-  d.us = w.up.scales;
-  d.n_gu_scales = cdiv(I, kScaleBlock) * cdiv(H, kScaleBlock);
-  d.hid_shift = g.hid_shift;
-  d.yexp = yexp;
-  d.yexp_rows = yexp_rows;
-  d.wait_ns = wait_ns;
-  if (stall_down) d.slot_need += 1;
-  const int gu_grid = min(nsm, max_ttiles * g.n_wblocks);
-  if (gu_grid == nsm && min(nsm, max_ttiles * d.n_wblocks) == nsm) {
-    d.gu_grid = gu_grid;
-    d.gu_wblocks = g.n_wblocks;
+  f.all_wait = prev_wrote_offsets ? 1 : 0;
+  f.slot_done = slot_done;
+  f.slot_need = (I / BW) * kEpiWarps + (stall_down ? 1 : 0);
+  f.status = status;
+  f.xexp = xexp;
+  f.hid_shift = log2H + 4;
+  f.yexp = yexp;
+  f.yexp_rows = yexp_rows;
+  f.wait_ns = wait_ns;
+  // One launch for both GEMMs when gate/up tiles fill every SM and the list
+  // is short (at most 16 tiles per SM, bounded from the shapes): measured,
+  // it saves the second launch's start on every SM (decode T = 32 / 64 / 96
+  // of the Qwen3 shape: -7.6 / -3.8 / -7 us).  With more tiles per SM the
+  // single kernel's larger code costs more than that, and a grid that
+  // gate/up alone does not fill (the shared expert) gains nothing from it,
+  // so gate/up and down launch apart.  MOE_FP8_GEMM_LAUNCHES=1 or =2 forces
+  // either (diagnostics and tests).
+  const int nsm = num_sms();
+  const int gu_tiles = max_ttiles * (I / BW), dn_tiles = max_ttiles * (H / (2 * BW));
+  bool one = gu_tiles >= nsm && gu_tiles + dn_tiles <= 16 * nsm;
+  if (const char* v = getenv("MOE_FP8_GEMM_LAUNCHES")) {
+    if (strcmp(v, "1") == 0) one = true;
+    if (strcmp(v, "2") == 0) one = false;
   }
-  return launch_k(k_expert_gemm_ws<false>, dim3(min(nsm, max_ttiles * d.n_wblocks)), blk,
-                  (size_t)SMEM_WS, s, pdl, dmap, dmap, hmap, ymap, d);
+  if (one)
+    return launch_k(k_expert_ffn_ws<kBoth>, dim3(min(nsm, gu_tiles + dn_tiles)), dim3(kThreadsWS),
+                    (size_t)SMEM_WS, s, pdl, gmap, umap, dmap, xmap, hmap, ymap, f);
+  err = launch_k(k_expert_ffn_ws<kGateUp>, dim3(min(nsm, gu_tiles)), dim3(kThreadsWS),
+                 (size_t)SMEM_WS, s, pdl, gmap, umap, dmap, xmap, hmap, ymap, f);
+  if (err != cudaSuccess) return err;
+  f.all_wait = 0;  // the gate/up launch is the previous kernel: waited for per token tile
+  return launch_k(k_expert_ffn_ws<kDown>, dim3(min(nsm, dn_tiles)), dim3(kThreadsWS),
+                  (size_t)SMEM_WS, s, pdl, gmap, umap, dmap, xmap, hmap, ymap, f);
 }
 
 }  // namespace moe

@@ -215,7 +215,10 @@ moe_status moe_combine(const float* y_perm, const int32_t* tok_slot_row,
  * row per routed expert on average (T*k >= E) when H*I >= 2^20, else from
  * 32 rows per expert; the shared expert: from 32 tokens.  The
  * environment variable MOE_FP8_EXPERT_PATH=gemm or =gemv overrides the choice
- * (diagnostics and tests; read on every call).  Two more diagnostic
+ * (diagnostics and tests; read on every call).  The GEMM runs its gate/up
+ * and down tiles in one launch when gate/up tiles alone fill the SMs and
+ * there are at most 16 tiles per SM (bounded from the shapes), else in two;
+ * MOE_FP8_GEMM_LAUNCHES=1 or =2 forces either.  Two more diagnostic
  * variables, read on every call of the tensor-core GEMM, exist to test the
  * failure path: MOE_FP8_WAIT_LIMIT_US shortens its bounded device waits
  * (default 2 s), and MOE_FP8_TEST_STALL=down makes its down projection wait

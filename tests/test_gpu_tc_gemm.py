@@ -126,3 +126,19 @@ def test_largest_gemm_shape(torch):
     ref = oracle.moe_layer(xb, L, keep_intermediates=False)
     assert np.array_equal(idx.cpu().numpy(), ref["topk_idx"])
     assert_within_tol(oracle.bf16_to_f64(bf16_bits(out)), ref["out"], "H = I = 4096 gemm")
+
+
+@pytest.mark.parametrize("launches", ["1", "2"])
+@pytest.mark.parametrize("name,T", [("qwen3moe_decode", 64), ("tiny", 300), ("skewed", 256)])
+def test_one_or_two_launches_match_oracle(torch, monkeypatch, launches, name, T):
+    """The tile list run by one launch (gate/up then down tiles in every CTA's
+    sequence) or by two (gate/up, then down): same oracle, either form forced
+    with MOE_FP8_GEMM_LAUNCHES, so both are covered at every size."""
+    monkeypatch.setenv("MOE_FP8_EXPERT_PATH", "gemm")
+    monkeypatch.setenv("MOE_FP8_GEMM_LAUNCHES", launches)
+    L = host_layer(name)
+    xb, out, idx, w = _run(torch, L, T)
+    ref = oracle.moe_layer(xb, L, keep_intermediates=False)
+    assert np.array_equal(idx.cpu().numpy(), ref["topk_idx"])
+    assert_within_tol(oracle.bf16_to_f64(bf16_bits(out)), ref["out"],
+                      f"{name} T={T}, {launches} launch(es)")
