@@ -142,3 +142,19 @@ def test_one_or_two_launches_match_oracle(torch, monkeypatch, launches, name, T)
     assert np.array_equal(idx.cpu().numpy(), ref["topk_idx"])
     assert_within_tol(oracle.bf16_to_f64(bf16_bits(out)), ref["out"],
                       f"{name} T={T}, {launches} launch(es)")
+
+
+@pytest.mark.parametrize("name,T", [("qwen3moe_decode", 64), ("qwen3moe_decode", 1),
+                                    ("tiny", 300), ("skewed", 256)])
+def test_one_and_two_launches_bit_identical(torch, monkeypatch, name, T):
+    """One launch (gate/up and down tiles in every CTA's sequence) and two
+    launches run each tile with the same arithmetic, so the layer outputs
+    agree bit for bit on the same inputs."""
+    monkeypatch.setenv("MOE_FP8_EXPERT_PATH", "gemm")
+    L = host_layer(name)
+    outs = []
+    for launches in ("1", "2"):
+        monkeypatch.setenv("MOE_FP8_GEMM_LAUNCHES", launches)
+        xb, out, idx, w = _run(torch, L, T, seed=3)
+        outs.append(bf16_bits(out))
+    assert np.array_equal(outs[0], outs[1]), f"{name} T={T}: one vs two launches"
