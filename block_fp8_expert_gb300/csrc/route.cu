@@ -25,6 +25,86 @@ namespace moe {
 constexpr int kRouteWarps = 4;
 constexpr int kMaxKSlices = 8;  // K-slices of the router logits (route_kslices)
 
+// One 64-column chunk of the router logits for one warp: lane (g, c) holds
+// experts ea = e0 + g and eb = e0 + g + 8, columns kk .. kk + 15 of the
+// chunk (kk = k0 + 16 c), and the activations of tokens trow[nt].
+template <int NT>
+struct RouterChunk {
+  float wa[16], wb[16];
+  uint4 xa[NT][2];
+  __device__ __forceinline__ void load(const uint16_t* __restrict__ x,
+                                       const float* __restrict__ Wr, int H, int E, int ea,
+                                       int eb, const int (&trow)[NT], int kk) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const float4 fa = ea < E ? __ldg(reinterpret_cast<const float4*>(Wr + (size_t)ea * H + kk) + v)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 fb = eb < E ? __ldg(reinterpret_cast<const float4*>(Wr + (size_t)eb * H + kk) + v)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+      wa[4 * v + 0] = fa.x; wa[4 * v + 1] = fa.y; wa[4 * v + 2] = fa.z; wa[4 * v + 3] = fa.w;
+      wb[4 * v + 0] = fb.x; wb[4 * v + 1] = fb.y; wb[4 * v + 2] = fb.z; wb[4 * v + 3] = fb.w;
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      if (trow[nt] >= 0) {
+        const uint16_t* xp = x + (size_t)trow[nt] * H + kk;
+        xa[nt][0] = ldg16(xp);
+        xa[nt][1] = ldg16(xp + 8);
+      } else {
+        xa[nt][0] = xa[nt][1] = make_uint4(0, 0, 0, 0);
+      }
+    }
+  }
+  // the streamed kernels' activations: the quad of lanes 4g .. 4g + 3 holds
+  // token trow's 64 columns k0 .. k0 + 63 (all lanes take part in the quad's
+  // shuffles)
+  __device__ __forceinline__ void write_xn(uint16_t* __restrict__ xn, int8_t* __restrict__ xe,
+                                           int H, const int (&trow)[NT], int k0, int c) const {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      uint4 v[2] = {xa[nt][0], xa[nt][1]};
+      bool bad = false;  // a non-finite x shows in the expert kernels' results
+      const int ex = bf16x16_to_f16_norm(v, bad);
+      if (trow[nt] >= 0) {
+        uint4* dst = reinterpret_cast<uint4*>(xn + (size_t)trow[nt] * H + k0 + 16 * c);
+        dst[0] = v[0];
+        dst[1] = v[1];
+        if (c == 0) xe[(size_t)trow[nt] * (H / 64) + k0 / 64] = (int8_t)min(ex, 127);
+      }
+    }
+  }
+  // acc += the chunk's products: the three bf16 parts of Wr, smallest first
+  __device__ __forceinline__ void mma(float (&acc)[NT][4]) const {
+    // bf16x2 registers of the three parts, element pairs (2m, 2m+1)
+    uint32_t ah[8], am[8], al[8], bh[8], bm[8], bl[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      uint32_t h0, m0, l0, h1, m1, l1;
+      split3_bf16(wa[2 * m], h0, m0, l0);
+      split3_bf16(wa[2 * m + 1], h1, m1, l1);
+      ah[m] = h0 | (h1 << 16); am[m] = m0 | (m1 << 16); al[m] = l0 | (l1 << 16);
+      split3_bf16(wb[2 * m], h0, m0, l0);
+      split3_bf16(wb[2 * m + 1], h1, m1, l1);
+      bh[m] = h0 | (h1 << 16); bm[m] = m0 | (m1 << 16); bl[m] = l0 | (l1 << 16);
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const uint32_t xr[8] = {xa[nt][0].x, xa[nt][0].y, xa[nt][0].z, xa[nt][0].w,
+                              xa[nt][1].x, xa[nt][1].y, xa[nt][1].z, xa[nt][1].w};
+#pragma unroll
+      for (int st = 0; st < 4; ++st) {
+        const uint32_t b[2] = {xr[2 * st], xr[2 * st + 1]};
+        const uint32_t A0[4] = {al[2 * st], bl[2 * st], al[2 * st + 1], bl[2 * st + 1]};
+        const uint32_t A1[4] = {am[2 * st], bm[2 * st], am[2 * st + 1], bm[2 * st + 1]};
+        const uint32_t A2[4] = {ah[2 * st], bh[2 * st], ah[2 * st + 1], bh[2 * st + 1]};
+        mma_bf16_16x8x16(acc[nt], A0, b);
+        mma_bf16_16x8x16(acc[nt], A1, b);
+        mma_bf16_16x8x16(acc[nt], A2, b);
+      }
+    }
+  }
+};
+
 template <int NT>
 __global__ void __launch_bounds__(kRouteWarps * 32)
 k_router_mma(const uint16_t* __restrict__ x, const float* __restrict__ Wr, int T, int H, int E,
@@ -53,70 +133,23 @@ k_router_mma(const uint16_t* __restrict__ x, const float* __restrict__ Wr, int T
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
 
-  for (int k0 = kbeg + warp * 64; k0 < kend; k0 += kRouteWarps * 64) {
-    const int kk = k0 + 16 * c;
-    float wa[16], wb[16];
+  // up to kAhead chunks' loads in flight (4 for one 8-token group, fewer
+  // for more tokens: their activations take the registers), then the
+  // chunks' MMAs in ascending k0, as one chunk at a time would
+  constexpr int kAhead = NT == 1 ? 4 : NT == 2 ? 2 : 1;
+  for (int k0 = kbeg + warp * 64; k0 < kend; k0 += kAhead * kRouteWarps * 64) {
+    RouterChunk<NT> ch[kAhead];
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const float4 fa = ea < E ? __ldg(reinterpret_cast<const float4*>(Wr + (size_t)ea * H + kk) + v)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 fb = eb < E ? __ldg(reinterpret_cast<const float4*>(Wr + (size_t)eb * H + kk) + v)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-      wa[4 * v + 0] = fa.x; wa[4 * v + 1] = fa.y; wa[4 * v + 2] = fa.z; wa[4 * v + 3] = fa.w;
-      wb[4 * v + 0] = fb.x; wb[4 * v + 1] = fb.y; wb[4 * v + 2] = fb.z; wb[4 * v + 3] = fb.w;
-    }
-    uint4 xa[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      if (trow[nt] >= 0) {
-        const uint16_t* xp = x + (size_t)trow[nt] * H + kk;
-        xa[nt][0] = ldg16(xp);
-        xa[nt][1] = ldg16(xp + 8);
-      } else {
-        xa[nt][0] = xa[nt][1] = make_uint4(0, 0, 0, 0);
-      }
-    }
-    if (write_xn) {
-      // the quad of lanes 4g .. 4g + 3 holds token trow's 64 columns k0 ..
-      // k0 + 63 (all lanes take part in the quad's shuffles)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        uint4 v[2] = {xa[nt][0], xa[nt][1]};
-        bool bad = false;  // a non-finite x shows in the expert kernels' results
-        const int ex = bf16x16_to_f16_norm(v, bad);
-        if (trow[nt] >= 0) {
-          uint4* dst = reinterpret_cast<uint4*>(xn + (size_t)trow[nt] * H + kk);
-          dst[0] = v[0];
-          dst[1] = v[1];
-          if (c == 0) xe[(size_t)trow[nt] * (H / 64) + k0 / 64] = (int8_t)min(ex, 127);
-        }
-      }
-    }
-    // bf16x2 registers of the three parts, element pairs (2m, 2m+1)
-    uint32_t ah[8], am[8], al[8], bh[8], bm[8], bl[8];
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      uint32_t h0, m0, l0, h1, m1, l1;
-      split3_bf16(wa[2 * m], h0, m0, l0);
-      split3_bf16(wa[2 * m + 1], h1, m1, l1);
-      ah[m] = h0 | (h1 << 16); am[m] = m0 | (m1 << 16); al[m] = l0 | (l1 << 16);
-      split3_bf16(wb[2 * m], h0, m0, l0);
-      split3_bf16(wb[2 * m + 1], h1, m1, l1);
-      bh[m] = h0 | (h1 << 16); bm[m] = m0 | (m1 << 16); bl[m] = l0 | (l1 << 16);
+    for (int u = 0; u < kAhead; ++u) {
+      const int ku = k0 + u * kRouteWarps * 64;
+      if (ku < kend) ch[u].load(x, Wr, H, E, ea, eb, trow, ku + 16 * c);
     }
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const uint32_t xr[8] = {xa[nt][0].x, xa[nt][0].y, xa[nt][0].z, xa[nt][0].w,
-                              xa[nt][1].x, xa[nt][1].y, xa[nt][1].z, xa[nt][1].w};
-#pragma unroll
-      for (int st = 0; st < 4; ++st) {
-        const uint32_t b[2] = {xr[2 * st], xr[2 * st + 1]};
-        const uint32_t A0[4] = {al[2 * st], bl[2 * st], al[2 * st + 1], bl[2 * st + 1]};
-        const uint32_t A1[4] = {am[2 * st], bm[2 * st], am[2 * st + 1], bm[2 * st + 1]};
-        const uint32_t A2[4] = {ah[2 * st], bh[2 * st], ah[2 * st + 1], bh[2 * st + 1]};
-        mma_bf16_16x8x16(acc[nt], A0, b);  // smallest part first
-        mma_bf16_16x8x16(acc[nt], A1, b);
-        mma_bf16_16x8x16(acc[nt], A2, b);
+    for (int u = 0; u < kAhead; ++u) {
+      const int ku = k0 + u * kRouteWarps * 64;
+      if (ku < kend) {
+        if (write_xn) ch[u].write_xn(xn, xe, H, trow, ku, c);
+        ch[u].mma(acc);
       }
     }
   }
