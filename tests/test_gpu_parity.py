@@ -303,3 +303,49 @@ def test_identity_expert_closed_form(torch):
     expect = c ** 3 * x ** 2 / (1 + np.exp(-c * x))
     assert idx.cpu().numpy().ravel().tolist() == [0] * 5
     assert_within_tol(oracle.bf16_to_f64(bf16_bits(out)), expect, "identity expert")
+
+
+# Degenerate routing: a single expert (every token's one slot, weight 1),
+# every expert selected (k = E: the weights are the full softmax) and top-1,
+# on both expert paths, with a ragged token count.
+DEGENERATE = [(1, 1), (8, 8), (32, 1)]
+
+
+@pytest.mark.parametrize("path", ["gemv", "gemm"])
+@pytest.mark.parametrize("E,k", DEGENERATE)
+@pytest.mark.parametrize("T", [1, 37, 200])
+def test_layer_forward_degenerate_routing(torch, monkeypatch, path, E, k, T):
+    from block_fp8_expert_gb300.device import DeviceLayer
+    monkeypatch.setenv("MOE_FP8_EXPERT_PATH", path)
+    w = mi.Workload(f"degenerate_E{E}_k{k}", H=256, I=128, E=E, k=k)
+    L = mi.make_layer(w, seed=11)
+    D = DeviceLayer.from_host(L)
+    xb, _ = mi.make_tokens(L, T, seed=11)
+    out, idx, wts = _forward(torch, D, _x(torch, xb))
+    ref = oracle.moe_layer(xb, L, keep_intermediates=False)
+    assert np.array_equal(idx.cpu().numpy(), ref["topk_idx"])
+    if k == E:
+        # every expert once per token
+        assert np.array_equal(np.sort(idx.cpu().numpy(), axis=1),
+                              np.tile(np.arange(E), (T, 1)))
+    if k == 1:
+        assert np.all(wts.cpu().numpy() == 1.0)
+    assert_within_tol(wts.cpu().numpy(), ref["topk_w"], "topk_w", rel=W_REL)
+    assert_within_tol(oracle.bf16_to_f64(bf16_bits(out)), ref["out"],
+                      f"out E={E} k={k} T={T} {path}")
+
+
+# Token counts on both sides of every host-side switch of the layer call:
+# T*k = 64 (tiny one-CTA permutation) / 72, 15 / 16 (top-k split into its own
+# launch), 127 / 128 (mma.sync router / tensor-core router), T*k = 4096 /
+# 4104 (one-CTA permutation / three permutation kernels).
+@pytest.mark.parametrize("T", [8, 9, 15, 16, 127, 128, 512, 513])
+def test_layer_forward_switch_boundaries(torch, T):
+    L = host_layer("qwen3moe_decode")
+    D = dev_layer("qwen3moe_decode")
+    xb, _ = mi.make_tokens(L, T, seed=12)
+    out, idx, w = _forward(torch, D, _x(torch, xb))
+    ref = oracle.moe_layer(xb, L, keep_intermediates=False)
+    assert np.array_equal(idx.cpu().numpy(), ref["topk_idx"])
+    assert_within_tol(w.cpu().numpy(), ref["topk_w"], "topk_w", rel=W_REL)
+    assert_within_tol(oracle.bf16_to_f64(bf16_bits(out)), ref["out"], f"out T={T}")
