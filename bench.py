@@ -26,6 +26,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -350,6 +351,18 @@ def aggregate(t_rank: float, world: int, tokens_per_rank: int, steps: int, dist=
     return world * tokens_per_rank * steps / t_all, t_all
 
 
+def step_stats(times, per=1):
+    """Median, min, 90th percentile and max of the step times in ms, each
+    divided by `per` (the passes a step replays), next to the mean that the
+    line reports."""
+    v = sorted(t * 1e3 / per for t in times)
+    if not v:
+        return None
+    p90 = v[min(len(v) - 1, int(math.ceil(0.9 * len(v))) - 1)]
+    return {"median": statistics.median(v), "min": v[0], "p90": p90, "max": v[-1],
+            "n": len(v)}
+
+
 def time_steps(torch, fn, steps, warmup, flush):
     for _ in range(warmup):
         fn()
@@ -507,6 +520,7 @@ def measure_workload(torch, name, T, steps, warmup, flush, pk, dev_cache, seed=0
            "passes": len(times) * M, "layer_copies": R,
            "device_status": pg.device_status(), "distinct_experts": Dn, "bytes": B,
            "flops": F, "hbm_gbs": B / t / 1e9, "tflops": F / t / 1e12, "bound": bound,
+           "ms_stats": step_stats(times, M),
            "roofline_frac": max(t_hbm, t_tc) / t, "clocks": ck,
            "kcycles": t * ck["sm_mhz"] * 1e3 if ck["sm_mhz"] else None}
     del pg
@@ -683,6 +697,7 @@ def run_gpu(args):
             "device_status": headline_status,
             "verify": verify,
             "ms_step_max": max(times) * 1e3,
+            "ms_per_pass_stats": step_stats(times, M),
             "clocks": ck,
             "sweep": sweep,
         }
