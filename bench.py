@@ -351,6 +351,20 @@ def aggregate(t_rank: float, world: int, tokens_per_rank: int, steps: int, dist=
     return world * tokens_per_rank * steps / t_all, t_all
 
 
+# Nominal GB300 figures, for context beside the measured denominators.
+NOMINAL_HBM_GBS = 7900.0
+
+
+def other_denominators(pk, gbs, tflops, act8=False):
+    """The same achieved figures against the nominal HBM rate and, for the
+    contraction, the measured sustained bf16 rate (x2 for fp8)."""
+    out = {"frac_hbm_nominal_7900gbs": gbs / NOMINAL_HBM_GBS}
+    sus = pk.get("bf16_tflops_sustained")
+    if sus:
+        out["frac_tc_sustained"] = tflops / (sus * (2.0 if act8 else 1.0))
+    return out
+
+
 def step_stats(times, per=1):
     """Median, min, 90th percentile and max of the step times in ms, each
     divided by `per` (the passes a step replays), next to the mean that the
@@ -521,6 +535,7 @@ def measure_workload(torch, name, T, steps, warmup, flush, pk, dev_cache, seed=0
            "device_status": pg.device_status(), "distinct_experts": Dn, "bytes": B,
            "flops": F, "hbm_gbs": B / t / 1e9, "tflops": F / t / 1e12, "bound": bound,
            "ms_stats": step_stats(times, M),
+           "other_denominators": other_denominators(pk, B / t / 1e9, F / t / 1e12, act8),
            "roofline_frac": max(t_hbm, t_tc) / t, "clocks": ck,
            "kcycles": t * ck["sm_mhz"] * 1e3 if ck["sm_mhz"] else None}
     del pg
@@ -687,7 +702,9 @@ def run_gpu(args):
             "ms_per_pass": ms_per_pass,
             "kcycles_per_pass": ms_per_pass * ck["sm_mhz"] if ck["sm_mhz"] else None,
             "layer_roofline": {"bytes": B, "flops": F, "achieved_gbs": B / (ms_per_pass * 1e-3) / 1e9,
-                               "frac_hbm": B / (ms_per_pass * 1e-3) / 1e9 / pk["hbm_gbs"]},
+                               "frac_hbm": B / (ms_per_pass * 1e-3) / 1e9 / pk["hbm_gbs"],
+                               **other_denominators(pk, B / (ms_per_pass * 1e-3) / 1e9,
+                                                    F / (ms_per_pass * 1e-3) / 1e12)},
             "roofline": roof,
             "phases_us": {k: v * 1e6 for k, v in ph.items()},
             "cpu_baseline": cpu,
